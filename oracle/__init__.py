@@ -1,0 +1,131 @@
+"""Row-wise softmax oracle (double precision, single-threaded CPU).
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, ``__graft_entry__.smoke()`` and
+bench.py's ``cpu_baseline`` / ``--impl reference`` leg may import this module.
+The library (``row_wise_softmax_gb300``) never imports it and shares no code
+with it; the C source ``softmax_oracle.c`` includes nothing from the CUDA path.
+
+The functions restate the pages' softmax (the "Level 1: Softmax" formula of
+the cs336 lecture 6 notes and the fused-softmax example of "Triton: write
+CUDA-grade GPU operators in Python"), the online (m, l) recurrence of
+"Triton GPU programming deep dive" section 3.3, and the tiled row sum of the
+lecture notes' "Level 2".  See ``softmax_oracle.c`` for each function's
+citation.  Every function is pinned in tests/test_oracle_pins.py.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "softmax_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+
+F32 = 0
+BF16 = 1
+
+# -ffp-contract=off: no fused multiply-add contraction, so x86 and Arm hosts
+# produce the same doubles.  No fast-math: rint() must round ties to even.
+_CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the oracle with gcc into ``out`` (default: oracle/liboracle.so)."""
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    tmp = out + ".tmp%d" % os.getpid()
+    subprocess.run(["gcc", *_CFLAGS, src, "-o", tmp, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+class Oracle:
+    """ctypes view of one compiled oracle library."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        i64, dbl, vp = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
+        lib.oracle_softmax_rows.argtypes = [vp, vp, i64, i64, i64, i64, ctypes.c_int, i64]
+        lib.oracle_softmax_rows.restype = ctypes.c_int
+        lib.oracle_double_to_bf16.argtypes = [dbl]
+        lib.oracle_double_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_double.restype = dbl
+        lib.oracle_double_to_bf16_array.argtypes = [vp, vp, i64]
+        lib.oracle_bf16_to_double_array.argtypes = [vp, vp, i64]
+        lib.oracle_tiled_row_sum.argtypes = [vp, i64, i64, i64, vp]
+        lib.oracle_tiled_row_sum.restype = dbl
+        self._lib = lib
+
+    def softmax_rows(self, buf: np.ndarray, n_rows: int, n_cols: int,
+                     in_row_stride: int | None = None, dtype: int = F32,
+                     tile: int = 0) -> np.ndarray:
+        """Softmax of each row of a strided row matrix, in double.
+
+        ``buf`` is the flat input buffer: float32 values (dtype F32) or bf16
+        bit patterns as uint16 (dtype BF16).  Row r starts at element
+        ``r * in_row_stride``.  Returns a dense float64 array [n_rows, n_cols].
+        ``tile > 0`` uses the online (m, l) recurrence with that tile width.
+        """
+        if in_row_stride is None:
+            in_row_stride = n_cols
+        want = np.float32 if dtype == F32 else np.uint16
+        buf = np.ascontiguousarray(buf).reshape(-1)
+        if buf.dtype != want:
+            raise TypeError("oracle: buffer dtype %s, expected %s" % (buf.dtype, want))
+        if n_rows > 0 and n_cols > 0 and buf.size < (n_rows - 1) * in_row_stride + n_cols:
+            raise ValueError("oracle: buffer too small for the strided rows")
+        out = np.empty((n_rows, n_cols), dtype=np.float64)
+        rc = self._lib.oracle_softmax_rows(buf.ctypes.data, out.ctypes.data, n_rows, n_cols,
+                                           in_row_stride, n_cols, dtype, tile)
+        if rc != 0:
+            raise ValueError("oracle_softmax_rows rejected its arguments")
+        return out
+
+    def to_bf16(self, values: np.ndarray) -> np.ndarray:
+        """Round doubles to bf16 (ties to even); returns uint16 bit patterns."""
+        v = np.ascontiguousarray(values, dtype=np.float64)
+        out = np.empty(v.shape, dtype=np.uint16)
+        self._lib.oracle_double_to_bf16_array(v.ctypes.data, out.ctypes.data, v.size)
+        return out
+
+    def bf16_to_double(self, bits: np.ndarray) -> np.ndarray:
+        b = np.ascontiguousarray(bits, dtype=np.uint16)
+        out = np.empty(b.shape, dtype=np.float64)
+        self._lib.oracle_bf16_to_double_array(b.ctypes.data, out.ctypes.data, b.size)
+        return out
+
+    def tiled_row_sum(self, x: np.ndarray, block: int, snapshot_tiles: int):
+        """Returns (row sum, lane accumulators after ``snapshot_tiles`` tiles)."""
+        xv = np.ascontiguousarray(x, dtype=np.float64)
+        acc = np.zeros(block, dtype=np.float64)
+        s = self._lib.oracle_tiled_row_sum(xv.ctypes.data, xv.size, block,
+                                           snapshot_tiles, acc.ctypes.data)
+        return s, acc
+
+
+_default: Oracle | None = None
+
+
+def load() -> Oracle:
+    """Build (if needed) and load the oracle library."""
+    global _default
+    if _default is None:
+        _default = Oracle(build())
+    return _default
+
+
+def softmax_rows(*args, **kwargs) -> np.ndarray:
+    return load().softmax_rows(*args, **kwargs)
+
+
+def to_bf16(values: np.ndarray) -> np.ndarray:
+    return load().to_bf16(values)
+
+
+def bf16_to_double(bits: np.ndarray) -> np.ndarray:
+    return load().bf16_to_double(bits)

@@ -1,0 +1,310 @@
+"""Pins for the oracle: checks against things other than the oracle itself.
+
+Each test fixes the oracle to a closed form, an invariant, a high-precision
+brute force (mpmath), a library routine (torch CPU in double), or the pages'
+worked example, so that a dropped term, a wrong sign or index, or a wrong
+stride in oracle/softmax_oracle.c fails at least one of them.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import BF16, F32
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- bf16 codec
+
+def test_bf16_decode_exhaustive(oracle_lib):
+    torch = pytest.importorskip("torch")
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    got = oracle_lib.bf16_to_double(bits)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def _positive_bf16_table():
+    """Exact values of all finite non-negative bf16 patterns, ascending."""
+    pats = np.arange(0, 0x7F80, dtype=np.uint32)
+    f32 = (pats << 16).astype(np.uint32).view(np.float32)
+    return pats, [Fraction(float(v)) for v in f32]
+
+
+_TABLE = None
+
+
+def _nearest_even_bf16(v: float) -> int:
+    """Brute-force RNE: bracket |v| among all bf16 values with exact fractions."""
+    global _TABLE
+    if _TABLE is None:
+        _TABLE = _positive_bf16_table()
+    pats, vals = _TABLE
+    if math.isnan(v):
+        return 0x7FC0 | (0x8000 if math.copysign(1.0, v) < 0 else 0)
+    sign = 0x8000 if math.copysign(1.0, v) < 0 else 0
+    a = Fraction(abs(v)) if math.isfinite(v) else None
+    top = vals[-1]
+    next_binade = Fraction(2) ** 128
+    if a is None or a >= (top + next_binade) / 2:
+        return sign | 0x7F80
+    lo, hi = 0, len(vals) - 1
+    if a >= top:
+        return sign | int(pats[-1])
+    while hi - lo > 1:                      # vals[lo] <= a < vals[hi]
+        mid = (lo + hi) // 2
+        if vals[mid] <= a:
+            lo = mid
+        else:
+            hi = mid
+    dlo, dhi = a - vals[lo], vals[hi] - a
+    if dlo < dhi:
+        pick = lo
+    elif dhi < dlo:
+        pick = hi
+    else:
+        pick = lo if (int(pats[lo]) & 1) == 0 else hi
+    return sign | int(pats[pick])
+
+
+def test_bf16_round_bruteforce(oracle_lib):
+    rng = np.random.default_rng(11)
+    vals = list(rng.standard_normal(400) * np.exp2(rng.integers(-140, 130, 400)))
+    # Exact ties between neighbouring bf16 values, and their double neighbours.
+    for p in list(rng.integers(0, 0x7F7F, 200)) + [0, 1, 0x7F, 0x80, 0x7F7E]:
+        a = float(((np.uint32(p) << 16).astype(np.uint32)).view(np.float32))
+        b = float(((np.uint32(p + 1) << 16).astype(np.uint32)).view(np.float32))
+        mid = (a + b) / 2.0                 # exact in double
+        vals += [mid, np.nextafter(mid, 0.0), np.nextafter(mid, np.inf), -mid]
+    top = float(((np.uint32(0x7F7F) << 16).astype(np.uint32)).view(np.float32))
+    over = (top + 2.0 ** 128) / 2.0
+    vals += [0.0, -0.0, np.inf, -np.inf, top, over, np.nextafter(over, 0.0), 1e-300,
+             2.0 ** -134, np.nextafter(2.0 ** -134, 1.0), 2.0 ** -133, 1.0, 1.0 / 3.0]
+    vals = np.array(vals, dtype=np.float64)
+    got = oracle_lib.to_bf16(vals)
+    want = np.array([_nearest_even_bf16(float(v)) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got, want), vals[got != want][:5]
+    assert oracle_lib.to_bf16(np.array([np.nan]))[0] & 0x7FFF == 0x7FC0
+
+
+# --------------------------------------------------- closed forms and invariants
+
+def _rows(x):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    return x.reshape(-1), x.shape[0], x.shape[1]
+
+
+def test_constant_row_is_exactly_one_over_n(oracle_lib):
+    for n in (1, 7, 1000, 4096):
+        buf, r, c = _rows(np.full((2, n), 0.5))
+        y = oracle_lib.softmax_rows(buf, r, c)
+        assert np.all(y == 1.0 / n)
+    buf, r, c = _rows(np.full((1, 4096), -3.25))
+    assert np.all(oracle_lib.softmax_rows(buf, r, c) == 2.0 ** -12)
+
+
+def test_all_but_one_neg_inf_gives_exactly_one(oracle_lib):
+    n = 1024
+    x = np.full((n, n), -np.inf, dtype=np.float32)
+    rng = np.random.default_rng(3)
+    keep = rng.integers(0, n, n)
+    x[np.arange(n), keep] = rng.standard_normal(n).astype(np.float32) * 8
+    y = oracle_lib.softmax_rows(*_rows(x))
+    want = np.zeros((n, n))
+    want[np.arange(n), keep] = 1.0
+    assert np.array_equal(y, want)
+    assert not np.any(np.signbit(y))        # zeros are +0
+
+
+def test_one_hot_spike_matches_logistic_form(oracle_lib):
+    rng = np.random.default_rng(5)
+    n = 4096
+    x = rng.standard_normal((3, n)).astype(np.float32)
+    s = rng.integers(0, n, 3)
+    x[np.arange(3), s] = 50.0
+    y = oracle_lib.softmax_rows(*_rows(x))
+    for r in range(3):
+        rest = [math.exp(float(x[r, j]) - 50.0) for j in range(n) if j != s[r]]
+        ys = 1.0 / (1.0 + math.fsum(rest))
+        assert abs(y[r, s[r]] - ys) <= 2e-16
+        assert y[r, s[r]] > 1.0 - 1e-15
+        j = (s[r] + 1) % n
+        assert math.isclose(y[r, j], math.exp(float(x[r, j]) - 50.0) * ys, rel_tol=1e-14)
+
+
+def test_shift_invariance_exact_shifts(oracle_lib):
+    rng = np.random.default_rng(7)
+    base = rng.integers(-40, 40, size=(16, 300)).astype(np.float32) / 4   # exact
+    y0 = oracle_lib.softmax_rows(*_rows(base))
+    for c in (-1000.0, -64.0, 64.0, 1000.0):
+        y = oracle_lib.softmax_rows(*_rows(base + np.float32(c)))
+        assert np.array_equal(y, y0), c     # x_j - max is exact, so bitwise equal
+
+
+def test_rows_sum_to_one_and_are_in_range(oracle_lib):
+    w = oracle.softmax_rows  # module-level helper also works
+    rng = np.random.default_rng(9)
+    x = (rng.standard_normal((64, 777)) * 6).astype(np.float32)
+    y = w(*_rows(x))
+    assert np.all(y >= 0) and np.all(y <= 1)
+    assert np.max(np.abs(y.sum(axis=1) - 1.0)) <= 777 * 2.0 ** -52
+
+
+def test_row_permutation_permutes_output(oracle_lib):
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((50, 129)).astype(np.float32)
+    p = rng.permutation(50)
+    y = oracle_lib.softmax_rows(*_rows(x))
+    yp = oracle_lib.softmax_rows(*_rows(x[p]))
+    assert np.array_equal(yp, y[p])
+
+
+def test_two_element_closed_form(oracle_lib):
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 40
+    rng = np.random.default_rng(17)
+    x = (rng.standard_normal((200, 2)) * 10).astype(np.float32)
+    y = oracle_lib.softmax_rows(*_rows(x))
+    for r in range(200):
+        a, b = mpmath.mpf(float(x[r, 0])), mpmath.mpf(float(x[r, 1]))
+        y0 = 1 / (1 + mpmath.exp(b - a))
+        assert abs(y[r, 0] - float(y0)) <= 4e-16 * max(float(y0), 1e-300) + 1e-300
+        assert abs(y[r, 1] - float(1 - y0)) <= 4e-16 * max(float(1 - y0), 1e-300) + 1e-300
+
+
+def test_bruteforce_high_precision_tiny_rows(oracle_lib):
+    """Unshifted exp(x_j) / sum exp(x_k) at 50 digits, on rows of 1..9 values."""
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 50
+    rng = np.random.default_rng(19)
+    for n in range(1, 10):
+        x = (rng.standard_normal((20, n)) * 5).astype(np.float32)
+        if n > 2:
+            x[::3, 0] = -np.inf                       # some masked entries
+        y = oracle_lib.softmax_rows(*_rows(x))
+        for r in range(20):
+            ex = [mpmath.exp(mpmath.mpf(float(v))) if np.isfinite(v) else mpmath.mpf(0)
+                  for v in x[r]]
+            tot = mpmath.fsum(ex)
+            for j in range(n):
+                want = float(ex[j] / tot)
+                assert abs(y[r, j] - want) <= (n + 2) * 2.0 ** -53 * want + 1e-300, (n, r, j)
+
+
+def test_bf16_input_matches_torch_double(oracle_lib):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(23)
+    xf = (rng.standard_normal((33, 1024)) * 8).astype(np.float32)
+    xf[np.arange(33)[:, None] < np.arange(1024)[None, :] - 500] = -np.inf
+    xb = torch.from_numpy(xf).to(torch.bfloat16)
+    bits = xb.view(torch.int16).numpy().view(np.uint16)
+    y = oracle_lib.softmax_rows(bits.reshape(-1), 33, 1024, dtype=BF16)
+    ref = torch.softmax(xb.to(torch.float64), dim=-1).numpy()
+    # Two double implementations differ by a few ulp (summation order).
+    assert np.all(np.abs(y - ref) <= 1e-14 * ref + 1e-300)
+
+
+def test_f32_matches_torch_double(oracle_lib):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(29)
+    x = (rng.standard_normal((40, 333)) * 3).astype(np.float32)
+    x[rng.random(x.shape) < 0.05] = -np.inf
+    x[5, :] = 0.5
+    y = oracle_lib.softmax_rows(*_rows(x))
+    ref = torch.softmax(torch.from_numpy(x).double(), dim=-1).numpy()
+    assert np.all(np.abs(y - ref) <= 1e-14 * ref + 1e-300)
+
+
+def test_degenerate_rows_are_nan(oracle_lib):
+    torch = pytest.importorskip("torch")
+    x = np.zeros((4, 8), dtype=np.float32)
+    x[0, :] = -np.inf                      # all masked
+    x[1, 3] = np.nan                       # one NaN
+    x[2, 5] = np.inf                       # one +inf
+    x[3, :] = np.arange(8)                 # ordinary row
+    y = oracle_lib.softmax_rows(*_rows(x))
+    assert np.all(np.isnan(y[:3]))
+    assert np.all(np.isfinite(y[3]))
+    ref = torch.softmax(torch.from_numpy(x).double(), dim=-1).numpy()
+    assert np.array_equal(np.isnan(ref), np.isnan(y))
+
+
+def test_padded_input_stride_never_reads_padding(oracle_lib):
+    rng = np.random.default_rng(31)
+    dense = rng.standard_normal((9, 127)).astype(np.float32)
+    for pad in (np.nan, np.inf, 1e30):
+        buf = np.full((9, 128), pad, dtype=np.float32)
+        buf[:, :127] = dense
+        flat = buf.reshape(-1)[: 8 * 128 + 127]       # exact extent: no last pad
+        y = oracle_lib.softmax_rows(flat, 9, 127, in_row_stride=128)
+        assert np.array_equal(y, oracle_lib.softmax_rows(dense.reshape(-1), 9, 127))
+
+
+def test_bad_arguments_rejected(oracle_lib):
+    with pytest.raises(ValueError):
+        oracle_lib.softmax_rows(np.zeros(10, np.float32), 2, 6)     # buffer too small
+    with pytest.raises(TypeError):
+        oracle_lib.softmax_rows(np.zeros(10, np.float64), 1, 10)
+    assert oracle_lib.softmax_rows(np.zeros(0, np.float32), 0, 5).shape == (0, 5)
+
+
+# ----------------------------------------------------------- online recurrence
+
+@pytest.mark.parametrize("tile", [1, 3, 4, 64, 1000])
+def test_online_recurrence_equals_definition(oracle_lib, tile):
+    rng = np.random.default_rng(37)
+    x = (rng.standard_normal((24, 700)) * 6).astype(np.float32)
+    x[:8][np.arange(8)[:, None] * 90 < np.arange(700)[None, :]] = -np.inf   # causal-like tails
+    x[8:16, :200] = -np.inf                                                  # leading -inf tiles
+    x[16, :] = 0.5
+    plain = oracle_lib.softmax_rows(*_rows(x))
+    online = oracle_lib.softmax_rows(*_rows(x), tile=tile)
+    # Same result up to rounding order: each rescale adds a few ulp.
+    assert np.all(np.abs(online - plain) <= 1e-14 * plain + 1e-300)
+    assert np.array_equal(online == 0, plain == 0)
+
+
+def test_online_recurrence_degenerate_rows(oracle_lib):
+    x = np.full((3, 12), -np.inf, dtype=np.float32)
+    x[1, 2] = np.nan                       # NaN inside a leading all -inf tile
+    x[2, 9] = 1.0                          # survivor in the last tile
+    y = oracle_lib.softmax_rows(*_rows(x), tile=4)
+    assert np.all(np.isnan(y[0])) and np.all(np.isnan(y[1]))
+    assert y[2, 9] == 1.0 and np.count_nonzero(y[2]) == 1
+
+
+# ----------------------------------------------------- the pages' worked example
+
+def _read_golden(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, *v = line.split()
+                out[k] = [float(t) for t in v]
+    return out
+
+
+def test_level2_tiled_row_sum_worked_example(oracle_lib):
+    g = _read_golden("level2_row_sum.txt")
+    block = int(g["block"][0])
+    rng = np.random.default_rng(41)
+    row = np.concatenate([g["row_prefix"], rng.integers(0, 10, 6)]).astype(np.float64)
+    assert row.size == 12                      # the page's row length
+    _, acc0 = oracle_lib.tiled_row_sum(row, block, snapshot_tiles=1)
+    assert list(acc0) == g["after_tile0"]
+    _, acc1 = oracle_lib.tiled_row_sum(row, block, snapshot_tiles=2)
+    assert acc1[0] == g["after_tile1_lane0"][0] and acc1[1] == g["after_tile1_lane1"][0]
+    total, acc3 = oracle_lib.tiled_row_sum(row, block, snapshot_tiles=99)
+    assert total == math.fsum(row) and math.fsum(acc3) == total
+    # A ragged row: masked lanes add nothing.
+    total, _ = oracle_lib.tiled_row_sum(row[:10], block, snapshot_tiles=99)
+    assert total == math.fsum(row[:10])
