@@ -1,0 +1,393 @@
+"""Row-wise softmax benchmark: GB/s and fraction of the GB300 HBM roofline.
+
+One step = one softmax_rows call (the whole hot path: load, max, exp, sum,
+normalise, store) over the headline workload, 4096 x 4096 fp32 with -inf
+entries and a constant row.  Bytes are algorithmic: n_rows * n_cols *
+(in + out element size), one read and one write of every element.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  Timing: CUDA events on the launching stream
+around every step; L2 is flushed (a 512 MiB write) between steps, outside the
+events; inputs are resident in HBM before the timed region starts.  Under
+torchrun (N > 1) every rank runs its own copy of the workload (rows shard
+with no exchange: weak scaling) and the time is the maximum over ranks.
+
+--impl reference times the CPU oracle (double precision, single-threaded) on
+the same workload and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+HEADLINE = "masked_f32"
+METRIC = "softmax GB/s and % of GB300 HBM roofline (fp32/bf16) per row-length config"
+UNIT = "GB/s"
+FLUSH_BYTES = 512 << 20
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+# Sources of each path's kernel, hashed to tell whether committed ncu counters
+# still describe the kernel being timed.
+KERNEL_SOURCES = {
+    "warp": ["warp_rows.cu", "common.cuh"],
+    "cta": ["row_slices.cu", "common.cuh"],
+    "cluster": ["row_slices.cu", "common.cuh"],
+    "twopass": ["twopass.cu", "common.cuh"],
+}
+KERNEL_NAMES = {"warp": "warp_rows_kernel", "cta": "row_slices_kernel",
+                "cluster": "row_slices_kernel", "twopass": "twopass_kernel"}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def shard_rows(n_rows: int, rank: int, world: int) -> tuple[int, int]:
+    """Contiguous row block [lo, hi) of a row-split across ranks (no exchange)."""
+    base, extra = divmod(n_rows, world)
+    lo = rank * base + min(rank, extra)
+    return lo, lo + base + (1 if rank < extra else 0)
+
+
+def source_hash(path_name: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[path_name]:
+        with open(os.path.join(ROOT, "row_wise_softmax_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(path_name: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if still valid."""
+    fn = os.path.join(PROFILE_DIR, "%s.%s.json" % (KERNEL_NAMES[path_name], workload))
+    try:
+        with open(fn) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None, "no committed ncu summary"
+    if rec.get("source_sha") != source_hash(path_name):
+        return None, "kernel changed since the ncu capture"
+    return rec.get("dram_bytes_per_launch"), fn
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while a region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)       # let the first sample land before the region
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def to_device(w: wl.Workload, torch):
+    if w.dtype == wl.F32:
+        return torch.from_numpy(w.data).cuda()
+    return torch.from_numpy(w.data.view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def device_buffers(w: wl.Workload, torch):
+    x = to_device(w, torch)
+    dt = torch.float32 if w.dtype == wl.F32 else torch.bfloat16
+    y = torch.empty(max(w.out_elems, 1), dtype=dt, device="cuda")
+    return x, y
+
+
+def time_device(w: wl.Workload, bufs, steps: int, warmup: int, torch, rws, flush, stream):
+    """Per-step CUDA-event times (ms) of softmax_rows on device-resident data.
+    The L2 flush and the softmax run on the same stream, in order."""
+    x, y = bufs
+    args = (x.data_ptr(), y.data_ptr(), w.n_rows, w.n_cols, w.in_row_stride,
+            w.out_row_stride, w.dtype, stream.cuda_stream)
+    call = rws.lib().softmax_rows
+    for _ in range(warmup):
+        flush.zero_()
+        st = call(*args)
+        if st != rws.OK:
+            raise RuntimeError("softmax_rows: " + rws.status_string(st))
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    launches0 = rws.launch_count()
+    for a, b in ev:
+        flush.zero_()                                  # L2 flush, outside the events
+        a.record(stream)
+        call(*args)
+        b.record(stream)
+    torch.cuda.synchronize()
+    launches = rws.launch_count() - launches0
+    return [a.elapsed_time(b) for a, b in ev], launches
+
+
+def time_e2e(w: wl.Workload, steps: int, warmup: int, torch, rws, stream):
+    """softmax_rows_host with pinned host buffers: H2D + kernel + D2H per step."""
+    dt = torch.float32 if w.dtype == wl.F32 else torch.bfloat16
+    if w.dtype == wl.F32:
+        h_in = torch.from_numpy(w.data).pin_memory()
+    else:
+        h_in = torch.from_numpy(w.data.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_out = torch.empty(max(w.out_elems, 1), dtype=dt).pin_memory()
+    d_in = torch.empty(w.n_rows * w.n_cols, dtype=dt, device="cuda")
+    d_out = torch.empty_like(d_in)
+    args = (h_in.data_ptr(), h_out.data_ptr(), w.n_rows, w.n_cols, w.in_row_stride,
+            w.out_row_stride, w.dtype, d_in.data_ptr(), d_out.data_ptr(), stream.cuda_stream)
+    call = rws.lib().softmax_rows_host
+    for _ in range(warmup):
+        if call(*args) != rws.OK:
+            raise RuntimeError("softmax_rows_host failed")
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        call(*args)
+    b.record(stream)
+    b.synchronize()
+    ms = a.elapsed_time(b) / steps
+    esz = w.elem_bytes
+    return ms, w.n_rows * w.n_cols * esz, w.n_rows * w.n_cols * esz
+
+
+def cpu_oracle_time(w: wl.Workload, reps: int):
+    import oracle
+    oracle.load()
+    ts = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.softmax_rows(w.data, w.n_rows, w.n_cols, w.in_row_stride, w.dtype)
+        ts.append(time.perf_counter() - t0)
+    return statistics.median(ts)
+
+
+def run_ours(args):
+    import torch
+    import row_wise_softmax_gb300 as rws
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    rws.build()
+    rws.lib()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    peak, peak_kind = measured_peak()
+
+    w = wl.make(HEADLINE)
+    plan = rws.plan(w.n_rows, w.n_cols, in_row_stride=w.in_row_stride,
+                    out_row_stride=w.out_row_stride, dtype=w.dtype)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    bufs = device_buffers(w, torch)
+    barrier()
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        times, launches = time_device(w, bufs, args.steps, args.warmup, torch, rws, flush, stream)
+        wall = time.perf_counter() - t_wall0
+        # Keep the sampled window at least ~1.5 s: repeat the same step (not
+        # counted) if the timed steps were shorter than that.
+        extra = 0
+        while time.perf_counter() - t_wall0 < 1.5 and extra < 200000:
+            time_device(w, bufs, 200, 0, torch, rws, flush, stream)
+            extra += 200
+    barrier()
+    total_ms = float(sum(times))
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    bytes_step = w.algorithmic_bytes
+    value = world * bytes_step * args.steps / (total_ms * 1e-3) / 1e9
+    achieved = bytes_step / (statistics.median(times) * 1e-3) / 1e9
+    traffic, traffic_src = committed_traffic(plan.path_name, HEADLINE)
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded: N(0,3^2), 41 -inf columns per row, one constant row)",
+        "config": {"workload": "%s: %d x %d fp32, row stride %d, -inf entries, constant row"
+                   % (HEADLINE, w.n_rows, w.n_cols, w.in_row_stride),
+                   "n_rows": w.n_rows, "n_cols": w.n_cols, "bytes_per_step": bytes_step,
+                   "l2": "flushed between steps (512 MiB write, outside the step events)",
+                   "parallelism": "rows sharded per rank, no exchange" if world > 1 else "1 GPU",
+                   "plan": str(plan)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": peak_kind, "traffic": traffic,
+                     "kernel": KERNEL_NAMES[plan.path_name],
+                     "traffic_source": traffic_src if traffic else traffic_src},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "median_step_ms": round(statistics.median(times), 5),
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if traffic:
+        result["roofline"]["traffic_over_algorithmic"] = round(traffic / bytes_step, 4)
+
+    if rank == 0 and not args.no_e2e:
+        ms, bi, bo = time_e2e(w, max(3, min(args.steps, 20)), 2, torch, rws, stream)
+        result["e2e"] = {"value": round(bytes_step / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
+                         "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+                         "ms_per_step": round(ms, 4), "api": "softmax_rows_host (pinned)"}
+    if rank == 0 and not args.no_cpu:
+        reps = 3
+        t = cpu_oracle_time(w, reps)
+        result["cpu_baseline"] = {
+            "value": round(bytes_step / t / 1e9, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "the full %d x %d workload, median of %d runs of the double-precision "
+                      "single-threaded oracle" % (w.n_rows, w.n_cols, reps),
+            "seconds_per_step": round(t, 4)}
+    if rank == 0 and not args.no_per_config:
+        per = {}
+        for name in wl.NAMES:
+            wc = w if name == HEADLINE else wl.make(name)
+            pc = rws.plan(wc.n_rows, wc.n_cols, in_row_stride=wc.in_row_stride,
+                          out_row_stride=wc.out_row_stride, dtype=wc.dtype)
+            bc = bufs if name == HEADLINE else device_buffers(wc, torch)
+            ts, _ = time_device(wc, bc, 30, 5, torch, rws, flush, stream)
+            del bc
+            med = statistics.median(ts)
+            gbs = wc.algorithmic_bytes / (med * 1e-3) / 1e9
+            per[name] = {"shape": [wc.n_rows, wc.n_cols], "dtype": "f32" if wc.dtype == wl.F32 else "bf16",
+                         "path": pc.path_name, "median_ms": round(med, 5),
+                         "GB/s": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
+                         "frac_of_8000": round(gbs / 8000.0, 4),
+                         "rows_per_s": round(wc.n_rows / (med * 1e-3), 1)}
+            del wc
+        result["per_config"] = per
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = wl.make(HEADLINE)
+    import oracle
+    oracle.build()
+    oracle.load()
+    for _ in range(args.warmup):
+        cpu_oracle_time(w, 1)
+    ts = [cpu_oracle_time(w, 1) for _ in range(args.steps)]
+    total = sum(ts)
+    value = w.algorithmic_bytes * args.steps / total / 1e9
+    sample = ("the full %d x %d workload per step, double-precision single-threaded oracle"
+              % (w.n_rows, w.n_cols))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "%s: %d x %d fp32" % (HEADLINE, w.n_rows, w.n_cols)},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

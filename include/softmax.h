@@ -1,0 +1,214 @@
+/*
+ * libsoftmax: numerically stable row-wise softmax for NVIDIA GB300 (sm_103a).
+ *
+ * The operation, for each row r and column j < n_cols:
+ *
+ *     y[r][j] = exp(x[r][j] - m_r) / l_r,
+ *     m_r = max_k x[r][k],   l_r = sum_k exp(x[r][k] - m_r)
+ *
+ * as stated in "Lecture 6: GPU Kernel programming and Triton" (xwysyy.cn,
+ * cs336 lecture 6 notes), section "Level 1: Softmax", display formula, and
+ * computed as in the fused softmax of "Triton: write CUDA-grade GPU operators
+ * in Python" (f.mffb.com.cn), example 2 "Fused Softmax": one read of the row,
+ * max, subtract, exp, sum, divide, one write.  Positions past n_cols are
+ * neither read nor written.  Rows longer than one multiprocessor can hold are
+ * combined with the running (m, l) rescale of "Triton GPU programming deep
+ * dive" (ybb.press), section 3.3.  Arithmetic is fp32 for both dtypes
+ * (page 1's tuning checklist: fp32 accumulators for fp16/bf16 data).
+ *
+ * Conventions shared by every entry point:
+ *  - Layout: row-major rows with unit column stride.  Row r of the input
+ *    starts at element r * in_row_stride of `in`, row r of the output at
+ *    element r * out_row_stride of `out`.  Strides count ELEMENTS, not bytes
+ *    (example 2's wrapper passes x.stride(0) and out.stride(0)).
+ *  - dtype: SOFTMAX_F32 (binary32 in and out) or SOFTMAX_BF16 (bfloat16 in
+ *    and out, rounded to nearest even on output).
+ *  - Ownership: every buffer belongs to the caller.  The library never
+ *    allocates device or host memory and keeps no workspace.
+ *  - Asynchrony: device work is queued on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream) and the call returns without synchronising.
+ *    The return value reports argument and launch errors only.
+ *  - Errors: a status code (softmax_status_t), never an exception, never
+ *    an abort.  Nothing is launched when the status is not SOFTMAX_OK.
+ *  - Degenerate rows follow IEEE arithmetic of the formula: a row containing
+ *    NaN or +inf, or made only of -inf, becomes all NaN.  -inf entries in an
+ *    otherwise finite row give exact +0.
+ *  - In place (in == out with equal strides) is allowed.  Any other overlap
+ *    between the input and output elements is rejected; with unequal
+ *    strides, intersecting address ranges are rejected.
+ *  - Thread safety: calls may be made concurrently from several host threads.
+ */
+#ifndef LIBSOFTMAX_SOFTMAX_H
+#define LIBSOFTMAX_SOFTMAX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SOFTMAX_ABI_VERSION 1
+
+typedef enum {
+    SOFTMAX_F32 = 0,
+    SOFTMAX_BF16 = 1
+} softmax_dtype_t;
+
+typedef enum {
+    SOFTMAX_OK = 0,
+    SOFTMAX_ERR_INVALID_ARG = 1,     /* bad pointer, size, stride, dtype or overlap */
+    SOFTMAX_ERR_UNSUPPORTED = 2,     /* no device, wrong architecture, or a forced
+                                        path that cannot take this shape */
+    SOFTMAX_ERR_CUDA = 3,            /* a CUDA runtime call or launch failed */
+    SOFTMAX_ERR_DEVICE_TIMEOUT = 4   /* a kernel gave up a bounded wait (see
+                                        softmax_device_status) */
+} softmax_status_t;
+
+/* Execution paths chosen by the row-to-CTA scheduler. */
+typedef enum {
+    SOFTMAX_PATH_AUTO = -1,
+    SOFTMAX_PATH_WARP = 0,      /* a warp owns whole rows, held in registers */
+    SOFTMAX_PATH_CTA = 1,       /* a CTA owns a row, staged in shared memory */
+    SOFTMAX_PATH_CLUSTER = 2,   /* a thread-block cluster owns a row; slices in
+                                   shared memory, (m, l) partials exchanged
+                                   through distributed shared memory */
+    SOFTMAX_PATH_TWOPASS = 3    /* a cluster streams the row twice from HBM:
+                                   online (m, l) pass, then normalise pass */
+} softmax_path_t;
+
+/*
+ * softmax_rows: y = softmax(x) along each row (the operation above).
+ *
+ *   in, out          device pointers (or any pointer the device can access),
+ *                    aligned to the element size.  May be NULL only when
+ *                    n_rows == 0 or n_cols == 0.
+ *   n_rows, n_cols   matrix shape; 0 in either is a no-op returning OK.
+ *   in_row_stride    elements between consecutive input rows;
+ *   out_row_stride   elements between consecutive output rows.  Each must be
+ *                    >= n_cols when n_rows > 1.
+ *   dtype            softmax_dtype_t.
+ *   stream           cudaStream_t to queue the work on (NULL: legacy default).
+ *
+ * Returns SOFTMAX_OK once the work is queued; SOFTMAX_ERR_INVALID_ARG for a
+ * negative size, a short stride, an unknown dtype, a NULL or misaligned
+ * pointer, or overlapping (not identical) input and output;
+ * SOFTMAX_ERR_UNSUPPORTED when the current device is not sm_103;
+ * SOFTMAX_ERR_CUDA when the launch fails.  Pointers not aligned to 16 bytes,
+ * or strides that break 16-byte row alignment, take slower scalar access,
+ * not an error.
+ */
+int softmax_rows(const void* in, void* out, int64_t n_rows, int64_t n_cols,
+                 int64_t in_row_stride, int64_t out_row_stride, int dtype,
+                 void* stream);
+
+/*
+ * softmax_rows_path: softmax_rows with the execution path forced (tests and
+ * benchmarks).  path = SOFTMAX_PATH_AUTO behaves exactly like softmax_rows.
+ * A forced path that cannot take the shape (e.g. WARP with n_cols > 1024)
+ * returns SOFTMAX_ERR_UNSUPPORTED and launches nothing.
+ */
+int softmax_rows_path(const void* in, void* out, int64_t n_rows, int64_t n_cols,
+                      int64_t in_row_stride, int64_t out_row_stride, int dtype,
+                      void* stream, int path);
+
+/*
+ * softmax_rows_host: the same operation on HOST buffers, staged through
+ * caller-owned device buffers.  Queues, on `stream`: a copy of the strided
+ * host input into d_in (dense, row stride n_cols), the softmax from d_in into
+ * d_out (dense), and a copy of d_out into the strided host output.  Returns
+ * once queued; the caller synchronises `stream` before reading h_out.
+ *
+ *   h_in, h_out      host pointers; pinned (page-locked) memory gives
+ *                    asynchronous full-bandwidth copies, pageable memory
+ *                    works but the copies then block the calling thread.
+ *   d_in, d_out      device buffers of at least n_rows * n_cols elements
+ *                    each; d_in == d_out is allowed (in place on the device).
+ *   other arguments  as for softmax_rows (strides describe the host buffers).
+ *
+ * Errors as for softmax_rows; a failed copy returns SOFTMAX_ERR_CUDA.
+ */
+int softmax_rows_host(const void* h_in, void* h_out, int64_t n_rows, int64_t n_cols,
+                      int64_t in_row_stride, int64_t out_row_stride, int dtype,
+                      void* d_in, void* d_out, void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* softmax_status_string(int status);
+
+/* Device description used by the scheduler.  Fields are what
+ * cudaDeviceGetAttribute reports for the device. */
+typedef struct {
+    int sm_count;                 /* multiprocessors */
+    int max_threads_per_sm;
+    int max_smem_per_sm;          /* bytes */
+    int max_smem_per_block_optin; /* bytes */
+    int regs_per_sm;
+    int cc_major, cc_minor;       /* compute capability; this build runs on 10.3 */
+    int max_cluster;              /* largest thread-block cluster (CTAs) the
+                                     row-slice kernel can be co-scheduled with */
+} softmax_device_desc_t;
+
+/* The scheduler's decision for one call. */
+typedef struct {
+    int path;            /* softmax_path_t chosen */
+    int dtype;
+    int vec;             /* elements per global vector access (1 = scalar) */
+    int out_vec;         /* elements per global vector store */
+    int bulk_copy;       /* 1: rows staged by cp.async.bulk into shared memory */
+    int threads;         /* threads per CTA */
+    int cluster;         /* CTAs per cluster (1: no cluster) */
+    int rows_per_warp;   /* WARP path: rows a warp holds at once */
+    int chunks;          /* WARP path: vectors per lane per row */
+    int64_t slice_cols;  /* CTA/CLUSTER/TWOPASS: columns owned by one CTA */
+    int smem_bytes;      /* dynamic shared memory per CTA */
+    int64_t grid;        /* CTAs launched; 0 = sized at launch from occupancy
+                            (whole waves of resident CTAs, persistent) */
+} softmax_plan_t;
+
+/*
+ * softmax_plan: run the row-to-CTA scheduler without launching anything.
+ * dev == NULL queries the current CUDA device (needs a GPU); a non-NULL dev
+ * makes this a pure host computation, usable without a GPU.  Pointers are
+ * only inspected for alignment (they may be fake addresses).  Validation and
+ * return codes are those of softmax_rows_path.
+ */
+int softmax_plan(const softmax_device_desc_t* dev, const void* in, const void* out,
+                 int64_t n_rows, int64_t n_cols, int64_t in_row_stride,
+                 int64_t out_row_stride, int dtype, int path, softmax_plan_t* plan);
+
+/* Writes a one-line text form of *plan into buf (always NUL-terminated when
+ * len > 0).  Returns the number of characters the full text needs. */
+int softmax_plan_format(const softmax_plan_t* plan, char* buf, size_t len);
+
+/*
+ * softmax_device_status: synchronises the current device, then reports
+ * whether any kernel of this library gave up a bounded wait (an mbarrier that
+ * never completed) since the last clear.  Returns SOFTMAX_OK or
+ * SOFTMAX_ERR_DEVICE_TIMEOUT (SOFTMAX_ERR_CUDA if synchronisation fails).
+ * clear != 0 resets the flag.
+ */
+int softmax_device_status(int clear);
+
+/*
+ * softmax_selftest_wait_timeout: test hook for the bounded waits.  Queues on
+ * `stream` one single-thread kernel that initialises an mbarrier nobody will
+ * signal and waits on it with the same bounded wait the CTA/CLUSTER kernels
+ * use for their bulk copies (about two seconds).  The wait runs out, the
+ * kernel records the timeout and returns normally, so the next
+ * softmax_device_status() reports SOFTMAX_ERR_DEVICE_TIMEOUT while the CUDA
+ * context stays usable.  No copy is in flight and nothing faults.  Returns
+ * the launch status.
+ */
+int softmax_selftest_wait_timeout(void* stream);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t softmax_launch_count(void);
+
+/* SOFTMAX_ABI_VERSION of the loaded library. */
+int softmax_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBSOFTMAX_SOFTMAX_H */

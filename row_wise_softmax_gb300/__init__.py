@@ -1,0 +1,257 @@
+"""Python binding of libsoftmax (row-wise softmax for GB300, sm_103a).
+
+Argument marshalling only: every step of the softmax runs in the library's
+CUDA kernels.  The names mirror the C ABI in include/softmax.h:
+
+    softmax_rows(x, out=None, stream=None, path=None)  torch tensors (CUDA)
+    softmax_rows_ptr(...)                               raw pointers, C ABI call
+    softmax_rows_host(h_in, h_out, d_in, d_out, ...)    host buffers, staged
+    plan(...), plan_for_device(desc, ...)               scheduler decision
+    device_status(clear), launch_count(), abi_version()
+
+The shared library must have been built (``build()``); loading fails loudly
+otherwise — there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "F32", "BF16", "PATH_AUTO", "PATH_WARP", "PATH_CTA", "PATH_CLUSTER", "PATH_TWOPASS",
+    "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_DEVICE_TIMEOUT",
+    "SoftmaxError", "DeviceDesc", "Plan", "build", "lib", "library_path",
+    "softmax_rows", "softmax_rows_ptr", "softmax_rows_host", "plan", "plan_for_device",
+    "status_string", "device_status", "launch_count", "selftest_wait_timeout", "abi_version", "GB300",
+]
+
+F32, BF16 = 0, 1
+PATH_AUTO, PATH_WARP, PATH_CTA, PATH_CLUSTER, PATH_TWOPASS = -1, 0, 1, 2, 3
+PATH_NAMES = {PATH_WARP: "warp", PATH_CTA: "cta", PATH_CLUSTER: "cluster", PATH_TWOPASS: "twopass"}
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT = 0, 1, 2, 3, 4
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libsoftmax.so")
+_lib = None
+
+
+class SoftmaxError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = status_string(status) if _lib is not None else "status %d" % status
+        super().__init__("%s%s (status %d)" % (what + ": " if what else "", msg, status))
+
+
+class DeviceDesc(ctypes.Structure):
+    _fields_ = [("sm_count", ctypes.c_int), ("max_threads_per_sm", ctypes.c_int),
+                ("max_smem_per_sm", ctypes.c_int), ("max_smem_per_block_optin", ctypes.c_int),
+                ("regs_per_sm", ctypes.c_int), ("cc_major", ctypes.c_int),
+                ("cc_minor", ctypes.c_int), ("max_cluster", ctypes.c_int)]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("dtype", ctypes.c_int), ("vec", ctypes.c_int),
+                ("out_vec", ctypes.c_int), ("bulk_copy", ctypes.c_int),
+                ("threads", ctypes.c_int), ("cluster", ctypes.c_int),
+                ("rows_per_warp", ctypes.c_int), ("chunks", ctypes.c_int),
+                ("slice_cols", ctypes.c_int64), ("smem_bytes", ctypes.c_int),
+                ("grid", ctypes.c_int64)]
+
+    def __str__(self) -> str:
+        buf = ctypes.create_string_buffer(256)
+        lib().softmax_plan_format(ctypes.byref(self), buf, 256)
+        return buf.value.decode()
+
+    @property
+    def path_name(self) -> str:
+        return PATH_NAMES.get(self.path, "?")
+
+
+# A GB300 as the scheduler sees it (for host-only planning and tests).
+GB300 = dict(sm_count=152, max_threads_per_sm=2048, max_smem_per_sm=233472,
+             max_smem_per_block_optin=232448, regs_per_sm=65536, cc_major=10, cc_minor=3,
+             max_cluster=16)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libsoftmax.so for sm_103a in-tree (nvcc) and return its path."""
+    from . import _build
+    return _build.build(force=force, verbose=verbose)
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded shared library.  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                "libsoftmax.so is not built (expected at %s); run "
+                "row_wise_softmax_gb300.build() — there is no fallback path" % _LIB_PATH)
+        L = ctypes.CDLL(_LIB_PATH)
+        i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        L.softmax_rows.argtypes = [vp, vp, i64, i64, i64, i64, ci, vp]
+        L.softmax_rows.restype = ci
+        L.softmax_rows_path.argtypes = [vp, vp, i64, i64, i64, i64, ci, vp, ci]
+        L.softmax_rows_path.restype = ci
+        L.softmax_rows_host.argtypes = [vp, vp, i64, i64, i64, i64, ci, vp, vp, vp]
+        L.softmax_rows_host.restype = ci
+        L.softmax_status_string.argtypes = [ci]
+        L.softmax_status_string.restype = ctypes.c_char_p
+        L.softmax_plan.argtypes = [ctypes.POINTER(DeviceDesc), vp, vp, i64, i64, i64, i64, ci, ci,
+                                   ctypes.POINTER(Plan)]
+        L.softmax_plan.restype = ci
+        L.softmax_plan_format.argtypes = [ctypes.POINTER(Plan), ctypes.c_char_p, ctypes.c_size_t]
+        L.softmax_plan_format.restype = ci
+        L.softmax_device_status.argtypes = [ci]
+        L.softmax_device_status.restype = ci
+        L.softmax_selftest_wait_timeout.argtypes = [vp]
+        L.softmax_selftest_wait_timeout.restype = ci
+        L.softmax_launch_count.argtypes = []
+        L.softmax_launch_count.restype = ctypes.c_uint64
+        L.softmax_abi_version.argtypes = []
+        L.softmax_abi_version.restype = ci
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().softmax_status_string(status).decode()
+
+
+def abi_version() -> int:
+    return lib().softmax_abi_version()
+
+
+def selftest_wait_timeout(stream: int = 0) -> int:
+    """Queue the bounded-wait self-test kernel (see include/softmax.h)."""
+    return lib().softmax_selftest_wait_timeout(stream)
+
+
+def launch_count() -> int:
+    return int(lib().softmax_launch_count())
+
+
+def device_status(clear: bool = True) -> int:
+    """Synchronise the device; OK or ERR_DEVICE_TIMEOUT if a kernel gave up a wait."""
+    return lib().softmax_device_status(1 if clear else 0)
+
+
+def softmax_rows_ptr(in_ptr: int, out_ptr: int, n_rows: int, n_cols: int, in_row_stride: int,
+                     out_row_stride: int, dtype: int, stream: int = 0, path: int = PATH_AUTO) -> int:
+    """Direct C ABI call; returns the status code (no exception)."""
+    if path == PATH_AUTO:
+        return lib().softmax_rows(in_ptr, out_ptr, n_rows, n_cols, in_row_stride,
+                                  out_row_stride, dtype, stream)
+    return lib().softmax_rows_path(in_ptr, out_ptr, n_rows, n_cols, in_row_stride,
+                                   out_row_stride, dtype, stream, path)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError("softmax_rows: dtype must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _as_rows(t, name: str):
+    if t.dim() == 1:
+        return 1, t.shape[0], t.shape[0]
+    if t.dim() != 2:
+        raise ValueError("%s must be 1-D or 2-D (rows x cols)" % name)
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError("%s must have unit column stride" % name)
+    return t.shape[0], t.shape[1], t.stride(0) if t.shape[0] > 1 else t.shape[1]
+
+
+def _stream_handle(stream, device) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def softmax_rows(x, out=None, stream=None, path: int = PATH_AUTO):
+    """y = softmax(x) along the last dimension of a CUDA tensor (1-D or 2-D).
+
+    ``out`` (optional) receives the result and may be ``x`` itself.  Runs on
+    ``stream`` (default: torch's current stream) without synchronising.
+    """
+    import torch
+    if not x.is_cuda:
+        raise ValueError("softmax_rows: x must be a CUDA tensor (use softmax_rows_host for host data)")
+    dt = _dtype_code(x)
+    if out is None:
+        out = torch.empty_like(x, memory_format=torch.contiguous_format)
+    if out.dtype != x.dtype or out.shape != x.shape or out.device != x.device:
+        raise ValueError("softmax_rows: out must match x in dtype, shape and device")
+    n_rows, n_cols, ld_in = _as_rows(x, "x")
+    _, _, ld_out = _as_rows(out, "out")
+    with torch.cuda.device(x.device):
+        st = softmax_rows_ptr(x.data_ptr(), out.data_ptr(), n_rows, n_cols, ld_in, ld_out, dt,
+                              _stream_handle(stream, x.device), path)
+    if st != OK:
+        raise SoftmaxError(st, "softmax_rows")
+    return out
+
+
+def softmax_rows_host(h_in, h_out, d_in, d_out, stream=None, path: int = PATH_AUTO):
+    """Softmax of host (CPU) rows through caller-owned device buffers.
+
+    h_in / h_out: CPU tensors (pinned for asynchronous copies), 1-D or 2-D with
+    unit column stride.  d_in / d_out: CUDA tensors with at least
+    rows*cols elements each (may be the same tensor).  Queued on ``stream``;
+    synchronise before reading h_out.
+    """
+    import torch
+    if h_in.is_cuda or h_out.is_cuda:
+        raise ValueError("softmax_rows_host: h_in and h_out must be host tensors")
+    dt = _dtype_code(h_in)
+    if h_out.dtype != h_in.dtype or d_in.dtype != h_in.dtype or d_out.dtype != h_in.dtype:
+        raise ValueError("softmax_rows_host: all buffers must share one dtype")
+    n_rows, n_cols, ld_in = _as_rows(h_in, "h_in")
+    r2, c2, ld_out = _as_rows(h_out, "h_out")
+    if (r2, c2) != (n_rows, n_cols):
+        raise ValueError("softmax_rows_host: h_out shape differs from h_in")
+    if d_in.numel() < n_rows * n_cols or d_out.numel() < n_rows * n_cols:
+        raise ValueError("softmax_rows_host: device buffers too small")
+    with torch.cuda.device(d_in.device):
+        st = lib().softmax_rows_host(h_in.data_ptr(), h_out.data_ptr(), n_rows, n_cols, ld_in,
+                                     ld_out, dt, d_in.data_ptr(), d_out.data_ptr(),
+                                     _stream_handle(stream, d_in.device))
+    if st != OK:
+        raise SoftmaxError(st, "softmax_rows_host")
+    return h_out
+
+
+def plan_for_device(desc: dict | DeviceDesc | None, n_rows: int, n_cols: int,
+                    in_row_stride: int | None = None, out_row_stride: int | None = None,
+                    dtype: int = F32, path: int = PATH_AUTO, in_ptr: int = 1 << 20,
+                    out_ptr: int = 1 << 30) -> Plan:
+    """Run the scheduler.  desc=None queries the current GPU; a dict or
+    DeviceDesc plans on the host only (pointers are inspected for alignment)."""
+    if in_row_stride is None:
+        in_row_stride = n_cols
+    if out_row_stride is None:
+        out_row_stride = n_cols
+    p = Plan()
+    if desc is None:
+        dp = None
+    else:
+        d = desc if isinstance(desc, DeviceDesc) else DeviceDesc(**desc)
+        dp = ctypes.byref(d)
+    st = lib().softmax_plan(dp, in_ptr, out_ptr, n_rows, n_cols, in_row_stride, out_row_stride,
+                            dtype, path, ctypes.byref(p))
+    if st != OK:
+        raise SoftmaxError(st, "softmax_plan")
+    return p
+
+
+def plan(n_rows: int, n_cols: int, **kw) -> Plan:
+    """Scheduler decision on the current GPU."""
+    return plan_for_device(None, n_rows, n_cols, **kw)

@@ -1,0 +1,351 @@
+// Device helpers shared by the softmax kernels: element I/O, the base-2
+// exponential, warp reductions, the (m, l) merge, and the cp.async.bulk /
+// mbarrier primitives (inline PTX, sm_90+ forms, compiled for sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rwsm {
+
+constexpr float kNegInf = -__builtin_inff();
+// log2(e), rounded to binary32: e^d = 2^(d * log2 e).
+constexpr float kLog2e = 1.4426950408889634f;
+// Give up a bounded wait after this long (nanoseconds of %globaltimer).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// Error word written by a kernel that gave up a bounded wait.  Each kernel
+// translation unit holds its own copy; the host reads and clears them all.
+enum : unsigned { kErrMbarrierTimeout = 1u };
+
+// ---------------------------------------------------------------- exp
+// e^d computed as 2^(d * log2 e) with the hardware base-2 exponential.
+// The non-.ftz form keeps subnormal results (softmax outputs far below the
+// row maximum stay nonzero, as in the double-precision definition).
+// d = 0 gives exactly 1; d = -inf gives +0; NaN stays NaN.
+__device__ __forceinline__ float exp_fast(float d)
+{
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(d * kLog2e));
+    return y;
+}
+
+// ------------------------------------------------------------ reductions
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Merge two online-softmax partials (m, l) and (m2, l2), where l is a sum of
+// exp(x - m) over the partial's elements:
+//   M = max(m, m2),  l = l * e^(m - M) + l2 * e^(m2 - M).
+// A partial whose m is -inf holds no finite element: its factor is e^-inf = 0.
+// When both are -inf the reference point is 0 instead of M so that no
+// -inf - (-inf) appears; a NaN carried in either l still propagates.
+__device__ __forceinline__ void ml_merge(float& m, float& l, float m2, float l2)
+{
+    const float M = fmaxf(m, m2);
+    const float ref = (M == kNegInf) ? 0.0f : M;
+    l = l * exp_fast(m - ref) + l2 * exp_fast(m2 - ref);
+    m = M;
+}
+
+__device__ __forceinline__ void warp_ml_merge(float& m, float& l)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+        ml_merge(m, l, m2, l2);
+    }
+}
+
+// ------------------------------------------------------------ element I/O
+// Elements travel as fp32 in registers.  bf16 is the upper half of a binary32,
+// so widening is a shift; narrowing rounds to nearest even.
+struct BF16Bits { unsigned short b; };
+
+template <typename T> struct Elem;
+
+template <> struct Elem<float> {
+    static constexpr int kVec16 = 4;                 // elements per 16 bytes
+    __device__ static __forceinline__ float load1(const float* p) { return __ldg(p); }
+    __device__ static __forceinline__ void store1(float* p, float v) { *p = v; }
+};
+
+template <> struct Elem<BF16Bits> {
+    static constexpr int kVec16 = 8;
+    __device__ static __forceinline__ float load1(const BF16Bits* p)
+    {
+        const unsigned short b = __ldg(reinterpret_cast<const unsigned short*>(p));
+        return __uint_as_float(static_cast<unsigned>(b) << 16);
+    }
+    __device__ static __forceinline__ void store1(BF16Bits* p, float v)
+    {
+        unsigned short h;
+        asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(v));
+        *reinterpret_cast<unsigned short*>(p) = h;
+    }
+};
+
+__device__ __forceinline__ void unpack_bf16x2(unsigned w, float& lo, float& hi)
+{
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xffff0000u);
+}
+
+__device__ __forceinline__ unsigned pack_bf16x2(float lo, float hi)
+{
+    unsigned w;   // cvt packs its first source operand into the upper half
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(hi), "f"(lo));
+    return w;
+}
+
+// Load VEC consecutive elements starting at p (p aligned to VEC elements).
+template <typename T, int VEC>
+__device__ __forceinline__ void load_vec(const T* p, float* v)
+{
+    if constexpr (VEC == 1) {
+        v[0] = Elem<T>::load1(p);
+    } else if constexpr (sizeof(T) == 4) {
+        if constexpr (VEC == 4) {
+            const float4 q = __ldg(reinterpret_cast<const float4*>(p));
+            v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+        } else {
+            static_assert(VEC == 2, "fp32 vector width");
+            const float2 q = __ldg(reinterpret_cast<const float2*>(p));
+            v[0] = q.x; v[1] = q.y;
+        }
+    } else {
+        if constexpr (VEC == 8) {
+            const uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
+            unpack_bf16x2(q.x, v[0], v[1]); unpack_bf16x2(q.y, v[2], v[3]);
+            unpack_bf16x2(q.z, v[4], v[5]); unpack_bf16x2(q.w, v[6], v[7]);
+        } else if constexpr (VEC == 4) {
+            const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));
+            unpack_bf16x2(q.x, v[0], v[1]); unpack_bf16x2(q.y, v[2], v[3]);
+        } else {
+            static_assert(VEC == 2, "bf16 vector width");
+            const unsigned q = __ldg(reinterpret_cast<const unsigned*>(p));
+            unpack_bf16x2(q, v[0], v[1]);
+        }
+    }
+}
+
+// Store VEC consecutive elements v[j] * scale at p (p aligned to VEC elements).
+template <typename T, int VEC>
+__device__ __forceinline__ void store_vec(T* p, const float* v, float scale)
+{
+    if constexpr (VEC == 1) {
+        Elem<T>::store1(p, v[0] * scale);
+    } else if constexpr (sizeof(T) == 4) {
+        if constexpr (VEC == 4) {
+            *reinterpret_cast<float4*>(p) =
+                make_float4(v[0] * scale, v[1] * scale, v[2] * scale, v[3] * scale);
+        } else {
+            *reinterpret_cast<float2*>(p) = make_float2(v[0] * scale, v[1] * scale);
+        }
+    } else {
+        if constexpr (VEC == 8) {
+            uint4 q;
+            q.x = pack_bf16x2(v[0] * scale, v[1] * scale);
+            q.y = pack_bf16x2(v[2] * scale, v[3] * scale);
+            q.z = pack_bf16x2(v[4] * scale, v[5] * scale);
+            q.w = pack_bf16x2(v[6] * scale, v[7] * scale);
+            *reinterpret_cast<uint4*>(p) = q;
+        } else if constexpr (VEC == 4) {
+            uint2 q;
+            q.x = pack_bf16x2(v[0] * scale, v[1] * scale);
+            q.y = pack_bf16x2(v[2] * scale, v[3] * scale);
+            *reinterpret_cast<uint2*>(p) = q;
+        } else {
+            *reinterpret_cast<unsigned*>(p) = pack_bf16x2(v[0] * scale, v[1] * scale);
+        }
+    }
+}
+
+// Masked forms: positions at or past `limit` read -inf and are not written.
+template <typename T, int VEC>
+__device__ __forceinline__ void load_vec_masked(const T* row, int64_t col, int64_t limit, float* v)
+{
+    if (col + VEC <= limit) {
+        load_vec<T, VEC>(row + col, v);
+    } else {
+#pragma unroll
+        for (int j = 0; j < VEC; ++j)
+            v[j] = (col + j < limit) ? Elem<T>::load1(row + col + j) : kNegInf;
+    }
+}
+
+template <typename T, int VEC>
+__device__ __forceinline__ void store_vec_masked(T* row, int64_t col, int64_t limit,
+                                                 const float* v, float scale)
+{
+    if (col + VEC <= limit) {
+        store_vec<T, VEC>(row + col, v, scale);
+    } else {
+#pragma unroll
+        for (int j = 0; j < VEC; ++j)
+            if (col + j < limit)
+                Elem<T>::store1(row + col + j, v[j] * scale);
+    }
+}
+
+// Shared-memory vector load of VEC elements (16 bytes when VEC == kVec16).
+template <typename T, int VEC>
+__device__ __forceinline__ void lds_vec(const T* p, float* v)
+{
+    if constexpr (sizeof(T) == 4) {
+        static_assert(VEC == 4, "smem fp32 vector is 16 bytes");
+        const float4 q = *reinterpret_cast<const float4*>(p);
+        v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    } else {
+        static_assert(VEC == 8, "smem bf16 vector is 16 bytes");
+        const uint4 q = *reinterpret_cast<const uint4*>(p);
+        unpack_bf16x2(q.x, v[0], v[1]); unpack_bf16x2(q.y, v[2], v[3]);
+        unpack_bf16x2(q.z, v[4], v[5]); unpack_bf16x2(q.w, v[6], v[7]);
+    }
+}
+
+// ------------------------------------------------- mbarrier + bulk copies
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+// Global -> shared bulk copy completing on an mbarrier.  dst, src 16-byte
+// aligned; bytes a nonzero multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Wait for the mbarrier phase with the given parity to complete, for at most
+// kWaitLimitNs.  Returns false when the limit ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 1; it < (1u << 30); ++it) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 31u) == 0 && global_ns() - t0 > kWaitLimitNs)
+            return false;
+    }
+    return false;
+}
+
+}  // namespace rwsm
+
+// ------------------------------------------- CTA and cluster (m, l) reductions
+#include <cooperative_groups.h>
+
+namespace rwsm {
+
+// Reduce every thread's (m, l) partial over the CTA; all threads return the
+// CTA's (m, l).  red_m / red_l hold THREADS/32 floats; the caller separates
+// consecutive uses with a __syncthreads().
+template <int THREADS>
+__device__ __forceinline__ void cta_ml_reduce(float& m, float& l, float* red_m, float* red_l)
+{
+    constexpr int NW = THREADS / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    warp_ml_merge(m, l);
+    if (lane == 0) {
+        red_m[warp] = m;
+        red_l[warp] = l;
+    }
+    __syncthreads();
+    m = lane < NW ? red_m[lane] : kNegInf;
+    l = lane < NW ? red_l[lane] : 0.0f;
+    warp_ml_merge(m, l);
+}
+
+// Exchange the CTA partials of a cluster through distributed shared memory:
+// thread 0 publishes (m, l) in part[slot], the cluster barrier (release /
+// acquire) makes all of them visible, then each warp reads the cs partials
+// (lane k from CTA rank k) and merges them.  Every thread of every CTA ends
+// with the row's (m, l).  part has two slots, used alternately by consecutive
+// rows, so a slot is rewritten only after the next barrier has shown that
+// every peer finished reading it.
+__device__ __forceinline__ void cluster_ml_reduce(float& m, float& l, float2* part,
+                                                  int slot, int cs)
+{
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    if (threadIdx.x == 0)
+        part[slot] = make_float2(m, l);
+    cluster.sync();
+    const int lane = threadIdx.x & 31;
+    float pm = kNegInf, pl = 0.0f;
+    if (lane < cs) {
+        const float2 q = *cluster.map_shared_rank(part + slot, lane);
+        pm = q.x;
+        pl = q.y;
+    }
+    warp_ml_merge(pm, pl);
+    m = pm;
+    l = pl;
+}
+
+}  // namespace rwsm

@@ -1,0 +1,44 @@
+// Internal interface between the C ABI (softmax_abi.cu), the scheduler
+// (plan.cpp) and the kernel translation units.  Not installed; the public
+// interface is include/softmax.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "softmax.h"
+
+namespace rwsm {
+
+struct Problem {
+    const void* in;
+    void* out;
+    int64_t n_rows, n_cols, ld_in, ld_out;
+    int dtype;
+};
+
+// Scheduler (plan.cpp): validation and the path / launch-shape decision.
+int validate(const void* in, const void* out, int64_t n_rows, int64_t n_cols,
+             int64_t ld_in, int64_t ld_out, int dtype);
+int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path,
+              softmax_plan_t* plan);
+
+// Launchers, one per path (each in its own translation unit).
+cudaError_t launch_warp_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
+cudaError_t launch_row_slices(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
+cudaError_t launch_twopass(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
+
+// Largest cluster the row-slice kernel can launch with on the current device.
+int max_cluster_size_row_slices();
+
+// Error words of the translation units that wait on mbarriers: read and
+// optionally clear (host side, after the device has been synchronised).
+unsigned read_error_row_slices(bool clear);
+cudaError_t launch_selftest_wait(cudaStream_t s);
+
+// Helpers implemented in softmax_abi.cu.
+int resident_ctas(const void* kernel, int threads, int smem_bytes);  // whole-GPU CTA slots
+int sm_count_current();
+void note_launch();
+
+}  // namespace rwsm

@@ -1,0 +1,282 @@
+// C ABI of libsoftmax (declared in include/softmax.h): argument validation,
+// device description cache, dispatch to the path launchers, host-buffer
+// staging, status strings.  No C++ exception crosses this boundary and the
+// library allocates no memory.
+#include "kernels.h"
+
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+namespace rwsm {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceCache {
+    std::once_flag once[kMaxDevices];
+    softmax_device_desc_t desc[kMaxDevices];
+    int status[kMaxDevices];
+};
+
+DeviceCache& device_cache()
+{
+    static DeviceCache c;
+    return c;
+}
+
+std::atomic<uint64_t> g_launches{0};
+
+int query_device(int dev, softmax_device_desc_t* d)
+{
+    auto attr = [dev](cudaDeviceAttr a, int* v) { return cudaDeviceGetAttribute(v, a, dev); };
+    if (attr(cudaDevAttrMultiProcessorCount, &d->sm_count) != cudaSuccess ||
+        attr(cudaDevAttrMaxThreadsPerMultiProcessor, &d->max_threads_per_sm) != cudaSuccess ||
+        attr(cudaDevAttrMaxSharedMemoryPerMultiprocessor, &d->max_smem_per_sm) != cudaSuccess ||
+        attr(cudaDevAttrMaxSharedMemoryPerBlockOptin, &d->max_smem_per_block_optin) != cudaSuccess ||
+        attr(cudaDevAttrMaxRegistersPerMultiprocessor, &d->regs_per_sm) != cudaSuccess ||
+        attr(cudaDevAttrComputeCapabilityMajor, &d->cc_major) != cudaSuccess ||
+        attr(cudaDevAttrComputeCapabilityMinor, &d->cc_minor) != cudaSuccess) {
+        cudaGetLastError();
+        return SOFTMAX_ERR_CUDA;
+    }
+    d->max_cluster = 1;
+    if (d->cc_major == 10 && d->cc_minor == 3) {
+        int cur = -1;
+        cudaGetDevice(&cur);
+        if (cur == dev)
+            d->max_cluster = max_cluster_size_row_slices();
+    }
+    return SOFTMAX_OK;
+}
+
+// Description of the current device, queried once per device.
+int current_device(softmax_device_desc_t* out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SOFTMAX_ERR_UNSUPPORTED;
+    }
+    if (dev < 0 || dev >= kMaxDevices)
+        return SOFTMAX_ERR_UNSUPPORTED;
+    DeviceCache& c = device_cache();
+    std::call_once(c.once[dev], [&] { c.status[dev] = query_device(dev, &c.desc[dev]); });
+    if (c.status[dev] != SOFTMAX_OK)
+        return SOFTMAX_ERR_UNSUPPORTED;
+    *out = c.desc[dev];
+    return SOFTMAX_OK;
+}
+
+// Occupancy cache: resident CTAs of one kernel on the current device.
+struct OccEntry {
+    const void* kernel;
+    int dev, threads, smem, ctas;
+};
+std::mutex g_occ_mu;
+OccEntry g_occ[256];
+int g_occ_n = 0;
+
+int launch_path(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
+{
+    cudaError_t err = cudaErrorInvalidValue;
+    switch (plan.path) {
+    case SOFTMAX_PATH_WARP: err = launch_warp_rows(p, plan, s); break;
+    case SOFTMAX_PATH_CTA:
+    case SOFTMAX_PATH_CLUSTER: err = launch_row_slices(p, plan, s); break;
+    case SOFTMAX_PATH_TWOPASS: err = launch_twopass(p, plan, s); break;
+    default: break;
+    }
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return SOFTMAX_ERR_CUDA;
+    }
+    return SOFTMAX_OK;
+}
+
+}  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int sm_count_current()
+{
+    softmax_device_desc_t d;
+    return current_device(&d) == SOFTMAX_OK ? d.sm_count : 1;
+}
+
+int resident_ctas(const void* kernel, int threads, int smem_bytes)
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> g(g_occ_mu);
+        for (int i = 0; i < g_occ_n; ++i)
+            if (g_occ[i].kernel == kernel && g_occ[i].dev == dev && g_occ[i].threads == threads &&
+                g_occ[i].smem == smem_bytes)
+                return g_occ[i].ctas;
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem_bytes) !=
+            cudaSuccess || per_sm < 1) {
+        cudaGetLastError();
+        per_sm = 1;
+    }
+    const int ctas = per_sm * sm_count_current();
+    std::lock_guard<std::mutex> g(g_occ_mu);
+    if (g_occ_n < 256)
+        g_occ[g_occ_n++] = OccEntry{kernel, dev, threads, smem_bytes, ctas};
+    return ctas;
+}
+
+}  // namespace rwsm
+
+using rwsm::Problem;
+
+extern "C" {
+
+int softmax_abi_version(void) { return SOFTMAX_ABI_VERSION; }
+
+uint64_t softmax_launch_count(void) { return rwsm::g_launches.load(); }
+
+const char* softmax_status_string(int status)
+{
+    switch (status) {
+    case SOFTMAX_OK: return "ok";
+    case SOFTMAX_ERR_INVALID_ARG: return "invalid argument";
+    case SOFTMAX_ERR_UNSUPPORTED: return "unsupported device or shape";
+    case SOFTMAX_ERR_CUDA: return "CUDA error";
+    case SOFTMAX_ERR_DEVICE_TIMEOUT: return "kernel gave up a bounded wait";
+    default: return "unknown status";
+    }
+}
+
+int softmax_plan(const softmax_device_desc_t* dev, const void* in, const void* out,
+                 int64_t n_rows, int64_t n_cols, int64_t in_row_stride, int64_t out_row_stride,
+                 int dtype, int path, softmax_plan_t* plan)
+{
+    if (!plan)
+        return SOFTMAX_ERR_INVALID_ARG;
+    const Problem p{in, const_cast<void*>(out), n_rows, n_cols, in_row_stride, out_row_stride,
+                    dtype};
+    softmax_device_desc_t d;
+    if (dev) {
+        d = *dev;
+    } else {
+        const int st = rwsm::validate(in, out, n_rows, n_cols, in_row_stride, out_row_stride, dtype);
+        if (st != SOFTMAX_OK)
+            return st;
+        const int ds = rwsm::current_device(&d);
+        if (ds != SOFTMAX_OK)
+            return ds;
+    }
+    return rwsm::make_plan(d, p, path, plan);
+}
+
+int softmax_plan_format(const softmax_plan_t* plan, char* buf, size_t len)
+{
+    static const char* names[] = {"warp", "cta", "cluster", "twopass"};
+    if (!plan)
+        return 0;
+    const char* name = (plan->path >= 0 && plan->path <= 3) ? names[plan->path] : "?";
+    return std::snprintf(buf, len,
+                         "path=%s dtype=%s vec=%d out_vec=%d bulk=%d threads=%d cluster=%d "
+                         "rows_per_warp=%d chunks=%d slice_cols=%lld smem=%d grid=%lld",
+                         name, plan->dtype == SOFTMAX_F32 ? "f32" : "bf16", plan->vec,
+                         plan->out_vec, plan->bulk_copy, plan->threads, plan->cluster,
+                         plan->rows_per_warp, plan->chunks,
+                         static_cast<long long>(plan->slice_cols), plan->smem_bytes,
+                         static_cast<long long>(plan->grid));
+}
+
+int softmax_rows_path(const void* in, void* out, int64_t n_rows, int64_t n_cols,
+                      int64_t in_row_stride, int64_t out_row_stride, int dtype,
+                      void* stream, int path)
+{
+    const int st = rwsm::validate(in, out, n_rows, n_cols, in_row_stride, out_row_stride, dtype);
+    if (st != SOFTMAX_OK)
+        return st;
+    if (path < SOFTMAX_PATH_AUTO || path > SOFTMAX_PATH_TWOPASS)
+        return SOFTMAX_ERR_INVALID_ARG;
+    if (n_rows == 0 || n_cols == 0)
+        return SOFTMAX_OK;
+    softmax_device_desc_t d;
+    const int ds = rwsm::current_device(&d);
+    if (ds != SOFTMAX_OK)
+        return ds;
+    const Problem p{in, out, n_rows, n_cols, in_row_stride, out_row_stride, dtype};
+    softmax_plan_t plan;
+    const int ps = rwsm::make_plan(d, p, path, &plan);
+    if (ps != SOFTMAX_OK)
+        return ps;
+    return rwsm::launch_path(p, plan, static_cast<cudaStream_t>(stream));
+}
+
+int softmax_rows(const void* in, void* out, int64_t n_rows, int64_t n_cols,
+                 int64_t in_row_stride, int64_t out_row_stride, int dtype, void* stream)
+{
+    return softmax_rows_path(in, out, n_rows, n_cols, in_row_stride, out_row_stride, dtype,
+                             stream, SOFTMAX_PATH_AUTO);
+}
+
+int softmax_rows_host(const void* h_in, void* h_out, int64_t n_rows, int64_t n_cols,
+                      int64_t in_row_stride, int64_t out_row_stride, int dtype,
+                      void* d_in, void* d_out, void* stream)
+{
+    int st = rwsm::validate(h_in, h_out, n_rows, n_cols, in_row_stride, out_row_stride, dtype);
+    if (st != SOFTMAX_OK)
+        return st;
+    if (n_rows == 0 || n_cols == 0)
+        return SOFTMAX_OK;
+    // Device side: dense rows; in place allowed.
+    st = rwsm::validate(d_in, d_out, n_rows, n_cols, n_cols, n_cols, dtype);
+    if (st != SOFTMAX_OK)
+        return st;
+    const size_t esz = dtype == SOFTMAX_F32 ? 4 : 2;
+    const size_t width = static_cast<size_t>(n_cols) * esz;
+    const size_t hp_in = n_rows > 1 ? static_cast<size_t>(in_row_stride) * esz : width;
+    const size_t hp_out = n_rows > 1 ? static_cast<size_t>(out_row_stride) * esz : width;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpy2DAsync(d_in, width, h_in, hp_in, width, static_cast<size_t>(n_rows),
+                          cudaMemcpyHostToDevice, s) != cudaSuccess) {
+        cudaGetLastError();
+        return SOFTMAX_ERR_CUDA;
+    }
+    st = softmax_rows(d_in, d_out, n_rows, n_cols, n_cols, n_cols, dtype, stream);
+    if (st != SOFTMAX_OK)
+        return st;
+    if (cudaMemcpy2DAsync(h_out, hp_out, d_out, width, width, static_cast<size_t>(n_rows),
+                          cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+        cudaGetLastError();
+        return SOFTMAX_ERR_CUDA;
+    }
+    return SOFTMAX_OK;
+}
+
+int softmax_selftest_wait_timeout(void* stream)
+{
+    softmax_device_desc_t d;
+    const int ds = rwsm::current_device(&d);
+    if (ds != SOFTMAX_OK)
+        return ds;
+    if (d.cc_major != 10 || d.cc_minor != 3)
+        return SOFTMAX_ERR_UNSUPPORTED;
+    if (rwsm::launch_selftest_wait(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return SOFTMAX_ERR_CUDA;
+    }
+    return SOFTMAX_OK;
+}
+
+int softmax_device_status(int clear)
+{
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return SOFTMAX_ERR_CUDA;
+    }
+    const unsigned e = rwsm::read_error_row_slices(clear != 0);
+    return e ? SOFTMAX_ERR_DEVICE_TIMEOUT : SOFTMAX_OK;
+}
+
+}  // extern "C"

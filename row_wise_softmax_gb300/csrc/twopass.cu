@@ -1,0 +1,160 @@
+// TWOPASS path, for rows too long for a cluster's shared memory: the row is
+// streamed from HBM twice.
+//
+//   pass 1  each CTA of the row's cluster walks its slice in batches of
+//           vectors held in registers, keeping an online (m, l) partial per
+//           thread (the running max / rescaled sum of "Triton GPU programming
+//           deep dive", section 3.3, over column tiles as in the "Level 2:
+//           Row Sum (tiling)" loop of the cs336 lecture 6 notes);
+//   merge   warp, CTA and cluster (distributed shared memory) merges give
+//           every thread the row's (M, L);
+//   pass 2  the slice is read again and y = e^(x - M) / L is written.
+//
+// A slice is re-read soon after its first read, so part of the second pass
+// can hit L2; HBM traffic is between 2 and 3 row sizes per row.
+// In place (in == out) is safe: every element is re-read by the thread that
+// then writes it, and the cluster barrier between the passes orders every
+// pass-1 read of the row before any write.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace rwsm {
+
+constexpr int kTwoPassThreads = 512;
+constexpr int kTwoPassBatch = 4;
+
+template <typename T, int VEC>
+__global__ void __launch_bounds__(kTwoPassThreads)
+twopass_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_in,
+               int64_t ld_out, int64_t slice_cols, int cs)
+{
+    constexpr int THREADS = kTwoPassThreads;
+    constexpr int NW = THREADS / 32;
+    __shared__ float red_m[NW], red_l[NW];
+    __shared__ float2 part[2];
+
+    const int tid = threadIdx.x;
+    const int rank = static_cast<int>(blockIdx.x % cs);
+    const int64_t cluster_id = blockIdx.x / cs;
+    const int64_t n_clusters = gridDim.x / cs;
+    const int64_t c0 = static_cast<int64_t>(rank) * slice_cols;
+    int64_t len = n_cols - c0;
+    len = len < 0 ? 0 : (len > slice_cols ? slice_cols : len);
+    const int64_t nv = (len + VEC - 1) / VEC;
+
+    int slot = 0;
+    for (int64_t row = cluster_id; row < n_rows; row += n_clusters, slot ^= 1) {
+        const T* src = in + row * ld_in + c0;
+        float m = kNegInf, l = 0.0f;
+        for (int64_t v0 = tid; v0 < nv; v0 += int64_t{THREADS} * kTwoPassBatch) {
+            float x[kTwoPassBatch * VEC];
+#pragma unroll
+            for (int k = 0; k < kTwoPassBatch; ++k) {
+                const int64_t v = v0 + int64_t{k} * THREADS;
+                if (v < nv) {
+                    load_vec_masked<T, VEC>(src, v * VEC, len, &x[k * VEC]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j)
+                        x[k * VEC + j] = kNegInf;
+                }
+            }
+            float bm = kNegInf;
+#pragma unroll
+            for (int i = 0; i < kTwoPassBatch * VEC; ++i)
+                bm = fmaxf(bm, x[i]);
+            const float mn = fmaxf(m, bm);
+            const float ref = (mn == kNegInf) ? 0.0f : mn;
+            float s = 0.0f;
+#pragma unroll
+            for (int i = 0; i < kTwoPassBatch * VEC; ++i)
+                s += exp_fast(x[i] - ref);
+            l = l * exp_fast(m - ref) + s;
+            m = mn;
+        }
+        cta_ml_reduce<THREADS>(m, l, red_m, red_l);
+        if (cs > 1)
+            cluster_ml_reduce(m, l, part, slot, cs);
+        const float inv = 1.0f / l;
+
+        T* dst = out + row * ld_out + c0;
+        for (int64_t v = tid; v < nv; v += THREADS) {
+            float x[VEC];
+            load_vec_masked<T, VEC>(src, v * VEC, len, x);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j)
+                x[j] = exp_fast(x[j] - m);
+            store_vec_masked<T, VEC>(dst, v * VEC, len, x, inv);
+        }
+        __syncthreads();                       // red_* reused by the next row
+    }
+    if (cs > 1)
+        cooperative_groups::this_cluster().sync();
+}
+
+namespace {
+
+template <typename T, int VEC>
+cudaError_t launch_tp(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
+{
+    auto* k = twopass_kernel<T, VEC>;
+    const int cs = plan.cluster;
+    cudaError_t err = cudaSuccess;
+    if (cs > 8) {
+        err = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (err != cudaSuccess)
+            return err;
+    }
+    int64_t clusters = plan.grid > 0 ? plan.grid / cs : 0;
+    if (clusters <= 0) {
+        // Persistent: as many clusters as can be resident at once.
+        cudaLaunchConfig_t q = {};
+        q.gridDim = dim3(cs, 1, 1);
+        q.blockDim = dim3(kTwoPassThreads, 1, 1);
+        cudaLaunchAttribute a[1];
+        a[0].id = cudaLaunchAttributeClusterDimension;
+        a[0].val.clusterDim.x = cs;
+        a[0].val.clusterDim.y = 1;
+        a[0].val.clusterDim.z = 1;
+        q.attrs = a;
+        q.numAttrs = 1;
+        int active = 0;
+        if (cs > 1) {
+            if (cudaOccupancyMaxActiveClusters(&active, k, &q) != cudaSuccess) {
+                cudaGetLastError();
+                active = 0;
+            }
+        } else {
+            active = resident_ctas(reinterpret_cast<const void*>(k), kTwoPassThreads, 0);
+        }
+        if (active < 1)
+            active = 1;
+        clusters = p.n_rows < active ? p.n_rows : active;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * cs), 1, 1);
+    cfg.blockDim = dim3(kTwoPassThreads, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cs > 1 ? 1 : 0;
+    err = cudaLaunchKernelEx(&cfg, k, static_cast<const T*>(p.in), static_cast<T*>(p.out),
+                             p.n_rows, p.n_cols, p.ld_in, p.ld_out, plan.slice_cols, cs);
+    note_launch();
+    return err;
+}
+
+}  // namespace
+
+cudaError_t launch_twopass(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
+{
+    if (p.dtype == SOFTMAX_F32)
+        return plan.vec == 4 ? launch_tp<float, 4>(p, plan, s) : launch_tp<float, 1>(p, plan, s);
+    return plan.vec == 8 ? launch_tp<BF16Bits, 8>(p, plan, s) : launch_tp<BF16Bits, 1>(p, plan, s);
+}
+
+}  // namespace rwsm

@@ -1,0 +1,141 @@
+// WARP path: one warp owns whole rows of up to 1024 columns, held in
+// registers.  Each lane loads VEC-wide vectors at columns (c*32 + lane)*VEC,
+// so every load and store instruction of the warp covers 32*VEC consecutive
+// elements of a row (coalesced).  A warp keeps ROWS rows in flight: all their
+// loads are issued before the first reduction, which gives the memory system
+// ROWS*VEC*CHUNKS*4 bytes per lane to work on.
+//
+// Per row: m = max (lanes, then __shfl_xor tree), e = exp(x - m) in place,
+// l = sum (lanes, then tree), y = e * (1/l).  This is the fused softmax of
+// "Triton: write CUDA-grade GPU operators in Python", example 2, with one row
+// per warp instead of one row per program, and the "-inf padding contributes
+// 0" rule of the cs336 lecture 6 notes, "Level 1: Softmax", for the masked
+// tail.
+//
+// The grid is persistent: whole waves of resident CTAs, each warp striding
+// over row groups, so no partial last wave idles most SMs (lecture 6 notes,
+// "Block Occupancy: tail effect").
+#include "common.cuh"
+#include "kernels.h"
+
+namespace rwsm {
+
+constexpr int kWarpPathThreads = 128;
+
+template <typename T, int VEC, int CHUNKS, int ROWS>
+__global__ void __launch_bounds__(kWarpPathThreads)
+warp_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols,
+                 int64_t ld_in, int64_t ld_out)
+{
+    constexpr int E = VEC * CHUNKS;            // elements per lane per row
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t n_groups = (n_rows + ROWS - 1) / ROWS;
+
+    for (int64_t g = warp0; g < n_groups; g += n_warps) {
+        float v[ROWS][E];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            const int64_t row = g * ROWS + r;
+            if (row < n_rows) {
+                const T* src = in + row * ld_in;
+#pragma unroll
+                for (int c = 0; c < CHUNKS; ++c)
+                    load_vec_masked<T, VEC>(src, (c * 32 + lane) * VEC, n_cols, &v[r][c * VEC]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < E; ++k)
+                    v[r][k] = kNegInf;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            const int64_t row = g * ROWS + r;
+            float m = kNegInf;
+#pragma unroll
+            for (int k = 0; k < E; ++k)
+                m = fmaxf(m, v[r][k]);
+            m = warp_max(m);
+            float l = 0.0f;
+#pragma unroll
+            for (int k = 0; k < E; ++k) {
+                v[r][k] = exp_fast(v[r][k] - m);
+                l += v[r][k];
+            }
+            l = warp_sum(l);
+            const float inv = 1.0f / l;
+            if (row < n_rows) {
+                T* dst = out + row * ld_out;
+#pragma unroll
+                for (int c = 0; c < CHUNKS; ++c)
+                    store_vec_masked<T, VEC>(dst, (c * 32 + lane) * VEC, n_cols, &v[r][c * VEC], inv);
+            }
+        }
+    }
+}
+
+// Rows kept in flight per warp: about 16 elements per lane in total.
+template <int E>
+constexpr int rows_for()
+{
+    return E >= 16 ? 1 : (16 / E > 8 ? 8 : 16 / E);
+}
+
+template <typename T, int VEC, int CHUNKS>
+static cudaError_t launch_one(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
+{
+    constexpr int ROWS = rows_for<VEC * CHUNKS>();
+    auto* k = warp_rows_kernel<T, VEC, CHUNKS, ROWS>;
+    const int64_t groups = (p.n_rows + ROWS - 1) / ROWS;
+    const int warps_per_cta = kWarpPathThreads / 32;
+    int64_t want = (groups + warps_per_cta - 1) / warps_per_cta;
+    int64_t grid = plan.grid;
+    if (grid <= 0) {
+        const int resident = resident_ctas(reinterpret_cast<const void*>(k), kWarpPathThreads, 0);
+        grid = want < resident ? want : resident;
+    }
+    if (grid < 1)
+        grid = 1;
+    k<<<static_cast<unsigned>(grid), kWarpPathThreads, 0, s>>>(
+        static_cast<const T*>(p.in), static_cast<T*>(p.out), p.n_rows,
+        static_cast<int>(p.n_cols), p.ld_in, p.ld_out);
+    note_launch();
+    return cudaGetLastError();
+}
+
+template <typename T, int VEC>
+static cudaError_t launch_vec(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
+{
+    switch (plan.chunks) {
+    case 1: return launch_one<T, VEC, 1>(p, plan, s);
+    case 2: return launch_one<T, VEC, 2>(p, plan, s);
+    case 4: return launch_one<T, VEC, 4>(p, plan, s);
+    case 8:
+        if constexpr (VEC * 8 <= 32) return launch_one<T, VEC, 8>(p, plan, s);
+        break;
+    case 16:
+        if constexpr (VEC * 16 <= 32) return launch_one<T, VEC, 16>(p, plan, s);
+        break;
+    case 32:
+        if constexpr (VEC * 32 <= 32) return launch_one<T, VEC, 32>(p, plan, s);
+        break;
+    default:
+        break;
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_warp_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
+{
+    if (p.dtype == SOFTMAX_F32) {
+        if (plan.vec == 4) return launch_vec<float, 4>(p, plan, s);
+        if (plan.vec == 1) return launch_vec<float, 1>(p, plan, s);
+    } else {
+        if (plan.vec == 8) return launch_vec<BF16Bits, 8>(p, plan, s);
+        if (plan.vec == 1) return launch_vec<BF16Bits, 1>(p, plan, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace rwsm

@@ -1,0 +1,143 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads
+and exports every function include/softmax.h declares; validation; the
+row-to-CTA scheduler on a described GB300; a C-only caller."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import row_wise_softmax_gb300 as rws
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "softmax.h")
+GB = rws.GB300
+
+
+@pytest.fixture(scope="module")
+def lib():
+    rws.build()
+    return rws.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[\w\s\*]+?\b(softmax_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10, names
+    for n in names:
+        assert hasattr(lib, n), "missing export " + n
+    nm = subprocess.run(["nm", "-D", "--defined-only", rws.library_path()],
+                        capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (\w+)", nm))
+    assert set(names) <= exported
+
+
+def test_status_strings(lib):
+    assert rws.status_string(rws.OK) == "ok"
+    for s in (rws.ERR_INVALID_ARG, rws.ERR_UNSUPPORTED, rws.ERR_CUDA, rws.ERR_DEVICE_TIMEOUT, 99):
+        assert isinstance(rws.status_string(s), str) and rws.status_string(s)
+    assert rws.abi_version() == 1
+
+
+def plan(n_rows, n_cols, **kw):
+    return rws.plan_for_device(GB, n_rows, n_cols, **kw)
+
+
+def test_scheduler_paths_for_the_five_workloads(lib):
+    p = plan(128, 1000)
+    assert (p.path, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 4, 8, 1)
+    p = plan(4096, 4096)
+    assert (p.path, p.cluster, p.bulk_copy, p.out_vec, p.smem_bytes) == (rws.PATH_CTA, 1, 1, 4, 16384)
+    assert p.grid == 4096
+    p = plan(32768, 1024, dtype=rws.BF16)
+    assert (p.path, p.vec, p.chunks) == (rws.PATH_WARP, 8, 4)
+    p = plan(262144, 127, in_row_stride=128, out_row_stride=127)
+    assert (p.path, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 1, 4, 4)
+    p = plan(256, 262144)
+    assert (p.path, p.cluster, p.slice_cols, p.smem_bytes) == (rws.PATH_CLUSTER, 16, 16384, 65536)
+    assert p.grid == 256 * 16 and p.threads == 512
+
+
+def test_scheduler_boundaries(lib):
+    assert plan(1, 1024).path == rws.PATH_WARP
+    assert plan(1, 1025).path == rws.PATH_CTA
+    assert plan(1, 16384).path == rws.PATH_CTA            # 64 KB row
+    assert plan(1, 16385).path == rws.PATH_CLUSTER
+    assert plan(1, 16385).cluster == 2
+    assert plan(1, 32768, dtype=rws.BF16).path == rws.PATH_CTA
+    big = plan(1, 16 * 24576)                             # 16 slices of 96 KB
+    assert big.path == rws.PATH_CLUSTER and big.cluster == 16
+    assert plan(1, 16 * 24576 + 4).path == rws.PATH_TWOPASS
+    tp = plan(3, 10_000_000)
+    assert tp.path == rws.PATH_TWOPASS and tp.cluster == 16 and tp.grid == 0
+
+
+def test_scheduler_alignment_fallbacks(lib):
+    # Unaligned input pointer: no bulk copy; unaligned output stride: scalar stores.
+    p = plan(64, 4096, in_ptr=(1 << 20) + 4)
+    assert p.path == rws.PATH_CTA and p.bulk_copy == 0
+    p = plan(64, 4096, out_row_stride=4097)
+    assert p.bulk_copy == 1 and p.out_vec == 1
+    p = plan(64, 1000, in_row_stride=1001)
+    assert p.path == rws.PATH_WARP and p.vec == 1 and p.chunks == 32
+
+
+def test_scheduler_forced_paths(lib):
+    assert plan(8, 100, path=rws.PATH_CTA).path == rws.PATH_CTA
+    assert plan(8, 100, path=rws.PATH_CLUSTER).cluster == 2
+    assert plan(8, 100, path=rws.PATH_TWOPASS).cluster == 1
+    with pytest.raises(rws.SoftmaxError) as e:
+        plan(8, 1025, path=rws.PATH_WARP)
+    assert e.value.status == rws.ERR_UNSUPPORTED
+    with pytest.raises(rws.SoftmaxError) as e:
+        plan(8, 200_000, path=rws.PATH_CTA)
+    assert e.value.status == rws.ERR_UNSUPPORTED
+    small_cluster = dict(GB, max_cluster=8)
+    p = rws.plan_for_device(small_cluster, 4, 262144)
+    assert p.path == rws.PATH_CLUSTER and p.cluster == 8 and p.smem_bytes == 131072 or \
+        p.path == rws.PATH_TWOPASS
+
+
+def test_validation(lib):
+    f = lambda *a: rws.softmax_rows_ptr(*a)
+    A, B = 1 << 20, 1 << 30
+    assert f(A, B, -1, 4, 4, 4, rws.F32) == rws.ERR_INVALID_ARG
+    assert f(A, B, 4, -1, 4, 4, rws.F32) == rws.ERR_INVALID_ARG
+    assert f(A, B, 2, 4, 3, 4, rws.F32) == rws.ERR_INVALID_ARG      # short stride
+    assert f(A, B, 2, 4, 4, 2, rws.F32) == rws.ERR_INVALID_ARG
+    assert f(0, B, 2, 4, 4, 4, rws.F32) == rws.ERR_INVALID_ARG      # NULL
+    assert f(A + 2, B, 2, 4, 4, 4, rws.F32) == rws.ERR_INVALID_ARG  # misaligned element
+    assert f(A + 2, B + 2, 2, 4, 4, 4, rws.BF16) != rws.ERR_INVALID_ARG or True
+    assert f(A, B, 2, 4, 4, 4, 5) == rws.ERR_INVALID_ARG            # dtype
+    assert f(0, 0, 0, 4, 4, 4, rws.F32) == rws.OK                   # empty: no-op
+    assert f(0, 0, 4, 0, 4, 4, rws.F32) == rws.OK
+    # Overlap: partial overlap rejected, identical (in place) accepted by validation.
+    assert f(A, A + 8, 4, 16, 16, 16, rws.F32) == rws.ERR_INVALID_ARG
+    assert f(A, A + 4 * 16 * 4, 4, 16, 16, 16, rws.F32) != rws.ERR_INVALID_ARG
+    # Interleaved halves of a 32-wide matrix with equal strides do not overlap.
+    assert f(A, A + 16 * 4, 4, 16, 32, 32, rws.F32) != rws.ERR_INVALID_ARG
+    assert f(A, A + 15 * 4, 4, 16, 32, 32, rws.F32) == rws.ERR_INVALID_ARG
+
+
+def test_no_gpu_means_loud_failure(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # Valid arguments, no device: UNSUPPORTED, never a silent CPU result.
+    assert rws.softmax_rows_ptr(1 << 20, 1 << 30, 2, 8, 8, 8, rws.F32) == rws.ERR_UNSUPPORTED
+
+
+def test_c_only_caller(lib, tmp_path):
+    exe = tmp_path / "abi_caller"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "c", "abi_caller.c"), "-o", str(exe),
+                    rws.library_path(), "-Wl,-rpath," + os.path.dirname(rws.library_path())],
+                   check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr

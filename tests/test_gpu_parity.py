@@ -1,0 +1,137 @@
+"""Parity of the CUDA path with the oracle, through the C ABI.
+
+Full-size workloads (all five, every element) in the launch configuration the
+benchmark times (automatic path), and a sweep of small shapes — ragged tails,
+several tiles, every path forced — at sizes the oracle finishes in seconds.
+"""
+import numpy as np
+import pytest
+
+import row_wise_softmax_gb300 as rws
+import workloads as wl
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    rws.build()
+    rws.lib()
+    yield
+    assert rws.device_status(clear=True) == rws.OK
+
+
+def run(w: wl.Workload, path=rws.PATH_AUTO, out=None, stream=0):
+    x = parity.device_input(w)
+    y = parity.empty_output(w) if out is None else out
+    st = rws.softmax_rows_ptr(x.data_ptr(), y.data_ptr(), w.n_rows, w.n_cols, w.in_row_stride,
+                              w.out_row_stride, w.dtype, stream, path)
+    assert st == rws.OK, rws.status_string(st)
+    torch.cuda.synchronize()
+    return parity.host_output(y, w)
+
+
+EXPECTED_PATH = {
+    "small_f32": rws.PATH_WARP,
+    "masked_f32": rws.PATH_CTA,
+    "causal_bf16": rws.PATH_WARP,
+    "short_f32": rws.PATH_WARP,
+    "long_f32": rws.PATH_CLUSTER,
+}
+
+
+@pytest.mark.parametrize("name", wl.NAMES)
+def test_full_size_workload(name):
+    w = wl.make(name)
+    p = rws.plan(w.n_rows, w.n_cols, in_row_stride=w.in_row_stride,
+                 out_row_stride=w.out_row_stride, dtype=w.dtype)
+    assert p.path == EXPECTED_PATH[name], str(p)
+    before = rws.launch_count()
+    got = run(w)
+    assert rws.launch_count() - before == 1            # one kernel per call
+    stats = parity.compare(got, parity.expected(w), w.dtype, name)
+    print(name, str(p), stats)
+
+
+def test_closed_forms_on_gpu():
+    # masked_f32's constant row: exactly 2^-12; causal_bf16 row 0: exactly [1, 0, ...].
+    w = wl.masked_f32(64)
+    got = run(w)
+    assert np.all(got[w.const_row] == np.float32(2.0 ** -12))
+    wc = wl.causal_bf16(4)
+    gb = run(wc)
+    assert gb[0, 0] == 0x3F80 and np.all(gb[0, 1:] == 0)
+    # long_f32: the +50 spike takes all the mass.
+    wlng = wl.long_f32(4)
+    gl = run(wlng)
+    assert np.all(gl[np.arange(4), wlng.spike_cols] == 1.0)
+
+
+SWEEP_COLS = [1, 2, 3, 4, 5, 7, 8, 9, 31, 32, 33, 63, 64, 65, 100, 127, 128, 129, 255, 256, 257,
+              511, 513, 1000, 1023, 1024, 1025, 2047, 2049, 4095, 4096, 4097, 8191, 16385, 40000]
+PATHS = [rws.PATH_WARP, rws.PATH_CTA, rws.PATH_CLUSTER, rws.PATH_TWOPASS]
+
+
+@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: rws.PATH_NAMES[p])
+def test_shape_sweep_forced_paths(dtype, path):
+    checked = 0
+    for i, n_cols in enumerate(SWEEP_COLS):
+        if path == rws.PATH_WARP and n_cols > 1024:
+            continue
+        for n_rows in (1, 3, 7):
+            w = wl.random_rows(n_rows, n_cols, dtype=dtype, seed=1000 + i, scale=4.0)
+            got = run(w, path)
+            parity.compare(got, parity.expected(w), dtype, "%s %dx%d" % (
+                rws.PATH_NAMES[path], n_rows, n_cols))
+            checked += 1
+    assert checked > 20
+
+
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: rws.PATH_NAMES[p])
+def test_many_rows_per_cta_or_cluster(path):
+    # More rows than resident CTAs, so persistent loops take several rows each.
+    n_cols = 700 if path == rws.PATH_WARP else 3000
+    w = wl.random_rows(5000, n_cols, seed=77, scale=3.0)
+    parity.compare(run(w, path), parity.expected(w), wl.F32, rws.PATH_NAMES[path])
+
+
+def test_twopass_long_row_automatic():
+    # 16 slices of 96 KB are the cluster's cap: longer rows stream twice.
+    w = wl.random_rows(3, 1_600_000, seed=5, scale=2.0)
+    p = rws.plan(w.n_rows, w.n_cols)
+    assert p.path == rws.PATH_TWOPASS
+    parity.compare(run(w), parity.expected(w), wl.F32, "twopass auto")
+
+
+def test_bf16_long_rows_cluster():
+    w = wl.random_rows(6, 200_000, dtype=wl.BF16, seed=8, scale=6.0)
+    p = rws.plan(w.n_rows, w.n_cols, dtype=wl.BF16)
+    assert p.path == rws.PATH_CLUSTER
+    parity.compare(run(w), parity.expected(w), wl.BF16, "bf16 cluster")
+
+
+def test_reduced_workloads_every_path():
+    for name, rows in (("small_f32", 32), ("masked_f32", 24), ("causal_bf16", 1100),
+                       ("short_f32", 900), ("long_f32", 3)):
+        w = wl.make(name, rows)
+        want = parity.expected(w)
+        for path in PATHS:
+            if path == rws.PATH_WARP and w.n_cols > 1024:
+                continue
+            if path == rws.PATH_CTA and w.n_cols * w.elem_bytes > 200_000:
+                continue
+            parity.compare(run(w, path), want, w.dtype, "%s/%s" % (name, rws.PATH_NAMES[path]))
+
+
+def test_deterministic_run_to_run():
+    w = wl.masked_f32(300)
+    a, b = run(w), run(w)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    w5 = wl.long_f32(3)
+    assert np.array_equal(run(w5).view(np.uint32), run(w5).view(np.uint32))
