@@ -191,6 +191,27 @@ def time_device(w: wl.Workload, bufs, steps: int, warmup: int, torch, rws, flush
     return [a.elapsed_time(b) for a, b in ev], launches
 
 
+def copy_calibration(w: wl.Workload, bufs, torch, flush, stream, peak):
+    """torch copy_ of the same number of bytes (read n, write n), timed like a
+    step: the achievable HBM rate for a transfer of this size."""
+    x, y = bufs
+    n = min(x.numel(), y.numel(), w.n_rows * w.n_cols)
+    src, dst = x[:n], y[:n]
+    ts = []
+    for i in range(25):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dst.copy_(src)
+        b.record(stream)
+        b.synchronize()
+        if i >= 5:
+            ts.append(a.elapsed_time(b))
+    med = statistics.median(ts)
+    gbs = 2 * n * src.element_size() / (med * 1e-3) / 1e9
+    return {"GB/s": round(gbs, 1), "median_ms": round(med, 5), "frac_of_peak": round(gbs / peak, 4)}
+
+
 def time_e2e(w: wl.Workload, steps: int, warmup: int, torch, rws, stream):
     """softmax_rows_host with pinned host buffers: H2D + kernel + D2H per step."""
     dt = torch.float32 if w.dtype == wl.F32 else torch.bfloat16
@@ -245,7 +266,7 @@ def run_ours(args):
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     peak, peak_kind = measured_peak()
 
-    w = wl.make(HEADLINE)
+    w = wl.make(args.workload)
     plan = rws.plan(w.n_rows, w.n_cols, in_row_stride=w.in_row_stride,
                     out_row_stride=w.out_row_stride, dtype=w.dtype)
 
@@ -264,7 +285,8 @@ def run_ours(args):
         # Keep the sampled window at least ~1.5 s: repeat the same step (not
         # counted) if the timed steps were shorter than that.
         extra = 0
-        while time.perf_counter() - t_wall0 < 1.5 and extra < 200000:
+        while (not args.no_clock_window and time.perf_counter() - t_wall0 < 1.5
+               and extra < 200000):
             time_device(w, bufs, 200, 0, torch, rws, flush, stream)
             extra += 200
     barrier()
@@ -278,15 +300,16 @@ def run_ours(args):
     bytes_step = w.algorithmic_bytes
     value = world * bytes_step * args.steps / (total_ms * 1e-3) / 1e9
     achieved = bytes_step / (statistics.median(times) * 1e-3) / 1e9
-    traffic, traffic_src = committed_traffic(plan.path_name, HEADLINE)
+    traffic, traffic_src = committed_traffic(plan.path_name, args.workload)
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded: N(0,3^2), 41 -inf columns per row, one constant row)",
-        "config": {"workload": "%s: %d x %d fp32, row stride %d, -inf entries, constant row"
-                   % (HEADLINE, w.n_rows, w.n_cols, w.in_row_stride),
+        "config": {"workload": "%s: %d x %d %s, row strides %d/%d" % (
+                       args.workload, w.n_rows, w.n_cols, "fp32" if w.dtype == wl.F32 else "bf16",
+                       w.in_row_stride, w.out_row_stride),
                    "n_rows": w.n_rows, "n_cols": w.n_cols, "bytes_per_step": bytes_step,
                    "l2": "flushed between steps (512 MiB write, outside the step events)",
                    "parallelism": "rows sharded per rank, no exchange" if world > 1 else "1 GPU",
@@ -299,6 +322,7 @@ def run_ours(args):
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "median_step_ms": round(statistics.median(times), 5),
+        "copy_same_bytes": copy_calibration(w, bufs, torch, flush, stream, peak),
         "wall_s_timed_region": round(wall, 3),
     }
     if traffic:
@@ -320,10 +344,10 @@ def run_ours(args):
     if rank == 0 and not args.no_per_config:
         per = {}
         for name in wl.NAMES:
-            wc = w if name == HEADLINE else wl.make(name)
+            wc = w if name == args.workload else wl.make(name)
             pc = rws.plan(wc.n_rows, wc.n_cols, in_row_stride=wc.in_row_stride,
                           out_row_stride=wc.out_row_stride, dtype=wc.dtype)
-            bc = bufs if name == HEADLINE else device_buffers(wc, torch)
+            bc = bufs if name == args.workload else device_buffers(wc, torch)
             ts, _ = time_device(wc, bc, 30, 5, torch, rws, flush, stream)
             del bc
             med = statistics.median(ts)
@@ -380,6 +404,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--no-clock-window", action="store_true",
+                    help="do not extend the clock-sampling window past the timed steps")
+    ap.add_argument("--workload", default=HEADLINE, choices=list(wl.NAMES),
+                    help="workload timed as the step (default: the headline)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -158,8 +158,10 @@ typedef struct {
     int threads;         /* threads per CTA */
     int cluster;         /* CTAs per cluster (1: no cluster) */
     int rows_per_warp;   /* WARP path: rows a warp holds at once */
-    int chunks;          /* WARP path: vectors per lane per row */
+    int chunks;          /* vectors per thread (WARP: per lane per row; CTA and
+                            CLUSTER: 16-byte vectors of the slice) */
     int64_t slice_cols;  /* CTA/CLUSTER/TWOPASS: columns owned by one CTA */
+    int stages;          /* CTA/CLUSTER: slices in flight per CTA (ring depth) */
     int smem_bytes;      /* dynamic shared memory per CTA */
     int64_t grid;        /* CTAs launched; 0 = sized at launch from occupancy
                             (whole waves of resident CTAs, persistent) */
@@ -175,6 +177,20 @@ typedef struct {
 int softmax_plan(const softmax_device_desc_t* dev, const void* in, const void* out,
                  int64_t n_rows, int64_t n_cols, int64_t in_row_stride,
                  int64_t out_row_stride, int dtype, int path, softmax_plan_t* plan);
+
+/*
+ * softmax_rows_planned: launch with an explicit scheduler decision (tuning
+ * sweeps and tests).  *plan must describe this problem: typically the result
+ * of softmax_plan with some launch-shape fields changed.  The plan is checked
+ * before anything is launched (path and dtype, vector widths against pointer
+ * and stride alignment, slice coverage of the row, threads x vectors
+ * covering the slice, stage count and shared memory against the device,
+ * cluster size); a plan that could read or write outside the rows returns
+ * SOFTMAX_ERR_INVALID_ARG.  Otherwise behaves like softmax_rows.
+ */
+int softmax_rows_planned(const void* in, void* out, int64_t n_rows, int64_t n_cols,
+                         int64_t in_row_stride, int64_t out_row_stride, int dtype,
+                         const softmax_plan_t* plan, void* stream);
 
 /* Writes a one-line text form of *plan into buf (always NUL-terminated when
  * len > 0).  Returns the number of characters the full text needs. */

@@ -21,7 +21,7 @@ __all__ = [
     "F32", "BF16", "PATH_AUTO", "PATH_WARP", "PATH_CTA", "PATH_CLUSTER", "PATH_TWOPASS",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_DEVICE_TIMEOUT",
     "SoftmaxError", "DeviceDesc", "Plan", "build", "lib", "library_path",
-    "softmax_rows", "softmax_rows_ptr", "softmax_rows_host", "plan", "plan_for_device",
+    "softmax_rows", "softmax_rows_ptr", "softmax_rows_planned_ptr", "softmax_rows_host", "plan", "plan_for_device",
     "status_string", "device_status", "launch_count", "selftest_wait_timeout", "abi_version", "GB300",
 ]
 
@@ -54,7 +54,8 @@ class Plan(ctypes.Structure):
                 ("out_vec", ctypes.c_int), ("bulk_copy", ctypes.c_int),
                 ("threads", ctypes.c_int), ("cluster", ctypes.c_int),
                 ("rows_per_warp", ctypes.c_int), ("chunks", ctypes.c_int),
-                ("slice_cols", ctypes.c_int64), ("smem_bytes", ctypes.c_int),
+                ("slice_cols", ctypes.c_int64), ("stages", ctypes.c_int),
+                ("smem_bytes", ctypes.c_int),
                 ("grid", ctypes.c_int64)]
 
     def __str__(self) -> str:
@@ -97,6 +98,8 @@ def lib() -> ctypes.CDLL:
         L.softmax_rows.restype = ci
         L.softmax_rows_path.argtypes = [vp, vp, i64, i64, i64, i64, ci, vp, ci]
         L.softmax_rows_path.restype = ci
+        L.softmax_rows_planned.argtypes = [vp, vp, i64, i64, i64, i64, ci, ctypes.POINTER(Plan), vp]
+        L.softmax_rows_planned.restype = ci
         L.softmax_rows_host.argtypes = [vp, vp, i64, i64, i64, i64, ci, vp, vp, vp]
         L.softmax_rows_host.restype = ci
         L.softmax_status_string.argtypes = [ci]
@@ -148,6 +151,14 @@ def softmax_rows_ptr(in_ptr: int, out_ptr: int, n_rows: int, n_cols: int, in_row
                                   out_row_stride, dtype, stream)
     return lib().softmax_rows_path(in_ptr, out_ptr, n_rows, n_cols, in_row_stride,
                                    out_row_stride, dtype, stream, path)
+
+
+def softmax_rows_planned_ptr(in_ptr: int, out_ptr: int, n_rows: int, n_cols: int,
+                             in_row_stride: int, out_row_stride: int, dtype: int, plan: Plan,
+                             stream: int = 0) -> int:
+    """C ABI call with an explicit (checked) scheduler decision; returns the status."""
+    return lib().softmax_rows_planned(in_ptr, out_ptr, n_rows, n_cols, in_row_stride,
+                                      out_row_stride, dtype, ctypes.byref(plan), stream)
 
 
 def _dtype_code(t) -> int:

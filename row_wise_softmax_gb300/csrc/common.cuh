@@ -19,15 +19,34 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 enum : unsigned { kErrMbarrierTimeout = 1u };
 
 // ---------------------------------------------------------------- exp
-// e^d computed as 2^(d * log2 e) with the hardware base-2 exponential.
-// The non-.ftz form keeps subnormal results (softmax outputs far below the
-// row maximum stay nonzero, as in the double-precision definition).
-// d = 0 gives exactly 1; d = -inf gives +0; NaN stays NaN.
-__device__ __forceinline__ float exp_fast(float d)
+// e^d = 2^(d * log2 e), with the hardware base-2 exponential (ex2.approx,
+// flush-to-zero form: one instruction).
+//
+// exp_biased(d) = 2^64 * e^d for d <= 0.  The bias of 2^64 keeps the result a
+// normal float down to d = -131 instead of -87, so a softmax output
+// y = exp_biased(x - m) * (1 / (2^64 * l)) is formed by one correctly rounded
+// multiply, which produces subnormal outputs where the exact value is
+// subnormal.  Sums of biased terms stay below 2^95 for rows of up to 2^31
+// elements.  d = 0 gives exactly 2^64 (a row's maximum maps to exactly 1 before
+// the final scale); d = -inf gives +0; NaN stays NaN.
+constexpr float kExpBias = 64.0f;
+
+__device__ __forceinline__ float ex2_ftz(float t)
 {
     float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(d * kLog2e));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(t));
     return y;
+}
+
+__device__ __forceinline__ float exp_biased(float d)
+{
+    return ex2_ftz(fmaf(d, kLog2e, kExpBias));
+}
+
+// Unbiased e^d for d <= 0, flushed to zero below 2^-126 (rescale factors).
+__device__ __forceinline__ float exp_ftz(float d)
+{
+    return ex2_ftz(d * kLog2e);
 }
 
 // ------------------------------------------------------------ reductions
@@ -48,16 +67,18 @@ __device__ __forceinline__ float warp_sum(float v)
 }
 
 // Merge two online-softmax partials (m, l) and (m2, l2), where l is a sum of
-// exp(x - m) over the partial's elements:
+// exp_biased(x - m) over the partial's elements:
 //   M = max(m, m2),  l = l * e^(m - M) + l2 * e^(m2 - M).
 // A partial whose m is -inf holds no finite element: its factor is e^-inf = 0.
 // When both are -inf the reference point is 0 instead of M so that no
-// -inf - (-inf) appears; a NaN carried in either l still propagates.
+// -inf - (-inf) appears; a NaN carried in either l still propagates.  A
+// factor below 2^-126 flushes to zero: that partial is then below 2^-62 of
+// the merged sum, which is at least 2^64.
 __device__ __forceinline__ void ml_merge(float& m, float& l, float m2, float l2)
 {
     const float M = fmaxf(m, m2);
     const float ref = (M == kNegInf) ? 0.0f : M;
-    l = l * exp_fast(m - ref) + l2 * exp_fast(m2 - ref);
+    l = l * exp_ftz(m - ref) + l2 * exp_ftz(m2 - ref);
     m = M;
 }
 

@@ -22,6 +22,8 @@ int validate(const void* in, const void* out, int64_t n_rows, int64_t n_cols,
              int64_t ld_in, int64_t ld_out, int dtype);
 int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path,
               softmax_plan_t* plan);
+// Is a caller-supplied plan safe and complete for this problem?
+int check_plan(const softmax_device_desc_t& dev, const Problem& p, const softmax_plan_t& plan);
 
 // Launchers, one per path (each in its own translation unit).
 cudaError_t launch_warp_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);

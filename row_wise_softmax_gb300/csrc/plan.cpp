@@ -4,19 +4,19 @@
 //
 // Paths by row length (n_cols, element size esz):
 //   WARP     n_cols <= 1024: a warp owns rows in registers (short rows).
-//   CTA      row <= 64 KB: one CTA per row, the row staged in shared memory.
-//   CLUSTER  row <= max_cluster slices of <= 96 KB: a cluster per row, each
-//            CTA holding a slice in shared memory (long rows, single HBM pass).
+//   CTA      row <= 32 KB: a persistent CTA walks rows through a ring of
+//            shared-memory stages (cp.async.bulk), each row held in registers.
+//   CLUSTER  longer rows up to 16 slices of <= 128 KB (fp32) / 64 KB (bf16):
+//            a cluster per row, slices on different SMs, one HBM pass.
 //   TWOPASS  anything longer: a cluster streams the row twice.
-// The 64 KB / 96 KB slice caps keep two or three CTAs resident per SM
-// (228 KB of shared memory each on GB300), so the copy engine has several
-// slices in flight per SM while others are being reduced or stored.
+// Slices are kept at <= 32 KB when a cluster of <= 16 CTAs allows it; the ring
+// gets about 64 KB of shared memory per CTA, so two or three CTAs stay resident
+// per SM (228 KB of shared memory each on GB300) with several slices in flight.
 //
 // Whole waves (the "Block Occupancy: tail effect" rule of the cs336 lecture
-// 6 notes): the WARP and TWOPASS grids are persistent, sized at launch to the
-// number of CTAs (clusters) the device can hold at once; the CTA and CLUSTER
-// grids launch one CTA (cluster) per row and rely on many resident CTAs per
-// SM and the hardware block scheduler to balance the tail.
+// 6 notes): every grid is persistent, sized at launch to the number of CTAs
+// (clusters) the device holds at once, so the last wave is never a small
+// fraction of the machine; rows are dealt round-robin to CTAs (clusters).
 #include "kernels.h"
 
 #include <stdint.h>
@@ -26,10 +26,11 @@ namespace rwsm {
 namespace {
 
 constexpr int64_t kWarpMaxCols = 1024;
-constexpr int64_t kCtaMaxBytes = 64 * 1024;
-constexpr int64_t kSliceBytesSmallCluster = 64 * 1024;   // cluster <= 8
-constexpr int64_t kSliceBytesLargeCluster = 96 * 1024;   // cluster 16
-constexpr int kSmemReserve = 2048;                        // static smem + slack
+constexpr int64_t kSliceTargetBytes = 32 * 1024;   // preferred slice (CTA path: whole row)
+constexpr int64_t kRingBudgetBytes = 64 * 1024;    // shared memory for the ring, per CTA
+constexpr int kMaxStages = 8;                       // must match row_slices.cu
+constexpr int kMaxSliceThreads = 1024;
+constexpr int kSmemReserve = 2048;                  // static smem + slack
 
 int esize(int dtype) { return dtype == SOFTMAX_F32 ? 4 : 2; }
 
@@ -64,16 +65,28 @@ int warp_rows_for(int e)
     return e >= 16 ? 1 : (16 / e > 8 ? 8 : 16 / e);
 }
 
-// Threads for a shared-memory slice of nv 16-byte vectors: about four
-// vectors per thread, between 128 and 512 threads.
-int slice_threads(int64_t nv)
+// 16-byte vectors a thread of the slice kernel holds at most (32 floats).
+int max_vectors_per_thread(int esz) { return esz == 4 ? 8 : 4; }
+
+// Columns one CTA of the slice kernel can hold in registers.
+int64_t slice_capacity(int esz) { return int64_t{kMaxSliceThreads} * max_vectors_per_thread(esz) * (16 / esz); }
+
+// Threads and vectors per thread for a slice of nvec 16-byte vectors: as
+// few threads as hold the slice at the largest vectors-per-thread, at least
+// 128, then the smallest power-of-two vectors per thread that covers it.
+void slice_shape(int64_t nvec, int esz, int* threads, int* nv)
 {
-    int64_t t = pow2_floor(ceil_div(nv, 4) > 0 ? ceil_div(nv, 4) : 1);
+    const int nvmax = max_vectors_per_thread(esz);
+    int64_t t = pow2_ceil(ceil_div(nvec, nvmax));
     if (t < 128)
         t = 128;
-    if (t > 512)
-        t = 512;
-    return static_cast<int>(t);
+    if (t > kMaxSliceThreads)
+        t = kMaxSliceThreads;
+    int64_t v = pow2_ceil(ceil_div(nvec, t));
+    if (v < 1)
+        v = 1;
+    *threads = static_cast<int>(t);
+    *nv = static_cast<int>(v);
 }
 
 // Does [a_lo, a_hi) intersect [b_lo, b_hi)?
@@ -160,23 +173,26 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
     const int64_t smem_cap = static_cast<int64_t>(dev.max_smem_per_block_optin) - kSmemReserve;
     const int max_cluster = dev.max_cluster < 1 ? 1 : (dev.max_cluster > 16 ? 16 : dev.max_cluster);
 
-    // Smallest cluster (>= 2) whose slices fit the per-slice cap.
-    auto cluster_for = [&](int64_t cap_small, int64_t cap_large) -> int {
-        for (int cs = 2; cs <= max_cluster; cs *= 2) {
-            const int64_t slice_bytes = round_up(ceil_div(p.n_cols, cs), vmax) * esz;
-            const int64_t cap = cs <= 8 ? cap_small : cap_large;
-            if (slice_bytes <= cap && slice_bytes <= smem_cap)
+    const int64_t cap = slice_capacity(esz);
+    auto slice_cols_for = [&](int cs) { return round_up(ceil_div(p.n_cols, cs), vmax); };
+    // Smallest cluster (>= 2) whose slices fit the preferred size, else the
+    // largest cluster if its slices fit a CTA's registers.
+    auto cluster_for = [&]() -> int {
+        for (int cs = 2; cs <= max_cluster; cs *= 2)
+            if (slice_cols_for(cs) * esz <= kSliceTargetBytes)
                 return cs;
-        }
+        const int big = static_cast<int>(pow2_floor(max_cluster));
+        if (big >= 2 && slice_cols_for(big) <= cap && slice_cols_for(big) * esz <= smem_cap)
+            return big;
         return 0;
     };
 
     if (path == SOFTMAX_PATH_AUTO) {
         if (p.n_cols <= kWarpMaxCols)
             path = SOFTMAX_PATH_WARP;
-        else if (row_bytes <= kCtaMaxBytes && row_bytes <= smem_cap)
+        else if (row_bytes <= kSliceTargetBytes)
             path = SOFTMAX_PATH_CTA;
-        else if (cluster_for(kSliceBytesSmallCluster, kSliceBytesLargeCluster))
+        else if (cluster_for())
             path = SOFTMAX_PATH_CLUSTER;
         else
             path = SOFTMAX_PATH_TWOPASS;
@@ -203,25 +219,33 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
     case SOFTMAX_PATH_CLUSTER: {
         int cs = 1;
         if (path == SOFTMAX_PATH_CLUSTER) {
-            // Forced or automatic: prefer the regular caps, else anything
-            // that fits shared memory.
-            cs = cluster_for(kSliceBytesSmallCluster, kSliceBytesLargeCluster);
-            if (!cs)
-                cs = cluster_for(smem_cap, smem_cap);
+            cs = cluster_for();
             if (!cs)
                 return SOFTMAX_ERR_UNSUPPORTED;
         }
-        const int64_t slice = round_up(ceil_div(p.n_cols, cs), vmax);
-        if (slice * esz > smem_cap)
+        const int64_t slice = slice_cols_for(cs);
+        const int64_t stage_bytes = slice * esz;
+        if (slice > cap || stage_bytes > smem_cap)
             return SOFTMAX_ERR_UNSUPPORTED;
+        int threads = 0, nv = 0;
+        slice_shape(slice / vmax, esz, &threads, &nv);
+        int64_t stages = kRingBudgetBytes / stage_bytes;
+        if (stages < 1)
+            stages = 1;
+        if (stages > kMaxStages)
+            stages = kMaxStages;
+        while (stages > 1 && stages * stage_bytes > smem_cap)
+            --stages;
         q.cluster = cs;
         q.slice_cols = slice;
-        q.smem_bytes = static_cast<int>(slice * esz);
         q.vec = vmax;
         q.out_vec = out_al ? vmax : 1;
         q.bulk_copy = in_al ? 1 : 0;
-        q.threads = slice_threads(slice / vmax);
-        q.grid = p.n_rows * cs;
+        q.threads = threads;
+        q.chunks = nv;
+        q.stages = in_al ? static_cast<int>(stages) : 0;
+        q.smem_bytes = in_al ? static_cast<int>(stages * stage_bytes) : 0;
+        q.grid = 0;
         break;
     }
     case SOFTMAX_PATH_TWOPASS: {
@@ -241,6 +265,78 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
     }
     *plan = q;
     return SOFTMAX_OK;
+}
+
+int check_plan(const softmax_device_desc_t& dev, const Problem& p, const softmax_plan_t& q)
+{
+    const int st = validate(p.in, p.out, p.n_rows, p.n_cols, p.ld_in, p.ld_out, p.dtype);
+    if (st != SOFTMAX_OK)
+        return st;
+    if (dev.cc_major != 10 || dev.cc_minor != 3)
+        return SOFTMAX_ERR_UNSUPPORTED;
+    if (q.dtype != p.dtype || q.grid < 0)
+        return SOFTMAX_ERR_INVALID_ARG;
+    const int esz = esize(p.dtype);
+    const int vmax = 16 / esz;
+    const bool in_al = aligned16(p.in, p.n_rows, p.ld_in, esz);
+    const bool out_al = aligned16(p.out, p.n_rows, p.ld_out, esz);
+    const int64_t smem_cap = static_cast<int64_t>(dev.max_smem_per_block_optin) - kSmemReserve;
+    const int max_cluster = dev.max_cluster < 1 ? 1 : (dev.max_cluster > 16 ? 16 : dev.max_cluster);
+    auto pow2_in = [](int64_t v, int64_t lo, int64_t hi) {
+        return v >= lo && v <= hi && (v & (v - 1)) == 0;
+    };
+    auto vec_ok = [&](int v, bool aligned) { return v == 1 || (v == vmax && aligned); };
+    switch (q.path) {
+    case SOFTMAX_PATH_WARP: {
+        if (p.n_cols > kWarpMaxCols || !vec_ok(q.vec, in_al && out_al) || q.out_vec != q.vec)
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (!pow2_in(q.chunks, 1, 32) || q.vec * q.chunks > 32 ||
+            int64_t{32} * q.vec * q.chunks < p.n_cols)
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (q.grid > 0x7fffffff)
+            return SOFTMAX_ERR_INVALID_ARG;
+        return SOFTMAX_OK;
+    }
+    case SOFTMAX_PATH_CTA:
+    case SOFTMAX_PATH_CLUSTER: {
+        const int cs = q.cluster;
+        if (q.path == SOFTMAX_PATH_CTA ? cs != 1 : !pow2_in(cs, 2, max_cluster))
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (q.vec != vmax || q.slice_cols <= 0 || q.slice_cols % vmax ||
+            q.slice_cols * cs < p.n_cols)
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (!pow2_in(q.threads, 128, kMaxSliceThreads) ||
+            !pow2_in(q.chunks, 1, max_vectors_per_thread(esz)) ||
+            int64_t{q.threads} * q.chunks * vmax < q.slice_cols)
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (!vec_ok(q.out_vec, out_al) || (q.bulk_copy && !in_al) ||
+            (q.bulk_copy != 0 && q.bulk_copy != 1))
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (q.bulk_copy) {
+            if (q.stages < 1 || q.stages > kMaxStages ||
+                q.smem_bytes != q.stages * q.slice_cols * esz || q.smem_bytes > smem_cap)
+                return SOFTMAX_ERR_INVALID_ARG;
+        } else if (q.smem_bytes != 0) {
+            return SOFTMAX_ERR_INVALID_ARG;
+        }
+        if (q.grid % cs || q.grid > 0x7fffffff)
+            return SOFTMAX_ERR_INVALID_ARG;
+        return SOFTMAX_OK;
+    }
+    case SOFTMAX_PATH_TWOPASS: {
+        const int cs = q.cluster;
+        if (!pow2_in(cs, 1, max_cluster) || !vec_ok(q.vec, in_al && out_al) || q.out_vec != q.vec)
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (q.slice_cols <= 0 || q.slice_cols % vmax || q.slice_cols * cs < p.n_cols ||
+            q.threads != 512)
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (q.grid % cs || q.grid > 0x7fffffff)
+            return SOFTMAX_ERR_INVALID_ARG;
+        return SOFTMAX_OK;
+    }
+    default:
+        return SOFTMAX_ERR_INVALID_ARG;
+    }
 }
 
 }  // namespace rwsm

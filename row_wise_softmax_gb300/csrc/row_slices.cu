@@ -1,50 +1,42 @@
 // CTA and CLUSTER paths: a row (CTA path, cs == 1) or a slice of a row
-// (CLUSTER path, cs CTAs per row) is staged in shared memory, read from HBM
-// exactly once.
+// (CLUSTER path, cs CTAs per row) is read from HBM exactly once.
 //
-//   stage   one elected thread starts cp.async.bulk copies of the CTA's slice
-//           (global -> shared, completing on an mbarrier); a ragged tail of
-//           fewer than 16 bytes is loaded by plain loads.  Without 16-byte
-//           alignment every thread copies elements instead.
-//   pass A  each thread walks its shared-memory vectors in batches and keeps
-//           an online (m, l) partial: m_new = max(m, batch max),
-//           l = l * e^(m - m_new) + sum e^(x - m_new) — the running-max
-//           rescale of "Triton GPU programming deep dive", section 3.3, here
-//           over slices of one row instead of key blocks.
-//   merge   (m, l) partials are merged across the warp (__shfl_xor), the CTA
-//           (shared memory) and, for cs > 1, the cluster: each CTA publishes
-//           its partial, a cluster barrier orders the writes, and every warp
-//           reads the cs partials through distributed shared memory.
-//   pass B  y = e^(x - M) * (1/L) from shared memory, stored to HBM with
-//           16-byte vector stores when the output rows are 16-byte aligned.
+// Persistent CTAs (clusters) walk their rows r, r + G, r + 2G, ... with a ring
+// of `stages` shared-memory buffers, one slice each:
 //
-// Tiling a row too long for one block and carrying an accumulator across the
-// tiles is the "Level 2: Row Sum (tiling)" pattern of the cs336 lecture 6
-// notes; the slices of one row live on several SMs at once, so the row is
-// read once and written once however long it is (up to the cluster's
-// shared memory).  Rows are independent (lecture 6, "Level 1: Softmax"),
-// so CTAs for different rows never communicate.
+//   ring    one elected thread keeps up to `stages` slices in flight with
+//           cp.async.bulk copies (global -> shared, completing on one mbarrier
+//           per stage).  A ragged tail of fewer than 16 bytes is read with
+//           plain loads by the thread that owns it.
+//   load    every thread copies its vectors of the slice from shared memory
+//           into registers; after a CTA barrier the stage is refilled with the
+//           slice `stages` rows ahead, so HBM reads continue while this row is
+//           reduced and stored.
+//   max     m: thread, warp (__shfl_xor), CTA (shared memory), and for a
+//           cluster, every CTA's maximum read through distributed shared
+//           memory after a cluster barrier.
+//   exp/sum e = exp(x - m) kept in registers (exp_biased, one ex2 per element),
+//           l = sum reduced the same way.
+//   store   y = e * (1/l), 16-byte vector stores when the output rows allow.
+//
+// This is the fused softmax of "Triton: write CUDA-grade GPU operators in
+// Python" (example 2) — one HBM read and one write per element — with the row
+// split over the SMs of a cluster when it is longer than one SM can hold;
+// tiling a row over several blocks and combining their partial results is the
+// "Level 2: Row Sum (tiling)" pattern of the cs336 lecture 6 notes.  Without
+// 16-byte alignment the kernel reads the slice straight into registers with
+// plain loads (no ring).
 #include "common.cuh"
 #include "kernels.h"
 
 #include <atomic>
-#include <mutex>
 
 namespace rwsm {
 
 __device__ unsigned g_error_row_slices = 0;
 
+constexpr int kMaxStages = 8;
 constexpr uint32_t kBulkChunkBytes = 32768;
-constexpr int kBatch = 4;          // shared-memory vectors per thread per pass-A step
-
-template <typename T>
-__device__ __forceinline__ void copy_elem(T* dst, const T* src)
-{
-    if constexpr (sizeof(T) == 4)
-        *reinterpret_cast<float*>(dst) = __ldg(reinterpret_cast<const float*>(src));
-    else
-        *reinterpret_cast<unsigned short*>(dst) = __ldg(reinterpret_cast<const unsigned short*>(src));
-}
 
 template <typename T>
 __device__ __forceinline__ void set_neg_inf(T* dst)
@@ -55,134 +47,197 @@ __device__ __forceinline__ void set_neg_inf(T* dst)
         *reinterpret_cast<unsigned short*>(dst) = 0xff80u;   // bf16 -inf
 }
 
-template <typename T, int THREADS, bool BULK, bool OUTVEC>
+// Cluster-wide reduction of one float per CTA: thread 0 publishes v in its
+// shared slot, a cluster barrier (release / acquire) orders the writes, then
+// each warp reads the cs slots through distributed shared memory and reduces
+// them.  The slot of a given kind is rewritten only one row later, after at
+// least one more cluster barrier that every peer reaches only once it has
+// read the previous value.
+template <bool IS_MAX>
+__device__ __forceinline__ float cluster_reduce(float v, float* slot, int cs)
+{
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    if (threadIdx.x == 0)
+        *slot = v;
+    cluster.sync();
+    const int lane = threadIdx.x & 31;
+    float r = IS_MAX ? kNegInf : 0.0f;
+    if (lane < cs)
+        r = *cluster.map_shared_rank(slot, lane);
+    return IS_MAX ? warp_max(r) : warp_sum(r);
+}
+
+template <typename T, int THREADS, int NV, bool BULK, bool OUTVEC>
 __global__ void __launch_bounds__(THREADS)
-row_slices_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_in,
-                  int64_t ld_out, int slice_cols, int cs)
+row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
+                  int64_t ld_out, int slice_cols, int cs, int stages)
 {
     constexpr int VEC = Elem<T>::kVec16;
     constexpr int NW = THREADS / 32;
+    constexpr int E = NV * VEC;
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    T* buf = reinterpret_cast<T*>(smem_raw);
-    __shared__ float red_m[NW], red_l[NW];
-    __shared__ float2 part[2];
-    __shared__ __align__(8) unsigned long long bar;
+    __shared__ float red_max[NW], red_sum[NW];
+    __shared__ float part[2][2];
+    __shared__ __align__(8) unsigned long long full[kMaxStages];
+    __shared__ unsigned issued[kMaxStages];
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rank = static_cast<int>(blockIdx.x % cs);
     const int64_t cluster_id = blockIdx.x / cs;
     const int64_t n_clusters = gridDim.x / cs;
+    const int c0 = rank * slice_cols;
+    int len = n_cols - c0;
+    len = len < 0 ? 0 : (len > slice_cols ? slice_cols : len);
+    const int nv = (len + VEC - 1) / VEC;
+    const uint32_t bulk_bytes = static_cast<uint32_t>(len * sizeof(T)) & ~15u;
+    const int bulk_elems = static_cast<int>(bulk_bytes / sizeof(T));
+    const int tail_vec = bulk_elems < len ? bulk_elems / VEC : -1;   // vector patched from HBM
 
-    const int64_t c0 = static_cast<int64_t>(rank) * slice_cols;
-    int64_t len64 = n_cols - c0;
-    len64 = len64 < 0 ? 0 : (len64 > slice_cols ? slice_cols : len64);
-    const int len = static_cast<int>(len64);
-    const int len_pad = (len + VEC - 1) / VEC * VEC;
-    const int nv = len_pad / VEC;
-
-    const uint32_t bar_a = smem_addr(&bar);
-    if (BULK && tid == 0) {
-        mbar_init(bar_a, 1);
-        fence_mbar_init();
-    }
-    for (int e = len + tid; e < len_pad; e += THREADS)
-        set_neg_inf(buf + e);                       // pad to whole vectors
-    __syncthreads();
-
-    bool failed = false;                            // CTA-uniform
-    uint32_t failed_phase = 0;
-    uint32_t phase = 0;
-    int slot = 0;
-    for (int64_t row = cluster_id; row < n_rows; row += n_clusters, phase ^= 1u, slot ^= 1) {
-        const T* src = in + row * ld_in + c0;
-        // ---- stage the slice in shared memory
-        if constexpr (BULK) {
-            const uint32_t bytes = static_cast<uint32_t>(len * sizeof(T)) & ~15u;
-            if (tid == 0 && !failed) {
-                fence_proxy_async_smem();           // earlier generic reads of buf
-                if (bytes) {
-                    mbar_arrive_expect_tx(bar_a, bytes);
-                    const uint32_t dst = smem_addr(buf);
-                    for (uint32_t off = 0; off < bytes; off += kBulkChunkBytes) {
-                        const uint32_t n = bytes - off < kBulkChunkBytes ? bytes - off : kBulkChunkBytes;
-                        bulk_g2s(dst + off, reinterpret_cast<const char*>(src) + off, n, bar_a);
-                    }
-                } else {
-                    mbar_arrive(bar_a);
-                }
-            }
-            for (int e = static_cast<int>(bytes / sizeof(T)) + tid; e < len; e += THREADS)
-                copy_elem(buf + e, src + e);        // < 16-byte ragged tail
-            const bool ok = failed ? true : mbar_wait_bounded(bar_a, phase);
-            if (__syncthreads_or(!ok) && !failed) {
-                failed = true;
-                failed_phase = phase;
+    T* ring = reinterpret_cast<T*>(smem_raw);
+    auto stage_ptr = [&](int s) { return ring + static_cast<int64_t>(s) * slice_cols; };
+    auto issue = [&](int s, int64_t row) {      // thread 0 only
+        const uint32_t bar = smem_addr(&full[s]);
+        fence_proxy_async_smem();
+        issued[s] += 1;
+        if (bulk_bytes) {
+            mbar_arrive_expect_tx(bar, bulk_bytes);
+            const char* src = reinterpret_cast<const char*>(in + row * ld_in + c0);
+            const uint32_t dst = smem_addr(stage_ptr(s));
+            for (uint32_t off = 0; off < bulk_bytes; off += kBulkChunkBytes) {
+                const uint32_t n = bulk_bytes - off < kBulkChunkBytes ? bulk_bytes - off : kBulkChunkBytes;
+                bulk_g2s(dst + off, src + off, n, bar);
             }
         } else {
-            for (int e = tid; e < len; e += THREADS)
-                copy_elem(buf + e, src + e);
-            __syncthreads();
+            mbar_arrive(bar);
         }
+    };
 
-        // ---- pass A: online (m, l) over this thread's vectors
-        float m = kNegInf, l = 0.0f;
-        for (int v0 = tid; v0 < nv; v0 += THREADS * kBatch) {
-            float x[kBatch * VEC];
+    bool failed = false;                      // CTA-uniform
+    if constexpr (BULK) {
+        if (tid == 0) {
+            for (int s = 0; s < stages; ++s) {
+                mbar_init(smem_addr(&full[s]), 1);
+                issued[s] = 0;
+            }
+            fence_mbar_init();
+        }
+        // Positions the copies never write read as -inf (whole trailing vector).
+        for (int s = 0; s < stages; ++s)
+            for (int e = bulk_elems + tid; e < nv * VEC; e += THREADS)
+                set_neg_inf(stage_ptr(s) + e);
+        __syncthreads();
+        if (tid == 0)
+            for (int s = 0; s < stages; ++s) {
+                const int64_t row = cluster_id + s * n_clusters;
+                if (row < n_rows)
+                    issue(s, row);
+            }
+    }
+
+    int64_t i = 0;
+    for (int64_t row = cluster_id; row < n_rows; row += n_clusters, ++i) {
+        float x[E];
+        const T* src = in + row * ld_in + c0;
+        if constexpr (BULK) {
+            const int s = static_cast<int>(i % stages);
+            const uint32_t parity = static_cast<uint32_t>((i / stages) & 1);
+            const bool ok = failed ? true : mbar_wait_bounded(smem_addr(&full[s]), parity);
+            const T* st = stage_ptr(s);
 #pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                const int v = v0 + k * THREADS;
+            for (int k = 0; k < NV; ++k) {
+                const int v = tid + k * THREADS;
                 if (v < nv) {
-                    lds_vec<T, VEC>(buf + v * VEC, &x[k * VEC]);
+                    lds_vec<T, VEC>(st + v * VEC, &x[k * VEC]);
+                    if (v == tail_vec) {             // < 16-byte ragged tail
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) {
+                            const int e = v * VEC + j;
+                            if (e >= bulk_elems)
+                                x[k * VEC + j] = e < len ? Elem<T>::load1(src + e) : kNegInf;
+                        }
+                    }
                 } else {
 #pragma unroll
                     for (int j = 0; j < VEC; ++j)
                         x[k * VEC + j] = kNegInf;
                 }
             }
-            float bm = kNegInf;
+            // Every thread has its slice in registers: the stage is free.
+            if (__syncthreads_or(!ok))
+                failed = true;
+            if (tid == 0 && !failed) {
+                const int64_t next = row + static_cast<int64_t>(stages) * n_clusters;
+                if (next < n_rows)
+                    issue(s, next);
+            }
+        } else {
 #pragma unroll
-            for (int i = 0; i < kBatch * VEC; ++i)
-                bm = fmaxf(bm, x[i]);
-            const float mn = fmaxf(m, bm);
-            const float ref = (mn == kNegInf) ? 0.0f : mn;
-            float s = 0.0f;
+            for (int k = 0; k < NV; ++k) {
+                const int v = tid + k * THREADS;
+                if (v < nv) {
+                    load_vec_masked<T, VEC>(src, v * VEC, len, &x[k * VEC]);
+                } else {
 #pragma unroll
-            for (int i = 0; i < kBatch * VEC; ++i)
-                s += exp_fast(x[i] - ref);
-            l = l * exp_fast(m - ref) + s;
-            m = mn;
-        }
-
-        // ---- merge: warp, CTA, cluster
-        cta_ml_reduce<THREADS>(m, l, red_m, red_l);
-        if (cs > 1)
-            cluster_ml_reduce(m, l, part, slot, cs);
-        const float inv = 1.0f / l;
-
-        // ---- pass B: normalise and store
-        T* dst = out + row * ld_out + c0;
-        for (int v = tid; v < nv; v += THREADS) {
-            float x[VEC];
-            lds_vec<T, VEC>(buf + v * VEC, x);
-#pragma unroll
-            for (int j = 0; j < VEC; ++j)
-                x[j] = exp_fast(x[j] - m);
-            if constexpr (OUTVEC) {
-                store_vec_masked<T, VEC>(dst, static_cast<int64_t>(v) * VEC, len, x, inv);
-            } else {
-#pragma unroll
-                for (int j = 0; j < VEC; ++j)
-                    if (v * VEC + j < len)
-                        Elem<T>::store1(dst + v * VEC + j, x[j] * inv);
+                    for (int j = 0; j < VEC; ++j)
+                        x[k * VEC + j] = kNegInf;
+                }
             }
         }
-        __syncthreads();                            // buf and red_* are reused
+
+        // ---- row maximum
+        float m = kNegInf;
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            m = fmaxf(m, x[e]);
+        m = warp_max(m);
+        if (lane == 0)
+            red_max[warp] = m;
+        __syncthreads();
+        m = warp_max(lane < NW ? red_max[lane] : kNegInf);
+        if (cs > 1)
+            m = cluster_reduce<true>(m, &part[i & 1][0], cs);
+
+        // ---- exponentials and their sum (biased by 2^64, see exp_biased)
+        float l = 0.0f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            x[e] = exp_biased(x[e] - m);
+            l += x[e];
+        }
+        l = warp_sum(l);
+        if (lane == 0)
+            red_sum[warp] = l;
+        __syncthreads();
+        l = warp_sum(lane < NW ? red_sum[lane] : 0.0f);
+        if (cs > 1)
+            l = cluster_reduce<false>(l, &part[i & 1][1], cs);
+        const float inv = 1.0f / l;
+
+        // ---- normalise and store
+        T* dst = out + row * ld_out + c0;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int v = tid + k * THREADS;
+            if (v < nv) {
+                if constexpr (OUTVEC) {
+                    store_vec_masked<T, VEC>(dst, v * VEC, len, &x[k * VEC], inv);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j)
+                        if (v * VEC + j < len)
+                            Elem<T>::store1(dst + v * VEC + j, x[k * VEC + j] * inv);
+                }
+            }
+        }
     }
     if (cs > 1)
         cooperative_groups::this_cluster().sync();  // peers may still read `part`
     if (BULK && failed && tid == 0) {
         atomicOr(&g_error_row_slices, kErrMbarrierTimeout);
-        mbar_wait_bounded(bar_a, failed_phase);     // the copy still in flight
+        for (int s = 0; s < stages; ++s)             // copies possibly still in flight
+            if (issued[s])
+                mbar_wait_bounded(smem_addr(&full[s]), (issued[s] - 1) & 1u);
     }
 }
 
@@ -224,18 +279,16 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-// Per-device, per-instantiation attribute state (dynamic smem limit set so far).
-template <typename Kernel>
 struct KernelAttrs {
     std::atomic<int> smem_set[kMaxDevices];
-    std::atomic<bool> cluster_set[kMaxDevices];
+    std::atomic<bool> flags_set[kMaxDevices];
 };
 
-template <typename T, int THREADS, bool BULK, bool OUTVEC>
+template <typename T, int THREADS, int NV, bool BULK, bool OUTVEC>
 cudaError_t launch_rs(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
 {
-    auto* k = row_slices_kernel<T, THREADS, BULK, OUTVEC>;
-    static KernelAttrs<decltype(k)> attrs;
+    auto* k = row_slices_kernel<T, THREADS, NV, BULK, OUTVEC>;
+    static KernelAttrs attrs;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
@@ -248,56 +301,90 @@ cudaError_t launch_rs(const Problem& p, const softmax_plan_t& plan, cudaStream_t
             return err;
         attrs.smem_set[dev].store(plan.smem_bytes);
     }
-    if (!attrs.cluster_set[dev].load()) {
+    if (!attrs.flags_set[dev].load()) {
         err = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (err != cudaSuccess)
             return err;
         cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
-        attrs.cluster_set[dev].store(true);
+        attrs.flags_set[dev].store(true);
     }
     const int cs = plan.cluster;
-    int64_t grid = p.n_rows * cs;
-    const int64_t cap = (int64_t{0x7fffffff} / cs) * cs;
-    if (grid > cap)
-        grid = cap;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = static_cast<size_t>(plan.smem_bytes);
-    cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    int64_t clusters = plan.grid > 0 ? plan.grid / cs : 0;
+    if (clusters <= 0) {
+        // Persistent: as many CTAs (clusters) as can be resident at once.
+        int active = 0;
+        if (cs > 1) {
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(static_cast<unsigned>(cs), 1, 1);
+            q.blockDim = dim3(THREADS, 1, 1);
+            q.dynamicSmemBytes = static_cast<size_t>(plan.smem_bytes);
+            q.attrs = attr;
+            q.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&active, k, &q) != cudaSuccess) {
+                cudaGetLastError();
+                active = 0;
+            }
+        } else {
+            active = resident_ctas(reinterpret_cast<const void*>(k), THREADS, plan.smem_bytes);
+        }
+        if (active < 1)
+            active = 1;
+        clusters = p.n_rows < active ? p.n_rows : active;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * cs), 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(plan.smem_bytes);
+    cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = cs > 1 ? 1 : 0;
     err = cudaLaunchKernelEx(&cfg, k, static_cast<const T*>(p.in), static_cast<T*>(p.out),
-                             p.n_rows, p.n_cols, p.ld_in, p.ld_out,
-                             static_cast<int>(plan.slice_cols), cs);
+                             p.n_rows, static_cast<int>(p.n_cols), p.ld_in, p.ld_out,
+                             static_cast<int>(plan.slice_cols), cs, plan.stages);
     note_launch();
     return err;
 }
 
-template <typename T, int THREADS>
+template <typename T, int THREADS, int NV>
 cudaError_t launch_flags(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
 {
     const bool outvec = plan.out_vec > 1;
     if (plan.bulk_copy)
-        return outvec ? launch_rs<T, THREADS, true, true>(p, plan, s)
-                      : launch_rs<T, THREADS, true, false>(p, plan, s);
-    return outvec ? launch_rs<T, THREADS, false, true>(p, plan, s)
-                  : launch_rs<T, THREADS, false, false>(p, plan, s);
+        return outvec ? launch_rs<T, THREADS, NV, true, true>(p, plan, s)
+                      : launch_rs<T, THREADS, NV, true, false>(p, plan, s);
+    return outvec ? launch_rs<T, THREADS, NV, false, true>(p, plan, s)
+                  : launch_rs<T, THREADS, NV, false, false>(p, plan, s);
+}
+
+template <typename T, int THREADS>
+cudaError_t launch_nv(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
+{
+    switch (plan.chunks) {
+    case 1: return launch_flags<T, THREADS, 1>(p, plan, s);
+    case 2: return launch_flags<T, THREADS, 2>(p, plan, s);
+    case 4: return launch_flags<T, THREADS, 4>(p, plan, s);
+    case 8:
+        if constexpr (sizeof(T) == 4) return launch_flags<T, THREADS, 8>(p, plan, s);
+        break;
+    default: break;
+    }
+    return cudaErrorInvalidValue;
 }
 
 template <typename T>
 cudaError_t launch_threads(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
 {
     switch (plan.threads) {
-    case 128: return launch_flags<T, 128>(p, plan, s);
-    case 256: return launch_flags<T, 256>(p, plan, s);
-    case 512: return launch_flags<T, 512>(p, plan, s);
+    case 128: return launch_nv<T, 128>(p, plan, s);
+    case 256: return launch_nv<T, 256>(p, plan, s);
+    case 512: return launch_nv<T, 512>(p, plan, s);
+    case 1024: return launch_nv<T, 1024>(p, plan, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -306,16 +393,18 @@ cudaError_t launch_threads(const Problem& p, const softmax_plan_t& plan, cudaStr
 
 cudaError_t launch_row_slices(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
 {
+    if (plan.bulk_copy && (plan.stages < 1 || plan.stages > kMaxStages))
+        return cudaErrorInvalidValue;
     return p.dtype == SOFTMAX_F32 ? launch_threads<float>(p, plan, s)
                                   : launch_threads<BF16Bits>(p, plan, s);
 }
 
 int max_cluster_size_row_slices()
 {
-    auto* k = row_slices_kernel<float, 512, true, true>;
+    auto* k = row_slices_kernel<float, 512, 8, true, true>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
         return 8;
-    const int smem = 96 * 1024;
+    const int smem = 64 * 1024;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return 8;
     cudaLaunchConfig_t cfg = {};

@@ -182,11 +182,11 @@ int softmax_plan_format(const softmax_plan_t* plan, char* buf, size_t len)
     const char* name = (plan->path >= 0 && plan->path <= 3) ? names[plan->path] : "?";
     return std::snprintf(buf, len,
                          "path=%s dtype=%s vec=%d out_vec=%d bulk=%d threads=%d cluster=%d "
-                         "rows_per_warp=%d chunks=%d slice_cols=%lld smem=%d grid=%lld",
+                         "rows_per_warp=%d chunks=%d slice_cols=%lld stages=%d smem=%d grid=%lld",
                          name, plan->dtype == SOFTMAX_F32 ? "f32" : "bf16", plan->vec,
                          plan->out_vec, plan->bulk_copy, plan->threads, plan->cluster,
                          plan->rows_per_warp, plan->chunks,
-                         static_cast<long long>(plan->slice_cols), plan->smem_bytes,
+                         static_cast<long long>(plan->slice_cols), plan->stages, plan->smem_bytes,
                          static_cast<long long>(plan->grid));
 }
 
@@ -211,6 +211,28 @@ int softmax_rows_path(const void* in, void* out, int64_t n_rows, int64_t n_cols,
     if (ps != SOFTMAX_OK)
         return ps;
     return rwsm::launch_path(p, plan, static_cast<cudaStream_t>(stream));
+}
+
+int softmax_rows_planned(const void* in, void* out, int64_t n_rows, int64_t n_cols,
+                         int64_t in_row_stride, int64_t out_row_stride, int dtype,
+                         const softmax_plan_t* plan, void* stream)
+{
+    if (!plan)
+        return SOFTMAX_ERR_INVALID_ARG;
+    const int st = rwsm::validate(in, out, n_rows, n_cols, in_row_stride, out_row_stride, dtype);
+    if (st != SOFTMAX_OK)
+        return st;
+    if (n_rows == 0 || n_cols == 0)
+        return SOFTMAX_OK;
+    softmax_device_desc_t d;
+    const int ds = rwsm::current_device(&d);
+    if (ds != SOFTMAX_OK)
+        return ds;
+    const Problem p{in, out, n_rows, n_cols, in_row_stride, out_row_stride, dtype};
+    const int cs = rwsm::check_plan(d, p, *plan);
+    if (cs != SOFTMAX_OK)
+        return cs;
+    return rwsm::launch_path(p, *plan, static_cast<cudaStream_t>(stream));
 }
 
 int softmax_rows(const void* in, void* out, int64_t n_rows, int64_t n_cols,

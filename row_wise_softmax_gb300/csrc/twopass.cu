@@ -68,8 +68,8 @@ twopass_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_i
             float s = 0.0f;
 #pragma unroll
             for (int i = 0; i < kTwoPassBatch * VEC; ++i)
-                s += exp_fast(x[i] - ref);
-            l = l * exp_fast(m - ref) + s;
+                s += exp_biased(x[i] - ref);
+            l = l * exp_ftz(m - ref) + s;
             m = mn;
         }
         cta_ml_reduce<THREADS>(m, l, red_m, red_l);
@@ -83,7 +83,7 @@ twopass_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_i
             load_vec_masked<T, VEC>(src, v * VEC, len, x);
 #pragma unroll
             for (int j = 0; j < VEC; ++j)
-                x[j] = exp_fast(x[j] - m);
+                x[j] = exp_biased(x[j] - m);
             store_vec_masked<T, VEC>(dst, v * VEC, len, x, inv);
         }
         __syncthreads();                       // red_* reused by the next row

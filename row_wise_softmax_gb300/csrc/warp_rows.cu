@@ -1,9 +1,10 @@
 // WARP path: one warp owns whole rows of up to 1024 columns, held in
 // registers.  Each lane loads VEC-wide vectors at columns (c*32 + lane)*VEC,
 // so every load and store instruction of the warp covers 32*VEC consecutive
-// elements of a row (coalesced).  A warp keeps ROWS rows in flight: all their
-// loads are issued before the first reduction, which gives the memory system
-// ROWS*VEC*CHUNKS*4 bytes per lane to work on.
+// elements of a row (coalesced).  A warp works on a group of ROWS rows at a
+// time and is software-pipelined: the loads of its next group are issued
+// before the current group is reduced and stored, so each warp keeps a group
+// of rows in flight from HBM while it computes.
 //
 // Per row: m = max (lanes, then __shfl_xor tree), e = exp(x - m) in place,
 // l = sum (lanes, then tree), y = e * (1/l).  This is the fused softmax of
@@ -23,55 +24,87 @@ namespace rwsm {
 constexpr int kWarpPathThreads = 128;
 
 template <typename T, int VEC, int CHUNKS, int ROWS>
+__device__ __forceinline__ void load_group(const T* in, int64_t g, int64_t n_rows, int n_cols,
+                                           int64_t ld_in, int lane, float (&v)[ROWS][VEC * CHUNKS])
+{
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        const int64_t row = g * ROWS + r;
+        if (row < n_rows) {
+            const T* src = in + row * ld_in;
+#pragma unroll
+            for (int c = 0; c < CHUNKS; ++c)
+                load_vec_masked<T, VEC>(src, (c * 32 + lane) * VEC, n_cols, &v[r][c * VEC]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < VEC * CHUNKS; ++k)
+                v[r][k] = kNegInf;
+        }
+    }
+}
+
+template <typename T, int VEC, int CHUNKS, int ROWS>
+__device__ __forceinline__ void softmax_group(T* out, int64_t g, int64_t n_rows, int n_cols,
+                                              int64_t ld_out, int lane, float (&v)[ROWS][VEC * CHUNKS])
+{
+    constexpr int E = VEC * CHUNKS;
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        const int64_t row = g * ROWS + r;
+        float m = kNegInf;
+#pragma unroll
+        for (int k = 0; k < E; ++k)
+            m = fmaxf(m, v[r][k]);
+        m = warp_max(m);
+        float l = 0.0f;
+#pragma unroll
+        for (int k = 0; k < E; ++k) {
+            v[r][k] = exp_biased(v[r][k] - m);
+            l += v[r][k];
+        }
+        l = warp_sum(l);
+        const float inv = 1.0f / l;
+        if (row < n_rows) {
+            T* dst = out + row * ld_out;
+#pragma unroll
+            for (int c = 0; c < CHUNKS; ++c)
+                store_vec_masked<T, VEC>(dst, (c * 32 + lane) * VEC, n_cols, &v[r][c * VEC], inv);
+        }
+    }
+}
+
+template <typename T, int VEC, int CHUNKS, int ROWS>
 __global__ void __launch_bounds__(kWarpPathThreads)
 warp_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols,
                  int64_t ld_in, int64_t ld_out)
 {
-    constexpr int E = VEC * CHUNKS;            // elements per lane per row
+    constexpr int E = VEC * CHUNKS;
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int64_t n_groups = (n_rows + ROWS - 1) / ROWS;
+    if (warp0 >= n_groups)
+        return;
 
-    for (int64_t g = warp0; g < n_groups; g += n_warps) {
-        float v[ROWS][E];
-#pragma unroll
-        for (int r = 0; r < ROWS; ++r) {
-            const int64_t row = g * ROWS + r;
-            if (row < n_rows) {
-                const T* src = in + row * ld_in;
-#pragma unroll
-                for (int c = 0; c < CHUNKS; ++c)
-                    load_vec_masked<T, VEC>(src, (c * 32 + lane) * VEC, n_cols, &v[r][c * VEC]);
-            } else {
-#pragma unroll
-                for (int k = 0; k < E; ++k)
-                    v[r][k] = kNegInf;
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < ROWS; ++r) {
-            const int64_t row = g * ROWS + r;
-            float m = kNegInf;
-#pragma unroll
-            for (int k = 0; k < E; ++k)
-                m = fmaxf(m, v[r][k]);
-            m = warp_max(m);
-            float l = 0.0f;
-#pragma unroll
-            for (int k = 0; k < E; ++k) {
-                v[r][k] = exp_fast(v[r][k] - m);
-                l += v[r][k];
-            }
-            l = warp_sum(l);
-            const float inv = 1.0f / l;
-            if (row < n_rows) {
-                T* dst = out + row * ld_out;
-#pragma unroll
-                for (int c = 0; c < CHUNKS; ++c)
-                    store_vec_masked<T, VEC>(dst, (c * 32 + lane) * VEC, n_cols, &v[r][c * VEC], inv);
-            }
-        }
+    // Two register buffers, A and B, alternate: while one group is reduced
+    // and stored, the loads of the next group are already in flight.
+    float a[ROWS][E], b[ROWS][E];
+    int64_t g = warp0;
+    load_group<T, VEC, CHUNKS, ROWS>(in, g, n_rows, n_cols, ld_in, lane, a);
+    while (true) {
+        const int64_t gb = g + n_warps;
+        if (gb < n_groups)
+            load_group<T, VEC, CHUNKS, ROWS>(in, gb, n_rows, n_cols, ld_in, lane, b);
+        softmax_group<T, VEC, CHUNKS, ROWS>(out, g, n_rows, n_cols, ld_out, lane, a);
+        if (gb >= n_groups)
+            break;
+        const int64_t ga = gb + n_warps;
+        if (ga < n_groups)
+            load_group<T, VEC, CHUNKS, ROWS>(in, ga, n_rows, n_cols, ld_in, lane, a);
+        softmax_group<T, VEC, CHUNKS, ROWS>(out, gb, n_rows, n_cols, ld_out, lane, b);
+        if (ga >= n_groups)
+            break;
+        g = ga;
     }
 }
 

@@ -53,35 +53,45 @@ def test_scheduler_paths_for_the_five_workloads(lib):
     p = plan(128, 1000)
     assert (p.path, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 4, 8, 1)
     p = plan(4096, 4096)
-    assert (p.path, p.cluster, p.bulk_copy, p.out_vec, p.smem_bytes) == (rws.PATH_CTA, 1, 1, 4, 16384)
-    assert p.grid == 4096
+    assert (p.path, p.cluster, p.bulk_copy, p.out_vec) == (rws.PATH_CTA, 1, 1, 4)
+    assert (p.threads, p.chunks, p.stages, p.smem_bytes, p.grid) == (128, 8, 4, 65536, 0)
     p = plan(32768, 1024, dtype=rws.BF16)
     assert (p.path, p.vec, p.chunks) == (rws.PATH_WARP, 8, 4)
     p = plan(262144, 127, in_row_stride=128, out_row_stride=127)
     assert (p.path, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 1, 4, 4)
     p = plan(256, 262144)
     assert (p.path, p.cluster, p.slice_cols, p.smem_bytes) == (rws.PATH_CLUSTER, 16, 16384, 65536)
-    assert p.grid == 256 * 16 and p.threads == 512
+    assert (p.threads, p.chunks, p.stages, p.grid) == (512, 8, 1, 0)
 
 
 def test_scheduler_boundaries(lib):
     assert plan(1, 1024).path == rws.PATH_WARP
     assert plan(1, 1025).path == rws.PATH_CTA
-    assert plan(1, 16384).path == rws.PATH_CTA            # 64 KB row
-    assert plan(1, 16385).path == rws.PATH_CLUSTER
-    assert plan(1, 16385).cluster == 2
-    assert plan(1, 32768, dtype=rws.BF16).path == rws.PATH_CTA
-    big = plan(1, 16 * 24576)                             # 16 slices of 96 KB
-    assert big.path == rws.PATH_CLUSTER and big.cluster == 16
-    assert plan(1, 16 * 24576 + 4).path == rws.PATH_TWOPASS
+    assert plan(1, 8192).path == rws.PATH_CTA             # 32 KB row
+    p = plan(1, 8193)
+    assert p.path == rws.PATH_CLUSTER and p.cluster == 2
+    assert plan(1, 16384, dtype=rws.BF16).path == rws.PATH_CTA
+    assert plan(1, 16385, dtype=rws.BF16).path == rws.PATH_CLUSTER
+    big = plan(1, 16 * 32768)                             # 16 slices of 128 KB
+    assert big.path == rws.PATH_CLUSTER and big.cluster == 16 and big.threads == 1024
+    assert big.stages == 1 and big.smem_bytes == 131072
+    assert plan(1, 16 * 32768 + 4).path == rws.PATH_TWOPASS
+    assert plan(1, 16 * 32768, dtype=rws.BF16).path == rws.PATH_CLUSTER
+    assert plan(1, 16 * 32768 + 8, dtype=rws.BF16).path == rws.PATH_TWOPASS
     tp = plan(3, 10_000_000)
     assert tp.path == rws.PATH_TWOPASS and tp.cluster == 16 and tp.grid == 0
+    for n in (1025, 3000, 4096, 5000, 8192, 8193, 20000, 262144, 524288):
+        q = plan(2, n)
+        if q.path in (rws.PATH_CTA, rws.PATH_CLUSTER):
+            assert q.threads * q.chunks * 4 >= q.slice_cols          # slice fits registers
+            assert q.stages * q.slice_cols * 4 == q.smem_bytes
+            assert q.smem_bytes <= rws.GB300["max_smem_per_block_optin"] - 2048
 
 
 def test_scheduler_alignment_fallbacks(lib):
-    # Unaligned input pointer: no bulk copy; unaligned output stride: scalar stores.
+    # Unaligned input pointer: no bulk copy, no ring; unaligned output stride: scalar stores.
     p = plan(64, 4096, in_ptr=(1 << 20) + 4)
-    assert p.path == rws.PATH_CTA and p.bulk_copy == 0
+    assert p.path == rws.PATH_CTA and p.bulk_copy == 0 and p.stages == 0 and p.smem_bytes == 0
     p = plan(64, 4096, out_row_stride=4097)
     assert p.bulk_copy == 1 and p.out_vec == 1
     p = plan(64, 1000, in_row_stride=1001)
@@ -100,8 +110,8 @@ def test_scheduler_forced_paths(lib):
     assert e.value.status == rws.ERR_UNSUPPORTED
     small_cluster = dict(GB, max_cluster=8)
     p = rws.plan_for_device(small_cluster, 4, 262144)
-    assert p.path == rws.PATH_CLUSTER and p.cluster == 8 and p.smem_bytes == 131072 or \
-        p.path == rws.PATH_TWOPASS
+    assert p.path == rws.PATH_CLUSTER and p.cluster == 8 and p.slice_cols == 32768
+    assert p.threads == 1024 and p.stages == 1
 
 
 def test_validation(lib):

@@ -102,7 +102,7 @@ def test_many_rows_per_cta_or_cluster(path):
 
 
 def test_twopass_long_row_automatic():
-    # 16 slices of 96 KB are the cluster's cap: longer rows stream twice.
+    # 16 slices of 128 KB are the cluster path's cap: longer rows stream twice.
     w = wl.random_rows(3, 1_600_000, seed=5, scale=2.0)
     p = rws.plan(w.n_rows, w.n_cols)
     assert p.path == rws.PATH_TWOPASS
@@ -135,3 +135,63 @@ def test_deterministic_run_to_run():
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
     w5 = wl.long_f32(3)
     assert np.array_equal(run(w5).view(np.uint32), run(w5).view(np.uint32))
+
+
+def _planned(w, plan):
+    x = parity.device_input(w)
+    y = parity.empty_output(w)
+    st = rws.softmax_rows_planned_ptr(x.data_ptr(), y.data_ptr(), w.n_rows, w.n_cols,
+                                      w.in_row_stride, w.out_row_stride, w.dtype, plan)
+    torch.cuda.synchronize()
+    return st, parity.host_output(y, w)
+
+
+def test_planned_launch_shapes():
+    w = wl.masked_f32(300)
+    want = parity.expected(w)
+    base = rws.plan(w.n_rows, w.n_cols)
+    for threads, chunks in ((128, 8), (256, 4), (512, 2), (1024, 1), (1024, 8)):
+        for stages in (1, 2, 3, 8):
+            q = rws.Plan.from_buffer_copy(base)
+            q.threads, q.chunks, q.stages = threads, chunks, stages
+            q.smem_bytes = stages * q.slice_cols * 4
+            st, got = _planned(w, q)
+            assert st == rws.OK, str(q)
+            parity.compare(got, want, wl.F32, str(q))
+    q = rws.Plan.from_buffer_copy(base)
+    q.grid = 7                                    # explicit, non-whole-wave grid still correct
+    st, got = _planned(w, q)
+    assert st == rws.OK
+    parity.compare(got, want, wl.F32, "grid 7")
+    w5 = wl.long_f32(5)
+    b5 = rws.plan(w5.n_rows, w5.n_cols)
+    for cs in (8, 16):
+        q = rws.Plan.from_buffer_copy(b5)
+        q.cluster = cs
+        q.slice_cols = w5.n_cols // cs
+        q.threads = 1024 if cs == 8 else 512
+        q.chunks = 8
+        q.stages = 1
+        q.smem_bytes = q.slice_cols * 4
+        st, got = _planned(w5, q)
+        assert st == rws.OK, str(q)
+        parity.compare(got, parity.expected(w5), wl.F32, str(q))
+
+
+def test_planned_rejects_unsafe_plans():
+    w = wl.masked_f32(8)
+    base = rws.plan(w.n_rows, w.n_cols)
+    before = rws.launch_count()
+    bad = []
+    q = rws.Plan.from_buffer_copy(base); q.slice_cols = 2048; bad.append(q)        # row not covered
+    q = rws.Plan.from_buffer_copy(base); q.threads = 128; q.chunks = 2; bad.append(q)  # slice > regs
+    q = rws.Plan.from_buffer_copy(base); q.stages = 9; q.smem_bytes = 9 * 16384; bad.append(q)
+    q = rws.Plan.from_buffer_copy(base); q.smem_bytes = 1024; bad.append(q)        # smem mismatch
+    q = rws.Plan.from_buffer_copy(base); q.threads = 96; bad.append(q)
+    q = rws.Plan.from_buffer_copy(base); q.path = rws.PATH_WARP; bad.append(q)     # 4096 > 1024
+    q = rws.Plan.from_buffer_copy(base); q.dtype = rws.BF16; bad.append(q)
+    q = rws.Plan.from_buffer_copy(base); q.cluster = 2; bad.append(q)              # CTA with cluster
+    for q in bad:
+        st, _ = _planned(w, q)
+        assert st == rws.ERR_INVALID_ARG, str(q)
+    assert rws.launch_count() == before
