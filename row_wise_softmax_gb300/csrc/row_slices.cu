@@ -37,6 +37,9 @@ __device__ unsigned g_error_row_slices = 0;
 
 constexpr int kMaxStages = 8;
 constexpr uint32_t kBulkChunkBytes = 32768;
+// The ring starts at the first 128-byte boundary of dynamic shared memory;
+// launches request this much slack on top of the plan's ring size.
+constexpr int kRingAlign = 128;
 
 template <typename T>
 __device__ __forceinline__ void set_neg_inf(T* dst)
@@ -94,7 +97,8 @@ row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in
     const int bulk_elems = static_cast<int>(bulk_bytes / sizeof(T));
     const int tail_vec = bulk_elems < len ? bulk_elems / VEC : -1;   // vector patched from HBM
 
-    T* ring = reinterpret_cast<T*>(smem_raw);
+    T* ring = reinterpret_cast<T*>((reinterpret_cast<uintptr_t>(smem_raw) + (kRingAlign - 1)) &
+                                   ~static_cast<uintptr_t>(kRingAlign - 1));
     auto stage_ptr = [&](int s) { return ring + static_cast<int64_t>(s) * slice_cols; };
     auto issue = [&](int s, int64_t row) {      // thread 0 only
         const uint32_t bar = smem_addr(&full[s]);
@@ -172,15 +176,15 @@ row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in
                     issue(s, next);
             }
         } else {
+            // Input rows not 16-byte aligned: element loads only (same
+            // register layout as the vector path).
 #pragma unroll
             for (int k = 0; k < NV; ++k) {
                 const int v = tid + k * THREADS;
-                if (v < nv) {
-                    load_vec_masked<T, VEC>(src, v * VEC, len, &x[k * VEC]);
-                } else {
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j)
-                        x[k * VEC + j] = kNegInf;
+                for (int j = 0; j < VEC; ++j) {
+                    const int e = v * VEC + j;
+                    x[k * VEC + j] = (v < nv && e < len) ? Elem<T>::load1(src + e) : kNegInf;
                 }
             }
         }
@@ -295,11 +299,12 @@ cudaError_t launch_rs(const Problem& p, const softmax_plan_t& plan, cudaStream_t
         return err;
     if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
-    if (attrs.smem_set[dev].load() < plan.smem_bytes) {
-        err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem_bytes);
+    const int smem = plan.bulk_copy ? plan.smem_bytes + kRingAlign : 0;
+    if (attrs.smem_set[dev].load() < smem) {
+        err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (err != cudaSuccess)
             return err;
-        attrs.smem_set[dev].store(plan.smem_bytes);
+        attrs.smem_set[dev].store(smem);
     }
     if (!attrs.flags_set[dev].load()) {
         err = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -323,7 +328,7 @@ cudaError_t launch_rs(const Problem& p, const softmax_plan_t& plan, cudaStream_t
             cudaLaunchConfig_t q = {};
             q.gridDim = dim3(static_cast<unsigned>(cs), 1, 1);
             q.blockDim = dim3(THREADS, 1, 1);
-            q.dynamicSmemBytes = static_cast<size_t>(plan.smem_bytes);
+            q.dynamicSmemBytes = static_cast<size_t>(smem);
             q.attrs = attr;
             q.numAttrs = 1;
             if (cudaOccupancyMaxActiveClusters(&active, k, &q) != cudaSuccess) {
@@ -331,7 +336,7 @@ cudaError_t launch_rs(const Problem& p, const softmax_plan_t& plan, cudaStream_t
                 active = 0;
             }
         } else {
-            active = resident_ctas(reinterpret_cast<const void*>(k), THREADS, plan.smem_bytes);
+            active = resident_ctas(reinterpret_cast<const void*>(k), THREADS, smem);
         }
         if (active < 1)
             active = 1;
@@ -340,7 +345,7 @@ cudaError_t launch_rs(const Problem& p, const softmax_plan_t& plan, cudaStream_t
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * cs), 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = static_cast<size_t>(plan.smem_bytes);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = cs > 1 ? 1 : 0;
@@ -404,7 +409,7 @@ int max_cluster_size_row_slices()
     auto* k = row_slices_kernel<float, 512, 8, true, true>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
         return 8;
-    const int smem = 64 * 1024;
+    const int smem = 64 * 1024 + kRingAlign;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return 8;
     cudaLaunchConfig_t cfg = {};
