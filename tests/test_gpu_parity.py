@@ -75,6 +75,14 @@ def test_closed_forms_on_gpu():
 SWEEP_COLS = [1, 2, 3, 4, 5, 7, 8, 9, 31, 32, 33, 63, 64, 65, 100, 127, 128, 129, 255, 256, 257,
               511, 513, 1000, 1023, 1024, 1025, 2047, 2049, 4095, 4096, 4097, 8191, 16385, 40000]
 PATHS = [rws.PATH_WARP, rws.PATH_CTA, rws.PATH_CLUSTER, rws.PATH_TWOPASS]
+CTA_CAPACITY_COLS = 32768        # a CTA holds at most 32 elements x 1024 threads
+
+
+def test_forced_cta_beyond_capacity_is_unsupported():
+    with pytest.raises(rws.SoftmaxError) as e:
+        rws.plan(2, CTA_CAPACITY_COLS + 4, path=rws.PATH_CTA)
+    assert e.value.status == rws.ERR_UNSUPPORTED
+    assert rws.plan(2, CTA_CAPACITY_COLS, path=rws.PATH_CTA).path == rws.PATH_CTA
 
 
 @pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
@@ -83,6 +91,8 @@ def test_shape_sweep_forced_paths(dtype, path):
     checked = 0
     for i, n_cols in enumerate(SWEEP_COLS):
         if path == rws.PATH_WARP and n_cols > 1024:
+            continue
+        if path == rws.PATH_CTA and n_cols > CTA_CAPACITY_COLS:
             continue
         for n_rows in (1, 3, 7):
             w = wl.random_rows(n_rows, n_cols, dtype=dtype, seed=1000 + i, scale=4.0)
@@ -124,7 +134,7 @@ def test_reduced_workloads_every_path():
         for path in PATHS:
             if path == rws.PATH_WARP and w.n_cols > 1024:
                 continue
-            if path == rws.PATH_CTA and w.n_cols * w.elem_bytes > 200_000:
+            if path == rws.PATH_CTA and w.n_cols > CTA_CAPACITY_COLS:
                 continue
             parity.compare(run(w, path), want, w.dtype, "%s/%s" % (name, rws.PATH_NAMES[path]))
 
