@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libsoftmax.so")
 
-SOURCES = ["softmax_abi.cu", "plan.cpp", "warp_rows.cu", "row_slices.cu", "twopass.cu"]
+SOURCES = ["softmax_abi.cu", "plan.cpp", "warp_rows.cu", "tile_rows.cu", "row_slices.cu",
+           "twopass.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "kernels.h")] + [
     os.path.join(INCLUDE, "softmax.h")]
 

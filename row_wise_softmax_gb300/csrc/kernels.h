@@ -27,6 +27,7 @@ int check_plan(const softmax_device_desc_t& dev, const Problem& p, const softmax
 
 // Launchers, one per path (each in its own translation unit).
 cudaError_t launch_warp_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
+cudaError_t launch_tile_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
 cudaError_t launch_row_slices(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
 cudaError_t launch_twopass(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
 
@@ -36,6 +37,7 @@ int max_cluster_size_row_slices();
 // Error words of the translation units that wait on mbarriers: read and
 // optionally clear (host side, after the device has been synchronised).
 unsigned read_error_row_slices(bool clear);
+unsigned read_error_tile_rows(bool clear);
 cudaError_t launch_selftest_wait(cudaStream_t s);
 
 // Helpers implemented in softmax_abi.cu.

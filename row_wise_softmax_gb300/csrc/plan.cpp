@@ -31,6 +31,8 @@ constexpr int64_t kRingBudgetBytes = 64 * 1024;    // shared memory for the ring
 constexpr int kMaxStages = 8;                       // must match row_slices.cu
 constexpr int kMaxSliceThreads = 1024;
 constexpr int kSmemReserve = 2048;                  // static smem + slack
+constexpr int64_t kTileStageBytes = 16 * 1024;     // WARP path (staged): rows per stage
+constexpr int64_t kTileMaxRowsPerWarp = 16;
 
 int esize(int dtype) { return dtype == SOFTMAX_F32 ? 4 : 2; }
 
@@ -206,13 +208,35 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
     case SOFTMAX_PATH_WARP: {
         if (p.n_cols > kWarpMaxCols)
             return SOFTMAX_ERR_UNSUPPORTED;
-        q.vec = (in_al && out_al) ? vmax : 1;
-        q.out_vec = q.vec;
-        q.chunks = static_cast<int>(pow2_ceil(ceil_div(p.n_cols, 32 * q.vec)));
-        q.rows_per_warp = warp_rows_for(q.vec * q.chunks);
         q.threads = 128;
-        q.slice_cols = p.n_cols;
         q.grid = 0;
+        if (in_al) {
+            // Staged tile kernel: stages of 4 * rows_per_warp rows of
+            // row_pad elements (about 16 KB), about 64 KB of ring per CTA.
+            const int64_t row_pad = round_up(p.n_cols, vmax);
+            const int64_t row_bytes_pad = row_pad * esz;
+            int64_t rpw = pow2_floor(kTileStageBytes / (4 * row_bytes_pad) > 0
+                                         ? kTileStageBytes / (4 * row_bytes_pad) : 1);
+            if (rpw > kTileMaxRowsPerWarp)
+                rpw = kTileMaxRowsPerWarp;
+            const int64_t stage_bytes = 4 * rpw * row_bytes_pad;
+            int64_t stages = kRingBudgetBytes / stage_bytes;
+            stages = stages < 1 ? 1 : (stages > kMaxStages ? kMaxStages : stages);
+            q.bulk_copy = 1;
+            q.vec = out_al ? vmax : 1;
+            q.out_vec = q.vec;
+            q.chunks = static_cast<int>(pow2_ceil(ceil_div(p.n_cols, 32 * q.vec)));
+            q.rows_per_warp = static_cast<int>(rpw);
+            q.slice_cols = row_pad;
+            q.stages = static_cast<int>(stages);
+            q.smem_bytes = static_cast<int>(stages * stage_bytes);
+        } else {
+            q.vec = (in_al && out_al) ? vmax : 1;
+            q.out_vec = q.vec;
+            q.chunks = static_cast<int>(pow2_ceil(ceil_div(p.n_cols, 32 * q.vec)));
+            q.rows_per_warp = warp_rows_for(q.vec * q.chunks);
+            q.slice_cols = p.n_cols;
+        }
         break;
     }
     case SOFTMAX_PATH_CTA:
@@ -288,12 +312,22 @@ int check_plan(const softmax_device_desc_t& dev, const Problem& p, const softmax
     auto vec_ok = [&](int v, bool aligned) { return v == 1 || (v == vmax && aligned); };
     switch (q.path) {
     case SOFTMAX_PATH_WARP: {
-        if (p.n_cols > kWarpMaxCols || !vec_ok(q.vec, in_al && out_al) || q.out_vec != q.vec)
+        if (p.n_cols > kWarpMaxCols || q.out_vec != q.vec || q.grid > 0x7fffffff)
             return SOFTMAX_ERR_INVALID_ARG;
         if (!pow2_in(q.chunks, 1, 32) || q.vec * q.chunks > 32 ||
             int64_t{32} * q.vec * q.chunks < p.n_cols)
             return SOFTMAX_ERR_INVALID_ARG;
-        if (q.grid > 0x7fffffff)
+        if (q.bulk_copy == 0)
+            return vec_ok(q.vec, in_al && out_al) ? SOFTMAX_OK : SOFTMAX_ERR_INVALID_ARG;
+        // Staged tile kernel.
+        const int64_t row_pad = round_up(p.n_cols, vmax);
+        if (q.bulk_copy != 1 || !in_al || !vec_ok(q.vec, out_al) || q.slice_cols != row_pad ||
+            q.rows_per_warp < 1 || q.rows_per_warp > kTileMaxRowsPerWarp ||
+            q.stages < 1 || q.stages > kMaxStages || q.threads != 128)
+            return SOFTMAX_ERR_INVALID_ARG;
+        const int64_t stage_bytes = 4 * int64_t{q.rows_per_warp} * row_pad * esz;
+        if (stage_bytes >= (1 << 20) || q.smem_bytes != q.stages * stage_bytes ||
+            q.smem_bytes > smem_cap)
             return SOFTMAX_ERR_INVALID_ARG;
         return SOFTMAX_OK;
     }

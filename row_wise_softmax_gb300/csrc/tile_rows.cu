@@ -1,0 +1,256 @@
+// WARP path, staged: short rows (<= 1024 columns) whose input rows are
+// 16-byte aligned.  A persistent CTA of four warps walks tiles of R
+// consecutive rows through a ring of `stages` shared-memory buffers:
+//
+//   ring    one elected thread starts one cp.async.bulk copy per row of a tile
+//           (global -> shared, all completing on the stage's mbarrier); the
+//           last < 16 bytes of a row whose byte length is not a multiple of 16
+//           are read by the lane that owns them with a plain load.
+//   rows    each warp owns R/4 rows of the tile and reduces them one after the
+//           other straight out of shared memory: lane l reads the vectors at
+//           columns (c*32 + l)*VEC, then max (__shfl_xor), e = exp(x - max),
+//           sum (__shfl_xor), y = e * (1/sum), coalesced stores.
+//   refill  after a CTA barrier (every warp done with the tile) the stage is
+//           refilled with the tile `stages` ahead.
+//
+// Shared memory, not registers, holds the rows in flight, so an SM keeps
+// stages x R rows loading while its warps compute.  VEC is the width of the
+// output stores: 16 bytes when the output rows are 16-byte aligned, else one
+// element (then each store instruction of a warp writes 32 consecutive
+// elements).  The softmax itself is the fused kernel of "Triton: write
+// CUDA-grade GPU operators in Python", example 2, with -inf padding
+// contributing 0 as in the cs336 lecture 6 notes, "Level 1: Softmax".
+#include "common.cuh"
+#include "kernels.h"
+
+#include <atomic>
+
+namespace rwsm {
+
+__device__ unsigned g_error_tile_rows = 0;
+
+constexpr int kTileWarps = 4;
+constexpr int kTileThreads = kTileWarps * 32;
+constexpr int kTileMaxStages = 8;
+constexpr int kTileRingAlign = 128;
+
+template <typename T, int VEC>
+__device__ __forceinline__ void lds_any(const T* p, float* v)
+{
+    if constexpr (VEC == 1) {
+        if constexpr (sizeof(T) == 4)
+            v[0] = *reinterpret_cast<const float*>(p);
+        else
+            v[0] = __uint_as_float(static_cast<unsigned>(*reinterpret_cast<const unsigned short*>(p)) << 16);
+    } else {
+        lds_vec<T, VEC>(p, v);
+    }
+}
+
+template <typename T, int VEC, int CHUNKS>
+__global__ void __launch_bounds__(kTileThreads)
+tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
+                 int64_t ld_out, int rows_per_warp, int stages, int row_pad)
+{
+    constexpr int E = VEC * CHUNKS;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    __shared__ __align__(8) unsigned long long full[kTileMaxStages];
+    __shared__ unsigned issued[kTileMaxStages];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int R = kTileWarps * rows_per_warp;
+    const int64_t n_tiles = (n_rows + R - 1) / R;
+    const uint32_t row_bytes = static_cast<uint32_t>(n_cols * sizeof(T)) & ~15u;
+    const int bulk_elems = static_cast<int>(row_bytes / sizeof(T));
+
+    T* ring = reinterpret_cast<T*>((reinterpret_cast<uintptr_t>(smem_raw) + (kTileRingAlign - 1)) &
+                                   ~static_cast<uintptr_t>(kTileRingAlign - 1));
+    auto row_ptr = [&](int s, int r) { return ring + (static_cast<int64_t>(s) * R + r) * row_pad; };
+    auto issue = [&](int s, int64_t tile) {     // thread 0 only
+        const uint32_t bar = smem_addr(&full[s]);
+        const int64_t r0 = tile * R;
+        const int nr = static_cast<int>(n_rows - r0 < R ? n_rows - r0 : R);
+        fence_proxy_async_smem();
+        issued[s] += 1;
+        if (row_bytes) {
+            mbar_arrive_expect_tx(bar, row_bytes * static_cast<uint32_t>(nr));
+            for (int r = 0; r < nr; ++r)
+                bulk_g2s(smem_addr(row_ptr(s, r)), in + (r0 + r) * ld_in, row_bytes, bar);
+        } else {
+            mbar_arrive(bar);
+        }
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(smem_addr(&full[s]), 1);
+            issued[s] = 0;
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0)
+        for (int s = 0; s < stages; ++s) {
+            const int64_t t = blockIdx.x + static_cast<int64_t>(s) * gridDim.x;
+            if (t < n_tiles)
+                issue(s, t);
+        }
+
+    bool failed = false;                         // CTA-uniform
+    int64_t k = 0;
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++k) {
+        const int s = static_cast<int>(k % stages);
+        const uint32_t parity = static_cast<uint32_t>((k / stages) & 1);
+        const bool ok = failed ? true : mbar_wait_bounded(smem_addr(&full[s]), parity);
+        for (int rr = 0; rr < rows_per_warp; ++rr) {
+            const int r = warp * rows_per_warp + rr;
+            const int64_t row = tile * R + r;
+            if (row >= n_rows)
+                break;                           // warp-uniform
+            const T* sp = row_ptr(s, r);
+            const T* gp = in + row * ld_in;
+            float x[E];
+#pragma unroll
+            for (int c = 0; c < CHUNKS; ++c) {
+                const int col = (c * 32 + lane) * VEC;
+                if (col + VEC <= bulk_elems) {
+                    lds_any<T, VEC>(sp + col, &x[c * VEC]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        const int e = col + j;
+                        if (e < bulk_elems)
+                            lds_any<T, 1>(sp + e, &x[c * VEC + j]);
+                        else                                       // < 16-byte tail
+                            x[c * VEC + j] = e < n_cols ? Elem<T>::load1(gp + e) : kNegInf;
+                    }
+                }
+            }
+            float m = kNegInf;
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                m = fmaxf(m, x[e]);
+            m = warp_max(m);
+            float l = 0.0f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                x[e] = exp_biased(x[e] - m);
+                l += x[e];
+            }
+            l = warp_sum(l);
+            const float inv = 1.0f / l;
+            T* dst = out + row * ld_out;
+#pragma unroll
+            for (int c = 0; c < CHUNKS; ++c)
+                store_vec_masked<T, VEC>(dst, (c * 32 + lane) * VEC, n_cols, &x[c * VEC], inv);
+        }
+        if (__syncthreads_or(!ok))
+            failed = true;
+        if (tid == 0 && !failed) {
+            const int64_t next = tile + static_cast<int64_t>(stages) * gridDim.x;
+            if (next < n_tiles)
+                issue(s, next);
+        }
+    }
+    if (failed && tid == 0) {
+        atomicOr(&g_error_tile_rows, kErrMbarrierTimeout);
+        for (int s = 0; s < stages; ++s)
+            if (issued[s])
+                mbar_wait_bounded(smem_addr(&full[s]), (issued[s] - 1) & 1u);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+unsigned read_error_tile_rows(bool clear)
+{
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_error_tile_rows, sizeof v) != cudaSuccess)
+        return 0;
+    if (clear && v) {
+        const unsigned zero = 0;
+        cudaMemcpyToSymbol(g_error_tile_rows, &zero, sizeof zero);
+    }
+    return v;
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+template <typename T, int VEC, int CHUNKS>
+cudaError_t launch_tile(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
+{
+    auto* k = tile_rows_kernel<T, VEC, CHUNKS>;
+    static std::atomic<int> smem_set[kMaxDevices];
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    const int smem = plan.smem_bytes + kTileRingAlign;
+    if (smem_set[dev].load() < smem) {
+        err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (err != cudaSuccess)
+            return err;
+        cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+        smem_set[dev].store(smem);
+    }
+    const int64_t R = int64_t{kTileWarps} * plan.rows_per_warp;
+    const int64_t tiles = (p.n_rows + R - 1) / R;
+    int64_t grid = plan.grid;
+    if (grid <= 0) {
+        const int resident = resident_ctas(reinterpret_cast<const void*>(k), kTileThreads, smem);
+        grid = tiles < resident ? tiles : resident;
+    }
+    if (grid < 1)
+        grid = 1;
+    const int row_pad = static_cast<int>(plan.slice_cols);
+    k<<<static_cast<unsigned>(grid), kTileThreads, smem, s>>>(
+        static_cast<const T*>(p.in), static_cast<T*>(p.out), p.n_rows, static_cast<int>(p.n_cols),
+        p.ld_in, p.ld_out, plan.rows_per_warp, plan.stages, row_pad);
+    note_launch();
+    return cudaGetLastError();
+}
+
+template <typename T, int VEC>
+cudaError_t launch_chunks(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
+{
+    switch (plan.chunks) {
+    case 1: return launch_tile<T, VEC, 1>(p, plan, s);
+    case 2: return launch_tile<T, VEC, 2>(p, plan, s);
+    case 4: return launch_tile<T, VEC, 4>(p, plan, s);
+    case 8:
+        if constexpr (VEC * 8 <= 32) return launch_tile<T, VEC, 8>(p, plan, s);
+        break;
+    case 16:
+        if constexpr (VEC * 16 <= 32) return launch_tile<T, VEC, 16>(p, plan, s);
+        break;
+    case 32:
+        if constexpr (VEC * 32 <= 32) return launch_tile<T, VEC, 32>(p, plan, s);
+        break;
+    default:
+        break;
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_tile_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
+{
+    if (plan.stages < 1 || plan.stages > kTileMaxStages)
+        return cudaErrorInvalidValue;
+    if (p.dtype == SOFTMAX_F32) {
+        if (plan.vec == 4) return launch_chunks<float, 4>(p, plan, s);
+        if (plan.vec == 1) return launch_chunks<float, 1>(p, plan, s);
+    } else {
+        if (plan.vec == 8) return launch_chunks<BF16Bits, 8>(p, plan, s);
+        if (plan.vec == 1) return launch_chunks<BF16Bits, 1>(p, plan, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace rwsm

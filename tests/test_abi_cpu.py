@@ -51,14 +51,17 @@ def plan(n_rows, n_cols, **kw):
 
 def test_scheduler_paths_for_the_five_workloads(lib):
     p = plan(128, 1000)
-    assert (p.path, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 4, 8, 1)
+    assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 1, 4, 8, 1)
+    assert (p.stages, p.slice_cols, p.smem_bytes) == (4, 1000, 64000)
     p = plan(4096, 4096)
     assert (p.path, p.cluster, p.bulk_copy, p.out_vec) == (rws.PATH_CTA, 1, 1, 4)
     assert (p.threads, p.chunks, p.stages, p.smem_bytes, p.grid) == (128, 8, 4, 65536, 0)
     p = plan(32768, 1024, dtype=rws.BF16)
-    assert (p.path, p.vec, p.chunks) == (rws.PATH_WARP, 8, 4)
+    assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 1, 8, 4, 2)
+    assert (p.stages, p.smem_bytes) == (4, 65536)
     p = plan(262144, 127, in_row_stride=128, out_row_stride=127)
-    assert (p.path, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 1, 4, 4)
+    assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 1, 1, 4, 8)
+    assert (p.slice_cols, p.stages, p.smem_bytes) == (128, 4, 65536)
     p = plan(256, 262144)
     assert (p.path, p.cluster, p.slice_cols, p.smem_bytes) == (rws.PATH_CLUSTER, 16, 16384, 65536)
     assert (p.threads, p.chunks, p.stages, p.grid) == (512, 8, 1, 0)
@@ -95,7 +98,9 @@ def test_scheduler_alignment_fallbacks(lib):
     p = plan(64, 4096, out_row_stride=4097)
     assert p.bulk_copy == 1 and p.out_vec == 1
     p = plan(64, 1000, in_row_stride=1001)
-    assert p.path == rws.PATH_WARP and p.vec == 1 and p.chunks == 32
+    assert p.path == rws.PATH_WARP and p.bulk_copy == 0 and p.vec == 1 and p.chunks == 32
+    p = plan(64, 1000, out_row_stride=1001)          # staged input, scalar coalesced stores
+    assert p.path == rws.PATH_WARP and p.bulk_copy == 1 and p.vec == 1 and p.chunks == 32
 
 
 def test_scheduler_forced_paths(lib):
