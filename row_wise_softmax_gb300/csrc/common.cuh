@@ -239,6 +239,54 @@ __device__ __forceinline__ void lds_vec(const T* p, float* v)
     }
 }
 
+// ------------------------------------------------- L2 eviction priorities
+// Cache policies for loads and stores that should stay in L2 (evict_last:
+// data read again soon) or leave it first (evict_first: streamed once).
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 16-byte load / store with an L2 cache policy (p 16-byte aligned).
+template <typename T>
+__device__ __forceinline__ void load16_hint(const T* p, float* v, uint64_t pol)
+{
+    unsigned a, b, c, d;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "l"(p), "l"(pol));
+    if constexpr (sizeof(T) == 4) {
+        v[0] = __uint_as_float(a); v[1] = __uint_as_float(b);
+        v[2] = __uint_as_float(c); v[3] = __uint_as_float(d);
+    } else {
+        unpack_bf16x2(a, v[0], v[1]); unpack_bf16x2(b, v[2], v[3]);
+        unpack_bf16x2(c, v[4], v[5]); unpack_bf16x2(d, v[6], v[7]);
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void store16_hint(T* p, const float* v, float scale, uint64_t pol)
+{
+    unsigned a, b, c, d;
+    if constexpr (sizeof(T) == 4) {
+        a = __float_as_uint(v[0] * scale); b = __float_as_uint(v[1] * scale);
+        c = __float_as_uint(v[2] * scale); d = __float_as_uint(v[3] * scale);
+    } else {
+        a = pack_bf16x2(v[0] * scale, v[1] * scale); b = pack_bf16x2(v[2] * scale, v[3] * scale);
+        c = pack_bf16x2(v[4] * scale, v[5] * scale); d = pack_bf16x2(v[6] * scale, v[7] * scale);
+    }
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;"
+                 :: "l"(p), "r"(a), "r"(b), "r"(c), "r"(d), "l"(pol) : "memory");
+}
+
 // ------------------------------------------------- mbarrier + bulk copies
 __device__ __forceinline__ uint32_t smem_addr(const void* p)
 {

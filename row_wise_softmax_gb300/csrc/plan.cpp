@@ -6,9 +6,11 @@
 //   WARP     n_cols <= 1024: a warp owns rows in registers (short rows).
 //   CTA      row <= 32 KB: a persistent CTA walks rows through a ring of
 //            shared-memory stages (cp.async.bulk), each row held in registers.
-//   CLUSTER  longer rows up to 16 slices of <= 128 KB (fp32) / 64 KB (bf16):
-//            a cluster per row, slices on different SMs, one HBM pass.
-//   TWOPASS  anything longer: a cluster streams the row twice.
+//   CLUSTER  longer rows up to 16 slices of <= 32 KB: a cluster per row,
+//            slices on different SMs, one HBM pass.  (When forced, slices up
+//            to 128 KB fp32 / 64 KB bf16 per CTA.)
+//   TWOPASS  anything longer: a cluster streams the row twice, the second
+//            read mostly from L2.
 // Slices are kept at <= 32 KB when a cluster of <= 16 CTAs allows it; the ring
 // gets about 64 KB of shared memory per CTA, so two or three CTAs stay resident
 // per SM (228 KB of shared memory each on GB300) with several slices in flight.
@@ -27,7 +29,8 @@ namespace {
 
 constexpr int64_t kWarpMaxCols = 1024;
 constexpr int64_t kSliceTargetBytes = 32 * 1024;   // preferred slice (CTA path: whole row)
-constexpr int64_t kRingBudgetBytes = 64 * 1024;    // shared memory for the ring, per CTA
+constexpr int64_t kRingBudgetBytes = 32 * 1024;    // shared memory for the slice ring, per CTA
+constexpr int64_t kTileRingBudgetBytes = 48 * 1024; // shared memory for the tile ring, per CTA
 constexpr int kMaxStages = 8;                       // must match row_slices.cu
 constexpr int kMaxSliceThreads = 1024;
 constexpr int kSmemReserve = 2048;                  // static smem + slack
@@ -73,13 +76,14 @@ int max_vectors_per_thread(int esz) { return esz == 4 ? 8 : 4; }
 // Columns one CTA of the slice kernel can hold in registers.
 int64_t slice_capacity(int esz) { return int64_t{kMaxSliceThreads} * max_vectors_per_thread(esz) * (16 / esz); }
 
-// Threads and vectors per thread for a slice of nvec 16-byte vectors: as
-// few threads as hold the slice at the largest vectors-per-thread, at least
-// 128, then the smallest power-of-two vectors per thread that covers it.
+// Threads and vectors per thread for a slice of nvec 16-byte vectors: about
+// 16 elements per thread (more only when 1024 threads do not suffice), at
+// least 128 threads, then the smallest power-of-two vectors per thread that
+// covers the slice.
 void slice_shape(int64_t nvec, int esz, int* threads, int* nv)
 {
-    const int nvmax = max_vectors_per_thread(esz);
-    int64_t t = pow2_ceil(ceil_div(nvec, nvmax));
+    const int nv_target = esz == 4 ? 4 : 2;
+    int64_t t = pow2_ceil(ceil_div(nvec, nv_target));
     if (t < 128)
         t = 128;
     if (t > kMaxSliceThreads)
@@ -177,24 +181,28 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
 
     const int64_t cap = slice_capacity(esz);
     auto slice_cols_for = [&](int cs) { return round_up(ceil_div(p.n_cols, cs), vmax); };
-    // Smallest cluster (>= 2) whose slices fit the preferred size, else the
-    // largest cluster if its slices fit a CTA's registers.
-    auto cluster_for = [&]() -> int {
+    // Smallest cluster (>= 2) whose slices fit the preferred size; when
+    // forced, else the largest cluster if its slices fit a CTA's registers.
+    auto cluster_for = [&](bool allow_big) -> int {
         for (int cs = 2; cs <= max_cluster; cs *= 2)
             if (slice_cols_for(cs) * esz <= kSliceTargetBytes)
                 return cs;
         const int big = static_cast<int>(pow2_floor(max_cluster));
-        if (big >= 2 && slice_cols_for(big) <= cap && slice_cols_for(big) * esz <= smem_cap)
+        if (allow_big && big >= 2 && slice_cols_for(big) <= cap &&
+            slice_cols_for(big) * esz <= smem_cap)
             return big;
         return 0;
     };
 
+    // Rows whose slices would exceed 32 KB even on 16 SMs go to the two-pass
+    // kernel: on-chip staging would then hold too few rows in flight, while
+    // the second pass re-reads the row mostly from L2.
     if (path == SOFTMAX_PATH_AUTO) {
         if (p.n_cols <= kWarpMaxCols)
             path = SOFTMAX_PATH_WARP;
         else if (row_bytes <= kSliceTargetBytes)
             path = SOFTMAX_PATH_CTA;
-        else if (cluster_for())
+        else if (cluster_for(false))
             path = SOFTMAX_PATH_CLUSTER;
         else
             path = SOFTMAX_PATH_TWOPASS;
@@ -220,7 +228,7 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
             if (rpw > kTileMaxRowsPerWarp)
                 rpw = kTileMaxRowsPerWarp;
             const int64_t stage_bytes = 4 * rpw * row_bytes_pad;
-            int64_t stages = kRingBudgetBytes / stage_bytes;
+            int64_t stages = kTileRingBudgetBytes / stage_bytes;
             stages = stages < 1 ? 1 : (stages > kMaxStages ? kMaxStages : stages);
             q.bulk_copy = 1;
             q.vec = out_al ? vmax : 1;
@@ -243,7 +251,7 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
     case SOFTMAX_PATH_CLUSTER: {
         int cs = 1;
         if (path == SOFTMAX_PATH_CLUSTER) {
-            cs = cluster_for();
+            cs = cluster_for(true);
             if (!cs)
                 return SOFTMAX_ERR_UNSUPPORTED;
         }

@@ -3,9 +3,11 @@
 // consecutive rows through a ring of `stages` shared-memory buffers:
 //
 //   ring    one elected thread starts one cp.async.bulk copy per row of a tile
-//           (global -> shared, all completing on the stage's mbarrier); the
-//           last < 16 bytes of a row whose byte length is not a multiple of 16
-//           are read by the lane that owns them with a plain load.
+//           (global -> shared, all completing on the stage's mbarrier).  A row
+//           is copied with its padding up to the next 16 bytes when that
+//           padding lies before the next row's start (the padding is then
+//           masked to -inf); only the matrix's last row can leave a < 16-byte
+//           tail, read by the lane that owns it with a plain load.
 //   rows    each warp owns R/4 rows of the tile and reduces them one after the
 //           other straight out of shared memory: lane l reads the vectors at
 //           columns (c*32 + l)*VEC, then max (__shfl_xor), e = exp(x - max),
@@ -62,6 +64,13 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
     const int64_t n_tiles = (n_rows + R - 1) / R;
     const uint32_t row_bytes = static_cast<uint32_t>(n_cols * sizeof(T)) & ~15u;
     const int bulk_elems = static_cast<int>(row_bytes / sizeof(T));
+    // Whole padded rows (row_pad elements) may be copied for every row but the
+    // last when the row stride covers them.
+    const bool pad_ok = ld_in >= row_pad;
+    const uint32_t pad_bytes = static_cast<uint32_t>(row_pad * sizeof(T));
+    auto copy_bytes = [&](int64_t row) {
+        return (pad_ok && row + 1 < n_rows) ? pad_bytes : row_bytes;
+    };
 
     T* ring = reinterpret_cast<T*>((reinterpret_cast<uintptr_t>(smem_raw) + (kTileRingAlign - 1)) &
                                    ~static_cast<uintptr_t>(kTileRingAlign - 1));
@@ -72,10 +81,16 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
         const int nr = static_cast<int>(n_rows - r0 < R ? n_rows - r0 : R);
         fence_proxy_async_smem();
         issued[s] += 1;
-        if (row_bytes) {
-            mbar_arrive_expect_tx(bar, row_bytes * static_cast<uint32_t>(nr));
-            for (int r = 0; r < nr; ++r)
-                bulk_g2s(smem_addr(row_ptr(s, r)), in + (r0 + r) * ld_in, row_bytes, bar);
+        uint32_t total = 0;
+        for (int r = 0; r < nr; ++r)
+            total += copy_bytes(r0 + r);
+        if (total) {
+            mbar_arrive_expect_tx(bar, total);
+            for (int r = 0; r < nr; ++r) {
+                const uint32_t n = copy_bytes(r0 + r);
+                if (n)
+                    bulk_g2s(smem_addr(row_ptr(s, r)), in + (r0 + r) * ld_in, n, bar);
+            }
         } else {
             mbar_arrive(bar);
         }
@@ -109,19 +124,22 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
                 break;                           // warp-uniform
             const T* sp = row_ptr(s, r);
             const T* gp = in + row * ld_in;
+            // Columns [0, avail) are in shared memory; [avail, n_cols) is the
+            // last row's < 16-byte tail; from n_cols on the row is padding.
+            const int avail = copy_bytes(row) == pad_bytes ? n_cols : bulk_elems;
             float x[E];
 #pragma unroll
             for (int c = 0; c < CHUNKS; ++c) {
                 const int col = (c * 32 + lane) * VEC;
-                if (col + VEC <= bulk_elems) {
+                if (col + VEC <= avail) {
                     lds_any<T, VEC>(sp + col, &x[c * VEC]);
                 } else {
 #pragma unroll
                     for (int j = 0; j < VEC; ++j) {
                         const int e = col + j;
-                        if (e < bulk_elems)
+                        if (e < avail)
                             lds_any<T, 1>(sp + e, &x[c * VEC + j]);
-                        else                                       // < 16-byte tail
+                        else
                             x[c * VEC + j] = e < n_cols ? Elem<T>::load1(gp + e) : kNegInf;
                     }
                 }

@@ -10,8 +10,10 @@
 //           every thread the row's (M, L);
 //   pass 2  the slice is read again and y = e^(x - M) / L is written.
 //
-// A slice is re-read soon after its first read, so part of the second pass
-// can hit L2; HBM traffic is between 2 and 3 row sizes per row.
+// A slice is re-read soon after its first read: the first pass reads with an
+// L2 evict-last policy and the second pass (and the stores) with evict-first,
+// so the second read mostly hits L2 and HBM traffic stays close to one read
+// and one write per element.
 // In place (in == out) is safe: every element is re-read by the thread that
 // then writes it, and the cluster barrier between the passes orders every
 // pass-1 read of the row before any write.
@@ -23,6 +25,21 @@ namespace rwsm {
 constexpr int kTwoPassThreads = 512;
 constexpr int kTwoPassBatch = 4;
 
+// Load the k-th batch vector of this thread: 16-byte vectors with an L2
+// policy when VEC covers 16 bytes, element loads (masked) otherwise.
+template <typename T, int VEC>
+__device__ __forceinline__ void tp_load(const T* src, int64_t v, int64_t len, float* x,
+                                        uint64_t pol)
+{
+    if constexpr (VEC * sizeof(T) == 16) {
+        if ((v + 1) * VEC <= len) {
+            load16_hint<T>(src + v * VEC, x, pol);
+            return;
+        }
+    }
+    load_vec_masked<T, VEC>(src, v * VEC, len, x);
+}
+
 template <typename T, int VEC>
 __global__ void __launch_bounds__(kTwoPassThreads)
 twopass_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_in,
@@ -30,6 +47,7 @@ twopass_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_i
 {
     constexpr int THREADS = kTwoPassThreads;
     constexpr int NW = THREADS / 32;
+    constexpr int B = kTwoPassBatch;
     __shared__ float red_m[NW], red_l[NW];
     __shared__ float2 part[2];
 
@@ -41,18 +59,20 @@ twopass_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_i
     int64_t len = n_cols - c0;
     len = len < 0 ? 0 : (len > slice_cols ? slice_cols : len);
     const int64_t nv = (len + VEC - 1) / VEC;
+    const uint64_t keep = policy_evict_last();     // first read: stay in L2
+    const uint64_t stream = policy_evict_first();  // second read and stores
 
     int slot = 0;
     for (int64_t row = cluster_id; row < n_rows; row += n_clusters, slot ^= 1) {
         const T* src = in + row * ld_in + c0;
         float m = kNegInf, l = 0.0f;
-        for (int64_t v0 = tid; v0 < nv; v0 += int64_t{THREADS} * kTwoPassBatch) {
-            float x[kTwoPassBatch * VEC];
+        for (int64_t v0 = tid; v0 < nv; v0 += int64_t{THREADS} * B) {
+            float x[B * VEC];
 #pragma unroll
-            for (int k = 0; k < kTwoPassBatch; ++k) {
+            for (int k = 0; k < B; ++k) {
                 const int64_t v = v0 + int64_t{k} * THREADS;
                 if (v < nv) {
-                    load_vec_masked<T, VEC>(src, v * VEC, len, &x[k * VEC]);
+                    tp_load<T, VEC>(src, v, len, &x[k * VEC], keep);
                 } else {
 #pragma unroll
                     for (int j = 0; j < VEC; ++j)
@@ -61,13 +81,13 @@ twopass_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_i
             }
             float bm = kNegInf;
 #pragma unroll
-            for (int i = 0; i < kTwoPassBatch * VEC; ++i)
+            for (int i = 0; i < B * VEC; ++i)
                 bm = fmaxf(bm, x[i]);
             const float mn = fmaxf(m, bm);
             const float ref = (mn == kNegInf) ? 0.0f : mn;
             float s = 0.0f;
 #pragma unroll
-            for (int i = 0; i < kTwoPassBatch * VEC; ++i)
+            for (int i = 0; i < B * VEC; ++i)
                 s += exp_biased(x[i] - ref);
             l = l * exp_ftz(m - ref) + s;
             m = mn;
@@ -78,13 +98,27 @@ twopass_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_i
         const float inv = 1.0f / l;
 
         T* dst = out + row * ld_out + c0;
-        for (int64_t v = tid; v < nv; v += THREADS) {
-            float x[VEC];
-            load_vec_masked<T, VEC>(src, v * VEC, len, x);
+        for (int64_t v0 = tid; v0 < nv; v0 += int64_t{THREADS} * B) {
+            float x[B * VEC];
 #pragma unroll
-            for (int j = 0; j < VEC; ++j)
-                x[j] = exp_biased(x[j] - m);
-            store_vec_masked<T, VEC>(dst, v * VEC, len, x, inv);
+            for (int k = 0; k < B; ++k) {
+                const int64_t v = v0 + int64_t{k} * THREADS;
+                if (v < nv)
+                    tp_load<T, VEC>(src, v, len, &x[k * VEC], stream);
+            }
+#pragma unroll
+            for (int k = 0; k < B; ++k) {
+                const int64_t v = v0 + int64_t{k} * THREADS;
+                if (v < nv) {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j)
+                        x[k * VEC + j] = exp_biased(x[k * VEC + j] - m);
+                    if (VEC * sizeof(T) == 16 && (v + 1) * VEC <= len)
+                        store16_hint<T>(dst + v * VEC, &x[k * VEC], inv, stream);
+                    else
+                        store_vec_masked<T, VEC>(dst, v * VEC, len, &x[k * VEC], inv);
+                }
+            }
         }
         __syncthreads();                       // red_* reused by the next row
     }

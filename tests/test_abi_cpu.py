@@ -52,19 +52,19 @@ def plan(n_rows, n_cols, **kw):
 def test_scheduler_paths_for_the_five_workloads(lib):
     p = plan(128, 1000)
     assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 1, 4, 8, 1)
-    assert (p.stages, p.slice_cols, p.smem_bytes) == (4, 1000, 64000)
+    assert (p.stages, p.slice_cols, p.smem_bytes) == (3, 1000, 48000)
     p = plan(4096, 4096)
     assert (p.path, p.cluster, p.bulk_copy, p.out_vec) == (rws.PATH_CTA, 1, 1, 4)
-    assert (p.threads, p.chunks, p.stages, p.smem_bytes, p.grid) == (128, 8, 4, 65536, 0)
+    assert (p.threads, p.chunks, p.stages, p.smem_bytes, p.grid) == (256, 4, 2, 32768, 0)
     p = plan(32768, 1024, dtype=rws.BF16)
     assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 1, 8, 4, 2)
-    assert (p.stages, p.smem_bytes) == (4, 65536)
+    assert (p.stages, p.smem_bytes) == (3, 49152)
     p = plan(262144, 127, in_row_stride=128, out_row_stride=127)
     assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 1, 1, 4, 8)
-    assert (p.slice_cols, p.stages, p.smem_bytes) == (128, 4, 65536)
+    assert (p.slice_cols, p.stages, p.smem_bytes) == (128, 3, 49152)
     p = plan(256, 262144)
-    assert (p.path, p.cluster, p.slice_cols, p.smem_bytes) == (rws.PATH_CLUSTER, 16, 16384, 65536)
-    assert (p.threads, p.chunks, p.stages, p.grid) == (512, 8, 1, 0)
+    assert (p.path, p.cluster, p.slice_cols, p.threads, p.grid) == (rws.PATH_TWOPASS, 16, 16384, 512, 0)
+    assert (p.vec, p.out_vec) == (4, 4)
 
 
 def test_scheduler_boundaries(lib):
@@ -75,15 +75,18 @@ def test_scheduler_boundaries(lib):
     assert p.path == rws.PATH_CLUSTER and p.cluster == 2
     assert plan(1, 16384, dtype=rws.BF16).path == rws.PATH_CTA
     assert plan(1, 16385, dtype=rws.BF16).path == rws.PATH_CLUSTER
-    big = plan(1, 16 * 32768)                             # 16 slices of 128 KB
-    assert big.path == rws.PATH_CLUSTER and big.cluster == 16 and big.threads == 1024
-    assert big.stages == 1 and big.smem_bytes == 131072
-    assert plan(1, 16 * 32768 + 4).path == rws.PATH_TWOPASS
-    assert plan(1, 16 * 32768, dtype=rws.BF16).path == rws.PATH_CLUSTER
-    assert plan(1, 16 * 32768 + 8, dtype=rws.BF16).path == rws.PATH_TWOPASS
+    big = plan(1, 16 * 8192)                              # 16 slices of 32 KB
+    assert big.path == rws.PATH_CLUSTER and big.cluster == 16 and big.threads == 512
+    assert big.stages == 1 and big.smem_bytes == 32768
+    assert plan(1, 16 * 8192 + 4).path == rws.PATH_TWOPASS
+    assert plan(1, 16 * 16384, dtype=rws.BF16).path == rws.PATH_CLUSTER
+    assert plan(1, 16 * 16384 + 8, dtype=rws.BF16).path == rws.PATH_TWOPASS
+    forced = plan(1, 16 * 32768, path=rws.PATH_CLUSTER)    # forced: 128 KB slices
+    assert forced.cluster == 16 and forced.threads == 1024 and forced.chunks == 8
+    assert forced.smem_bytes == 131072
     tp = plan(3, 10_000_000)
     assert tp.path == rws.PATH_TWOPASS and tp.cluster == 16 and tp.grid == 0
-    for n in (1025, 3000, 4096, 5000, 8192, 8193, 20000, 262144, 524288):
+    for n in (1025, 3000, 4096, 5000, 8192, 8193, 20000, 131072, 262144, 524288):
         q = plan(2, n)
         if q.path in (rws.PATH_CTA, rws.PATH_CLUSTER):
             assert q.threads * q.chunks * 4 >= q.slice_cols          # slice fits registers
@@ -114,9 +117,10 @@ def test_scheduler_forced_paths(lib):
         plan(8, 200_000, path=rws.PATH_CTA)
     assert e.value.status == rws.ERR_UNSUPPORTED
     small_cluster = dict(GB, max_cluster=8)
-    p = rws.plan_for_device(small_cluster, 4, 262144)
+    assert rws.plan_for_device(small_cluster, 4, 262144).path == rws.PATH_TWOPASS
+    p = rws.plan_for_device(small_cluster, 4, 262144, path=rws.PATH_CLUSTER)
     assert p.path == rws.PATH_CLUSTER and p.cluster == 8 and p.slice_cols == 32768
-    assert p.threads == 1024 and p.stages == 1
+    assert p.threads == 1024 and p.stages == 1 and p.chunks == 8
 
 
 def test_validation(lib):
