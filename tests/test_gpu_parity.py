@@ -177,6 +177,7 @@ def test_planned_launch_shapes():
     b5 = rws.plan(w5.n_rows, w5.n_cols)
     for cs in (8, 16):
         q = rws.Plan.from_buffer_copy(b5)
+        q.path, q.bulk_copy, q.vec, q.out_vec = rws.PATH_CLUSTER, 1, 4, 4
         q.cluster = cs
         q.slice_cols = w5.n_cols // cs
         q.threads = 1024 if cs == 8 else 512
