@@ -2,18 +2,20 @@
 // and launch shape.  Pure host code: it reads a device description and the
 // pointers' alignment, never the device, so it runs without a GPU.
 //
-// Paths by row length (n_cols, element size esz):
-//   WARP     n_cols <= 1024: a warp owns rows in registers (short rows).
-//   CTA      row <= 32 KB: a persistent CTA walks rows through a ring of
-//            shared-memory stages (cp.async.bulk), each row held in registers.
-//   CLUSTER  longer rows up to 16 slices of <= 32 KB: a cluster per row,
-//            slices on different SMs, one HBM pass.  (When forced, slices up
-//            to 128 KB fp32 / 64 KB bf16 per CTA.)
-//   TWOPASS  anything longer: a cluster streams the row twice, the second
-//            read mostly from L2.
-// Slices are kept at <= 32 KB when a cluster of <= 16 CTAs allows it; the ring
-// gets about 64 KB of shared memory per CTA, so two or three CTAs stay resident
-// per SM (228 KB of shared memory each on GB300) with several slices in flight.
+// Paths by row length (n_cols, element size esz), chosen from measured
+// GB300 sweeps over row lengths:
+//   WARP     n_cols <= 1024: a warp owns rows.  fp32 rows stay in registers
+//            (software-pipelined loads); bf16 rows with 16-byte aligned input
+//            go through the staged tile kernel (cp.async.bulk ring of rows).
+//   CTA      row <= 32 KB: a persistent CTA per row at a time, the row staged
+//            by cp.async.bulk and held in registers (one ring stage: the
+//            register copy is the second buffer).
+//   CLUSTER  longer rows whose slices fit 32 KB on a cluster of <= 16 CTAs,
+//            for fp32 only up to 64 KB rows: one HBM pass, slices on
+//            different SMs, max and sum exchanged through distributed shared
+//            memory.  (When forced: slices up to 128 KB fp32 / 64 KB bf16.)
+//   TWOPASS  longer rows: a cluster of 2..16 CTAs (about 256 KB of row per
+//            CTA) streams the row twice; the second read mostly hits L2.
 //
 // Whole waves (the "Block Occupancy: tail effect" rule of the cs336 lecture
 // 6 notes): every grid is persistent, sized at launch to the number of CTAs
@@ -29,8 +31,10 @@ namespace {
 
 constexpr int64_t kWarpMaxCols = 1024;
 constexpr int64_t kSliceTargetBytes = 32 * 1024;   // preferred slice (CTA path: whole row)
-constexpr int64_t kRingBudgetBytes = 32 * 1024;    // shared memory for the slice ring, per CTA
-constexpr int64_t kTileRingBudgetBytes = 48 * 1024; // shared memory for the tile ring, per CTA
+constexpr int kSliceStages = 1;                    // ring stages of the slice kernel
+constexpr int64_t kTileRingBudgetBytes = 32 * 1024; // shared memory for the tile ring, per CTA
+constexpr int64_t kClusterMaxRowBytesF32 = 64 * 1024;  // fp32: longer rows take TWOPASS
+constexpr int64_t kTwoPassBytesPerCta = 256 * 1024;
 constexpr int kMaxStages = 8;                       // must match row_slices.cu
 constexpr int kMaxSliceThreads = 1024;
 constexpr int kSmemReserve = 2048;                  // static smem + slack
@@ -161,6 +165,7 @@ int validate(const void* in, const void* out, int64_t n_rows, int64_t n_cols,
 
 int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, softmax_plan_t* plan)
 {
+    const int path_in = path;
     if (!plan)
         return SOFTMAX_ERR_INVALID_ARG;
     const int st = validate(p.in, p.out, p.n_rows, p.n_cols, p.ld_in, p.ld_out, p.dtype);
@@ -202,11 +207,12 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
             path = SOFTMAX_PATH_WARP;
         else if (row_bytes <= kSliceTargetBytes)
             path = SOFTMAX_PATH_CTA;
-        else if (cluster_for(false))
+        else if (cluster_for(false) && (esz != 4 || row_bytes <= kClusterMaxRowBytesF32))
             path = SOFTMAX_PATH_CLUSTER;
         else
             path = SOFTMAX_PATH_TWOPASS;
     }
+    const bool automatic = path_in == SOFTMAX_PATH_AUTO;
 
     softmax_plan_t q = {};
     q.path = path;
@@ -218,7 +224,9 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
             return SOFTMAX_ERR_UNSUPPORTED;
         q.threads = 128;
         q.grid = 0;
-        if (in_al) {
+        // bf16 rows go through the staged tile kernel; fp32 rows measured
+        // faster in the register kernel (its loads are all in flight at once).
+        if (in_al && (p.dtype == SOFTMAX_BF16 || !automatic)) {
             // Staged tile kernel: stages of 4 * rows_per_warp rows of
             // row_pad elements (about 16 KB), about 64 KB of ring per CTA.
             const int64_t row_pad = round_up(p.n_cols, vmax);
@@ -261,13 +269,7 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
             return SOFTMAX_ERR_UNSUPPORTED;
         int threads = 0, nv = 0;
         slice_shape(slice / vmax, esz, &threads, &nv);
-        int64_t stages = kRingBudgetBytes / stage_bytes;
-        if (stages < 1)
-            stages = 1;
-        if (stages > kMaxStages)
-            stages = kMaxStages;
-        while (stages > 1 && stages * stage_bytes > smem_cap)
-            --stages;
+        const int64_t stages = kSliceStages;
         q.cluster = cs;
         q.slice_cols = slice;
         q.vec = vmax;
@@ -281,7 +283,11 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
         break;
     }
     case SOFTMAX_PATH_TWOPASS: {
-        int64_t cs = pow2_floor(p.n_cols / 8192 > 0 ? p.n_cols / 8192 : 1);
+        // About 256 KB of row per CTA; at least 2 CTAs when chosen
+        // automatically (forced on short rows a single CTA is allowed).
+        int64_t cs = pow2_ceil(ceil_div(row_bytes, kTwoPassBytesPerCta));
+        if (automatic && cs < 2)
+            cs = 2;
         if (cs > max_cluster)
             cs = pow2_floor(max_cluster);
         q.cluster = static_cast<int>(cs);

@@ -50,20 +50,18 @@ def plan(n_rows, n_cols, **kw):
 
 
 def test_scheduler_paths_for_the_five_workloads(lib):
-    p = plan(128, 1000)
-    assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 1, 4, 8, 1)
-    assert (p.stages, p.slice_cols, p.smem_bytes) == (3, 1000, 48000)
+    p = plan(128, 1000)                                   # fp32 short rows: register kernel
+    assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 0, 4, 8, 1)
     p = plan(4096, 4096)
     assert (p.path, p.cluster, p.bulk_copy, p.out_vec) == (rws.PATH_CTA, 1, 1, 4)
-    assert (p.threads, p.chunks, p.stages, p.smem_bytes, p.grid) == (256, 4, 2, 32768, 0)
-    p = plan(32768, 1024, dtype=rws.BF16)
+    assert (p.threads, p.chunks, p.stages, p.smem_bytes, p.grid) == (256, 4, 1, 16384, 0)
+    p = plan(32768, 1024, dtype=rws.BF16)                 # bf16 short rows: staged tiles
     assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 1, 8, 4, 2)
-    assert (p.stages, p.smem_bytes) == (3, 49152)
+    assert (p.stages, p.smem_bytes) == (2, 32768)
     p = plan(262144, 127, in_row_stride=128, out_row_stride=127)
-    assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 1, 1, 4, 8)
-    assert (p.slice_cols, p.stages, p.smem_bytes) == (128, 3, 49152)
+    assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 0, 1, 4, 4)
     p = plan(256, 262144)
-    assert (p.path, p.cluster, p.slice_cols, p.threads, p.grid) == (rws.PATH_TWOPASS, 16, 16384, 512, 0)
+    assert (p.path, p.cluster, p.slice_cols, p.threads, p.grid) == (rws.PATH_TWOPASS, 4, 65536, 512, 0)
     assert (p.vec, p.out_vec) == (4, 4)
 
 
@@ -71,14 +69,15 @@ def test_scheduler_boundaries(lib):
     assert plan(1, 1024).path == rws.PATH_WARP
     assert plan(1, 1025).path == rws.PATH_CTA
     assert plan(1, 8192).path == rws.PATH_CTA             # 32 KB row
-    p = plan(1, 8193)
-    assert p.path == rws.PATH_CLUSTER and p.cluster == 2
+    p = plan(1, 8196)
+    assert p.path == rws.PATH_CLUSTER and p.cluster == 2 and p.stages == 1
+    assert plan(1, 16384).path == rws.PATH_CLUSTER         # fp32 single pass up to 64 KB
+    p = plan(1, 16388)
+    assert p.path == rws.PATH_TWOPASS and p.cluster == 2
+    assert plan(1, 65536).cluster == 2 and plan(1, 65540).cluster == 2
+    assert plan(1, 131072).cluster == 2 and plan(1, 131076).cluster == 4
     assert plan(1, 16384, dtype=rws.BF16).path == rws.PATH_CTA
-    assert plan(1, 16385, dtype=rws.BF16).path == rws.PATH_CLUSTER
-    big = plan(1, 16 * 8192)                              # 16 slices of 32 KB
-    assert big.path == rws.PATH_CLUSTER and big.cluster == 16 and big.threads == 512
-    assert big.stages == 1 and big.smem_bytes == 32768
-    assert plan(1, 16 * 8192 + 4).path == rws.PATH_TWOPASS
+    assert plan(1, 16392, dtype=rws.BF16).path == rws.PATH_CLUSTER
     assert plan(1, 16 * 16384, dtype=rws.BF16).path == rws.PATH_CLUSTER
     assert plan(1, 16 * 16384 + 8, dtype=rws.BF16).path == rws.PATH_TWOPASS
     forced = plan(1, 16 * 32768, path=rws.PATH_CLUSTER)    # forced: 128 KB slices
@@ -86,12 +85,15 @@ def test_scheduler_boundaries(lib):
     assert forced.smem_bytes == 131072
     tp = plan(3, 10_000_000)
     assert tp.path == rws.PATH_TWOPASS and tp.cluster == 16 and tp.grid == 0
-    for n in (1025, 3000, 4096, 5000, 8192, 8193, 20000, 131072, 262144, 524288):
-        q = plan(2, n)
-        if q.path in (rws.PATH_CTA, rws.PATH_CLUSTER):
-            assert q.threads * q.chunks * 4 >= q.slice_cols          # slice fits registers
-            assert q.stages * q.slice_cols * 4 == q.smem_bytes
-            assert q.smem_bytes <= rws.GB300["max_smem_per_block_optin"] - 2048
+    for n in (1025, 3000, 4096, 5000, 8192, 8196, 16384, 20000, 131072, 262144, 524288):
+        for path in (rws.PATH_AUTO, rws.PATH_CLUSTER):
+            q = plan(2, n, path=path)
+            if q.path in (rws.PATH_CTA, rws.PATH_CLUSTER):
+                assert q.threads * q.chunks * 4 >= q.slice_cols          # slice fits registers
+                assert q.stages * q.slice_cols * 4 == q.smem_bytes
+                assert q.smem_bytes <= rws.GB300["max_smem_per_block_optin"] - 2048
+            if q.path == rws.PATH_TWOPASS:
+                assert q.slice_cols * q.cluster >= n
 
 
 def test_scheduler_alignment_fallbacks(lib):
@@ -102,8 +104,10 @@ def test_scheduler_alignment_fallbacks(lib):
     assert p.bulk_copy == 1 and p.out_vec == 1
     p = plan(64, 1000, in_row_stride=1001)
     assert p.path == rws.PATH_WARP and p.bulk_copy == 0 and p.vec == 1 and p.chunks == 32
-    p = plan(64, 1000, out_row_stride=1001)          # staged input, scalar coalesced stores
+    p = plan(64, 1000, out_row_stride=1001, dtype=rws.BF16)   # staged input, scalar stores
     assert p.path == rws.PATH_WARP and p.bulk_copy == 1 and p.vec == 1 and p.chunks == 32
+    p = plan(64, 1000, path=rws.PATH_WARP)                     # forced: staged tiles for fp32
+    assert p.bulk_copy == 1
 
 
 def test_scheduler_forced_paths(lib):
@@ -121,6 +125,7 @@ def test_scheduler_forced_paths(lib):
     p = rws.plan_for_device(small_cluster, 4, 262144, path=rws.PATH_CLUSTER)
     assert p.path == rws.PATH_CLUSTER and p.cluster == 8 and p.slice_cols == 32768
     assert p.threads == 1024 and p.stages == 1 and p.chunks == 8
+    assert rws.plan_for_device(small_cluster, 4, 40_000_000).cluster == 8
 
 
 def test_validation(lib):
