@@ -7,8 +7,8 @@ entries and a constant row.  Bytes are algorithmic: n_rows * n_cols *
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Prints ONE JSON line (rank 0).  Timing: CUDA events on the launching stream
-around every step, steps launched back to back.  L2 never holds a step's
+Prints ONE JSON line (rank 0).  Timing: one pair of CUDA events on the
+launching stream around the K steps, launched back to back.  L2 never holds a step's
 inputs: the steps rotate over enough input/output buffer sets that together
 they exceed three times the L2 size ("inputs larger than L2"), so each step
 reads its input from HBM and pays, like any steady stream of calls, for the
@@ -68,6 +68,17 @@ def shard_rows(n_rows: int, rank: int, world: int) -> tuple[int, int]:
     base, extra = divmod(n_rows, world)
     lo = rank * base + min(rank, extra)
     return lo, lo + base + (1 if rank < extra else 0)
+
+
+def max_over_ranks(value: float, world: int, device: str = "cpu") -> float:
+    """The largest value over all ranks (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def source_hash(path_name: str) -> str:
@@ -176,8 +187,9 @@ def device_buffers(w: wl.Workload, torch, l2_bytes: int):
 
 
 def time_device(w: wl.Workload, sets, steps: int, warmup: int, torch, rws, stream):
-    """Per-step CUDA-event times (ms) of softmax_rows, steps back to back over
-    rotating buffer sets (inputs resident in HBM, never in L2)."""
+    """softmax_rows over rotating buffer sets, steps back to back (inputs
+    resident in HBM, never in L2).  Returns (total ms of the timed steps from
+    one pair of CUDA events on the launching stream, kernel launches)."""
     calls = [(x.data_ptr(), y.data_ptr(), w.n_rows, w.n_cols, w.in_row_stride,
               w.out_row_stride, w.dtype, stream.cuda_stream) for x, y in sets]
     call = rws.lib().softmax_rows
@@ -186,16 +198,14 @@ def time_device(w: wl.Workload, sets, steps: int, warmup: int, torch, rws, strea
         if st != rws.OK:
             raise RuntimeError("softmax_rows: " + rws.status_string(st))
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = rws.launch_count()
-    for i, (a, b) in enumerate(ev):
-        a.record(stream)
+    a.record(stream)
+    for i in range(steps):
         call(*calls[(warmup + i) % len(calls)])
-        b.record(stream)
+    b.record(stream)
     torch.cuda.synchronize()
-    launches = rws.launch_count() - launches0
-    return [a.elapsed_time(b) for a, b in ev], launches
+    return a.elapsed_time(b), rws.launch_count() - launches0
 
 
 def copy_calibration(w: wl.Workload, sets, torch, stream, peak):
@@ -205,17 +215,17 @@ def copy_calibration(w: wl.Workload, sets, torch, stream, peak):
     pairs = [(x.reshape(-1)[:n], y.reshape(-1)[:n]) for x, y in sets if y.numel() >= n]
     if not pairs:
         return None
-    ts = []
+    for i in range(5):
+        src, dst = pairs[i % len(pairs)]
+        dst.copy_(src)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
     for i in range(30):
         src, dst = pairs[i % len(pairs)]
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
         dst.copy_(src)
-        b.record(stream)
-        if i >= 5:
-            ts.append((a, b))
+    b.record(stream)
     torch.cuda.synchronize()
-    ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
+    ms = a.elapsed_time(b) / 30
     gbs = 2 * n * pairs[0][0].element_size() / (ms * 1e-3) / 1e9
     return {"GB/s": round(gbs, 1), "mean_ms": round(ms, 5), "frac_of_peak": round(gbs / peak, 4)}
 
@@ -288,7 +298,7 @@ def run_ours(args):
     barrier()
     with ClockSampler(local) as clk:
         t_wall0 = time.perf_counter()
-        times, launches = time_device(w, bufs, args.steps, args.warmup, torch, rws, stream)
+        total_ms, launches = time_device(w, bufs, args.steps, args.warmup, torch, rws, stream)
         wall = time.perf_counter() - t_wall0
         # Keep the sampled window at least ~1.5 s: repeat the same step (not
         # counted) if the timed steps were shorter than that.
@@ -298,16 +308,12 @@ def run_ours(args):
             time_device(w, bufs, 2000, 0, torch, rws, stream)
             extra += 2000
     barrier()
-    total_ms = float(sum(times))
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, "cuda")
     ms_per_step = total_ms / args.steps
     bytes_step = w.algorithmic_bytes
     value = world * bytes_step * args.steps / (total_ms * 1e-3) / 1e9
-    achieved = bytes_step / (statistics.mean(times) * 1e-3) / 1e9
+    # One softmax kernel per step: average launch duration = timed region / launches.
+    achieved = bytes_step * launches / (total_ms * 1e-3) / 1e9
     traffic, traffic_src = committed_traffic(plan.path_name, args.workload)
 
     result = {
@@ -331,7 +337,6 @@ def run_ours(args):
                      "traffic_source": traffic_src if traffic else traffic_src},
         "gpu_launches": launches,
         "clocks": clk.summary(),
-        "median_step_ms": round(statistics.median(times), 5),
         "copy_same_bytes": copy_calibration(w, bufs, torch, stream, peak),
         "wall_s_timed_region": round(wall, 3),
     }
@@ -358,10 +363,10 @@ def run_ours(args):
             pc = rws.plan(wc.n_rows, wc.n_cols, in_row_stride=wc.in_row_stride,
                           out_row_stride=wc.out_row_stride, dtype=wc.dtype)
             bc = bufs if name == args.workload else device_buffers(wc, torch, l2_bytes)
-            ts, _ = time_device(wc, bc, 50, 5, torch, rws, stream)
+            tot, _ = time_device(wc, bc, 50, 5, torch, rws, stream)
             cal = copy_calibration(wc, bc, torch, stream, peak)
             del bc
-            med = statistics.mean(ts)
+            med = tot / 50
             gbs = wc.algorithmic_bytes / (med * 1e-3) / 1e9
             per[name] = {"shape": [wc.n_rows, wc.n_cols], "dtype": "f32" if wc.dtype == wl.F32 else "bf16",
                          "path": pc.path_name, "plan": str(pc), "mean_ms": round(med, 5),
