@@ -19,7 +19,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libsoftmax.so")
 
 SOURCES = ["softmax_abi.cu", "plan.cpp", "warp_rows.cu", "tile_rows.cu", "row_slices.cu",
-           "twopass.cu"]
+           "twopass.cu", "stream_rows.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "kernels.h")] + [
     os.path.join(INCLUDE, "softmax.h")]
 

@@ -330,6 +330,16 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
+// The same copy with an L2 cache policy (createpolicy) for the source lines.
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;"
+        :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(pol) : "memory");
+}
+
 __device__ __forceinline__ unsigned long long global_ns()
 {
     unsigned long long t;

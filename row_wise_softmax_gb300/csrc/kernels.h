@@ -30,6 +30,7 @@ cudaError_t launch_warp_rows(const Problem& p, const softmax_plan_t& plan, cudaS
 cudaError_t launch_tile_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
 cudaError_t launch_row_slices(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
 cudaError_t launch_twopass(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
+cudaError_t launch_stream_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
 
 // Largest cluster the row-slice kernel can launch with on the current device.
 int max_cluster_size_row_slices();
@@ -38,6 +39,7 @@ int max_cluster_size_row_slices();
 // optionally clear (host side, after the device has been synchronised).
 unsigned read_error_row_slices(bool clear);
 unsigned read_error_tile_rows(bool clear);
+unsigned read_error_stream_rows(bool clear);
 cudaError_t launch_selftest_wait(cudaStream_t s);
 
 // Helpers implemented in softmax_abi.cu.

@@ -35,6 +35,8 @@ constexpr int kSliceStages = 1;                    // ring stages of the slice k
 constexpr int64_t kTileRingBudgetBytes = 32 * 1024; // shared memory for the tile ring, per CTA
 constexpr int64_t kClusterMaxRowBytesF32 = 64 * 1024;  // fp32: longer rows take TWOPASS
 constexpr int64_t kTwoPassBytesPerCta = 256 * 1024;
+constexpr int kStreamThreads = 256;                 // staged two-pass: 16 KB chunks
+constexpr int kStreamStages = 4;
 constexpr int kMaxStages = 8;                       // must match row_slices.cu
 constexpr int kMaxSliceThreads = 1024;
 constexpr int kSmemReserve = 2048;                  // static smem + slack
@@ -291,11 +293,22 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
         if (cs > max_cluster)
             cs = pow2_floor(max_cluster);
         q.cluster = static_cast<int>(cs);
-        q.vec = (in_al && out_al) ? vmax : 1;
-        q.out_vec = q.vec;
         q.slice_cols = round_up(ceil_div(p.n_cols, cs), vmax);
-        q.threads = 512;
         q.grid = 0;
+        if (in_al) {
+            // Staged: the slice streams twice through a ring of 16 KB chunks.
+            q.bulk_copy = 1;
+            q.vec = vmax;
+            q.out_vec = out_al ? vmax : 1;
+            q.threads = kStreamThreads;
+            q.chunks = 4;
+            q.stages = kStreamStages;
+            q.smem_bytes = q.stages * q.threads * q.chunks * 16;
+        } else {
+            q.vec = (in_al && out_al) ? vmax : 1;
+            q.out_vec = q.vec;
+            q.threads = 512;
+        }
         break;
     }
     default:
@@ -373,12 +386,18 @@ int check_plan(const softmax_device_desc_t& dev, const Problem& p, const softmax
     }
     case SOFTMAX_PATH_TWOPASS: {
         const int cs = q.cluster;
-        if (!pow2_in(cs, 1, max_cluster) || !vec_ok(q.vec, in_al && out_al) || q.out_vec != q.vec)
+        if (!pow2_in(cs, 1, max_cluster) || q.grid % cs || q.grid > 0x7fffffff)
             return SOFTMAX_ERR_INVALID_ARG;
         if (q.slice_cols <= 0 || q.slice_cols % vmax || q.slice_cols * cs < p.n_cols ||
-            q.threads != 512)
+            (q.threads != 256 && q.threads != 512))
             return SOFTMAX_ERR_INVALID_ARG;
-        if (q.grid % cs || q.grid > 0x7fffffff)
+        if (q.bulk_copy == 0)
+            return (vec_ok(q.vec, in_al && out_al) && q.out_vec == q.vec) ? SOFTMAX_OK
+                                                                            : SOFTMAX_ERR_INVALID_ARG;
+        // Staged two-pass (ring of chunks of threads * chunks * 16 bytes).
+        if (q.bulk_copy != 1 || !in_al || q.vec != vmax || !vec_ok(q.out_vec, out_al) ||
+            (q.chunks != 2 && q.chunks != 4) || q.stages < 1 || q.stages > kMaxStages ||
+            q.smem_bytes != q.stages * q.threads * q.chunks * 16 || q.smem_bytes > smem_cap)
             return SOFTMAX_ERR_INVALID_ARG;
         return SOFTMAX_OK;
     }

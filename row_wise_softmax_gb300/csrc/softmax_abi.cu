@@ -88,7 +88,9 @@ int launch_path(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
         break;
     case SOFTMAX_PATH_CTA:
     case SOFTMAX_PATH_CLUSTER: err = launch_row_slices(p, plan, s); break;
-    case SOFTMAX_PATH_TWOPASS: err = launch_twopass(p, plan, s); break;
+    case SOFTMAX_PATH_TWOPASS:
+        err = plan.bulk_copy ? launch_stream_rows(p, plan, s) : launch_twopass(p, plan, s);
+        break;
     default: break;
     }
     if (err != cudaSuccess) {
@@ -300,7 +302,8 @@ int softmax_device_status(int clear)
         return SOFTMAX_ERR_CUDA;
     }
     const unsigned e = rwsm::read_error_row_slices(clear != 0) |
-                       rwsm::read_error_tile_rows(clear != 0);
+                       rwsm::read_error_tile_rows(clear != 0) |
+                       rwsm::read_error_stream_rows(clear != 0);
     return e ? SOFTMAX_ERR_DEVICE_TIMEOUT : SOFTMAX_OK;
 }
 

@@ -49,8 +49,10 @@ __device__ __forceinline__ void lds_any(const T* p, float* v)
     }
 }
 
+// At most 64 registers per thread (8 CTAs per SM): the kernel is latency
+// bound, so resident warps matter more than registers (no spills at 64).
 template <typename T, int VEC, int CHUNKS>
-__global__ void __launch_bounds__(kTileThreads)
+__global__ void __launch_bounds__(kTileThreads, 8)
 tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
                  int64_t ld_out, int rows_per_warp, int stages, int row_pad)
 {

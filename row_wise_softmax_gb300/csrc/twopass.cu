@@ -22,7 +22,6 @@
 
 namespace rwsm {
 
-constexpr int kTwoPassThreads = 512;
 constexpr int kTwoPassBatch = 4;
 
 // Load the k-th batch vector of this thread: 16-byte vectors with an L2
@@ -40,18 +39,60 @@ __device__ __forceinline__ void tp_load(const T* src, int64_t v, int64_t len, fl
     load_vec_masked<T, VEC>(src, v * VEC, len, x);
 }
 
-template <typename T, int VEC>
-__global__ void __launch_bounds__(kTwoPassThreads)
+// Walk this thread's batches of B vectors (v = v0 + k*THREADS, batches
+// THREADS*B apart) with two register buffers: the loads of the next batch are
+// issued before `body` consumes the current one, so every thread keeps one
+// batch in flight while it computes.
+template <typename T, int VEC, int B, int THREADS, typename Body>
+__device__ __forceinline__ void pipelined_batches(const T* src, int64_t nv, int64_t len,
+                                                  uint64_t pol, Body&& body)
+{
+    constexpr int64_t kStride = int64_t{THREADS} * B;
+    auto load_batch = [&](float (&x)[B * VEC], int64_t v0) {
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+            const int64_t v = v0 + int64_t{k} * THREADS;
+            if (v < nv) {
+                tp_load<T, VEC>(src, v, len, &x[k * VEC], pol);
+            } else {
+#pragma unroll
+                for (int j = 0; j < VEC; ++j)
+                    x[k * VEC + j] = kNegInf;
+            }
+        }
+    };
+    int64_t v0 = threadIdx.x;
+    if (v0 >= nv)
+        return;
+    float a[B * VEC], b[B * VEC];
+    load_batch(a, v0);
+    while (true) {
+        const int64_t v1 = v0 + kStride;
+        if (v1 < nv)
+            load_batch(b, v1);
+        body(a, v0);
+        if (v1 >= nv)
+            break;
+        const int64_t v2 = v1 + kStride;
+        if (v2 < nv)
+            load_batch(a, v2);
+        body(b, v1);
+        if (v2 >= nv)
+            break;
+        v0 = v2;
+    }
+}
+
+template <typename T, int VEC, int THREADS>
+__global__ void __launch_bounds__(THREADS)
 twopass_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_in,
                int64_t ld_out, int64_t slice_cols, int cs)
 {
-    constexpr int THREADS = kTwoPassThreads;
     constexpr int NW = THREADS / 32;
     constexpr int B = kTwoPassBatch;
     __shared__ float red_m[NW], red_l[NW];
     __shared__ float2 part[2];
 
-    const int tid = threadIdx.x;
     const int rank = static_cast<int>(blockIdx.x % cs);
     const int64_t cluster_id = blockIdx.x / cs;
     const int64_t n_clusters = gridDim.x / cs;
@@ -65,61 +106,47 @@ twopass_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_i
     int slot = 0;
     for (int64_t row = cluster_id; row < n_rows; row += n_clusters, slot ^= 1) {
         const T* src = in + row * ld_in + c0;
+        // ---- pass 1: online (m, l) over this thread's batches
         float m = kNegInf, l = 0.0f;
-        for (int64_t v0 = tid; v0 < nv; v0 += int64_t{THREADS} * B) {
-            float x[B * VEC];
+        pipelined_batches<T, VEC, B, THREADS>(src, nv, len, keep,
+            [&](const float (&x)[B * VEC], int64_t) {
+                float bm = kNegInf;
 #pragma unroll
-            for (int k = 0; k < B; ++k) {
-                const int64_t v = v0 + int64_t{k} * THREADS;
-                if (v < nv) {
-                    tp_load<T, VEC>(src, v, len, &x[k * VEC], keep);
-                } else {
+                for (int i = 0; i < B * VEC; ++i)
+                    bm = fmaxf(bm, x[i]);
+                const float mn = fmaxf(m, bm);
+                const float ref = (mn == kNegInf) ? 0.0f : mn;
+                float s = 0.0f;
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j)
-                        x[k * VEC + j] = kNegInf;
-                }
-            }
-            float bm = kNegInf;
-#pragma unroll
-            for (int i = 0; i < B * VEC; ++i)
-                bm = fmaxf(bm, x[i]);
-            const float mn = fmaxf(m, bm);
-            const float ref = (mn == kNegInf) ? 0.0f : mn;
-            float s = 0.0f;
-#pragma unroll
-            for (int i = 0; i < B * VEC; ++i)
-                s += exp_biased(x[i] - ref);
-            l = l * exp_ftz(m - ref) + s;
-            m = mn;
-        }
+                for (int i = 0; i < B * VEC; ++i)
+                    s += exp_biased(x[i] - ref);
+                l = l * exp_ftz(m - ref) + s;
+                m = mn;
+            });
         cta_ml_reduce<THREADS>(m, l, red_m, red_l);
         if (cs > 1)
             cluster_ml_reduce(m, l, part, slot, cs);
         const float inv = 1.0f / l;
 
+        // ---- pass 2: normalise (the re-read mostly hits L2)
         T* dst = out + row * ld_out + c0;
-        for (int64_t v0 = tid; v0 < nv; v0 += int64_t{THREADS} * B) {
-            float x[B * VEC];
+        pipelined_batches<T, VEC, B, THREADS>(src, nv, len, stream,
+            [&](const float (&xin)[B * VEC], int64_t v0) {
 #pragma unroll
-            for (int k = 0; k < B; ++k) {
-                const int64_t v = v0 + int64_t{k} * THREADS;
-                if (v < nv)
-                    tp_load<T, VEC>(src, v, len, &x[k * VEC], stream);
-            }
+                for (int k = 0; k < B; ++k) {
+                    const int64_t v = v0 + int64_t{k} * THREADS;
+                    if (v < nv) {
+                        float x[VEC];
 #pragma unroll
-            for (int k = 0; k < B; ++k) {
-                const int64_t v = v0 + int64_t{k} * THREADS;
-                if (v < nv) {
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j)
-                        x[k * VEC + j] = exp_biased(x[k * VEC + j] - m);
-                    if (VEC * sizeof(T) == 16 && (v + 1) * VEC <= len)
-                        store16_hint<T>(dst + v * VEC, &x[k * VEC], inv, stream);
-                    else
-                        store_vec_masked<T, VEC>(dst, v * VEC, len, &x[k * VEC], inv);
+                        for (int j = 0; j < VEC; ++j)
+                            x[j] = exp_biased(xin[k * VEC + j] - m);
+                        if (VEC * sizeof(T) == 16 && (v + 1) * VEC <= len)
+                            store16_hint<T>(dst + v * VEC, x, inv, stream);
+                        else
+                            store_vec_masked<T, VEC>(dst, v * VEC, len, x, inv);
+                    }
                 }
-            }
-        }
+            });
         __syncthreads();                       // red_* reused by the next row
     }
     if (cs > 1)
@@ -128,10 +155,10 @@ twopass_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_i
 
 namespace {
 
-template <typename T, int VEC>
+template <typename T, int VEC, int THREADS>
 cudaError_t launch_tp(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
 {
-    auto* k = twopass_kernel<T, VEC>;
+    auto* k = twopass_kernel<T, VEC, THREADS>;
     const int cs = plan.cluster;
     cudaError_t err = cudaSuccess;
     if (cs > 8) {
@@ -144,7 +171,7 @@ cudaError_t launch_tp(const Problem& p, const softmax_plan_t& plan, cudaStream_t
         // Persistent: as many clusters as can be resident at once.
         cudaLaunchConfig_t q = {};
         q.gridDim = dim3(cs, 1, 1);
-        q.blockDim = dim3(kTwoPassThreads, 1, 1);
+        q.blockDim = dim3(THREADS, 1, 1);
         cudaLaunchAttribute a[1];
         a[0].id = cudaLaunchAttributeClusterDimension;
         a[0].val.clusterDim.x = cs;
@@ -159,7 +186,7 @@ cudaError_t launch_tp(const Problem& p, const softmax_plan_t& plan, cudaStream_t
                 active = 0;
             }
         } else {
-            active = resident_ctas(reinterpret_cast<const void*>(k), kTwoPassThreads, 0);
+            active = resident_ctas(reinterpret_cast<const void*>(k), THREADS, 0);
         }
         if (active < 1)
             active = 1;
@@ -167,7 +194,7 @@ cudaError_t launch_tp(const Problem& p, const softmax_plan_t& plan, cudaStream_t
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * cs), 1, 1);
-    cfg.blockDim = dim3(kTwoPassThreads, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -182,13 +209,25 @@ cudaError_t launch_tp(const Problem& p, const softmax_plan_t& plan, cudaStream_t
     return err;
 }
 
+template <typename T, int VEC>
+cudaError_t launch_tp_threads(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
+{
+    switch (plan.threads) {
+    case 256: return launch_tp<T, VEC, 256>(p, plan, s);
+    case 512: return launch_tp<T, VEC, 512>(p, plan, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_twopass(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
 {
     if (p.dtype == SOFTMAX_F32)
-        return plan.vec == 4 ? launch_tp<float, 4>(p, plan, s) : launch_tp<float, 1>(p, plan, s);
-    return plan.vec == 8 ? launch_tp<BF16Bits, 8>(p, plan, s) : launch_tp<BF16Bits, 1>(p, plan, s);
+        return plan.vec == 4 ? launch_tp_threads<float, 4>(p, plan, s)
+                             : launch_tp_threads<float, 1>(p, plan, s);
+    return plan.vec == 8 ? launch_tp_threads<BF16Bits, 8>(p, plan, s)
+                         : launch_tp_threads<BF16Bits, 1>(p, plan, s);
 }
 
 }  // namespace rwsm

@@ -60,9 +60,11 @@ def test_scheduler_paths_for_the_five_workloads(lib):
     assert (p.stages, p.smem_bytes) == (2, 32768)
     p = plan(262144, 127, in_row_stride=128, out_row_stride=127)
     assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 0, 1, 4, 4)
-    p = plan(256, 262144)
-    assert (p.path, p.cluster, p.slice_cols, p.threads, p.grid) == (rws.PATH_TWOPASS, 4, 65536, 512, 0)
-    assert (p.vec, p.out_vec) == (4, 4)
+    p = plan(256, 262144)                                 # staged two-pass, 16 KB chunks
+    assert (p.path, p.cluster, p.slice_cols, p.threads, p.grid) == (rws.PATH_TWOPASS, 4, 65536, 256, 0)
+    assert (p.vec, p.out_vec, p.bulk_copy, p.chunks, p.stages, p.smem_bytes) == (4, 4, 1, 4, 4, 65536)
+    p = plan(256, 262144, in_ptr=(1 << 20) + 4)           # unaligned: register two-pass
+    assert (p.path, p.bulk_copy, p.vec, p.threads) == (rws.PATH_TWOPASS, 0, 1, 512)
 
 
 def test_scheduler_boundaries(lib):
