@@ -113,17 +113,28 @@ int softmax_rows_path(const void* in, void* out, int64_t n_rows, int64_t n_cols,
                       void* stream, int path);
 
 /*
- * softmax_rows_host: the same operation on HOST buffers, staged through
- * caller-owned device buffers.  Queues, on `stream`: a copy of the strided
- * host input into d_in (dense, row stride n_cols), the softmax from d_in into
- * d_out (dense), and a copy of d_out into the strided host output.  Returns
- * once queued; the caller synchronises `stream` before reading h_out.
+ * softmax_rows_host: the same operation on HOST buffers.  Two modes:
  *
- *   h_in, h_out      host pointers; pinned (page-locked) memory gives
- *                    asynchronous full-bandwidth copies, pageable memory
- *                    works but the copies then block the calling thread.
- *   d_in, d_out      device buffers of at least n_rows * n_cols elements
- *                    each; d_in == d_out is allowed (in place on the device).
+ *  staged  (d_in and d_out given): queues on `stream` a copy of the strided
+ *          host input into d_in (dense, row stride n_cols), the softmax from
+ *          d_in into d_out (dense), and a copy of d_out into the strided host
+ *          output.
+ *  direct  (d_in == d_out == NULL): h_in and h_out must be host memory the
+ *          device can access (pinned / registered with the CUDA runtime, or
+ *          managed); the kernel reads the input rows and writes the output
+ *          rows in host memory over the host link, with no device buffers and
+ *          no separate copies.  Pageable (unregistered) memory returns
+ *          SOFTMAX_ERR_INVALID_ARG in this mode.
+ *
+ * Returns once queued; the caller synchronises `stream` before reading h_out.
+ *
+ *   h_in, h_out      host pointers.  Staged: pinned memory gives asynchronous
+ *                    full-bandwidth copies, pageable memory works but the
+ *                    copies then block the calling thread.
+ *   d_in, d_out      staged: device buffers of at least n_rows * n_cols
+ *                    elements each (d_in == d_out is allowed: in place on the
+ *                    device); both NULL selects the direct mode; exactly one
+ *                    NULL is SOFTMAX_ERR_INVALID_ARG.
  *   other arguments  as for softmax_rows (strides describe the host buffers).
  *
  * Errors as for softmax_rows; a failed copy returns SOFTMAX_ERR_CUDA.

@@ -211,30 +211,42 @@ def softmax_rows(x, out=None, stream=None, path: int = PATH_AUTO):
     return out
 
 
-def softmax_rows_host(h_in, h_out, d_in, d_out, stream=None, path: int = PATH_AUTO):
-    """Softmax of host (CPU) rows through caller-owned device buffers.
+def softmax_rows_host(h_in, h_out, d_in=None, d_out=None, stream=None, device=None):
+    """Softmax of host (CPU) rows.
 
-    h_in / h_out: CPU tensors (pinned for asynchronous copies), 1-D or 2-D with
-    unit column stride.  d_in / d_out: CUDA tensors with at least
-    rows*cols elements each (may be the same tensor).  Queued on ``stream``;
-    synchronise before reading h_out.
+    h_in / h_out: CPU tensors, 1-D or 2-D with unit column stride.
+    Staged mode (d_in, d_out given): CUDA tensors with at least rows*cols
+    elements each (may be the same tensor); pinned h_in / h_out make the
+    copies asynchronous.  Direct mode (no device tensors): h_in / h_out must
+    be pinned; the kernel reads and writes them over the host link.  Queued
+    on ``stream``; synchronise before reading h_out.
     """
     import torch
     if h_in.is_cuda or h_out.is_cuda:
         raise ValueError("softmax_rows_host: h_in and h_out must be host tensors")
     dt = _dtype_code(h_in)
-    if h_out.dtype != h_in.dtype or d_in.dtype != h_in.dtype or d_out.dtype != h_in.dtype:
+    if h_out.dtype != h_in.dtype:
         raise ValueError("softmax_rows_host: all buffers must share one dtype")
     n_rows, n_cols, ld_in = _as_rows(h_in, "h_in")
     r2, c2, ld_out = _as_rows(h_out, "h_out")
     if (r2, c2) != (n_rows, n_cols):
         raise ValueError("softmax_rows_host: h_out shape differs from h_in")
-    if d_in.numel() < n_rows * n_cols or d_out.numel() < n_rows * n_cols:
-        raise ValueError("softmax_rows_host: device buffers too small")
-    with torch.cuda.device(d_in.device):
+    if (d_in is None) != (d_out is None):
+        raise ValueError("softmax_rows_host: give both device buffers or neither")
+    if d_in is not None:
+        if d_in.dtype != h_in.dtype or d_out.dtype != h_in.dtype:
+            raise ValueError("softmax_rows_host: all buffers must share one dtype")
+        if d_in.numel() < n_rows * n_cols or d_out.numel() < n_rows * n_cols:
+            raise ValueError("softmax_rows_host: device buffers too small")
+        device = d_in.device
+        dptr_in, dptr_out = d_in.data_ptr(), d_out.data_ptr()
+    else:
+        device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        dptr_in = dptr_out = None
+    with torch.cuda.device(device):
         st = lib().softmax_rows_host(h_in.data_ptr(), h_out.data_ptr(), n_rows, n_cols, ld_in,
-                                     ld_out, dt, d_in.data_ptr(), d_out.data_ptr(),
-                                     _stream_handle(stream, d_in.device))
+                                     ld_out, dt, dptr_in, dptr_out,
+                                     _stream_handle(stream, device))
     if st != OK:
         raise SoftmaxError(st, "softmax_rows_host")
     return h_out

@@ -15,6 +15,7 @@ struct Problem {
     void* out;
     int64_t n_rows, n_cols, ld_in, ld_out;
     int dtype;
+    bool no_bulk = false;   // rows live in host memory: no cp.async.bulk staging
 };
 
 // Scheduler (plan.cpp): validation and the path / launch-shape decision.

@@ -10,12 +10,13 @@
 //   CTA      row <= 32 KB: a persistent CTA per row at a time, the row staged
 //            by cp.async.bulk and held in registers (one ring stage: the
 //            register copy is the second buffer).
-//   CLUSTER  longer rows whose slices fit 32 KB on a cluster of <= 16 CTAs,
-//            for fp32 only up to 64 KB rows: one HBM pass, slices on
-//            different SMs, max and sum exchanged through distributed shared
+//   CLUSTER  rows of 32..64 KB: one HBM pass, a cluster of CTAs holding
+//            <= 32 KB slices, max and sum exchanged through distributed shared
 //            memory.  (When forced: slices up to 128 KB fp32 / 64 KB bf16.)
-//   TWOPASS  longer rows: a cluster of 2..16 CTAs (about 256 KB of row per
-//            CTA) streams the row twice; the second read mostly hits L2.
+//   TWOPASS  longer rows: a cluster of 1..16 CTAs (about 128 KB of row per
+//            CTA) streams the row twice through a cp.async.bulk chunk ring;
+//            the second read mostly hits L2.  Unaligned input: the register
+//            two-pass kernel (about 256 KB per CTA).
 //
 // Whole waves (the "Block Occupancy: tail effect" rule of the cs336 lecture
 // 6 notes): every grid is persistent, sized at launch to the number of CTAs
@@ -33,10 +34,11 @@ constexpr int64_t kWarpMaxCols = 1024;
 constexpr int64_t kSliceTargetBytes = 32 * 1024;   // preferred slice (CTA path: whole row)
 constexpr int kSliceStages = 1;                    // ring stages of the slice kernel
 constexpr int64_t kTileRingBudgetBytes = 32 * 1024; // shared memory for the tile ring, per CTA
-constexpr int64_t kClusterMaxRowBytesF32 = 64 * 1024;  // fp32: longer rows take TWOPASS
-constexpr int64_t kTwoPassBytesPerCta = 256 * 1024;
-constexpr int kStreamThreads = 256;                 // staged two-pass: 16 KB chunks
-constexpr int kStreamStages = 4;
+constexpr int64_t kClusterMaxRowBytes = 64 * 1024;  // longer rows take TWOPASS
+constexpr int64_t kTwoPassBytesPerCta = 256 * 1024;      // register two-pass
+constexpr int64_t kStreamBytesPerCta = 128 * 1024;       // staged two-pass
+constexpr int kStreamThreads = 256;                      // staged two-pass: 16 KB chunks
+constexpr int kStreamStages = 2;
 constexpr int kMaxStages = 8;                       // must match row_slices.cu
 constexpr int kMaxSliceThreads = 1024;
 constexpr int kSmemReserve = 2048;                  // static smem + slack
@@ -180,7 +182,8 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
 
     const int esz = esize(p.dtype);
     const int vmax = 16 / esz;
-    const bool in_al = aligned16(p.in, p.n_rows, p.ld_in, esz);
+    const bool in_vec = aligned16(p.in, p.n_rows, p.ld_in, esz);   // 16-byte input rows
+    const bool in_al = in_vec && !p.no_bulk;                        // ... and staging allowed
     const bool out_al = aligned16(p.out, p.n_rows, p.ld_out, esz);
     const int64_t row_bytes = p.n_cols * esz;
     const int64_t smem_cap = static_cast<int64_t>(dev.max_smem_per_block_optin) - kSmemReserve;
@@ -209,7 +212,7 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
             path = SOFTMAX_PATH_WARP;
         else if (row_bytes <= kSliceTargetBytes)
             path = SOFTMAX_PATH_CTA;
-        else if (cluster_for(false) && (esz != 4 || row_bytes <= kClusterMaxRowBytesF32))
+        else if (cluster_for(false) && row_bytes <= kClusterMaxRowBytes)
             path = SOFTMAX_PATH_CLUSTER;
         else
             path = SOFTMAX_PATH_TWOPASS;
@@ -249,7 +252,7 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
             q.stages = static_cast<int>(stages);
             q.smem_bytes = static_cast<int>(stages * stage_bytes);
         } else {
-            q.vec = (in_al && out_al) ? vmax : 1;
+            q.vec = (in_vec && out_al) ? vmax : 1;
             q.out_vec = q.vec;
             q.chunks = static_cast<int>(pow2_ceil(ceil_div(p.n_cols, 32 * q.vec)));
             q.rows_per_warp = warp_rows_for(q.vec * q.chunks);
@@ -274,7 +277,7 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
         const int64_t stages = kSliceStages;
         q.cluster = cs;
         q.slice_cols = slice;
-        q.vec = vmax;
+        q.vec = in_vec ? vmax : 1;        // global input loads (staged: always 16 bytes)
         q.out_vec = out_al ? vmax : 1;
         q.bulk_copy = in_al ? 1 : 0;
         q.threads = threads;
@@ -285,10 +288,10 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
         break;
     }
     case SOFTMAX_PATH_TWOPASS: {
-        // About 256 KB of row per CTA; at least 2 CTAs when chosen
-        // automatically (forced on short rows a single CTA is allowed).
-        int64_t cs = pow2_ceil(ceil_div(row_bytes, kTwoPassBytesPerCta));
-        if (automatic && cs < 2)
+        // About 128 KB of row per CTA when staged, 256 KB (and at least two
+        // CTAs) for the register kernel; a single CTA when forced on short rows.
+        int64_t cs = pow2_ceil(ceil_div(row_bytes, in_al ? kStreamBytesPerCta : kTwoPassBytesPerCta));
+        if (automatic && !in_al && cs < 2)
             cs = 2;
         if (cs > max_cluster)
             cs = pow2_floor(max_cluster);
@@ -305,7 +308,7 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
             q.stages = kStreamStages;
             q.smem_bytes = q.stages * q.threads * q.chunks * 16;
         } else {
-            q.vec = (in_al && out_al) ? vmax : 1;
+            q.vec = (in_vec && out_al) ? vmax : 1;
             q.out_vec = q.vec;
             q.threads = 512;
         }
@@ -329,7 +332,8 @@ int check_plan(const softmax_device_desc_t& dev, const Problem& p, const softmax
         return SOFTMAX_ERR_INVALID_ARG;
     const int esz = esize(p.dtype);
     const int vmax = 16 / esz;
-    const bool in_al = aligned16(p.in, p.n_rows, p.ld_in, esz);
+    const bool in_vec = aligned16(p.in, p.n_rows, p.ld_in, esz);
+    const bool in_al = in_vec && !p.no_bulk;
     const bool out_al = aligned16(p.out, p.n_rows, p.ld_out, esz);
     const int64_t smem_cap = static_cast<int64_t>(dev.max_smem_per_block_optin) - kSmemReserve;
     const int max_cluster = dev.max_cluster < 1 ? 1 : (dev.max_cluster > 16 ? 16 : dev.max_cluster);
@@ -345,7 +349,7 @@ int check_plan(const softmax_device_desc_t& dev, const Problem& p, const softmax
             int64_t{32} * q.vec * q.chunks < p.n_cols)
             return SOFTMAX_ERR_INVALID_ARG;
         if (q.bulk_copy == 0)
-            return vec_ok(q.vec, in_al && out_al) ? SOFTMAX_OK : SOFTMAX_ERR_INVALID_ARG;
+            return vec_ok(q.vec, in_vec && out_al) ? SOFTMAX_OK : SOFTMAX_ERR_INVALID_ARG;
         // Staged tile kernel.
         const int64_t row_pad = round_up(p.n_cols, vmax);
         if (q.bulk_copy != 1 || !in_al || !vec_ok(q.vec, out_al) || q.slice_cols != row_pad ||
@@ -363,8 +367,9 @@ int check_plan(const softmax_device_desc_t& dev, const Problem& p, const softmax
         const int cs = q.cluster;
         if (q.path == SOFTMAX_PATH_CTA ? cs != 1 : !pow2_in(cs, 2, max_cluster))
             return SOFTMAX_ERR_INVALID_ARG;
-        if (q.vec != vmax || q.slice_cols <= 0 || q.slice_cols % vmax ||
-            q.slice_cols * cs < p.n_cols)
+        if (q.slice_cols <= 0 || q.slice_cols % vmax || q.slice_cols * cs < p.n_cols)
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (q.bulk_copy ? q.vec != vmax : !vec_ok(q.vec, in_vec))
             return SOFTMAX_ERR_INVALID_ARG;
         if (!pow2_in(q.threads, 128, kMaxSliceThreads) ||
             !pow2_in(q.chunks, 1, max_vectors_per_thread(esz)) ||
@@ -392,8 +397,8 @@ int check_plan(const softmax_device_desc_t& dev, const Problem& p, const softmax
             (q.threads != 256 && q.threads != 512))
             return SOFTMAX_ERR_INVALID_ARG;
         if (q.bulk_copy == 0)
-            return (vec_ok(q.vec, in_al && out_al) && q.out_vec == q.vec) ? SOFTMAX_OK
-                                                                            : SOFTMAX_ERR_INVALID_ARG;
+            return (vec_ok(q.vec, in_vec && out_al) && q.out_vec == q.vec) ? SOFTMAX_OK
+                                                                             : SOFTMAX_ERR_INVALID_ARG;
         // Staged two-pass (ring of chunks of threads * chunks * 16 bytes).
         if (q.bulk_copy != 1 || !in_al || q.vec != vmax || !vec_ok(q.out_vec, out_al) ||
             (q.chunks != 2 && q.chunks != 4) || q.stages < 1 || q.stages > kMaxStages ||

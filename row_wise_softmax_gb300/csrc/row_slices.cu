@@ -24,8 +24,9 @@
 // split over the SMs of a cluster when it is longer than one SM can hold;
 // tiling a row over several blocks and combining their partial results is the
 // "Level 2: Row Sum (tiling)" pattern of the cs336 lecture 6 notes.  Without
-// 16-byte alignment the kernel reads the slice straight into registers with
-// plain loads (no ring).
+// staging (input rows not 16-byte aligned, or rows in host memory) the kernel
+// reads the slice straight into registers (no ring), with 16-byte loads when
+// the rows allow.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -74,7 +75,7 @@ __device__ __forceinline__ float cluster_reduce(float v, float* slot, int cs)
 template <typename T, int THREADS, int NV, bool BULK, bool OUTVEC>
 __global__ void __launch_bounds__(THREADS)
 row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
-                  int64_t ld_out, int slice_cols, int cs, int stages)
+                  int64_t ld_out, int slice_cols, int cs, int stages, int in_vec)
 {
     constexpr int VEC = Elem<T>::kVec16;
     constexpr int NW = THREADS / 32;
@@ -174,6 +175,19 @@ row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in
                 const int64_t next = row + static_cast<int64_t>(stages) * n_clusters;
                 if (next < n_rows)
                     issue(s, next);
+            }
+        } else if (in_vec) {
+            // No staging (rows in host memory): 16-byte loads into registers.
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const int v = tid + k * THREADS;
+                if (v < nv) {
+                    load_vec_masked<T, VEC>(src, v * VEC, len, &x[k * VEC]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j)
+                        x[k * VEC + j] = kNegInf;
+                }
             }
         } else {
             // Input rows not 16-byte aligned: element loads only (same
@@ -351,7 +365,8 @@ cudaError_t launch_rs(const Problem& p, const softmax_plan_t& plan, cudaStream_t
     cfg.numAttrs = cs > 1 ? 1 : 0;
     err = cudaLaunchKernelEx(&cfg, k, static_cast<const T*>(p.in), static_cast<T*>(p.out),
                              p.n_rows, static_cast<int>(p.n_cols), p.ld_in, p.ld_out,
-                             static_cast<int>(plan.slice_cols), cs, plan.stages);
+                             static_cast<int>(plan.slice_cols), cs, plan.stages,
+                             plan.vec > 1 ? 1 : 0);
     note_launch();
     return err;
 }

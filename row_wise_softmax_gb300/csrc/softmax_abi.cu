@@ -246,6 +246,24 @@ int softmax_rows(const void* in, void* out, int64_t n_rows, int64_t n_cols,
                              stream, SOFTMAX_PATH_AUTO);
 }
 
+namespace {
+
+// Device address of host memory the current device can access (pinned or
+// registered host memory, or managed memory); NULL otherwise.
+void* device_view(const void* p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (a.type != cudaMemoryTypeHost && a.type != cudaMemoryTypeManaged)
+        return nullptr;
+    return a.devicePointer;
+}
+
+}  // namespace
+
 int softmax_rows_host(const void* h_in, void* h_out, int64_t n_rows, int64_t n_cols,
                       int64_t in_row_stride, int64_t out_row_stride, int dtype,
                       void* d_in, void* d_out, void* stream)
@@ -255,6 +273,26 @@ int softmax_rows_host(const void* h_in, void* h_out, int64_t n_rows, int64_t n_c
         return st;
     if (n_rows == 0 || n_cols == 0)
         return SOFTMAX_OK;
+    if (!d_in && !d_out) {
+        // Direct: the kernel reads and writes the host rows over the host link.
+        softmax_device_desc_t d;
+        const int ds = rwsm::current_device(&d);
+        if (ds != SOFTMAX_OK)
+            return ds;
+        const void* vin = device_view(h_in);
+        void* vout = device_view(h_out);
+        if (!vin || !vout)
+            return SOFTMAX_ERR_INVALID_ARG;
+        Problem p{vin, vout, n_rows, n_cols, in_row_stride, out_row_stride, dtype};
+        p.no_bulk = true;
+        softmax_plan_t plan;
+        const int ps = rwsm::make_plan(d, p, SOFTMAX_PATH_AUTO, &plan);
+        if (ps != SOFTMAX_OK)
+            return ps;
+        return rwsm::launch_path(p, plan, static_cast<cudaStream_t>(stream));
+    }
+    if (!d_in || !d_out)
+        return SOFTMAX_ERR_INVALID_ARG;
     // Device side: dense rows; in place allowed.
     st = rwsm::validate(d_in, d_out, n_rows, n_cols, n_cols, n_cols, dtype);
     if (st != SOFTMAX_OK)

@@ -61,8 +61,8 @@ def test_scheduler_paths_for_the_five_workloads(lib):
     p = plan(262144, 127, in_row_stride=128, out_row_stride=127)
     assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 0, 1, 4, 4)
     p = plan(256, 262144)                                 # staged two-pass, 16 KB chunks
-    assert (p.path, p.cluster, p.slice_cols, p.threads, p.grid) == (rws.PATH_TWOPASS, 4, 65536, 256, 0)
-    assert (p.vec, p.out_vec, p.bulk_copy, p.chunks, p.stages, p.smem_bytes) == (4, 4, 1, 4, 4, 65536)
+    assert (p.path, p.cluster, p.slice_cols, p.threads, p.grid) == (rws.PATH_TWOPASS, 8, 32768, 256, 0)
+    assert (p.vec, p.out_vec, p.bulk_copy, p.chunks, p.stages, p.smem_bytes) == (4, 4, 1, 4, 2, 32768)
     p = plan(256, 262144, in_ptr=(1 << 20) + 4)           # unaligned: register two-pass
     assert (p.path, p.bulk_copy, p.vec, p.threads) == (rws.PATH_TWOPASS, 0, 1, 512)
 
@@ -73,15 +73,16 @@ def test_scheduler_boundaries(lib):
     assert plan(1, 8192).path == rws.PATH_CTA             # 32 KB row
     p = plan(1, 8196)
     assert p.path == rws.PATH_CLUSTER and p.cluster == 2 and p.stages == 1
-    assert plan(1, 16384).path == rws.PATH_CLUSTER         # fp32 single pass up to 64 KB
+    assert plan(1, 16384).path == rws.PATH_CLUSTER         # single pass up to 64 KB rows
     p = plan(1, 16388)
-    assert p.path == rws.PATH_TWOPASS and p.cluster == 2
-    assert plan(1, 65536).cluster == 2 and plan(1, 65540).cluster == 2
-    assert plan(1, 131072).cluster == 2 and plan(1, 131076).cluster == 4
+    assert p.path == rws.PATH_TWOPASS and p.cluster == 1 and p.bulk_copy == 1
+    assert plan(1, 32768).cluster == 1 and plan(1, 32772).cluster == 2
+    assert plan(1, 131072).cluster == 4 and plan(1, 262144).cluster == 8
+    assert plan(1, 4 << 20).cluster == 16
     assert plan(1, 16384, dtype=rws.BF16).path == rws.PATH_CTA
     assert plan(1, 16392, dtype=rws.BF16).path == rws.PATH_CLUSTER
-    assert plan(1, 16 * 16384, dtype=rws.BF16).path == rws.PATH_CLUSTER
-    assert plan(1, 16 * 16384 + 8, dtype=rws.BF16).path == rws.PATH_TWOPASS
+    assert plan(1, 32768, dtype=rws.BF16).path == rws.PATH_CLUSTER
+    assert plan(1, 32776, dtype=rws.BF16).path == rws.PATH_TWOPASS
     forced = plan(1, 16 * 32768, path=rws.PATH_CLUSTER)    # forced: 128 KB slices
     assert forced.cluster == 16 and forced.threads == 1024 and forced.chunks == 8
     assert forced.smem_bytes == 131072
@@ -124,10 +125,10 @@ def test_scheduler_forced_paths(lib):
     assert e.value.status == rws.ERR_UNSUPPORTED
     small_cluster = dict(GB, max_cluster=8)
     assert rws.plan_for_device(small_cluster, 4, 262144).path == rws.PATH_TWOPASS
+    assert rws.plan_for_device(small_cluster, 4, 4 << 20).cluster == 8
     p = rws.plan_for_device(small_cluster, 4, 262144, path=rws.PATH_CLUSTER)
     assert p.path == rws.PATH_CLUSTER and p.cluster == 8 and p.slice_cols == 32768
     assert p.threads == 1024 and p.stages == 1 and p.chunks == 8
-    assert rws.plan_for_device(small_cluster, 4, 40_000_000).cluster == 8
 
 
 def test_validation(lib):

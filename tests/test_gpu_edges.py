@@ -191,3 +191,45 @@ def test_bounded_wait_self_test_reports_timeout():
     assert rws.softmax_rows_ptr(x.data_ptr(), y.data_ptr(), 16, 4096, 4096, 4096, wl.F32) == rws.OK
     torch.cuda.synchronize()
     parity.compare(parity.host_output(y, w), parity.expected(w), wl.F32, "after self-test")
+
+
+def test_host_direct_mode_pinned_buffers():
+    """Direct mode: no device buffers; the kernel reads and writes pinned host rows."""
+    for w in (wl.masked_f32(300), wl.short_f32(5000), wl.causal_bf16(700),
+              wl.random_rows(3, 100_000, seed=4, scale=3.0)):
+        if w.dtype == wl.F32:
+            h_in = torch.from_numpy(w.data).pin_memory()
+            h_out = torch.full((w.out_elems,), -1.0).pin_memory()
+        else:
+            h_in = torch.from_numpy(w.data.view(np.int16)).view(torch.bfloat16).pin_memory()
+            h_out = torch.zeros(w.out_elems, dtype=torch.bfloat16).pin_memory()
+        s = torch.cuda.Stream()
+        before = rws.launch_count()
+        st = rws.lib().softmax_rows_host(h_in.data_ptr(), h_out.data_ptr(), w.n_rows, w.n_cols,
+                                         w.in_row_stride, w.out_row_stride, w.dtype,
+                                         None, None, s.cuda_stream)
+        assert st == rws.OK, rws.status_string(st)
+        s.synchronize()
+        assert rws.launch_count() - before == 1
+        flat = h_out.view(torch.int16).numpy().view(np.uint16) if w.dtype == wl.BF16 else h_out.numpy()
+        idx = np.arange(w.n_rows)[:, None] * w.out_row_stride + np.arange(w.n_cols)[None, :]
+        parity.compare(flat[idx], parity.expected(w), w.dtype, "direct " + w.name)
+
+
+def test_host_direct_mode_rejects_pageable_and_half_staged():
+    x = torch.randn(16, 64)                        # pageable: not device-accessible
+    y = torch.empty_like(x)
+    before = rws.launch_count()
+    st = rws.lib().softmax_rows_host(x.data_ptr(), y.data_ptr(), 16, 64, 64, 64, wl.F32,
+                                     None, None, None)
+    assert st == rws.ERR_INVALID_ARG
+    d = torch.empty(16 * 64, device="cuda")
+    st = rws.lib().softmax_rows_host(x.data_ptr(), y.data_ptr(), 16, 64, 64, 64, wl.F32,
+                                     d.data_ptr(), None, None)
+    assert st == rws.ERR_INVALID_ARG
+    assert rws.launch_count() == before
+    xp, yp = x.pin_memory(), torch.empty_like(x).pin_memory()
+    rws.softmax_rows_host(xp, yp)                  # Python wrapper, direct mode
+    torch.cuda.synchronize()
+    ref = torch.softmax(xp.double(), dim=-1)
+    assert float((yp.double() - ref).abs().max()) <= parity.F32_ABS_TOL
