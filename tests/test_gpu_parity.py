@@ -119,11 +119,15 @@ def test_twopass_long_row_automatic():
     parity.compare(run(w), parity.expected(w), wl.F32, "twopass auto")
 
 
-def test_bf16_long_rows_cluster():
-    w = wl.random_rows(6, 250_000, dtype=wl.BF16, seed=8, scale=6.0)
+def test_bf16_long_rows_cluster_and_twopass():
+    w = wl.random_rows(6, 30_000, dtype=wl.BF16, seed=8, scale=6.0)       # 60 KB rows
     p = rws.plan(w.n_rows, w.n_cols, dtype=wl.BF16)
     assert p.path == rws.PATH_CLUSTER
     parity.compare(run(w), parity.expected(w), wl.BF16, "bf16 cluster")
+    w = wl.random_rows(6, 250_000, dtype=wl.BF16, seed=8, scale=6.0)      # 500 KB rows
+    p = rws.plan(w.n_rows, w.n_cols, dtype=wl.BF16)
+    assert p.path == rws.PATH_TWOPASS and p.bulk_copy == 1
+    parity.compare(run(w), parity.expected(w), wl.BF16, "bf16 two-pass")
 
 
 def test_reduced_workloads_every_path():
