@@ -239,6 +239,24 @@ __device__ __forceinline__ void lds_vec(const T* p, float* v)
     }
 }
 
+// ------------------------------------------- programmatic dependent launch
+// Kernels are launched with programmatic stream serialisation: the next
+// kernel in the stream may start its CTAs once every CTA of this grid has
+// called pdl_launch_dependents() (done first thing: the grids are persistent
+// and already resident), and every kernel calls pdl_wait() before its first
+// global-memory access, which returns once the preceding grid has completed
+// and its writes are visible.  Launched without the attribute (or after a
+// kernel that does not trigger) both are no-ops in effect.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------- L2 eviction priorities
 // Cache policies for loads and stores that should stay in L2 (evict_last:
 // data read again soon) or leave it first (evict_first: streamed once).

@@ -43,6 +43,25 @@ unsigned read_error_tile_rows(bool clear);
 unsigned read_error_stream_rows(bool clear);
 cudaError_t launch_selftest_wait(cudaStream_t s);
 
+// Launch attributes shared by every kernel launch: a cluster dimension when
+// cs > 1, and programmatic stream serialisation (the kernels begin with
+// griddepcontrol.wait).  Returns the number of attributes written (<= 2).
+inline int launch_attrs(cudaLaunchAttribute* a, int cs)
+{
+    int n = 0;
+    if (cs > 1) {
+        a[n].id = cudaLaunchAttributeClusterDimension;
+        a[n].val.clusterDim.x = static_cast<unsigned>(cs);
+        a[n].val.clusterDim.y = 1;
+        a[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    a[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    return n;
+}
+
 // Helpers implemented in softmax_abi.cu.
 int resident_ctas(const void* kernel, int threads, int smem_bytes);  // whole-GPU CTA slots
 int sm_count_current();

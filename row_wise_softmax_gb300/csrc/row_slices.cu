@@ -119,6 +119,7 @@ row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in
     };
 
     bool failed = false;                      // CTA-uniform
+    pdl_launch_dependents();
     if constexpr (BULK) {
         if (tid == 0) {
             for (int s = 0; s < stages; ++s) {
@@ -132,12 +133,15 @@ row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in
             for (int e = bulk_elems + tid; e < nv * VEC; e += THREADS)
                 set_neg_inf(stage_ptr(s) + e);
         __syncthreads();
+        pdl_wait();
         if (tid == 0)
             for (int s = 0; s < stages; ++s) {
                 const int64_t row = cluster_id + s * n_clusters;
                 if (row < n_rows)
                     issue(s, row);
             }
+    } else {
+        pdl_wait();
     }
 
     int64_t i = 0;
@@ -329,11 +333,8 @@ cudaError_t launch_rs(const Problem& p, const softmax_plan_t& plan, cudaStream_t
         attrs.flags_set[dev].store(true);
     }
     const int cs = plan.cluster;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    const int n_attr = launch_attrs(attr, cs);
     int64_t clusters = plan.grid > 0 ? plan.grid / cs : 0;
     if (clusters <= 0) {
         // Persistent: as many CTAs (clusters) as can be resident at once.
@@ -344,7 +345,7 @@ cudaError_t launch_rs(const Problem& p, const softmax_plan_t& plan, cudaStream_t
             q.blockDim = dim3(THREADS, 1, 1);
             q.dynamicSmemBytes = static_cast<size_t>(smem);
             q.attrs = attr;
-            q.numAttrs = 1;
+            q.numAttrs = 1;                   // the cluster dimension
             if (cudaOccupancyMaxActiveClusters(&active, k, &q) != cudaSuccess) {
                 cudaGetLastError();
                 active = 0;
@@ -362,7 +363,7 @@ cudaError_t launch_rs(const Problem& p, const softmax_plan_t& plan, cudaStream_t
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = cs > 1 ? 1 : 0;
+    cfg.numAttrs = static_cast<unsigned>(n_attr);
     err = cudaLaunchKernelEx(&cfg, k, static_cast<const T*>(p.in), static_cast<T*>(p.out),
                              p.n_rows, static_cast<int>(p.n_cols), p.ld_in, p.ld_out,
                              static_cast<int>(plan.slice_cols), cs, plan.stages,

@@ -90,6 +90,7 @@ stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t 
         }
     };
 
+    pdl_launch_dependents();
     if (tid == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
@@ -98,6 +99,7 @@ stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t 
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();
     if (tid == 0)
         for (int64_t q = 0; q < stages && q < total_q; ++q)
             issue(q);
@@ -249,11 +251,8 @@ cudaError_t launch_stream(const Problem& p, const softmax_plan_t& plan, cudaStre
         attrs.flags_set[dev].store(true);
     }
     const int cs = plan.cluster;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    const int n_attr = launch_attrs(attr, cs);
     int64_t clusters = plan.grid > 0 ? plan.grid / cs : 0;
     if (clusters <= 0) {
         int active = 0;
@@ -281,7 +280,7 @@ cudaError_t launch_stream(const Problem& p, const softmax_plan_t& plan, cudaStre
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = cs > 1 ? 1 : 0;
+    cfg.numAttrs = static_cast<unsigned>(n_attr);
     err = cudaLaunchKernelEx(&cfg, k, static_cast<const T*>(p.in), static_cast<T*>(p.out),
                              p.n_rows, p.n_cols, p.ld_in, p.ld_out, plan.slice_cols, cs,
                              plan.stages);

@@ -98,6 +98,7 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
         }
     };
 
+    pdl_launch_dependents();
     if (tid == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
@@ -106,6 +107,7 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();
     if (tid == 0)
         for (int s = 0; s < stages; ++s) {
             const int64_t t = blockIdx.x + static_cast<int64_t>(s) * gridDim.x;
@@ -228,11 +230,19 @@ cudaError_t launch_tile(const Problem& p, const softmax_plan_t& plan, cudaStream
     if (grid < 1)
         grid = 1;
     const int row_pad = static_cast<int>(plan.slice_cols);
-    k<<<static_cast<unsigned>(grid), kTileThreads, smem, s>>>(
-        static_cast<const T*>(p.in), static_cast<T*>(p.out), p.n_rows, static_cast<int>(p.n_cols),
-        p.ld_in, p.ld_out, plan.rows_per_warp, plan.stages, row_pad);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kTileThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = static_cast<unsigned>(launch_attrs(attr, 1));
+    err = cudaLaunchKernelEx(&cfg, k, static_cast<const T*>(p.in), static_cast<T*>(p.out),
+                             p.n_rows, static_cast<int>(p.n_cols), p.ld_in, p.ld_out,
+                             plan.rows_per_warp, plan.stages, row_pad);
     note_launch();
-    return cudaGetLastError();
+    return err;
 }
 
 template <typename T, int VEC>

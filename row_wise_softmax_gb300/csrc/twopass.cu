@@ -102,6 +102,8 @@ twopass_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_i
     const int64_t nv = (len + VEC - 1) / VEC;
     const uint64_t keep = policy_evict_last();     // first read: stay in L2
     const uint64_t stream = policy_evict_first();  // second read and stores
+    pdl_launch_dependents();
+    pdl_wait();
 
     int slot = 0;
     for (int64_t row = cluster_id; row < n_rows; row += n_clusters, slot ^= 1) {
@@ -196,13 +198,9 @@ cudaError_t launch_tp(const Problem& p, const softmax_plan_t& plan, cudaStream_t
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * cs), 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
     cfg.attrs = attr;
-    cfg.numAttrs = cs > 1 ? 1 : 0;
+    cfg.numAttrs = static_cast<unsigned>(launch_attrs(attr, cs));
     err = cudaLaunchKernelEx(&cfg, k, static_cast<const T*>(p.in), static_cast<T*>(p.out),
                              p.n_rows, p.n_cols, p.ld_in, p.ld_out, plan.slice_cols, cs);
     note_launch();

@@ -83,6 +83,8 @@ warp_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols,
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int64_t n_groups = (n_rows + ROWS - 1) / ROWS;
+    pdl_launch_dependents();
+    pdl_wait();
     if (warp0 >= n_groups)
         return;
 
@@ -130,11 +132,18 @@ static cudaError_t launch_one(const Problem& p, const softmax_plan_t& plan, cuda
     }
     if (grid < 1)
         grid = 1;
-    k<<<static_cast<unsigned>(grid), kWarpPathThreads, 0, s>>>(
-        static_cast<const T*>(p.in), static_cast<T*>(p.out), p.n_rows,
-        static_cast<int>(p.n_cols), p.ld_in, p.ld_out);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kWarpPathThreads, 1, 1);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = static_cast<unsigned>(launch_attrs(attr, 1));
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, k, static_cast<const T*>(p.in),
+                                               static_cast<T*>(p.out), p.n_rows,
+                                               static_cast<int>(p.n_cols), p.ld_in, p.ld_out);
     note_launch();
-    return cudaGetLastError();
+    return err;
 }
 
 template <typename T, int VEC>
