@@ -119,7 +119,11 @@ row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in
     };
 
     bool failed = false;                      // CTA-uniform
-    pdl_launch_dependents();
+    // Cluster launches let the next grid start only after the row loop:
+    // clusters of the next grid placed early into leftover slots measured
+    // slower.  Single-CTA launches let it start at once.
+    if (cs == 1)
+        pdl_launch_dependents();
     if constexpr (BULK) {
         if (tid == 0) {
             for (int s = 0; s < stages; ++s) {
@@ -253,6 +257,8 @@ row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in
             }
         }
     }
+    if (cs > 1)
+        pdl_launch_dependents();
     if (cs > 1)
         cooperative_groups::this_cluster().sync();  // peers may still read `part`
     if (BULK && failed && tid == 0) {

@@ -90,7 +90,11 @@ stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t 
         }
     };
 
-    pdl_launch_dependents();
+    // Cluster launches let the next grid start only after the row loop:
+    // clusters of the next grid placed early into leftover slots measured
+    // slower.  Single-CTA launches let it start at once.
+    if (cs == 1)
+        pdl_launch_dependents();
     if (tid == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
@@ -191,6 +195,8 @@ stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t 
         }
         __syncthreads();        // red_* are rewritten by the next row's reduction
     }
+    if (cs > 1)
+        pdl_launch_dependents();
     if (cs > 1)
         cooperative_groups::this_cluster().sync();       // peers may still read `part`
     if (failed && tid == 0) {

@@ -102,7 +102,11 @@ twopass_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_i
     const int64_t nv = (len + VEC - 1) / VEC;
     const uint64_t keep = policy_evict_last();     // first read: stay in L2
     const uint64_t stream = policy_evict_first();  // second read and stores
-    pdl_launch_dependents();
+    // Cluster launches let the next grid start only after the row loop:
+    // clusters of the next grid placed early into leftover slots measured
+    // slower.  Single-CTA launches let it start at once.
+    if (cs == 1)
+        pdl_launch_dependents();
     pdl_wait();
 
     int slot = 0;
@@ -151,6 +155,8 @@ twopass_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_i
             });
         __syncthreads();                       // red_* reused by the next row
     }
+    if (cs > 1)
+        pdl_launch_dependents();
     if (cs > 1)
         cooperative_groups::this_cluster().sync();
 }
