@@ -401,7 +401,8 @@ int check_plan(const softmax_device_desc_t& dev, const Problem& p, const softmax
                                                                              : SOFTMAX_ERR_INVALID_ARG;
         // Staged two-pass (ring of chunks of threads * chunks * 16 bytes).
         if (q.bulk_copy != 1 || !in_al || q.vec != vmax || !vec_ok(q.out_vec, out_al) ||
-            (q.chunks != 2 && q.chunks != 4) || q.stages < 1 || q.stages > kMaxStages ||
+            (q.chunks != 2 && q.chunks != 4 && !(q.chunks == 8 && esz == 4)) ||
+            q.stages < 1 || q.stages > kMaxStages ||
             q.smem_bytes != q.stages * q.threads * q.chunks * 16 || q.smem_bytes > smem_cap)
             return SOFTMAX_ERR_INVALID_ARG;
         return SOFTMAX_OK;

@@ -303,8 +303,14 @@ cudaError_t launch_stream_nv(const Problem& p, const softmax_plan_t& plan, cudaS
                           : launch_stream<T, THREADS, 2, false>(p, plan, s);
     case 4: return outvec ? launch_stream<T, THREADS, 4, true>(p, plan, s)
                           : launch_stream<T, THREADS, 4, false>(p, plan, s);
-    default: return cudaErrorInvalidValue;
+    case 8:
+        if constexpr (sizeof(T) == 4)
+            return outvec ? launch_stream<T, THREADS, 8, true>(p, plan, s)
+                          : launch_stream<T, THREADS, 8, false>(p, plan, s);
+        break;
+    default: break;
     }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
