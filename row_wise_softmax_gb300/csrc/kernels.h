@@ -62,6 +62,40 @@ inline int launch_attrs(cudaLaunchAttribute* a, int cs)
     return n;
 }
 
+// Persistent grid size for `work` equal units (rows, tiles, row groups)
+// dealt round-robin to at most `max_active` resident CTAs (or clusters):
+// the last round should be as full as possible (the tail effect of the cs336
+// lecture 6 notes, "Block Occupancy", applied to units per CTA).  Among
+// g in [max_active/2, max_active], take those whose idle share of the last
+// round, (g * ceil(work/g) - work) / (g * ceil(work/g)), is within 1% of the
+// best; prefer a multiple of `sm_count`, then the largest.
+inline int64_t balanced_grid(int64_t work, int64_t max_active, int64_t sm_count)
+{
+    if (work <= 0 || max_active <= 0)
+        return 1;
+    if (work <= max_active)
+        return work;
+    const int64_t lo = (max_active + 1) / 2;
+    double best = 1.0;
+    for (int64_t g = lo; g <= max_active; ++g) {
+        const int64_t slots = g * ((work + g - 1) / g);
+        const double idle = static_cast<double>(slots - work) / static_cast<double>(slots);
+        if (idle < best)
+            best = idle;
+    }
+    int64_t pick = -1, pick_mult = -1;
+    for (int64_t g = lo; g <= max_active; ++g) {
+        const int64_t slots = g * ((work + g - 1) / g);
+        const double idle = static_cast<double>(slots - work) / static_cast<double>(slots);
+        if (idle > best + 0.01)
+            continue;
+        pick = g;
+        if (sm_count > 0 && g % sm_count == 0)
+            pick_mult = g;
+    }
+    return pick_mult > 0 ? pick_mult : pick;
+}
+
 // Helpers implemented in softmax_abi.cu.
 int resident_ctas(const void* kernel, int threads, int smem_bytes);  // whole-GPU CTA slots
 int sm_count_current();

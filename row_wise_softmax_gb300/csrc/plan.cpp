@@ -32,8 +32,8 @@ namespace {
 
 constexpr int64_t kWarpMaxCols = 1024;
 constexpr int64_t kSliceTargetBytes = 32 * 1024;   // preferred slice (CTA path: whole row)
-constexpr int kSliceStages = 1;                    // ring stages of the slice kernel
-constexpr int64_t kTileRingBudgetBytes = 32 * 1024; // shared memory for the tile ring, per CTA
+constexpr int kSliceStages = 2;                    // ring stages of the slice kernel
+constexpr int64_t kTileRingBudgetBytes = 16 * 1024; // shared memory for the tile ring, per CTA
 constexpr int64_t kClusterMaxRowBytes = 64 * 1024;  // longer rows take TWOPASS
 constexpr int64_t kTwoPassBytesPerCta = 256 * 1024;      // register two-pass
 constexpr int64_t kStreamBytesPerCta = 128 * 1024;       // staged two-pass
@@ -42,7 +42,7 @@ constexpr int kStreamStages = 2;
 constexpr int kMaxStages = 8;                       // must match row_slices.cu
 constexpr int kMaxSliceThreads = 1024;
 constexpr int kSmemReserve = 2048;                  // static smem + slack
-constexpr int64_t kTileStageBytes = 16 * 1024;     // WARP path (staged): rows per stage
+constexpr int64_t kTileStageBytes = 8 * 1024;      // WARP path (staged): rows per stage
 constexpr int64_t kTileMaxRowsPerWarp = 16;
 
 int esize(int dtype) { return dtype == SOFTMAX_F32 ? 4 : 2; }
@@ -85,12 +85,12 @@ int max_vectors_per_thread(int esz) { return esz == 4 ? 8 : 4; }
 int64_t slice_capacity(int esz) { return int64_t{kMaxSliceThreads} * max_vectors_per_thread(esz) * (16 / esz); }
 
 // Threads and vectors per thread for a slice of nvec 16-byte vectors: about
-// 16 elements per thread (more only when 1024 threads do not suffice), at
+// 32 elements per thread (more only when 1024 threads do not suffice), at
 // least 128 threads, then the smallest power-of-two vectors per thread that
 // covers the slice.
 void slice_shape(int64_t nvec, int esz, int* threads, int* nv)
 {
-    const int nv_target = esz == 4 ? 4 : 2;
+    const int nv_target = esz == 4 ? 8 : 4;
     int64_t t = pow2_ceil(ceil_div(nvec, nv_target));
     if (t < 128)
         t = 128;
@@ -274,7 +274,9 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
             return SOFTMAX_ERR_UNSUPPORTED;
         int threads = 0, nv = 0;
         slice_shape(slice / vmax, esz, &threads, &nv);
-        const int64_t stages = kSliceStages;
+        int64_t stages = kSliceStages;
+        while (stages > 1 && stages * stage_bytes > smem_cap)
+            --stages;
         q.cluster = cs;
         q.slice_cols = slice;
         q.vec = in_vec ? vmax : 1;        // global input loads (staged: always 16 bytes)
@@ -304,7 +306,7 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
             q.vec = vmax;
             q.out_vec = out_al ? vmax : 1;
             q.threads = kStreamThreads;
-            q.chunks = 4;
+            q.chunks = esz == 4 ? 8 : 4;          // 32 KB fp32 / 16 KB bf16 chunks
             q.stages = kStreamStages;
             q.smem_bytes = q.stages * q.threads * q.chunks * 16;
         } else {

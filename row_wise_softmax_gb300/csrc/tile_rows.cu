@@ -225,7 +225,7 @@ cudaError_t launch_tile(const Problem& p, const softmax_plan_t& plan, cudaStream
     int64_t grid = plan.grid;
     if (grid <= 0) {
         const int resident = resident_ctas(reinterpret_cast<const void*>(k), kTileThreads, smem);
-        grid = tiles < resident ? tiles : resident;
+        grid = balanced_grid(tiles, resident, sm_count_current());
     }
     if (grid < 1)
         grid = 1;

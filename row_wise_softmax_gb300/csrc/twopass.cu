@@ -198,7 +198,7 @@ cudaError_t launch_tp(const Problem& p, const softmax_plan_t& plan, cudaStream_t
         }
         if (active < 1)
             active = 1;
-        clusters = p.n_rows < active ? p.n_rows : active;
+        clusters = balanced_grid(p.n_rows, active, cs == 1 ? sm_count_current() : 0);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * cs), 1, 1);

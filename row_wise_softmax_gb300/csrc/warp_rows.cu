@@ -128,7 +128,11 @@ static cudaError_t launch_one(const Problem& p, const softmax_plan_t& plan, cuda
     int64_t grid = plan.grid;
     if (grid <= 0) {
         const int resident = resident_ctas(reinterpret_cast<const void*>(k), kWarpPathThreads, 0);
-        grid = want < resident ? want : resident;
+        const int64_t warps = balanced_grid(groups, int64_t{resident} * warps_per_cta,
+                                            int64_t{sm_count_current()} * warps_per_cta);
+        grid = (warps + warps_per_cta - 1) / warps_per_cta;
+        if (grid > want)
+            grid = want;
     }
     if (grid < 1)
         grid = 1;

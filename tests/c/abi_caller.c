@@ -28,7 +28,7 @@ int main(void)
     char text[256];
     CHECK(softmax_plan(&gb300, (void*)0x10000, (void*)0x20000000, 4096, 4096, 4096, 4096,
                        SOFTMAX_F32, SOFTMAX_PATH_AUTO, &plan) == SOFTMAX_OK);
-    CHECK(plan.path == SOFTMAX_PATH_CTA && plan.bulk_copy == 1 && plan.cluster == 1 && plan.stages == 1);
+    CHECK(plan.path == SOFTMAX_PATH_CTA && plan.bulk_copy == 1 && plan.cluster == 1 && plan.stages == 2);
     CHECK(softmax_plan_format(&plan, text, sizeof text) > 0 && strstr(text, "path=cta"));
     CHECK(softmax_plan(&gb300, (void*)0x10000, (void*)0x20000000, 256, 262144, 262144, 262144,
                        SOFTMAX_F32, SOFTMAX_PATH_AUTO, &plan) == SOFTMAX_OK);

@@ -54,15 +54,15 @@ def test_scheduler_paths_for_the_five_workloads(lib):
     assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 0, 4, 8, 1)
     p = plan(4096, 4096)
     assert (p.path, p.cluster, p.bulk_copy, p.out_vec) == (rws.PATH_CTA, 1, 1, 4)
-    assert (p.threads, p.chunks, p.stages, p.smem_bytes, p.grid) == (256, 4, 1, 16384, 0)
+    assert (p.threads, p.chunks, p.stages, p.smem_bytes, p.grid) == (128, 8, 2, 32768, 0)
     p = plan(32768, 1024, dtype=rws.BF16)                 # bf16 short rows: staged tiles
-    assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 1, 8, 4, 2)
-    assert (p.stages, p.smem_bytes) == (2, 32768)
+    assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 1, 8, 4, 1)
+    assert (p.stages, p.smem_bytes) == (2, 16384)
     p = plan(262144, 127, in_row_stride=128, out_row_stride=127)
     assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 0, 1, 4, 4)
     p = plan(256, 262144)                                 # staged two-pass, 16 KB chunks
     assert (p.path, p.cluster, p.slice_cols, p.threads, p.grid) == (rws.PATH_TWOPASS, 8, 32768, 256, 0)
-    assert (p.vec, p.out_vec, p.bulk_copy, p.chunks, p.stages, p.smem_bytes) == (4, 4, 1, 4, 2, 32768)
+    assert (p.vec, p.out_vec, p.bulk_copy, p.chunks, p.stages, p.smem_bytes) == (4, 4, 1, 8, 2, 65536)
     p = plan(256, 262144, in_ptr=(1 << 20) + 4)           # unaligned: register two-pass
     assert (p.path, p.bulk_copy, p.vec, p.threads) == (rws.PATH_TWOPASS, 0, 1, 512)
 
@@ -72,7 +72,7 @@ def test_scheduler_boundaries(lib):
     assert plan(1, 1025).path == rws.PATH_CTA
     assert plan(1, 8192).path == rws.PATH_CTA             # 32 KB row
     p = plan(1, 8196)
-    assert p.path == rws.PATH_CLUSTER and p.cluster == 2 and p.stages == 1
+    assert p.path == rws.PATH_CLUSTER and p.cluster == 2 and p.stages == 2
     assert plan(1, 16384).path == rws.PATH_CLUSTER         # single pass up to 64 KB rows
     p = plan(1, 16388)
     assert p.path == rws.PATH_TWOPASS and p.cluster == 1 and p.bulk_copy == 1
@@ -128,7 +128,7 @@ def test_scheduler_forced_paths(lib):
     assert rws.plan_for_device(small_cluster, 4, 4 << 20).cluster == 8
     p = rws.plan_for_device(small_cluster, 4, 262144, path=rws.PATH_CLUSTER)
     assert p.path == rws.PATH_CLUSTER and p.cluster == 8 and p.slice_cols == 32768
-    assert p.threads == 1024 and p.stages == 1 and p.chunks == 8
+    assert p.threads == 1024 and p.stages == 1 and p.chunks == 8   # 2 x 128 KB would not fit
 
 
 def test_validation(lib):
