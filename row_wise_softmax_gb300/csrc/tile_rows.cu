@@ -224,8 +224,10 @@ cudaError_t launch_tile(const Problem& p, const softmax_plan_t& plan, cudaStream
     const int64_t tiles = (p.n_rows + R - 1) / R;
     int64_t grid = plan.grid;
     if (grid <= 0) {
+        // Latency-bound (a warp reduces its rows one after another): every
+        // resident CTA is worth more than a fuller last round.
         const int resident = resident_ctas(reinterpret_cast<const void*>(k), kTileThreads, smem);
-        grid = balanced_grid(tiles, resident, sm_count_current());
+        grid = tiles < resident ? tiles : resident;
     }
     if (grid < 1)
         grid = 1;

@@ -127,12 +127,10 @@ static cudaError_t launch_one(const Problem& p, const softmax_plan_t& plan, cuda
     int64_t want = (groups + warps_per_cta - 1) / warps_per_cta;
     int64_t grid = plan.grid;
     if (grid <= 0) {
+        // Many small units per warp: full residency (the last round is
+        // already nearly full) hides the most latency.
         const int resident = resident_ctas(reinterpret_cast<const void*>(k), kWarpPathThreads, 0);
-        const int64_t warps = balanced_grid(groups, int64_t{resident} * warps_per_cta,
-                                            int64_t{sm_count_current()} * warps_per_cta);
-        grid = (warps + warps_per_cta - 1) / warps_per_cta;
-        if (grid > want)
-            grid = want;
+        grid = want < resident ? want : resident;
     }
     if (grid < 1)
         grid = 1;
