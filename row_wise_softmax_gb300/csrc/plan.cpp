@@ -13,7 +13,7 @@
 //   CLUSTER  rows of 32..64 KB: one HBM pass, a cluster of CTAs holding
 //            <= 32 KB slices, max and sum exchanged through distributed shared
 //            memory.  (When forced: slices up to 128 KB fp32 / 64 KB bf16.)
-//   TWOPASS  longer rows: a cluster of 1..16 CTAs (about 128 KB of row per
+//   TWOPASS  longer rows: a cluster of 1..8 CTAs (about 128 KB of row per
 //            CTA) streams the row twice through a cp.async.bulk chunk ring;
 //            the second read mostly hits L2.  Unaligned input: the register
 //            two-pass kernel (about 256 KB per CTA).
@@ -39,6 +39,7 @@ constexpr int64_t kTwoPassBytesPerCta = 256 * 1024;      // register two-pass
 constexpr int64_t kStreamBytesPerCta = 128 * 1024;       // staged two-pass
 constexpr int kStreamThreads = 256;                      // staged two-pass: 16 KB chunks
 constexpr int kStreamStages = 2;
+constexpr int64_t kTwoPassMaxCluster = 8;
 constexpr int kMaxStages = 8;                       // must match row_slices.cu
 constexpr int kMaxSliceThreads = 1024;
 constexpr int kSmemReserve = 2048;                  // static smem + slack
@@ -295,6 +296,8 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
         int64_t cs = pow2_ceil(ceil_div(row_bytes, in_al ? kStreamBytesPerCta : kTwoPassBytesPerCta));
         if (automatic && !in_al && cs < 2)
             cs = 2;
+        if (automatic && cs > kTwoPassMaxCluster)
+            cs = kTwoPassMaxCluster;       // 16-CTA clusters pack onto 74% of the SMs
         if (cs > max_cluster)
             cs = pow2_floor(max_cluster);
         q.cluster = static_cast<int>(cs);

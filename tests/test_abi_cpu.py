@@ -78,7 +78,7 @@ def test_scheduler_boundaries(lib):
     assert p.path == rws.PATH_TWOPASS and p.cluster == 1 and p.bulk_copy == 1
     assert plan(1, 32768).cluster == 1 and plan(1, 32772).cluster == 2
     assert plan(1, 131072).cluster == 4 and plan(1, 262144).cluster == 8
-    assert plan(1, 4 << 20).cluster == 16
+    assert plan(1, 4 << 20).cluster == 8                  # capped: 16-CTA clusters pack poorly
     assert plan(1, 16384, dtype=rws.BF16).path == rws.PATH_CTA
     assert plan(1, 16392, dtype=rws.BF16).path == rws.PATH_CLUSTER
     assert plan(1, 32768, dtype=rws.BF16).path == rws.PATH_CLUSTER
@@ -87,7 +87,8 @@ def test_scheduler_boundaries(lib):
     assert forced.cluster == 16 and forced.threads == 1024 and forced.chunks == 8
     assert forced.smem_bytes == 131072
     tp = plan(3, 10_000_000)
-    assert tp.path == rws.PATH_TWOPASS and tp.cluster == 16 and tp.grid == 0
+    assert tp.path == rws.PATH_TWOPASS and tp.cluster == 8 and tp.grid == 0
+    assert plan(3, 10_000_000, path=rws.PATH_TWOPASS).cluster == 16   # forced: up to 16
     for n in (1025, 3000, 4096, 5000, 8192, 8196, 16384, 20000, 131072, 262144, 524288):
         for path in (rws.PATH_AUTO, rws.PATH_CLUSTER):
             q = plan(2, n, path=path)
