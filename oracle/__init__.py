@@ -8,7 +8,9 @@ with it; the C source ``softmax_oracle.c`` includes nothing from the CUDA path.
 The functions restate the pages' softmax (the "Level 1: Softmax" formula of
 the cs336 lecture 6 notes and the fused-softmax example of "Triton: write
 CUDA-grade GPU operators in Python"), the online (m, l) recurrence of
-"Triton GPU programming deep dive" section 3.3, and the tiled row sum of the
+"Triton GPU programming deep dive" section 3.3, the scaled and causally
+masked softmax of attention scores (the same page, sections 3.1 and 3.3),
+and the tiled row sum of the
 lecture notes' "Level 2".  See ``softmax_oracle.c`` for each function's
 citation.  Every function is pinned in tests/test_oracle_pins.py.
 """
@@ -51,6 +53,9 @@ class Oracle:
         i64, dbl, vp = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
         lib.oracle_softmax_rows.argtypes = [vp, vp, i64, i64, i64, i64, ctypes.c_int, i64]
         lib.oracle_softmax_rows.restype = ctypes.c_int
+        lib.oracle_softmax_rows_ex.argtypes = [vp, vp, i64, i64, i64, i64, ctypes.c_int, i64,
+                                               dbl, ctypes.c_int, i64, i64]
+        lib.oracle_softmax_rows_ex.restype = ctypes.c_int
         lib.oracle_double_to_bf16.argtypes = [dbl]
         lib.oracle_double_to_bf16.restype = ctypes.c_uint16
         lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
@@ -63,13 +68,17 @@ class Oracle:
 
     def softmax_rows(self, buf: np.ndarray, n_rows: int, n_cols: int,
                      in_row_stride: int | None = None, dtype: int = F32,
-                     tile: int = 0) -> np.ndarray:
+                     tile: int = 0, scale: float = 1.0, causal: bool = False,
+                     causal_period: int = 0, causal_offset: int = 0) -> np.ndarray:
         """Softmax of each row of a strided row matrix, in double.
 
         ``buf`` is the flat input buffer: float32 values (dtype F32) or bf16
         bit patterns as uint16 (dtype BF16).  Row r starts at element
         ``r * in_row_stride``.  Returns a dense float64 array [n_rows, n_cols].
         ``tile > 0`` uses the online (m, l) recurrence with that tile width.
+        ``scale`` multiplies the inputs (exactly, in double) before the
+        softmax; ``causal`` keeps column c of row r iff c <= (r mod
+        causal_period) + causal_offset (period <= 0: n_rows), the rest -inf.
         """
         if in_row_stride is None:
             in_row_stride = n_cols
@@ -80,8 +89,14 @@ class Oracle:
         if n_rows > 0 and n_cols > 0 and buf.size < (n_rows - 1) * in_row_stride + n_cols:
             raise ValueError("oracle: buffer too small for the strided rows")
         out = np.empty((n_rows, n_cols), dtype=np.float64)
-        rc = self._lib.oracle_softmax_rows(buf.ctypes.data, out.ctypes.data, n_rows, n_cols,
-                                           in_row_stride, n_cols, dtype, tile)
+        if scale == 1.0 and not causal:
+            rc = self._lib.oracle_softmax_rows(buf.ctypes.data, out.ctypes.data, n_rows, n_cols,
+                                               in_row_stride, n_cols, dtype, tile)
+        else:
+            rc = self._lib.oracle_softmax_rows_ex(buf.ctypes.data, out.ctypes.data, n_rows,
+                                                  n_cols, in_row_stride, n_cols, dtype, tile,
+                                                  float(np.float32(scale)), 1 if causal else 0,
+                                                  causal_period, causal_offset)
         if rc != 0:
             raise ValueError("oracle_softmax_rows rejected its arguments")
         return out

@@ -22,6 +22,15 @@
  *    exp(m_i - m_ij)), with the reading that a tile whose running max is
  *    still -inf contributes nothing (the page does not say what happens when
  *    a whole tile is masked).
+ *  - the scaled, causally masked softmax of attention scores: "Triton GPU
+ *    programming deep dive", section 3.1 (the scores are divided by sqrt(d)
+ *    before the softmax: here a general factor `scale`) and section 3.3 (a
+ *    score whose key index exceeds its query index is replaced by -inf
+ *    before the running max).  Reading: row r of the matrix is query
+ *    (r mod period) of its block of `period` rows, column c is key c, and
+ *    an offset shifts the diagonal; so column c takes part iff
+ *    c <= (r mod period) + offset.  A masked column is never read.  A row
+ *    with no column taking part is the formula over only -inf: all NaN.
  *  - the tiled row sum with one accumulator per lane: lec06 section
  *    "Level 2: Row Sum (tiling)", worked example of 12 elements, BLOCK 4.
  *  - bf16 decoding (exact) and rounding of a double to bf16 with
@@ -164,35 +173,60 @@ static void online_softmax_row(const double* x, int64_t n, int64_t tile, double*
 
 /* ---- row-matrix entry points ----------------------------------------- */
 /*
+ * The number of leading columns of row r that take part in its softmax:
+ * n_cols without a mask; with one, the columns c <= (r mod period) + offset,
+ * i.e. (r mod period) + offset + 1 of them, clamped to [0, n_cols].
+ */
+static int64_t visible_cols(int64_t r, int64_t n_cols, int causal, int64_t period, int64_t offset)
+{
+    if (!causal)
+        return n_cols;
+    const int64_t last = r % period + offset;       /* last column taking part */
+    if (last < 0)
+        return 0;
+    return last + 1 < n_cols ? last + 1 : n_cols;
+}
+
+/*
  * dtype 0: `in` is binary32; dtype 1: `in` is bf16 bit patterns (uint16).
  * Row r of the input starts at element r * in_row_stride; row r of the
  * output (double) at element r * out_row_stride.  Only columns [0, n_cols)
- * are read or written.  `tile` <= 0 selects the plain definition, > 0 the
- * online recurrence with that tile width.  Returns 0, or -1 on a bad argument.
+ * are written, and only the columns taking part are read.  The softmax is
+ * taken over z_c = scale * x_c (exact in double: both factors have at most
+ * 24 significant bits) for the columns taking part, and z_c = -inf for the
+ * masked ones.  `tile` <= 0 selects the plain definition, > 0 the online
+ * recurrence with that tile width.  causal != 0 enables the mask; period
+ * <= 0 means n_rows.  Returns 0, or -1 on a bad argument.
  */
-int oracle_softmax_rows(const void* in, double* out, int64_t n_rows, int64_t n_cols,
-                        int64_t in_row_stride, int64_t out_row_stride, int dtype,
-                        int64_t tile)
+int oracle_softmax_rows_ex(const void* in, double* out, int64_t n_rows, int64_t n_cols,
+                           int64_t in_row_stride, int64_t out_row_stride, int dtype,
+                           int64_t tile, double scale, int causal, int64_t period,
+                           int64_t offset)
 {
-    if (n_rows < 0 || n_cols < 0 || (dtype != 0 && dtype != 1))
+    if (n_rows < 0 || n_cols < 0 || (dtype != 0 && dtype != 1) || !(scale > 0.0))
         return -1;
     if (n_rows == 0 || n_cols == 0)
         return 0;
     if (!in || !out)
         return -1;
+    if (period <= 0)
+        period = n_rows;
     double* x = (double*)malloc((size_t)n_cols * sizeof(double));
     if (!x)
         return -1;
     for (int64_t r = 0; r < n_rows; ++r) {
+        const int64_t vis = visible_cols(r, n_cols, causal, period, offset);
         if (dtype == 0) {
             const float* src = (const float*)in + r * in_row_stride;
-            for (int64_t j = 0; j < n_cols; ++j)
-                x[j] = (double)src[j];
+            for (int64_t j = 0; j < vis; ++j)
+                x[j] = scale * (double)src[j];
         } else {
             const uint16_t* src = (const uint16_t*)in + r * in_row_stride;
-            for (int64_t j = 0; j < n_cols; ++j)
-                x[j] = oracle_bf16_to_double(src[j]);
+            for (int64_t j = 0; j < vis; ++j)
+                x[j] = scale * oracle_bf16_to_double(src[j]);
         }
+        for (int64_t j = vis; j < n_cols; ++j)
+            x[j] = -INFINITY;
         double* y = out + r * out_row_stride;
         if (tile > 0)
             online_softmax_row(x, n_cols, tile, y);
@@ -201,6 +235,15 @@ int oracle_softmax_rows(const void* in, double* out, int64_t n_rows, int64_t n_c
     }
     free(x);
     return 0;
+}
+
+/* The plain softmax of each row: no scale, no mask. */
+int oracle_softmax_rows(const void* in, double* out, int64_t n_rows, int64_t n_cols,
+                        int64_t in_row_stride, int64_t out_row_stride, int dtype,
+                        int64_t tile)
+{
+    return oracle_softmax_rows_ex(in, out, n_rows, n_cols, in_row_stride, out_row_stride,
+                                  dtype, tile, 1.0, 0, 0, 0);
 }
 
 /*

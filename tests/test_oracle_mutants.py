@@ -30,6 +30,20 @@ MUTANTS = {
     "bf16_round_truncate": ("const double n = rint(", "const double n = trunc("),
     "bf16_decode_shift": ("uint32_t u = (uint32_t)bits << 16;", "uint32_t u = (uint32_t)bits << 15;"),
     "bf16_overflow_early": ("if (a >= overflow_at)", "if (a > ldexp(1.0, 127))"),
+    "causal_off_by_one": ("return last + 1 < n_cols ? last + 1 : n_cols;",
+                          "return last < n_cols ? last : n_cols;"),
+    "causal_period_ignored": ("const int64_t last = r % period + offset;",
+                              "const int64_t last = r + offset;"),
+    "causal_offset_sign": ("const int64_t last = r % period + offset;",
+                           "const int64_t last = r % period - offset;"),
+    "causal_default_period": ("if (period <= 0)\n        period = n_rows;",
+                              "if (period <= 0)\n        period = 1;"),
+    "causal_masked_as_zero": ("for (int64_t j = vis; j < n_cols; ++j)\n            x[j] = -INFINITY;",
+                              "for (int64_t j = vis; j < n_cols; ++j)\n            x[j] = 0.0;"),
+    "scale_dropped_f32": ("x[j] = scale * (double)src[j];", "x[j] = (double)src[j];"),
+    "scale_dropped_bf16": ("x[j] = scale * oracle_bf16_to_double(src[j]);",
+                           "x[j] = oracle_bf16_to_double(src[j]);"),
+    "scale_divides": ("x[j] = scale * (double)src[j];", "x[j] = (double)src[j] / scale;"),
     "tiled_sum_ragged_lane": ("if (t0 + i < n)         /* masked lanes load 0 */",
                               "if (t0 + i <= n)"),
 }

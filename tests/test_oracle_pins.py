@@ -308,3 +308,107 @@ def test_level2_tiled_row_sum_worked_example(oracle_lib):
     # A ragged row: masked lanes add nothing.
     total, _ = oracle_lib.tiled_row_sum(row[:10], block, snapshot_tiles=99)
     assert total == math.fsum(row[:10])
+
+
+# ------------------------------------------------ scaled, causally masked rows
+# "Triton GPU programming deep dive", section 3.1 (scores scaled before the
+# softmax) and section 3.3 (scores whose key index exceeds the query index are
+# -inf).  Row r is query (r mod period); column c takes part iff
+# c <= (r mod period) + offset.
+
+def test_causal_constant_rows_closed_form(oracle_lib):
+    """Equal inputs: row r is exactly 1/(visible columns) on its visible part, 0 after it."""
+    n_rows, n_cols = 11, 8
+    x = np.full((n_rows, n_cols), 0.75, dtype=np.float32)
+    for period, offset in ((0, 0), (4, 0), (3, 2), (5, -1)):
+        y = oracle_lib.softmax_rows(*_rows(x), scale=1.5, causal=True,
+                                    causal_period=period, causal_offset=offset)
+        per = period if period > 0 else n_rows
+        for r in range(n_rows):
+            vis = min(max(r % per + offset + 1, 0), n_cols)
+            if vis == 0:
+                assert np.all(np.isnan(y[r])), (period, offset, r)
+                continue
+            assert np.all(y[r, :vis] == 1.0 / vis), (period, offset, r)
+            assert np.all(y[r, vis:] == 0.0) and not np.any(np.signbit(y[r, vis:]))
+
+
+def _torch_causal(torch, xd, scale, period, offset):
+    """torch CPU double: scale, then -inf outside torch.tril(diagonal=offset) of each block."""
+    n_rows, n_cols = xd.shape
+    per = period if period > 0 else n_rows
+    q = torch.arange(n_rows) % per
+    keep = torch.tril(torch.ones(per, n_cols, dtype=torch.bool), diagonal=offset)[q]
+    z = (xd * scale).masked_fill(~keep, float("-inf"))
+    return torch.softmax(z, dim=-1).numpy()
+
+
+def test_causal_scaled_matches_torch_tril_mask(oracle_lib):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(37)
+    n_rows, n_cols = 23, 70
+    x = (rng.standard_normal((n_rows, n_cols)) * 4).astype(np.float32)
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    bits = xb.view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    for scale, period, offset in ((0.125, 0, 0), (1 / 3, 7, 0), (2.5, 9, 40), (0.7, 0, -4),
+                                  (1.0, 6, 100)):
+        s32 = float(np.float32(scale))
+        for dtype, buf, xd in ((F32, x.reshape(-1), torch.from_numpy(x).double()),
+                               (BF16, bits, xb.double())):
+            y = oracle_lib.softmax_rows(buf, n_rows, n_cols, dtype=dtype, scale=scale,
+                                        causal=True, causal_period=period, causal_offset=offset)
+            ref = _torch_causal(torch, xd, s32, period, offset)
+            assert np.array_equal(np.isnan(y), np.isnan(ref)), (scale, period, offset, dtype)
+            ok = ~np.isnan(ref)
+            assert np.all(np.abs(y[ok] - ref[ok]) <= 1e-14 * ref[ok] + 1e-300), (scale, dtype)
+
+
+def test_scale_two_element_closed_form(oracle_lib):
+    """softmax(s * [a, b]) = [1/(1+exp(s(b-a))), ...] at 40 digits, s as a float32."""
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 40
+    rng = np.random.default_rng(41)
+    x = (rng.standard_normal((64, 2)) * 6).astype(np.float32)
+    for scale in (0.125, 0.0883883476, 3.0):
+        s = mpmath.mpf(float(np.float32(scale)))
+        y = oracle_lib.softmax_rows(*_rows(x), scale=scale)
+        for r in range(64):
+            a, b = mpmath.mpf(float(x[r, 0])), mpmath.mpf(float(x[r, 1]))
+            y0 = float(1 / (1 + mpmath.exp(s * (b - a))))
+            assert abs(y[r, 0] - y0) <= 4e-16 * y0 + 1e-300, (scale, r)
+
+
+def test_power_of_two_scale_equals_rescaled_input(oracle_lib):
+    rng = np.random.default_rng(43)
+    x = (rng.standard_normal((12, 50)) * 3).astype(np.float32)
+    for s in (0.25, 2.0, 8.0):
+        y = oracle_lib.softmax_rows(*_rows(x), scale=s)
+        assert np.array_equal(y, oracle_lib.softmax_rows(*_rows((x * s).astype(np.float32))))
+
+
+def test_masked_columns_are_never_read(oracle_lib):
+    rng = np.random.default_rng(47)
+    n_rows, n_cols = 10, 33
+    x = rng.standard_normal((n_rows, n_cols)).astype(np.float32)
+    keep = np.arange(n_cols)[None, :] <= (np.arange(n_rows)[:, None] % 4) + 3
+    y0 = oracle_lib.softmax_rows(*_rows(np.where(keep, x, 0).astype(np.float32)),
+                                 causal=True, causal_period=4, causal_offset=3)
+    for junk in (np.nan, np.inf, -np.inf, 3e38):
+        xj = np.where(keep, x, junk).astype(np.float32)
+        y = oracle_lib.softmax_rows(*_rows(xj), causal=True, causal_period=4, causal_offset=3)
+        assert np.array_equal(y, y0), junk
+    assert np.all(np.isfinite(y0))
+
+
+@pytest.mark.parametrize("tile", [1, 3, 16])
+def test_online_recurrence_causal_equals_definition(oracle_lib, tile):
+    rng = np.random.default_rng(53)
+    n_rows, n_cols = 17, 45
+    x = (rng.standard_normal((n_rows, n_cols)) * 5).astype(np.float32)
+    kw = dict(scale=0.3, causal=True, causal_period=6, causal_offset=-2)
+    y = oracle_lib.softmax_rows(*_rows(x), **kw)
+    yt = oracle_lib.softmax_rows(*_rows(x), tile=tile, **kw)
+    assert np.array_equal(np.isnan(y), np.isnan(yt))
+    assert np.isnan(y[0]).all() and np.isnan(y[6]).all()       # rows with no visible column
+    ok = ~np.isnan(y)
+    assert np.all(np.abs(yt[ok] - y[ok]) <= 1e-14 * y[ok] + 1e-300)
