@@ -186,13 +186,22 @@ def device_buffers(w: wl.Workload, torch, l2_bytes: int):
     return sets
 
 
-def time_device(w: wl.Workload, sets, steps: int, warmup: int, torch, rws, stream):
-    """softmax_rows over rotating buffer sets, steps back to back (inputs
-    resident in HBM, never in L2).  Returns (total ms of the timed steps from
-    one pair of CUDA events on the launching stream, kernel launches)."""
-    calls = [(x.data_ptr(), y.data_ptr(), w.n_rows, w.n_cols, w.in_row_stride,
-              w.out_row_stride, w.dtype, stream.cuda_stream) for x, y in sets]
-    call = rws.lib().softmax_rows
+def time_device(w: wl.Workload, sets, steps: int, warmup: int, torch, rws, stream,
+                options=None):
+    """softmax_rows (softmax_rows_ex with ``options``, a rws.Options) over
+    rotating buffer sets, steps back to back (inputs resident in HBM, never in
+    L2).  Returns (total ms of the timed steps from one pair of CUDA events on
+    the launching stream, kernel launches)."""
+    if options is None:
+        calls = [(x.data_ptr(), y.data_ptr(), w.n_rows, w.n_cols, w.in_row_stride,
+                  w.out_row_stride, w.dtype, stream.cuda_stream) for x, y in sets]
+        call = rws.lib().softmax_rows
+    else:
+        import ctypes
+        calls = [(x.data_ptr(), y.data_ptr(), w.n_rows, w.n_cols, w.in_row_stride,
+                  w.out_row_stride, w.dtype, ctypes.byref(options), rws.PATH_AUTO,
+                  stream.cuda_stream) for x, y in sets]
+        call = rws.lib().softmax_rows_ex
     for i in range(warmup):
         st = call(*calls[i % len(calls)])
         if st != rws.OK:
@@ -228,6 +237,27 @@ def copy_calibration(w: wl.Workload, sets, torch, stream, peak):
     ms = a.elapsed_time(b) / 30
     gbs = 2 * n * pairs[0][0].element_size() / (ms * 1e-3) / 1e9
     return {"GB/s": round(gbs, 1), "mean_ms": round(ms, 5), "frac_of_peak": round(gbs / peak, 4)}
+
+
+def fused_causal_entry(torch, rws, stream, l2_bytes, peak):
+    """The causal bf16 workload with its mask computed from indices and a
+    1/sqrt(64) scale (softmax_rows_ex): the masked inputs are never read, so
+    the algorithmic bytes are the kept inputs plus every output."""
+    w = wl.make("causal_bf16")
+    period = w.n_cols
+    opt = rws.Options(0.125, 1, period, 0)
+    kept = sum(min(r % period + 1, w.n_cols) for r in range(w.n_rows))
+    algo = (kept + w.n_rows * w.n_cols) * w.elem_bytes
+    bc = device_buffers(w, torch, l2_bytes)
+    tot, launches = time_device(w, bc, 50, 5, torch, rws, stream, options=opt)
+    del bc
+    med = tot / 50
+    gbs = algo / (med * 1e-3) / 1e9
+    return {"shape": [w.n_rows, w.n_cols], "dtype": "bf16",
+            "options": {"scale": 0.125, "causal": 1, "causal_period": period, "causal_offset": 0},
+            "algorithmic_bytes": algo, "mean_ms": round(med, 5), "GB/s": round(gbs, 1),
+            "frac_of_measured_peak": round(gbs / peak, 4), "launches": launches,
+            "rows_per_s": round(w.n_rows / (med * 1e-3), 1)}
 
 
 def time_e2e(w: wl.Workload, steps: int, warmup: int, torch, rws, stream, staged: bool):
@@ -393,6 +423,8 @@ def run_ours(args):
                          "frac_of_8000": round(gbs / 8000.0, 4),
                          "rows_per_s": round(wc.n_rows / (med * 1e-3), 1)}
             del wc
+        per["causal_bf16_mask_from_indices"] = fused_causal_entry(torch, rws, stream, l2_bytes,
+                                                                  peak)
         result["per_config"] = per
     if world > 1:
         import torch.distributed as dist

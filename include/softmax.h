@@ -113,6 +113,61 @@ int softmax_rows_path(const void* in, void* out, int64_t n_rows, int64_t n_cols,
                       void* stream, int path);
 
 /*
+ * Options of softmax_rows_ex: a scaled, causally masked softmax, the form
+ * attention scores take.  "Triton GPU programming deep dive", section 3.1,
+ * divides the scores Q K^T by sqrt(d) before the softmax; its section 3.3
+ * sets a score to -inf unless the key index is at most the query index.
+ * Here the mask is computed from indices instead of -inf written into the
+ * input.
+ *
+ *   scale          the softmax is taken over z = scale * x; 0 < scale <=
+ *                  2^127 (1.0f: none).  The result is that of the exact
+ *                  product scale * x (the kernels fold the scale into the
+ *                  exponent).
+ *   causal         0: no mask.  1: column c of row r takes part iff
+ *                  c <= (r mod causal_period) + causal_offset; every other
+ *                  column counts as -inf: its input is never read and its
+ *                  output is exactly +0 (NaN when the row's result is NaN).
+ *                  A row with no column taking part is all NaN (the formula
+ *                  over only -inf).
+ *   causal_period  rows per masked block (e.g. the query length when rows
+ *                  are (batch, head, query) triples); <= 0 means n_rows (as
+ *                  does any period of n_rows or more).
+ *   causal_offset  shift of the diagonal (e.g. key length minus query
+ *                  length for a bottom-right aligned mask); |offset| < 2^62.
+ */
+typedef struct {
+    float scale;
+    int32_t causal;
+    int64_t causal_period;
+    int64_t causal_offset;
+} softmax_options_t;
+
+/*
+ * softmax_rows_ex: softmax_rows with softmax_options_t (NULL options: the
+ * same as softmax_rows) and a path choice as in softmax_rows_path
+ * (SOFTMAX_PATH_AUTO: the planner's).  Arguments, layout, ownership and
+ * errors as for softmax_rows_path; invalid options (scale NaN, <= 0 or
+ * > 2^127, causal not 0/1, |causal_offset| >= 2^62) return
+ * SOFTMAX_ERR_INVALID_ARG.  softmax_rows and softmax_rows_path are this call
+ * with NULL options.
+ */
+int softmax_rows_ex(const void* in, void* out, int64_t n_rows, int64_t n_cols,
+                    int64_t in_row_stride, int64_t out_row_stride, int dtype,
+                    const softmax_options_t* options, int path, void* stream);
+
+/*
+ * softmax_visible_cols: how many leading columns of row `row` take part in
+ * its softmax under `options` (NULL: no mask) for an n_rows x n_cols matrix,
+ * computed on the host with the same arithmetic the kernels use; every
+ * later column of that row is masked (output +0).  Returns -1 for invalid
+ * options or arguments (row outside [0, n_rows), negative sizes, n_rows
+ * above 2^62).
+ */
+int64_t softmax_visible_cols(const softmax_options_t* options, int64_t n_rows, int64_t n_cols,
+                             int64_t row);
+
+/*
  * softmax_rows_host: the same operation on HOST buffers.  Two modes:
  *
  *  staged  (d_in and d_out given): queues on `stream` a copy of the strided

@@ -21,7 +21,9 @@ __all__ = [
     "F32", "BF16", "PATH_AUTO", "PATH_WARP", "PATH_CTA", "PATH_CLUSTER", "PATH_TWOPASS",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_DEVICE_TIMEOUT",
     "SoftmaxError", "DeviceDesc", "Plan", "build", "lib", "library_path",
-    "softmax_rows", "softmax_rows_ptr", "softmax_rows_planned_ptr", "softmax_rows_host", "plan", "plan_for_device",
+    "softmax_rows", "softmax_rows_ptr", "softmax_rows_ex_ptr", "softmax_rows_planned_ptr",
+    "visible_cols",
+    "Options", "softmax_rows_host", "plan", "plan_for_device",
     "status_string", "device_status", "launch_count", "selftest_wait_timeout", "abi_version", "GB300",
 ]
 
@@ -47,6 +49,11 @@ class DeviceDesc(ctypes.Structure):
                 ("max_smem_per_sm", ctypes.c_int), ("max_smem_per_block_optin", ctypes.c_int),
                 ("regs_per_sm", ctypes.c_int), ("cc_major", ctypes.c_int),
                 ("cc_minor", ctypes.c_int), ("max_cluster", ctypes.c_int)]
+
+
+class Options(ctypes.Structure):
+    _fields_ = [("scale", ctypes.c_float), ("causal", ctypes.c_int32),
+                ("causal_period", ctypes.c_int64), ("causal_offset", ctypes.c_int64)]
 
 
 class Plan(ctypes.Structure):
@@ -98,6 +105,11 @@ def lib() -> ctypes.CDLL:
         L.softmax_rows.restype = ci
         L.softmax_rows_path.argtypes = [vp, vp, i64, i64, i64, i64, ci, vp, ci]
         L.softmax_rows_path.restype = ci
+        L.softmax_rows_ex.argtypes = [vp, vp, i64, i64, i64, i64, ci, ctypes.POINTER(Options), ci,
+                                      vp]
+        L.softmax_rows_ex.restype = ci
+        L.softmax_visible_cols.argtypes = [ctypes.POINTER(Options), i64, i64, i64]
+        L.softmax_visible_cols.restype = i64
         L.softmax_rows_planned.argtypes = [vp, vp, i64, i64, i64, i64, ci, ctypes.POINTER(Plan), vp]
         L.softmax_rows_planned.restype = ci
         L.softmax_rows_host.argtypes = [vp, vp, i64, i64, i64, i64, ci, vp, vp, vp]
@@ -153,6 +165,24 @@ def softmax_rows_ptr(in_ptr: int, out_ptr: int, n_rows: int, n_cols: int, in_row
                                    out_row_stride, dtype, stream, path)
 
 
+def softmax_rows_ex_ptr(in_ptr: int, out_ptr: int, n_rows: int, n_cols: int, in_row_stride: int,
+                       out_row_stride: int, dtype: int, scale: float = 1.0, causal: bool = False,
+                       causal_period: int = 0, causal_offset: int = 0, stream: int = 0,
+                       path: int = -1) -> int:
+    """C ABI call of the scaled / causally masked softmax; returns the status."""
+    o = Options(scale, 1 if causal else 0, causal_period, causal_offset)
+    return lib().softmax_rows_ex(in_ptr, out_ptr, n_rows, n_cols, in_row_stride, out_row_stride,
+                                 dtype, ctypes.byref(o), path, stream)
+
+
+def visible_cols(n_rows: int, n_cols: int, row: int, scale: float = 1.0, causal: bool = False,
+                 causal_period: int = 0, causal_offset: int = 0) -> int:
+    """Leading columns of ``row`` that take part in its softmax (host-side, the
+    kernels' own arithmetic); -1 for invalid arguments."""
+    o = Options(scale, 1 if causal else 0, causal_period, causal_offset)
+    return lib().softmax_visible_cols(ctypes.byref(o), n_rows, n_cols, row)
+
+
 def softmax_rows_planned_ptr(in_ptr: int, out_ptr: int, n_rows: int, n_cols: int,
                              in_row_stride: int, out_row_stride: int, dtype: int, plan: Plan,
                              stream: int = 0) -> int:
@@ -187,11 +217,15 @@ def _stream_handle(stream, device) -> int:
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def softmax_rows(x, out=None, stream=None, path: int = PATH_AUTO):
-    """y = softmax(x) along the last dimension of a CUDA tensor (1-D or 2-D).
+def softmax_rows(x, out=None, stream=None, path: int = PATH_AUTO, scale: float = 1.0,
+                 causal: bool = False, causal_period: int = 0, causal_offset: int = 0):
+    """y = softmax(scale * x) along the last dimension of a CUDA tensor (1-D or 2-D).
 
-    ``out`` (optional) receives the result and may be ``x`` itself.  Runs on
-    ``stream`` (default: torch's current stream) without synchronising.
+    ``out`` (optional) receives the result and may be ``x`` itself.  With
+    ``causal``, column c of row r takes part iff c <= (r mod causal_period) +
+    causal_offset (period <= 0: n_rows); masked inputs are not read and give
+    exactly 0.  Runs on ``stream`` (default: torch's current stream) without
+    synchronising.
     """
     import torch
     if not x.is_cuda:
@@ -203,9 +237,15 @@ def softmax_rows(x, out=None, stream=None, path: int = PATH_AUTO):
         raise ValueError("softmax_rows: out must match x in dtype, shape and device")
     n_rows, n_cols, ld_in = _as_rows(x, "x")
     _, _, ld_out = _as_rows(out, "out")
+    transform = scale != 1.0 or causal
     with torch.cuda.device(x.device):
-        st = softmax_rows_ptr(x.data_ptr(), out.data_ptr(), n_rows, n_cols, ld_in, ld_out, dt,
-                              _stream_handle(stream, x.device), path)
+        h = _stream_handle(stream, x.device)
+        if transform:
+            st = softmax_rows_ex_ptr(x.data_ptr(), out.data_ptr(), n_rows, n_cols, ld_in, ld_out,
+                                     dt, scale, causal, causal_period, causal_offset, h, path)
+        else:
+            st = softmax_rows_ptr(x.data_ptr(), out.data_ptr(), n_rows, n_cols, ld_in, ld_out, dt,
+                                  h, path)
     if st != OK:
         raise SoftmaxError(st, "softmax_rows")
     return out

@@ -19,7 +19,9 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libsoftmax.so")
 
 SOURCES = ["softmax_abi.cu", "plan.cpp", "warp_rows.cu", "tile_rows.cu", "row_slices.cu",
-           "twopass.cu", "stream_rows.cu"]
+           "row_slices_options.cu", "twopass.cu", "stream_rows.cu"]
+# Sources that include another source file.
+INCLUDED = {"row_slices_options.cu": ["row_slices.cu"]}
 HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "kernels.h")] + [
     os.path.join(INCLUDE, "softmax.h")]
 
@@ -59,8 +61,9 @@ def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     objs = [os.path.join(BUILD, os.path.basename(s) + ".o") for s in srcs]
-    todo = [(s, o) for s, o in zip(srcs, objs)
-            if force or verbose or _stale(o, [s] + HEADERS + [os.path.abspath(__file__)])]
+    deps = lambda s: ([s] + [os.path.join(CSRC, d) for d in INCLUDED.get(os.path.basename(s), [])]
+                      + HEADERS + [os.path.abspath(__file__)])
+    todo = [(s, o) for s, o in zip(srcs, objs) if force or verbose or _stale(o, deps(s))]
     logs = []
     with cf.ThreadPoolExecutor(max_workers=jobs or min(len(todo) or 1, os.cpu_count() or 4)) as ex:
         for log in ex.map(lambda so: _compile(so[0], so[1], verbose), todo):

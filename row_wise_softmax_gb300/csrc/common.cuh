@@ -38,15 +38,16 @@ __device__ __forceinline__ float ex2_ftz(float t)
     return y;
 }
 
-__device__ __forceinline__ float exp_biased(float d)
+__device__ __forceinline__ float exp_biased(float d, float k)
 {
-    return ex2_ftz(fmaf(d, kLog2e, kExpBias));
+    return ex2_ftz(fmaf(d, k, kExpBias));
 }
 
-// Unbiased e^d for d <= 0, flushed to zero below 2^-126 (rescale factors).
-__device__ __forceinline__ float exp_ftz(float d)
+// Unbiased e^(d * k / log2 e) for d <= 0, flushed to zero below 2^-126
+// (rescale factors).
+__device__ __forceinline__ float exp_ftz(float d, float k)
 {
-    return ex2_ftz(d * kLog2e);
+    return ex2_ftz(d * k);
 }
 
 // ------------------------------------------------------------ reductions
@@ -74,21 +75,21 @@ __device__ __forceinline__ float warp_sum(float v)
 // -inf - (-inf) appears; a NaN carried in either l still propagates.  A
 // factor below 2^-126 flushes to zero: that partial is then below 2^-62 of
 // the merged sum, which is at least 2^64.
-__device__ __forceinline__ void ml_merge(float& m, float& l, float m2, float l2)
+__device__ __forceinline__ void ml_merge(float& m, float& l, float m2, float l2, float k)
 {
     const float M = fmaxf(m, m2);
     const float ref = (M == kNegInf) ? 0.0f : M;
-    l = l * exp_ftz(m - ref) + l2 * exp_ftz(m2 - ref);
+    l = l * exp_ftz(m - ref, k) + l2 * exp_ftz(m2 - ref, k);
     m = M;
 }
 
-__device__ __forceinline__ void warp_ml_merge(float& m, float& l)
+__device__ __forceinline__ void warp_ml_merge(float& m, float& l, float k)
 {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
         const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
-        ml_merge(m, l, m2, l2);
+        ml_merge(m, l, m2, l2, k);
     }
 }
 
@@ -197,11 +198,15 @@ __device__ __forceinline__ void store_vec(T* p, const float* v, float scale)
 }
 
 // Masked forms: positions at or past `limit` read -inf and are not written.
-template <typename T, int VEC>
+template <typename T, int VEC, bool SKIP = false>
 __device__ __forceinline__ void load_vec_masked(const T* row, int64_t col, int64_t limit, float* v)
 {
     if (col + VEC <= limit) {
         load_vec<T, VEC>(row + col, v);
+    } else if (SKIP && col >= limit) {           // wholly masked: no per-element tests
+#pragma unroll
+        for (int j = 0; j < VEC; ++j)
+            v[j] = kNegInf;
     } else {
 #pragma unroll
         for (int j = 0; j < VEC; ++j)
@@ -339,6 +344,20 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
 }
 
+// Bytes to bulk-copy of a span (16-byte aligned start) whose first `keep`
+// elements take part in the softmax and whose first `inb` elements lie inside
+// the row (or its padding before the next row): whole 16-byte granules up to
+// the one that holds the last kept element when that granule is in bounds,
+// else only the whole granules below it (the rest is read with plain loads).
+// Elements copied past `keep` are never used.
+template <typename T>
+__device__ __forceinline__ uint32_t span_copy_bytes(int64_t keep, int64_t inb)
+{
+    const uint64_t b = static_cast<uint64_t>(keep) * sizeof(T);
+    const uint64_t up = (b + 15u) & ~uint64_t{15};
+    return static_cast<uint32_t>(up <= static_cast<uint64_t>(inb) * sizeof(T) ? up : (b & ~uint64_t{15}));
+}
+
 // Global -> shared bulk copy completing on an mbarrier.  dst, src 16-byte
 // aligned; bytes a nonzero multiple of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
@@ -403,11 +422,12 @@ namespace rwsm {
 // CTA's (m, l).  red_m / red_l hold THREADS/32 floats; the caller separates
 // consecutive uses with a __syncthreads().
 template <int THREADS>
-__device__ __forceinline__ void cta_ml_reduce(float& m, float& l, float* red_m, float* red_l)
+__device__ __forceinline__ void cta_ml_reduce(float& m, float& l, float* red_m, float* red_l,
+                                              float k)
 {
     constexpr int NW = THREADS / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    warp_ml_merge(m, l);
+    warp_ml_merge(m, l, k);
     if (lane == 0) {
         red_m[warp] = m;
         red_l[warp] = l;
@@ -415,7 +435,7 @@ __device__ __forceinline__ void cta_ml_reduce(float& m, float& l, float* red_m, 
     __syncthreads();
     m = lane < NW ? red_m[lane] : kNegInf;
     l = lane < NW ? red_l[lane] : 0.0f;
-    warp_ml_merge(m, l);
+    warp_ml_merge(m, l, k);
 }
 
 // Exchange the CTA partials of a cluster through distributed shared memory:
@@ -426,7 +446,7 @@ __device__ __forceinline__ void cta_ml_reduce(float& m, float& l, float* red_m, 
 // rows, so a slot is rewritten only after the next barrier has shown that
 // every peer finished reading it.
 __device__ __forceinline__ void cluster_ml_reduce(float& m, float& l, float2* part,
-                                                  int slot, int cs)
+                                                  int slot, int cs, float k)
 {
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
@@ -440,7 +460,7 @@ __device__ __forceinline__ void cluster_ml_reduce(float& m, float& l, float2* pa
         pm = q.x;
         pl = q.y;
     }
-    warp_ml_merge(pm, pl);
+    warp_ml_merge(pm, pl, k);
     m = pm;
     l = pl;
 }

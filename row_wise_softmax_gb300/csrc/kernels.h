@@ -16,13 +16,110 @@ struct Problem {
     int64_t n_rows, n_cols, ld_in, ld_out;
     int dtype;
     bool no_bulk = false;   // rows live in host memory: no cp.async.bulk staging
+    // Logit transform (softmax_rows_ex): z = scale * x, optional causal mask.
+    float scale = 1.0f;
+    int causal = 0;
+    int64_t causal_period = 0;   // > 0 when causal
+    int64_t causal_offset = 0;
 };
+
+// Logit transform passed to every kernel.  The softmax is taken over
+// z = scale * x (scale > 0, default 1) with an optional causal mask: column c
+// of row r takes part iff c <= (r mod period) + offset; every other column is
+// -inf.  Because scale > 0, max z = scale * max x and z - max z =
+// scale * (x - max x), so the scale only changes the exponent multiplier
+// k = scale * log2 e: e^(z - max z) = 2^((x - max x) * k).  Masked columns are
+// never loaded: a row's loads stop at logits_valid(row).
+struct LogitsArg {
+    float k;             // scale * log2(e)
+    int causal;          // 0: no mask
+    int64_t period;      // > 0
+    int64_t offset;
+    // row mod period without a 64-bit division: q = floor(row / period) is
+    // SRL(t + SRL(row - t, sh1), sh2) with t = MULUH(mul, row), the unsigned
+    // division by an invariant integer of Granlund and Montgomery, "Division
+    // by invariant integers using multiplication" (PLDI 1994), figure 4.1,
+    // for 64-bit words (exact for every row in [0, 2^64)).
+    uint64_t mul;
+    int sh1, sh2;
+};
+
+__host__ __device__ __forceinline__ uint64_t mulhi_u64(uint64_t a, uint64_t b)
+{
+#ifdef __CUDA_ARCH__
+    return __umul64hi(a, b);
+#else
+    return static_cast<uint64_t>((static_cast<unsigned __int128>(a) * b) >> 64);
+#endif
+}
+
+// Columns [0, valid) of `row` take part in its softmax: all of them, or with
+// the causal mask those c <= (row mod period) + offset.
+__host__ __device__ __forceinline__ int64_t logits_valid(const LogitsArg& lg, int64_t row,
+                                                         int64_t n_cols)
+{
+    if (!lg.causal)
+        return n_cols;
+    const uint64_t n = static_cast<uint64_t>(row);
+    const uint64_t t = mulhi_u64(lg.mul, n);
+    const uint64_t q = (t + ((n - t) >> lg.sh1)) >> lg.sh2;
+    const int64_t lim = static_cast<int64_t>(n - q * static_cast<uint64_t>(lg.period)) + lg.offset + 1;
+    return lim < 0 ? 0 : (lim > n_cols ? n_cols : lim);
+}
+
+// Kernels are compiled twice: OPTS = false for the plain softmax (scale 1, no
+// mask: the multiplier is the constant log2 e and every column takes part,
+// with no per-row arithmetic), OPTS = true for any softmax_options_t.
+inline bool has_options(const Problem& p)
+{
+    return p.causal != 0 || p.scale != 1.0f;
+}
+
+// logits_valid for either compilation.
+template <bool OPTS>
+__host__ __device__ __forceinline__ int64_t kept_cols(const LogitsArg& lg, int64_t row,
+                                                      int64_t n_cols)
+{
+    if constexpr (OPTS)
+        return logits_valid(lg, row, n_cols);
+    else
+        return n_cols;
+}
+
+// Multiplier and shifts of the division by d >= 1 (figure 4.1 above, N = 64):
+// l = ceil(log2 d), mul = floor(2^64 (2^l - d) / d) + 1, sh1 = min(l, 1),
+// sh2 = max(l - 1, 0).
+inline void divisor_magic(uint64_t d, uint64_t* mul, int* sh1, int* sh2)
+{
+    int l = 0;
+    while (l < 64 && (static_cast<unsigned __int128>(1) << l) < d)
+        ++l;
+    const unsigned __int128 two64 = static_cast<unsigned __int128>(1) << 64;
+    const unsigned __int128 num = two64 * ((static_cast<unsigned __int128>(1) << l) - d);
+    *mul = static_cast<uint64_t>(num / d + 1);
+    *sh1 = l < 1 ? l : 1;
+    *sh2 = l - 1 > 0 ? l - 1 : 0;
+}
+
+inline LogitsArg logits_of(const Problem& p)
+{
+    const float log2e = 1.4426950408889634f;
+    LogitsArg a;
+    a.k = p.scale == 1.0f ? log2e : static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
+    a.causal = p.causal;
+    a.period = p.causal_period > 0 ? p.causal_period : 1;
+    a.offset = p.causal_offset;
+    divisor_magic(static_cast<uint64_t>(a.period), &a.mul, &a.sh1, &a.sh2);
+    return a;
+}
 
 // Scheduler (plan.cpp): validation and the path / launch-shape decision.
 int validate(const void* in, const void* out, int64_t n_rows, int64_t n_cols,
              int64_t ld_in, int64_t ld_out, int dtype);
 int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path,
               softmax_plan_t* plan);
+// Validate softmax_options_t into the problem (softmax_abi.cu).
+int apply_options(const softmax_options_t* o, Problem* p);
 // Is a caller-supplied plan safe and complete for this problem?
 int check_plan(const softmax_device_desc_t& dev, const Problem& p, const softmax_plan_t& plan);
 
@@ -30,6 +127,7 @@ int check_plan(const softmax_device_desc_t& dev, const Problem& p, const softmax
 cudaError_t launch_warp_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
 cudaError_t launch_tile_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
 cudaError_t launch_row_slices(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
+cudaError_t launch_row_slices_options(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
 cudaError_t launch_twopass(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
 cudaError_t launch_stream_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
 
@@ -39,6 +137,7 @@ int max_cluster_size_row_slices();
 // Error words of the translation units that wait on mbarriers: read and
 // optionally clear (host side, after the device has been synchronised).
 unsigned read_error_row_slices(bool clear);
+unsigned read_error_row_slices_options(bool clear);
 unsigned read_error_tile_rows(bool clear);
 unsigned read_error_stream_rows(bool clear);
 cudaError_t launch_selftest_wait(cudaStream_t s);

@@ -27,14 +27,25 @@
 // staging (input rows not 16-byte aligned, or rows in host memory) the kernel
 // reads the slice straight into registers (no ring), with 16-byte loads when
 // the rows allow.
+//
+// The kernel is compiled twice: here for the plain softmax, and for
+// softmax_options_t (scale, causal mask) in row_slices_options.cu, which
+// defines RWSM_ROW_SLICES_OPTIONS and includes this file, so that the two
+// sets of instantiations build in parallel.
 #include "common.cuh"
 #include "kernels.h"
 
 #include <atomic>
 
+#ifndef RWSM_ROW_SLICES_OPTIONS
+#define RWSM_ROW_SLICES_OPTIONS 0
+#endif
+
 namespace rwsm {
 
-__device__ unsigned g_error_row_slices = 0;
+// Error word of this translation unit's kernels (the options unit has its own).
+static __device__ unsigned g_error_row_slices = 0;
+constexpr bool kOptions = RWSM_ROW_SLICES_OPTIONS != 0;
 
 constexpr int kMaxStages = 8;
 constexpr uint32_t kBulkChunkBytes = 32768;
@@ -49,6 +60,16 @@ __device__ __forceinline__ void set_neg_inf(T* dst)
         *reinterpret_cast<float*>(dst) = kNegInf;
     else
         *reinterpret_cast<unsigned short*>(dst) = 0xff80u;   // bf16 -inf
+}
+
+// One element from shared memory, widened to fp32.
+template <typename T>
+__device__ __forceinline__ float lds1(const T* p)
+{
+    if constexpr (sizeof(T) == 4)
+        return *reinterpret_cast<const float*>(p);
+    else
+        return __uint_as_float(static_cast<unsigned>(*reinterpret_cast<const unsigned short*>(p)) << 16);
 }
 
 // Cluster-wide reduction of one float per CTA: thread 0 publishes v in its
@@ -72,10 +93,10 @@ __device__ __forceinline__ float cluster_reduce(float v, float* slot, int cs)
     return IS_MAX ? warp_max(r) : warp_sum(r);
 }
 
-template <typename T, int THREADS, int NV, bool BULK, bool OUTVEC>
+template <typename T, int THREADS, int NV, bool BULK, bool OUTVEC, bool OPTS>
 __global__ void __launch_bounds__(THREADS)
 row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
-                  int64_t ld_out, int slice_cols, int cs, int stages, int in_vec)
+                  int64_t ld_out, int slice_cols, int cs, int stages, int in_vec, LogitsArg lg)
 {
     constexpr int VEC = Elem<T>::kVec16;
     constexpr int NW = THREADS / 32;
@@ -87,6 +108,7 @@ row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in
     __shared__ unsigned issued[kMaxStages];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float kk = OPTS ? lg.k : kLog2e;       // exponent multiplier, scale * log2 e
     const int rank = static_cast<int>(blockIdx.x % cs);
     const int64_t cluster_id = blockIdx.x / cs;
     const int64_t n_clusters = gridDim.x / cs;
@@ -94,15 +116,27 @@ row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in
     int len = n_cols - c0;
     len = len < 0 ? 0 : (len > slice_cols ? slice_cols : len);
     const int nv = (len + VEC - 1) / VEC;
-    const uint32_t bulk_bytes = static_cast<uint32_t>(len * sizeof(T)) & ~15u;
-    const int bulk_elems = static_cast<int>(bulk_bytes / sizeof(T));
-    const int tail_vec = bulk_elems < len ? bulk_elems / VEC : -1;   // vector patched from HBM
+    // Without options every row copies [0, plain_copied) of the slice; the
+    // vector holding a < 16-byte ragged tail (if any) is tail_vec.
+    const uint32_t plain_bytes = static_cast<uint32_t>(len * sizeof(T)) & ~15u;
+    const int plain_copied = static_cast<int>(plain_bytes / sizeof(T));
+    const int tail_vec = plain_copied < len ? plain_copied / VEC : -1;
+    // Columns of this slice that take part in `row` (all of them unless a
+    // causal mask stops the row inside or before the slice).
+    auto row_lim = [&](int64_t row) -> int {
+        if constexpr (!OPTS)
+            return len;
+        int64_t lim = logits_valid(lg, row, n_cols) - c0;
+        return static_cast<int>(lim < 0 ? 0 : (lim > len ? len : lim));
+    };
 
     T* ring = reinterpret_cast<T*>((reinterpret_cast<uintptr_t>(smem_raw) + (kRingAlign - 1)) &
                                    ~static_cast<uintptr_t>(kRingAlign - 1));
     auto stage_ptr = [&](int s) { return ring + static_cast<int64_t>(s) * slice_cols; };
     auto issue = [&](int s, int64_t row) {      // thread 0 only
         const uint32_t bar = smem_addr(&full[s]);
+        const uint32_t bulk_bytes = OPTS ? span_copy_bytes<T>(row_lim(row), n_cols - c0)
+                                         : plain_bytes;
         fence_proxy_async_smem();
         issued[s] += 1;
         if (bulk_bytes) {
@@ -132,10 +166,13 @@ row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in
             }
             fence_mbar_init();
         }
-        // Positions the copies never write read as -inf (whole trailing vector).
-        for (int s = 0; s < stages; ++s)
-            for (int e = bulk_elems + tid; e < nv * VEC; e += THREADS)
-                set_neg_inf(stage_ptr(s) + e);
+        if constexpr (!OPTS) {
+            // Every row copies the same span: positions of the last vector
+            // that the copies never write read as -inf.
+            for (int s = 0; s < stages; ++s)
+                for (int e = plain_copied + tid; e < nv * VEC; e += THREADS)
+                    set_neg_inf(stage_ptr(s) + e);
+        }
         __syncthreads();
         pdl_wait();
         if (tid == 0)
@@ -152,28 +189,57 @@ row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in
     for (int64_t row = cluster_id; row < n_rows; row += n_clusters, ++i) {
         float x[E];
         const T* src = in + row * ld_in + c0;
+        const int lim = row_lim(row);
         if constexpr (BULK) {
             const int s = static_cast<int>(i % stages);
             const uint32_t parity = static_cast<uint32_t>((i / stages) & 1);
             const bool ok = failed ? true : mbar_wait_bounded(smem_addr(&full[s]), parity);
             const T* st = stage_ptr(s);
+            if constexpr (!OPTS) {
+                // [0, plain_copied) was copied, the rest of its last vector
+                // is -inf in the ring; a < 16-byte ragged tail of the row is
+                // patched in from HBM.
 #pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                const int v = tid + k * THREADS;
-                if (v < nv) {
-                    lds_vec<T, VEC>(st + v * VEC, &x[k * VEC]);
-                    if (v == tail_vec) {             // < 16-byte ragged tail
+                for (int k = 0; k < NV; ++k) {
+                    const int v = tid + k * THREADS;
+                    if (v < nv) {
+                        lds_vec<T, VEC>(st + v * VEC, &x[k * VEC]);
+                        if (v == tail_vec) {
+#pragma unroll
+                            for (int j = 0; j < VEC; ++j) {
+                                const int e = v * VEC + j;
+                                if (e >= plain_copied)
+                                    x[k * VEC + j] = e < len ? Elem<T>::load1(src + e) : kNegInf;
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j)
+                            x[k * VEC + j] = kNegInf;
+                    }
+                }
+            } else {
+                // [0, copied) was copied; [copied, lim) is a < 16-byte tail read
+                // from HBM; from lim on the slice is masked or past the row (-inf).
+                int copied = static_cast<int>(span_copy_bytes<T>(lim, n_cols - c0) / sizeof(T));
+                copied = copied < lim ? copied : lim;
+#pragma unroll
+                for (int k = 0; k < NV; ++k) {
+                    const int e0 = (tid + k * THREADS) * VEC;
+                    if (e0 + VEC <= copied) {
+                        lds_vec<T, VEC>(st + e0, &x[k * VEC]);
+                    } else if (e0 >= lim) {
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j)
+                            x[k * VEC + j] = kNegInf;
+                    } else {
 #pragma unroll
                         for (int j = 0; j < VEC; ++j) {
-                            const int e = v * VEC + j;
-                            if (e >= bulk_elems)
-                                x[k * VEC + j] = e < len ? Elem<T>::load1(src + e) : kNegInf;
+                            const int e = e0 + j;
+                            x[k * VEC + j] = e < copied ? lds1(st + e)
+                                                        : (e < lim ? Elem<T>::load1(src + e) : kNegInf);
                         }
                     }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j)
-                        x[k * VEC + j] = kNegInf;
                 }
             }
             // Every thread has its slice in registers: the stage is free.
@@ -190,7 +256,7 @@ row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in
             for (int k = 0; k < NV; ++k) {
                 const int v = tid + k * THREADS;
                 if (v < nv) {
-                    load_vec_masked<T, VEC>(src, v * VEC, len, &x[k * VEC]);
+                    load_vec_masked<T, VEC, OPTS>(src, v * VEC, lim, &x[k * VEC]);
                 } else {
 #pragma unroll
                     for (int j = 0; j < VEC; ++j)
@@ -206,7 +272,7 @@ row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in
 #pragma unroll
                 for (int j = 0; j < VEC; ++j) {
                     const int e = v * VEC + j;
-                    x[k * VEC + j] = (v < nv && e < len) ? Elem<T>::load1(src + e) : kNegInf;
+                    x[k * VEC + j] = (v < nv && e < lim) ? Elem<T>::load1(src + e) : kNegInf;
                 }
             }
         }
@@ -228,7 +294,7 @@ row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in
         float l = 0.0f;
 #pragma unroll
         for (int e = 0; e < E; ++e) {
-            x[e] = exp_biased(x[e] - m);
+            x[e] = exp_biased(x[e] - m, kk);
             l += x[e];
         }
         l = warp_sum(l);
@@ -269,6 +335,19 @@ row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in
     }
 }
 
+static unsigned read_error_tu(bool clear)
+{
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_error_row_slices, sizeof v) != cudaSuccess)
+        return 0;
+    if (clear && v) {
+        const unsigned zero = 0;
+        cudaMemcpyToSymbol(g_error_row_slices, &zero, sizeof zero);
+    }
+    return v;
+}
+
+#if !RWSM_ROW_SLICES_OPTIONS
 // A single thread waits, with the bounded wait above, on an mbarrier that
 // expects one arrival nobody makes; the wait runs out and the timeout is
 // recorded in the same error word the row-slice kernel uses.
@@ -289,19 +368,16 @@ cudaError_t launch_selftest_wait(cudaStream_t s)
     return cudaGetLastError();
 }
 
-// ------------------------------------------------------------------ host side
-
 unsigned read_error_row_slices(bool clear)
 {
-    unsigned v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_error_row_slices, sizeof v) != cudaSuccess)
-        return 0;
-    if (clear && v) {
-        const unsigned zero = 0;
-        cudaMemcpyToSymbol(g_error_row_slices, &zero, sizeof zero);
-    }
-    return v;
+    return read_error_tu(clear) | read_error_row_slices_options(clear);
 }
+#else
+unsigned read_error_row_slices_options(bool clear)
+{
+    return read_error_tu(clear);
+}
+#endif
 
 namespace {
 
@@ -315,7 +391,7 @@ struct KernelAttrs {
 template <typename T, int THREADS, int NV, bool BULK, bool OUTVEC>
 cudaError_t launch_rs(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
 {
-    auto* k = row_slices_kernel<T, THREADS, NV, BULK, OUTVEC>;
+    auto* k = row_slices_kernel<T, THREADS, NV, BULK, OUTVEC, kOptions>;
     static KernelAttrs attrs;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -373,7 +449,7 @@ cudaError_t launch_rs(const Problem& p, const softmax_plan_t& plan, cudaStream_t
     err = cudaLaunchKernelEx(&cfg, k, static_cast<const T*>(p.in), static_cast<T*>(p.out),
                              p.n_rows, static_cast<int>(p.n_cols), p.ld_in, p.ld_out,
                              static_cast<int>(plan.slice_cols), cs, plan.stages,
-                             plan.vec > 1 ? 1 : 0);
+                             plan.vec > 1 ? 1 : 0, logits_of(p));
     note_launch();
     return err;
 }
@@ -418,17 +494,26 @@ cudaError_t launch_threads(const Problem& p, const softmax_plan_t& plan, cudaStr
 
 }  // namespace
 
+#if RWSM_ROW_SLICES_OPTIONS
+cudaError_t launch_row_slices_options(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
+{
+    return p.dtype == SOFTMAX_F32 ? launch_threads<float>(p, plan, s)
+                                  : launch_threads<BF16Bits>(p, plan, s);
+}
+#else
 cudaError_t launch_row_slices(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
 {
     if (plan.bulk_copy && (plan.stages < 1 || plan.stages > kMaxStages))
         return cudaErrorInvalidValue;
+    if (has_options(p))
+        return launch_row_slices_options(p, plan, s);
     return p.dtype == SOFTMAX_F32 ? launch_threads<float>(p, plan, s)
                                   : launch_threads<BF16Bits>(p, plan, s);
 }
 
 int max_cluster_size_row_slices()
 {
-    auto* k = row_slices_kernel<float, 512, 8, true, true>;
+    auto* k = row_slices_kernel<float, 512, 8, true, true, false>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
         return 8;
     const int smem = 64 * 1024 + kRingAlign;
@@ -445,5 +530,6 @@ int max_cluster_size_row_slices()
     }
     return size > 16 ? 16 : size;
 }
+#endif
 
 }  // namespace rwsm

@@ -79,6 +79,33 @@ std::mutex g_occ_mu;
 OccEntry g_occ[256];
 int g_occ_n = 0;
 
+}  // namespace
+
+// Validate softmax_options_t and copy it into the problem (NULL: defaults).
+int apply_options(const softmax_options_t* o, Problem* p)
+{
+    if (!o)
+        return SOFTMAX_OK;
+    // scale * log2(e) must stay finite in float: 0 < scale <= 2^127 (rejects NaN).
+    if (!(o->scale > 0.0f) || !(o->scale <= 0x1p127f))
+        return SOFTMAX_ERR_INVALID_ARG;
+    if (o->causal != 0 && o->causal != 1)
+        return SOFTMAX_ERR_INVALID_ARG;
+    const int64_t lim = int64_t{1} << 62;
+    if (o->causal_offset >= lim || o->causal_offset <= -lim)
+        return SOFTMAX_ERR_INVALID_ARG;
+    p->scale = o->scale;
+    p->causal = o->causal;
+    // Rows are < n_rows, so a period of n_rows or more is the same as n_rows;
+    // clamped, (row mod period) + offset + 1 stays far inside int64.
+    const int64_t whole = p->n_rows > 0 ? p->n_rows : 1;
+    p->causal_period = o->causal_period > 0 && o->causal_period < whole ? o->causal_period : whole;
+    p->causal_offset = o->causal_offset;
+    return SOFTMAX_OK;
+}
+
+namespace {
+
 int launch_path(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
 {
     cudaError_t err = cudaErrorInvalidValue;
@@ -198,23 +225,8 @@ int softmax_rows_path(const void* in, void* out, int64_t n_rows, int64_t n_cols,
                       int64_t in_row_stride, int64_t out_row_stride, int dtype,
                       void* stream, int path)
 {
-    const int st = rwsm::validate(in, out, n_rows, n_cols, in_row_stride, out_row_stride, dtype);
-    if (st != SOFTMAX_OK)
-        return st;
-    if (path < SOFTMAX_PATH_AUTO || path > SOFTMAX_PATH_TWOPASS)
-        return SOFTMAX_ERR_INVALID_ARG;
-    if (n_rows == 0 || n_cols == 0)
-        return SOFTMAX_OK;
-    softmax_device_desc_t d;
-    const int ds = rwsm::current_device(&d);
-    if (ds != SOFTMAX_OK)
-        return ds;
-    const Problem p{in, out, n_rows, n_cols, in_row_stride, out_row_stride, dtype};
-    softmax_plan_t plan;
-    const int ps = rwsm::make_plan(d, p, path, &plan);
-    if (ps != SOFTMAX_OK)
-        return ps;
-    return rwsm::launch_path(p, plan, static_cast<cudaStream_t>(stream));
+    return softmax_rows_ex(in, out, n_rows, n_cols, in_row_stride, out_row_stride, dtype,
+                           nullptr, path, stream);
 }
 
 int softmax_rows_planned(const void* in, void* out, int64_t n_rows, int64_t n_cols,
@@ -237,6 +249,43 @@ int softmax_rows_planned(const void* in, void* out, int64_t n_rows, int64_t n_co
     if (cs != SOFTMAX_OK)
         return cs;
     return rwsm::launch_path(p, *plan, static_cast<cudaStream_t>(stream));
+}
+
+int softmax_rows_ex(const void* in, void* out, int64_t n_rows, int64_t n_cols,
+                    int64_t in_row_stride, int64_t out_row_stride, int dtype,
+                    const softmax_options_t* options, int path, void* stream)
+{
+    const int st = rwsm::validate(in, out, n_rows, n_cols, in_row_stride, out_row_stride, dtype);
+    if (st != SOFTMAX_OK)
+        return st;
+    if (path < SOFTMAX_PATH_AUTO || path > SOFTMAX_PATH_TWOPASS)
+        return SOFTMAX_ERR_INVALID_ARG;
+    Problem p{in, out, n_rows, n_cols, in_row_stride, out_row_stride, dtype};
+    const int os = rwsm::apply_options(options, &p);
+    if (os != SOFTMAX_OK)
+        return os;
+    if (n_rows == 0 || n_cols == 0)
+        return SOFTMAX_OK;
+    softmax_device_desc_t d;
+    const int ds = rwsm::current_device(&d);
+    if (ds != SOFTMAX_OK)
+        return ds;
+    softmax_plan_t plan;
+    const int ps = rwsm::make_plan(d, p, path, &plan);
+    if (ps != SOFTMAX_OK)
+        return ps;
+    return rwsm::launch_path(p, plan, static_cast<cudaStream_t>(stream));
+}
+
+int64_t softmax_visible_cols(const softmax_options_t* options, int64_t n_rows, int64_t n_cols,
+                             int64_t row)
+{
+    if (n_rows < 0 || n_cols < 0 || row < 0 || row >= n_rows || n_rows > (int64_t{1} << 62))
+        return -1;
+    Problem p{nullptr, nullptr, n_rows, n_cols, n_cols, n_cols, SOFTMAX_F32};
+    if (rwsm::apply_options(options, &p) != SOFTMAX_OK)
+        return -1;
+    return rwsm::logits_valid(rwsm::logits_of(p), row, n_cols);
 }
 
 int softmax_rows(const void* in, void* out, int64_t n_rows, int64_t n_cols,

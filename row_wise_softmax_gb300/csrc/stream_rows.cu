@@ -35,10 +35,10 @@ __device__ unsigned g_error_stream_rows = 0;
 constexpr int kStreamMaxStages = 8;
 constexpr int kStreamRingAlign = 128;
 
-template <typename T, int THREADS, int NV, bool OUTVEC>
+template <typename T, int THREADS, int NV, bool OUTVEC, bool OPTS>
 __global__ void __launch_bounds__(THREADS)
 stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_in,
-                   int64_t ld_out, int64_t slice_cols, int cs, int stages)
+                   int64_t ld_out, int64_t slice_cols, int cs, int stages, LogitsArg lg)
 {
     constexpr int VEC = Elem<T>::kVec16;
     constexpr int NW = THREADS / 32;
@@ -51,6 +51,7 @@ stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t 
     __shared__ unsigned issued[kStreamMaxStages];
 
     const int tid = threadIdx.x;
+    const float kk = OPTS ? lg.k : kLog2e;       // exponent multiplier, scale * log2 e
     const int rank = static_cast<int>(blockIdx.x % cs);
     const int64_t cluster_id = blockIdx.x / cs;
     const int64_t n_clusters = gridDim.x / cs;
@@ -69,6 +70,15 @@ stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t 
         const int64_t rest = len - chunk * CHUNK;
         return static_cast<int>(rest < CHUNK ? rest : CHUNK);
     };
+    // Columns of this slice that take part in `row` (all of them unless a
+    // causal mask stops the row inside or before the slice), and of `chunk`
+    // given that count (masked columns are never copied).
+    auto row_keep = [&](int64_t row) -> int64_t { return kept_cols<OPTS>(lg, row, n_cols) - c0; };
+    auto chunk_lim = [&](int64_t keep, int64_t chunk) {
+        const int64_t rest = keep - chunk * CHUNK;
+        const int clen = chunk_len(chunk);
+        return static_cast<int>(rest < 0 ? 0 : (rest > clen ? clen : rest));
+    };
     const uint64_t keep = policy_evict_last();
     const uint64_t stream = policy_evict_first();
     auto issue = [&](int64_t q) {                       // thread 0 only
@@ -77,7 +87,11 @@ stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t 
         const bool second = ((q / K) & 1) != 0;
         const int64_t chunk = q % K;
         const int64_t row = cluster_id + i * n_clusters;
-        const uint32_t bytes = static_cast<uint32_t>(chunk_len(chunk) * sizeof(T)) & ~15u;
+        uint32_t bytes;
+        if constexpr (OPTS)
+            bytes = span_copy_bytes<T>(chunk_lim(row_keep(row), chunk), n_cols - c0 - chunk * CHUNK);
+        else
+            bytes = static_cast<uint32_t>(chunk_len(chunk) * sizeof(T)) & ~15u;
         const uint32_t bar = smem_addr(&full[s]);
         fence_proxy_async_smem();
         issued[s] += 1;
@@ -112,12 +126,19 @@ stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t 
     int64_t q = 0;
     // Wait for chunk q, copy this thread's vectors into registers (ragged
     // tail from HBM), release the stage and start the copy `stages` ahead.
-    auto take = [&](const T* src_row, int64_t chunk, float (&x)[E]) {
+    auto take = [&](int64_t keep, const T* src_row, int64_t chunk, float (&x)[E]) {
         const int s = static_cast<int>(q % stages);
         const uint32_t parity = static_cast<uint32_t>((q / stages) & 1);
         const bool ok = failed ? true : mbar_wait_bounded(smem_addr(&full[s]), parity);
-        const int clen = chunk_len(chunk);
-        const int bulk = static_cast<int>((clen * sizeof(T)) & ~size_t{15}) / static_cast<int>(sizeof(T));
+        int clen, bulk;                              // kept columns, copied columns
+        if constexpr (OPTS) {
+            clen = chunk_lim(keep, chunk);
+            bulk = static_cast<int>(span_copy_bytes<T>(clen, n_cols - c0 - chunk * CHUNK) / sizeof(T));
+            bulk = bulk < clen ? bulk : clen;
+        } else {
+            clen = chunk_len(chunk);
+            bulk = static_cast<int>((clen * sizeof(T)) & ~size_t{15}) / static_cast<int>(sizeof(T));
+        }
         const T* st = stage_ptr(s);
         const T* g = src_row + chunk * CHUNK;
 #pragma unroll
@@ -125,6 +146,10 @@ stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t 
             const int e0 = (tid + k * THREADS) * VEC;
             if (e0 + VEC <= bulk) {
                 lds_vec<T, VEC>(st + e0, &x[k * VEC]);
+            } else if (OPTS && e0 >= clen) {
+#pragma unroll
+                for (int j = 0; j < VEC; ++j)
+                    x[k * VEC + j] = kNegInf;
             } else {
 #pragma unroll
                 for (int j = 0; j < VEC; ++j) {
@@ -143,11 +168,12 @@ stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t 
     int slot = 0;
     for (int64_t row = cluster_id; row < n_rows; row += n_clusters, slot ^= 1) {
         const T* src = in + row * ld_in + c0;
+        const int64_t keep = row_keep(row);
         // ---- pass 1: online (m, l)
         float m = kNegInf, l = 0.0f;
         for (int64_t chunk = 0; chunk < K; ++chunk) {
             float x[E];
-            take(src, chunk, x);
+            take(keep, src, chunk, x);
             float bm = kNegInf;
 #pragma unroll
             for (int e = 0; e < E; ++e)
@@ -157,19 +183,19 @@ stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t 
             float sum = 0.0f;
 #pragma unroll
             for (int e = 0; e < E; ++e)
-                sum += exp_biased(x[e] - ref);
-            l = l * exp_ftz(m - ref) + sum;
+                sum += exp_biased(x[e] - ref, kk);
+            l = l * exp_ftz(m - ref, kk) + sum;
             m = mn;
         }
-        cta_ml_reduce<THREADS>(m, l, red_m, red_l);
+        cta_ml_reduce<THREADS>(m, l, red_m, red_l, kk);
         if (cs > 1)
-            cluster_ml_reduce(m, l, part, slot, cs);
+            cluster_ml_reduce(m, l, part, slot, cs, kk);
         const float inv = 1.0f / l;
         // ---- pass 2: normalise and store
         T* dst = out + row * ld_out + c0;
         for (int64_t chunk = 0; chunk < K; ++chunk) {
             float x[E];
-            take(src, chunk, x);
+            take(keep, src, chunk, x);
             const int clen = chunk_len(chunk);
             T* d = dst + chunk * CHUNK;
 #pragma unroll
@@ -178,7 +204,7 @@ stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t 
                 if (e0 < clen) {
 #pragma unroll
                     for (int j = 0; j < VEC; ++j)
-                        x[k * VEC + j] = exp_biased(x[k * VEC + j] - m);
+                        x[k * VEC + j] = exp_biased(x[k * VEC + j] - m, kk);
                     if constexpr (OUTVEC) {
                         if (e0 + VEC <= clen)
                             store16_hint<T>(d + e0, &x[k * VEC], inv, stream);
@@ -230,10 +256,10 @@ struct StreamAttrs {
     std::atomic<bool> flags_set[kMaxDevices];
 };
 
-template <typename T, int THREADS, int NV, bool OUTVEC>
-cudaError_t launch_stream(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
+template <typename T, int THREADS, int NV, bool OUTVEC, bool OPTS>
+cudaError_t launch_stream_opts(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
 {
-    auto* k = stream_rows_kernel<T, THREADS, NV, OUTVEC>;
+    auto* k = stream_rows_kernel<T, THREADS, NV, OUTVEC, OPTS>;
     static StreamAttrs attrs;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -289,9 +315,16 @@ cudaError_t launch_stream(const Problem& p, const softmax_plan_t& plan, cudaStre
     cfg.numAttrs = static_cast<unsigned>(n_attr);
     err = cudaLaunchKernelEx(&cfg, k, static_cast<const T*>(p.in), static_cast<T*>(p.out),
                              p.n_rows, p.n_cols, p.ld_in, p.ld_out, plan.slice_cols, cs,
-                             plan.stages);
+                             plan.stages, logits_of(p));
     note_launch();
     return err;
+}
+
+template <typename T, int THREADS, int NV, bool OUTVEC>
+cudaError_t launch_stream(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
+{
+    return has_options(p) ? launch_stream_opts<T, THREADS, NV, OUTVEC, true>(p, plan, s)
+                    : launch_stream_opts<T, THREADS, NV, OUTVEC, false>(p, plan, s);
 }
 
 template <typename T, int THREADS>

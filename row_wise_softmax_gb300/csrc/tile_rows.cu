@@ -4,10 +4,11 @@
 //
 //   ring    one elected thread starts one cp.async.bulk copy per row of a tile
 //           (global -> shared, all completing on the stage's mbarrier).  A row
-//           is copied with its padding up to the next 16 bytes when that
-//           padding lies before the next row's start (the padding is then
-//           masked to -inf); only the matrix's last row can leave a < 16-byte
-//           tail, read by the lane that owns it with a plain load.
+//           is copied up to the 16-byte granule holding its last kept column,
+//           with its padding when that lies before the next row's start (the
+//           padding and any masked columns copied are taken as -inf); only
+//           the matrix's last row can leave a < 16-byte tail, read by the
+//           lane that owns it with a plain load.
 //   rows    each warp owns R/4 rows of the tile and reduces them one after the
 //           other straight out of shared memory: lane l reads the vectors at
 //           columns (c*32 + l)*VEC, then max (__shfl_xor), e = exp(x - max),
@@ -51,10 +52,10 @@ __device__ __forceinline__ void lds_any(const T* p, float* v)
 
 // At most 64 registers per thread (8 CTAs per SM): the kernel is latency
 // bound, so resident warps matter more than registers (no spills at 64).
-template <typename T, int VEC, int CHUNKS>
+template <typename T, int VEC, int CHUNKS, bool OPTS>
 __global__ void __launch_bounds__(kTileThreads, 8)
 tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
-                 int64_t ld_out, int rows_per_warp, int stages, int row_pad)
+                 int64_t ld_out, int rows_per_warp, int stages, int row_pad, LogitsArg lg)
 {
     constexpr int E = VEC * CHUNKS;
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -62,16 +63,21 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
     __shared__ unsigned issued[kTileMaxStages];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float kk = OPTS ? lg.k : kLog2e;       // exponent multiplier, scale * log2 e
     const int R = kTileWarps * rows_per_warp;
     const int64_t n_tiles = (n_rows + R - 1) / R;
-    const uint32_t row_bytes = static_cast<uint32_t>(n_cols * sizeof(T)) & ~15u;
-    const int bulk_elems = static_cast<int>(row_bytes / sizeof(T));
-    // Whole padded rows (row_pad elements) may be copied for every row but the
-    // last when the row stride covers them.
+    // A row is copied up to the 16-byte granule that holds its last kept
+    // column (all of it without a mask).  That granule may reach into the
+    // row's padding (up to row_pad elements) when the row stride covers the
+    // padding and another row follows.
     const bool pad_ok = ld_in >= row_pad;
     const uint32_t pad_bytes = static_cast<uint32_t>(row_pad * sizeof(T));
-    auto copy_bytes = [&](int64_t row) {
-        return (pad_ok && row + 1 < n_rows) ? pad_bytes : row_bytes;
+    const uint32_t row_bytes = static_cast<uint32_t>(n_cols * sizeof(T)) & ~15u;
+    auto copy_bytes = [&](int64_t row, int64_t lim) -> uint32_t {
+        if constexpr (OPTS)
+            return span_copy_bytes<T>(lim, pad_ok && row + 1 < n_rows ? row_pad : n_cols);
+        else
+            return pad_ok && row + 1 < n_rows ? pad_bytes : row_bytes;
     };
 
     T* ring = reinterpret_cast<T*>((reinterpret_cast<uintptr_t>(smem_raw) + (kTileRingAlign - 1)) &
@@ -85,11 +91,11 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
         issued[s] += 1;
         uint32_t total = 0;
         for (int r = 0; r < nr; ++r)
-            total += copy_bytes(r0 + r);
+            total += copy_bytes(r0 + r, kept_cols<OPTS>(lg, r0 + r, n_cols));
         if (total) {
             mbar_arrive_expect_tx(bar, total);
             for (int r = 0; r < nr; ++r) {
-                const uint32_t n = copy_bytes(r0 + r);
+                const uint32_t n = copy_bytes(r0 + r, kept_cols<OPTS>(lg, r0 + r, n_cols));
                 if (n)
                     bulk_g2s(smem_addr(row_ptr(s, r)), in + (r0 + r) * ld_in, n, bar);
             }
@@ -128,15 +134,22 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
                 break;                           // warp-uniform
             const T* sp = row_ptr(s, r);
             const T* gp = in + row * ld_in;
-            // Columns [0, avail) are in shared memory; [avail, n_cols) is the
-            // last row's < 16-byte tail; from n_cols on the row is padding.
-            const int avail = copy_bytes(row) == pad_bytes ? n_cols : bulk_elems;
+            // Columns [0, avail) are in shared memory, [avail, lim) is a
+            // < 16-byte tail read from HBM, and from lim on the row is masked
+            // or padding (-inf).
+            const int lim = static_cast<int>(kept_cols<OPTS>(lg, row, n_cols));
+            const int copied = static_cast<int>(copy_bytes(row, lim) / sizeof(T));
+            const int avail = copied < lim ? copied : lim;
             float x[E];
 #pragma unroll
             for (int c = 0; c < CHUNKS; ++c) {
                 const int col = (c * 32 + lane) * VEC;
                 if (col + VEC <= avail) {
                     lds_any<T, VEC>(sp + col, &x[c * VEC]);
+                } else if (OPTS && col >= lim) {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j)
+                        x[c * VEC + j] = kNegInf;
                 } else {
 #pragma unroll
                     for (int j = 0; j < VEC; ++j) {
@@ -144,7 +157,7 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
                         if (e < avail)
                             lds_any<T, 1>(sp + e, &x[c * VEC + j]);
                         else
-                            x[c * VEC + j] = e < n_cols ? Elem<T>::load1(gp + e) : kNegInf;
+                            x[c * VEC + j] = e < lim ? Elem<T>::load1(gp + e) : kNegInf;
                     }
                 }
             }
@@ -156,7 +169,7 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
             float l = 0.0f;
 #pragma unroll
             for (int e = 0; e < E; ++e) {
-                x[e] = exp_biased(x[e] - m);
+                x[e] = exp_biased(x[e] - m, kk);
                 l += x[e];
             }
             l = warp_sum(l);
@@ -200,10 +213,10 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-template <typename T, int VEC, int CHUNKS>
-cudaError_t launch_tile(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
+template <typename T, int VEC, int CHUNKS, bool OPTS>
+cudaError_t launch_tile_opts(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
 {
-    auto* k = tile_rows_kernel<T, VEC, CHUNKS>;
+    auto* k = tile_rows_kernel<T, VEC, CHUNKS, OPTS>;
     static std::atomic<int> smem_set[kMaxDevices];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -242,9 +255,16 @@ cudaError_t launch_tile(const Problem& p, const softmax_plan_t& plan, cudaStream
     cfg.numAttrs = static_cast<unsigned>(launch_attrs(attr, 1));
     err = cudaLaunchKernelEx(&cfg, k, static_cast<const T*>(p.in), static_cast<T*>(p.out),
                              p.n_rows, static_cast<int>(p.n_cols), p.ld_in, p.ld_out,
-                             plan.rows_per_warp, plan.stages, row_pad);
+                             plan.rows_per_warp, plan.stages, row_pad, logits_of(p));
     note_launch();
     return err;
+}
+
+template <typename T, int VEC, int CHUNKS>
+cudaError_t launch_tile(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
+{
+    return has_options(p) ? launch_tile_opts<T, VEC, CHUNKS, true>(p, plan, s)
+                    : launch_tile_opts<T, VEC, CHUNKS, false>(p, plan, s);
 }
 
 template <typename T, int VEC>

@@ -86,7 +86,7 @@ __device__ __forceinline__ void pipelined_batches(const T* src, int64_t nv, int6
 template <typename T, int VEC, int THREADS>
 __global__ void __launch_bounds__(THREADS)
 twopass_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_in,
-               int64_t ld_out, int64_t slice_cols, int cs)
+               int64_t ld_out, int64_t slice_cols, int cs, LogitsArg lg)
 {
     constexpr int NW = THREADS / 32;
     constexpr int B = kTwoPassBatch;
@@ -112,9 +112,12 @@ twopass_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_i
     int slot = 0;
     for (int64_t row = cluster_id; row < n_rows; row += n_clusters, slot ^= 1) {
         const T* src = in + row * ld_in + c0;
+        // Kept columns of this slice (a causal mask can stop the row early).
+        int64_t lim = logits_valid(lg, row, n_cols) - c0;
+        lim = lim < 0 ? 0 : (lim > len ? len : lim);
         // ---- pass 1: online (m, l) over this thread's batches
         float m = kNegInf, l = 0.0f;
-        pipelined_batches<T, VEC, B, THREADS>(src, nv, len, keep,
+        pipelined_batches<T, VEC, B, THREADS>(src, nv, lim, keep,
             [&](const float (&x)[B * VEC], int64_t) {
                 float bm = kNegInf;
 #pragma unroll
@@ -125,18 +128,18 @@ twopass_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_i
                 float s = 0.0f;
 #pragma unroll
                 for (int i = 0; i < B * VEC; ++i)
-                    s += exp_biased(x[i] - ref);
-                l = l * exp_ftz(m - ref) + s;
+                    s += exp_biased(x[i] - ref, lg.k);
+                l = l * exp_ftz(m - ref, lg.k) + s;
                 m = mn;
             });
-        cta_ml_reduce<THREADS>(m, l, red_m, red_l);
+        cta_ml_reduce<THREADS>(m, l, red_m, red_l, lg.k);
         if (cs > 1)
-            cluster_ml_reduce(m, l, part, slot, cs);
+            cluster_ml_reduce(m, l, part, slot, cs, lg.k);
         const float inv = 1.0f / l;
 
         // ---- pass 2: normalise (the re-read mostly hits L2)
         T* dst = out + row * ld_out + c0;
-        pipelined_batches<T, VEC, B, THREADS>(src, nv, len, stream,
+        pipelined_batches<T, VEC, B, THREADS>(src, nv, lim, stream,
             [&](const float (&xin)[B * VEC], int64_t v0) {
 #pragma unroll
                 for (int k = 0; k < B; ++k) {
@@ -145,7 +148,7 @@ twopass_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_i
                         float x[VEC];
 #pragma unroll
                         for (int j = 0; j < VEC; ++j)
-                            x[j] = exp_biased(xin[k * VEC + j] - m);
+                            x[j] = exp_biased(xin[k * VEC + j] - m, lg.k);
                         if (VEC * sizeof(T) == 16 && (v + 1) * VEC <= len)
                             store16_hint<T>(dst + v * VEC, x, inv, stream);
                         else
@@ -208,7 +211,8 @@ cudaError_t launch_tp(const Problem& p, const softmax_plan_t& plan, cudaStream_t
     cfg.attrs = attr;
     cfg.numAttrs = static_cast<unsigned>(launch_attrs(attr, cs));
     err = cudaLaunchKernelEx(&cfg, k, static_cast<const T*>(p.in), static_cast<T*>(p.out),
-                             p.n_rows, p.n_cols, p.ld_in, p.ld_out, plan.slice_cols, cs);
+                             p.n_rows, p.n_cols, p.ld_in, p.ld_out, plan.slice_cols, cs,
+                             logits_of(p));
     note_launch();
     return err;
 }

@@ -23,18 +23,21 @@ namespace rwsm {
 
 constexpr int kWarpPathThreads = 128;
 
-template <typename T, int VEC, int CHUNKS, int ROWS>
+template <typename T, int VEC, int CHUNKS, int ROWS, bool OPTS>
 __device__ __forceinline__ void load_group(const T* in, int64_t g, int64_t n_rows, int n_cols,
-                                           int64_t ld_in, int lane, float (&v)[ROWS][VEC * CHUNKS])
+                                           int64_t ld_in, const LogitsArg lg, int lane,
+                                           float (&v)[ROWS][VEC * CHUNKS])
 {
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
         const int64_t row = g * ROWS + r;
         if (row < n_rows) {
             const T* src = in + row * ld_in;
+            const int64_t lim = kept_cols<OPTS>(lg, row, n_cols);   // masked columns: not read
 #pragma unroll
             for (int c = 0; c < CHUNKS; ++c)
-                load_vec_masked<T, VEC>(src, (c * 32 + lane) * VEC, n_cols, &v[r][c * VEC]);
+                load_vec_masked<T, VEC, OPTS && (VEC > 1)>(src, (c * 32 + lane) * VEC, lim,
+                                                          &v[r][c * VEC]);
         } else {
 #pragma unroll
             for (int k = 0; k < VEC * CHUNKS; ++k)
@@ -45,7 +48,8 @@ __device__ __forceinline__ void load_group(const T* in, int64_t g, int64_t n_row
 
 template <typename T, int VEC, int CHUNKS, int ROWS>
 __device__ __forceinline__ void softmax_group(T* out, int64_t g, int64_t n_rows, int n_cols,
-                                              int64_t ld_out, int lane, float (&v)[ROWS][VEC * CHUNKS])
+                                              int64_t ld_out, float k, int lane,
+                                              float (&v)[ROWS][VEC * CHUNKS])
 {
     constexpr int E = VEC * CHUNKS;
 #pragma unroll
@@ -53,14 +57,14 @@ __device__ __forceinline__ void softmax_group(T* out, int64_t g, int64_t n_rows,
         const int64_t row = g * ROWS + r;
         float m = kNegInf;
 #pragma unroll
-        for (int k = 0; k < E; ++k)
-            m = fmaxf(m, v[r][k]);
+        for (int e = 0; e < E; ++e)
+            m = fmaxf(m, v[r][e]);
         m = warp_max(m);
         float l = 0.0f;
 #pragma unroll
-        for (int k = 0; k < E; ++k) {
-            v[r][k] = exp_biased(v[r][k] - m);
-            l += v[r][k];
+        for (int e = 0; e < E; ++e) {
+            v[r][e] = exp_biased(v[r][e] - m, k);
+            l += v[r][e];
         }
         l = warp_sum(l);
         const float inv = 1.0f / l;
@@ -73,10 +77,10 @@ __device__ __forceinline__ void softmax_group(T* out, int64_t g, int64_t n_rows,
     }
 }
 
-template <typename T, int VEC, int CHUNKS, int ROWS>
+template <typename T, int VEC, int CHUNKS, int ROWS, bool OPTS>
 __global__ void __launch_bounds__(kWarpPathThreads)
 warp_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols,
-                 int64_t ld_in, int64_t ld_out)
+                 int64_t ld_in, int64_t ld_out, LogitsArg lg)
 {
     constexpr int E = VEC * CHUNKS;
     const int lane = threadIdx.x & 31;
@@ -92,18 +96,18 @@ warp_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols,
     // and stored, the loads of the next group are already in flight.
     float a[ROWS][E], b[ROWS][E];
     int64_t g = warp0;
-    load_group<T, VEC, CHUNKS, ROWS>(in, g, n_rows, n_cols, ld_in, lane, a);
+    load_group<T, VEC, CHUNKS, ROWS, OPTS>(in, g, n_rows, n_cols, ld_in, lg, lane, a);
     while (true) {
         const int64_t gb = g + n_warps;
         if (gb < n_groups)
-            load_group<T, VEC, CHUNKS, ROWS>(in, gb, n_rows, n_cols, ld_in, lane, b);
-        softmax_group<T, VEC, CHUNKS, ROWS>(out, g, n_rows, n_cols, ld_out, lane, a);
+            load_group<T, VEC, CHUNKS, ROWS, OPTS>(in, gb, n_rows, n_cols, ld_in, lg, lane, b);
+        softmax_group<T, VEC, CHUNKS, ROWS>(out, g, n_rows, n_cols, ld_out, (OPTS ? lg.k : kLog2e), lane, a);
         if (gb >= n_groups)
             break;
         const int64_t ga = gb + n_warps;
         if (ga < n_groups)
-            load_group<T, VEC, CHUNKS, ROWS>(in, ga, n_rows, n_cols, ld_in, lane, a);
-        softmax_group<T, VEC, CHUNKS, ROWS>(out, gb, n_rows, n_cols, ld_out, lane, b);
+            load_group<T, VEC, CHUNKS, ROWS, OPTS>(in, ga, n_rows, n_cols, ld_in, lg, lane, a);
+        softmax_group<T, VEC, CHUNKS, ROWS>(out, gb, n_rows, n_cols, ld_out, (OPTS ? lg.k : kLog2e), lane, b);
         if (ga >= n_groups)
             break;
         g = ga;
@@ -117,11 +121,11 @@ constexpr int rows_for()
     return E >= 16 ? 1 : (16 / E > 8 ? 8 : 16 / E);
 }
 
-template <typename T, int VEC, int CHUNKS>
-static cudaError_t launch_one(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
+template <typename T, int VEC, int CHUNKS, bool OPTS>
+static cudaError_t launch_opts(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
 {
     constexpr int ROWS = rows_for<VEC * CHUNKS>();
-    auto* k = warp_rows_kernel<T, VEC, CHUNKS, ROWS>;
+    auto* k = warp_rows_kernel<T, VEC, CHUNKS, ROWS, OPTS>;
     const int64_t groups = (p.n_rows + ROWS - 1) / ROWS;
     const int warps_per_cta = kWarpPathThreads / 32;
     int64_t want = (groups + warps_per_cta - 1) / warps_per_cta;
@@ -143,9 +147,17 @@ static cudaError_t launch_one(const Problem& p, const softmax_plan_t& plan, cuda
     cfg.numAttrs = static_cast<unsigned>(launch_attrs(attr, 1));
     const cudaError_t err = cudaLaunchKernelEx(&cfg, k, static_cast<const T*>(p.in),
                                                static_cast<T*>(p.out), p.n_rows,
-                                               static_cast<int>(p.n_cols), p.ld_in, p.ld_out);
+                                               static_cast<int>(p.n_cols), p.ld_in, p.ld_out,
+                                               logits_of(p));
     note_launch();
     return err;
+}
+
+template <typename T, int VEC, int CHUNKS>
+static cudaError_t launch_one(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
+{
+    return has_options(p) ? launch_opts<T, VEC, CHUNKS, true>(p, plan, s)
+                    : launch_opts<T, VEC, CHUNKS, false>(p, plan, s);
 }
 
 template <typename T, int VEC>

@@ -22,6 +22,23 @@ int main(void)
     CHECK(softmax_rows(buf, buf + 2, 2, 4, 4, 4, SOFTMAX_F32, NULL) == SOFTMAX_ERR_INVALID_ARG);
     CHECK(softmax_rows(NULL, NULL, 0, 4, 4, 4, SOFTMAX_F32, NULL) == SOFTMAX_OK);
     CHECK(softmax_rows_path(buf, buf + 32, 1, 4, 4, 4, SOFTMAX_F32, NULL, 9) == SOFTMAX_ERR_INVALID_ARG);
+    /* softmax_rows_ex: options are checked before any device call too. */
+    softmax_options_t opt = {0.125f, 1, 0, 0};
+    CHECK(softmax_rows_ex(NULL, NULL, 0, 4, 4, 4, SOFTMAX_F32, &opt, SOFTMAX_PATH_AUTO, NULL) == SOFTMAX_OK);
+    opt.scale = 0.0f;
+    CHECK(softmax_rows_ex(buf, buf + 32, 1, 4, 4, 4, SOFTMAX_F32, &opt, SOFTMAX_PATH_AUTO, NULL) == SOFTMAX_ERR_INVALID_ARG);
+    opt.scale = -1.0f;
+    CHECK(softmax_rows_ex(buf, buf + 32, 1, 4, 4, 4, SOFTMAX_F32, &opt, SOFTMAX_PATH_AUTO, NULL) == SOFTMAX_ERR_INVALID_ARG);
+    opt.scale = 3.0e38f;
+    CHECK(softmax_rows_ex(buf, buf + 32, 1, 4, 4, 4, SOFTMAX_F32, &opt, SOFTMAX_PATH_AUTO, NULL) == SOFTMAX_ERR_INVALID_ARG);
+    opt.scale = 1.0f;
+    opt.causal = 2;
+    CHECK(softmax_rows_ex(buf, buf + 32, 1, 4, 4, 4, SOFTMAX_F32, &opt, SOFTMAX_PATH_AUTO, NULL) == SOFTMAX_ERR_INVALID_ARG);
+    opt.causal = 1;
+    opt.causal_offset = (int64_t)1 << 62;
+    CHECK(softmax_rows_ex(buf, buf + 32, 1, 4, 4, 4, SOFTMAX_F32, &opt, SOFTMAX_PATH_AUTO, NULL) == SOFTMAX_ERR_INVALID_ARG);
+    opt.causal_offset = 0;
+    CHECK(softmax_rows_ex(buf, buf + 32, 1, 4, 4, 4, SOFTMAX_F32, &opt, 7, NULL) == SOFTMAX_ERR_INVALID_ARG);
 
     softmax_device_desc_t gb300 = {152, 2048, 233472, 232448, 65536, 10, 3, 16};
     softmax_plan_t plan;

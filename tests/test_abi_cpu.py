@@ -153,12 +153,54 @@ def test_validation(lib):
     assert f(A, A + 15 * 4, 4, 16, 32, 32, rws.F32) == rws.ERR_INVALID_ARG
 
 
+def test_options_validation(lib):
+    g = lambda **kw: rws.softmax_rows_ex_ptr(1 << 20, 1 << 30, 2, 8, 8, 8, rws.F32, **kw)
+    for bad in (dict(scale=0.0), dict(scale=-0.5), dict(scale=float("nan")),
+                dict(scale=float("inf")), dict(scale=2.0 ** 127 * 1.5),
+                dict(causal=True, causal_offset=1 << 62), dict(causal=True, causal_offset=-(1 << 62)),
+                dict(path=4), dict(path=-2)):
+        assert g(**bad) == rws.ERR_INVALID_ARG, bad
+    # Valid options on an empty matrix: a no-op, no device needed.
+    assert rws.softmax_rows_ex_ptr(0, 0, 0, 8, 8, 8, rws.F32, scale=0.125, causal=True) == rws.OK
+
+
+def test_visible_cols_division_by_invariant_period(lib):
+    """The kernels' row mod period (multiply-high, no division) against Python's
+    integer %, for periods and rows up to 2^62 (periods beyond the row count act
+    as the row count)."""
+    import random
+    rnd = random.Random(5)
+    big = 1 << 62
+    periods = [1, 2, 3, 5, 7, 641, 1024, 2047, 2048, 6700417, (1 << 31) - 1, 1 << 32,
+               (1 << 32) + 1, 10 ** 12 + 39, (1 << 61) + 1, big - 2, big - 1, big, (1 << 63) - 1]
+    periods += [rnd.randrange(1, big) for _ in range(40)]
+    n_cols = (1 << 31) - 1
+    for per in periods:
+        rows = [0, 1, per - 1, per, per + 1, big - 1, 2 * per - 1 if 2 * per <= big else big - 1]
+        rows += [rnd.randrange(0, big) for _ in range(25)]
+        for r in rows:
+            if not 0 <= r < big:
+                continue
+            for off in (0, 3, -7, (1 << 62) - 1, -(1 << 62) + 1):
+                want = min(max(r % per + off + 1, 0), n_cols)
+                got = rws.visible_cols(big, n_cols, r, causal=True, causal_period=per,
+                                       causal_offset=off)
+                assert got == want, (per, r, off)
+    assert rws.visible_cols(10, 8, 3) == 8                                  # no mask
+    assert rws.visible_cols(10, 8, 3, causal=True) == 4                     # period = n_rows
+    assert rws.visible_cols(10, 8, 9, causal=True, causal_period=4) == 2
+    assert rws.visible_cols(10, 8, 10, causal=True) == -1                   # row out of range
+    assert rws.visible_cols(10, 8, 1, scale=0.0) == -1
+
+
 def test_no_gpu_means_loud_failure(lib):
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     # Valid arguments, no device: UNSUPPORTED, never a silent CPU result.
     assert rws.softmax_rows_ptr(1 << 20, 1 << 30, 2, 8, 8, 8, rws.F32) == rws.ERR_UNSUPPORTED
+    assert rws.softmax_rows_ex_ptr(1 << 20, 1 << 30, 2, 8, 8, 8, rws.F32, scale=0.5,
+                                   causal=True) == rws.ERR_UNSUPPORTED
 
 
 def test_c_only_caller(lib, tmp_path):
