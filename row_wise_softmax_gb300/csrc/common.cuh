@@ -13,6 +13,9 @@ constexpr float kNegInf = -__builtin_inff();
 constexpr float kLog2e = 1.4426950408889634f;
 // Give up a bounded wait after this long (nanoseconds of %globaltimer).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// Longest suspension a bounded wait asks for in one try (the waiting thread
+// resumes as soon as the phase completes).
+constexpr uint32_t kWaitSuspendNs = 100000u;
 
 // Error word written by a kernel that gave up a bounded wait.  Each kernel
 // translation unit holds its own copy; the host reads and clears them all.
@@ -59,12 +62,88 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
+// Warp-wide maximum in one instruction (redux.sync on fp32, sm_100 family);
+// like fmaxf, a NaN operand is ignored unless every lane holds NaN.  Faster
+// than the shuffle tree in the kernels where a warp reduces whole rows on its
+// own (measured); the CTA kernels keep the tree.
+__device__ __forceinline__ float warp_max_redux(float v)
+{
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// ---- paired fp32 arithmetic (sm_100 family): one instruction computes two
+// fp32 results, each rounded exactly as the scalar instruction would.
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1)
+{
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1)
+{
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1)
+{
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// max(a, b, c) in one instruction; NaN operands are ignored as by fmaxf.
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Maximum of n floats (three-input max tree).
+template <int N>
+__device__ __forceinline__ float frag_max(const float* x, float m)
+{
+    int i = 0;
+#pragma unroll
+    for (; i + 1 < N; i += 2)
+        m = max3(m, x[i], x[i + 1]);
+    if constexpr (N % 2 == 1)
+        m = fmaxf(m, x[N - 1]);
+    return m;
+}
+
+// x[i] = exp_biased(x[i] - m, k) for n (even) elements, two per instruction,
+// summed into s0 (even positions) and s1 (odd positions).
+template <int N>
+__device__ __forceinline__ void frag_exp_acc(float* x, float m, float k, float& s0, float& s1)
+{
+    static_assert(N % 2 == 0, "pairs");
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+        float d0, d1;
+        add2(d0, d1, x[i], x[i + 1], -m, -m);
+        fma2(d0, d1, d0, d1, k, k, kExpBias, kExpBias);
+        x[i] = ex2_ftz(d0);
+        x[i + 1] = ex2_ftz(d1);
+        add2(s0, s1, s0, s1, x[i], x[i + 1]);
+    }
 }
 
 // Merge two online-softmax partials (m, l) and (m2, l2), where l is a sum of
@@ -195,6 +274,18 @@ __device__ __forceinline__ void store_vec(T* p, const float* v, float scale)
             *reinterpret_cast<unsigned*>(p) = pack_bf16x2(v[0] * scale, v[1] * scale);
         }
     }
+}
+
+// store_vec with the scaling done two elements per instruction (VEC even).
+template <typename T, int VEC>
+__device__ __forceinline__ void store_vec2(T* p, const float* v, float scale)
+{
+    static_assert(VEC % 2 == 0, "pairs");
+    float y[VEC];
+#pragma unroll
+    for (int j = 0; j < VEC; j += 2)
+        mul2(y[j], y[j + 1], v[j], v[j + 1], scale, scale);
+    store_vec<T, VEC>(p, y, 1.0f);
 }
 
 // Masked forms: positions at or past `limit` read -inf and are not written.
@@ -339,6 +430,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  :: "r"(bar), "r"(bytes) : "memory");
 }
 
+// Raise the transaction count the current phase waits for, without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
@@ -395,17 +492,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended for up to `hint_ns`
+// nanoseconds while the phase is incomplete (it resumes as soon as the phase
+// completes), so a waiting warp issues few instructions.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
+    return ok != 0;
+}
+
 // Wait for the mbarrier phase with the given parity to complete, for at most
-// kWaitLimitNs.  Returns false when the limit ran out.
+// kWaitLimitNs (checked every iteration; each iteration suspends at most
+// kWaitSuspendNs).  Returns false when the limit ran out.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const unsigned long long t0 = global_ns();
     for (uint32_t it = 1; it < (1u << 30); ++it) {
-        if (mbar_try_wait(bar, parity))
+        if (mbar_try_wait_suspend(bar, parity, kWaitSuspendNs))
             return true;
-        if ((it & 31u) == 0 && global_ns() - t0 > kWaitLimitNs)
+        if (global_ns() - t0 > kWaitLimitNs)
             return false;
     }
     return false;

@@ -89,6 +89,19 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
         const int nr = static_cast<int>(n_rows - r0 < R ? n_rows - r0 : R);
         fence_proxy_async_smem();
         issued[s] += 1;
+        if constexpr (OPTS) {
+            // One pass: each copy raises the phase's byte count before it
+            // starts; the single arrival comes after the last copy.
+            for (int r = 0; r < nr; ++r) {
+                const uint32_t n = copy_bytes(r0 + r, logits_valid(lg, r0 + r, n_cols));
+                if (n) {
+                    mbar_expect_tx(bar, n);
+                    bulk_g2s(smem_addr(row_ptr(s, r)), in + (r0 + r) * ld_in, n, bar);
+                }
+            }
+            mbar_arrive(bar);
+            return;
+        }
         uint32_t total = 0;
         for (int r = 0; r < nr; ++r)
             total += copy_bytes(r0 + r, kept_cols<OPTS>(lg, r0 + r, n_cols));
@@ -140,44 +153,92 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
             const int lim = static_cast<int>(kept_cols<OPTS>(lg, row, n_cols));
             const int copied = static_cast<int>(copy_bytes(row, lim) / sizeof(T));
             const int avail = copied < lim ? copied : lim;
+            // Whole vectors first: a vector that starts below `avail` is read
+            // from shared memory (inside the row's ring slot), any other is
+            // -inf.  Only a row whose edges do not fall on vector boundaries
+            // needs the per-element fix-up of its edge vectors.
             float x[E];
 #pragma unroll
             for (int c = 0; c < CHUNKS; ++c) {
                 const int col = (c * 32 + lane) * VEC;
-                if (col + VEC <= avail) {
+                if (col < avail) {
                     lds_any<T, VEC>(sp + col, &x[c * VEC]);
-                } else if (OPTS && col >= lim) {
+                } else {
 #pragma unroll
                     for (int j = 0; j < VEC; ++j)
                         x[c * VEC + j] = kNegInf;
-                } else {
+                }
+            }
+            if (OPTS && avail == lim && lim % VEC != 0) {              // warp-uniform
+                // Only the vector holding column lim - 1 straddles the edge:
+                // its copied elements past lim are masked.
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j) {
-                        const int e = col + j;
-                        if (e < avail)
-                            lds_any<T, 1>(sp + e, &x[c * VEC + j]);
-                        else
-                            x[c * VEC + j] = e < lim ? Elem<T>::load1(gp + e) : kNegInf;
+                for (int c = 0; c < CHUNKS; ++c) {
+                    const int keep_n = lim - (c * 32 + lane) * VEC;
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j)
+                        x[c * VEC + j] = j < keep_n ? x[c * VEC + j] : kNegInf;
+                }
+            } else if ((avail | lim) % VEC != 0 || avail < lim) {   // warp-uniform
+#pragma unroll
+                for (int c = 0; c < CHUNKS; ++c) {
+                    const int col = (c * 32 + lane) * VEC;
+                    if (col + VEC > avail && col < lim) {
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) {
+                            const int e = col + j;
+                            if (e >= avail)
+                                x[c * VEC + j] = e < lim ? Elem<T>::load1(gp + e) : kNegInf;
+                        }
                     }
                 }
             }
             float m = kNegInf;
+            if constexpr (OPTS) {
+                m = frag_max<E>(x, kNegInf);
+            } else {
 #pragma unroll
-            for (int e = 0; e < E; ++e)
-                m = fmaxf(m, x[e]);
-            m = warp_max(m);
-            float l = 0.0f;
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-                x[e] = exp_biased(x[e] - m, kk);
-                l += x[e];
+                for (int e = 0; e < E; ++e)
+                    m = fmaxf(m, x[e]);
             }
-            l = warp_sum(l);
-            const float inv = 1.0f / l;
-            T* dst = out + row * ld_out;
+            m = warp_max_redux(m);
+            // exp_biased and the sum.  With options: two elements per
+            // instruction, and chunks wholly past `lim` are 0 without
+            // computing.  (The plain rows measured faster with scalar math.)
+            float s0 = 0.0f, s1 = 0.0f;
+            if constexpr (OPTS && E % 2 == 0) {
 #pragma unroll
-            for (int c = 0; c < CHUNKS; ++c)
-                store_vec_masked<T, VEC>(dst, (c * 32 + lane) * VEC, n_cols, &x[c * VEC], inv);
+                for (int i = 0; i < E; i += 2) {
+                    if (!OPTS || ((i / VEC) * 32 * VEC < lim))          // warp-uniform
+                        frag_exp_acc<2>(&x[i], m, kk, s0, s1);
+                    else
+                        x[i] = x[i + 1] = 0.0f;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    x[e] = exp_biased(x[e] - m, kk);
+                    s0 += x[e];
+                }
+            }
+            const float inv = 1.0f / warp_sum(s0 + s1);
+            T* dst = out + row * ld_out;
+            if (OPTS && n_cols % VEC == 0) {                        // kernel-uniform
+#pragma unroll
+                for (int c = 0; c < CHUNKS; ++c) {
+                    const int col = (c * 32 + lane) * VEC;
+                    if (col < n_cols) {
+                        if constexpr (VEC % 2 == 0)
+                            store_vec2<T, VEC>(dst + col, &x[c * VEC], inv);
+                        else
+                            store_vec<T, VEC>(dst + col, &x[c * VEC], inv);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < CHUNKS; ++c)
+                    store_vec_masked<T, VEC>(dst, (c * 32 + lane) * VEC, n_cols, &x[c * VEC], inv);
+            }
         }
         if (__syncthreads_or(!ok))
             failed = true;

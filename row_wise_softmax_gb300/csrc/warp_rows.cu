@@ -59,7 +59,7 @@ __device__ __forceinline__ void softmax_group(T* out, int64_t g, int64_t n_rows,
 #pragma unroll
         for (int e = 0; e < E; ++e)
             m = fmaxf(m, v[r][e]);
-        m = warp_max(m);
+        m = warp_max_redux(m);
         float l = 0.0f;
 #pragma unroll
         for (int e = 0; e < E; ++e) {

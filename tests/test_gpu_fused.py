@@ -5,7 +5,8 @@ scaled before the softmax) and section 3.3 (a key index past the query index
 is -inf): column c of row r takes part iff c <= (r mod period) + offset, and
 the masked inputs are never read.  Every path is forced in turn on shapes with
 ragged tails; the full-size causal workload checks that the mask computed from
-indices gives bit for bit what the mask written into the input gives.
+indices gives what the mask written into the input gives (the same zeros, the
+other outputs within one bf16 ulp: the options kernels sum in pairs).
 """
 import numpy as np
 import pytest
@@ -124,7 +125,11 @@ def test_full_size_causal_mask_from_indices_matches_written_mask():
     fused = run_ex(w, x=xn, **opt)
     assert rws.launch_count() - before == 1
     torch.cuda.synchronize()
-    assert np.array_equal(parity.host_output(written, w), fused)
+    plain = parity.host_output(written, w)
+    zero = ~visible(w.n_rows, w.n_cols, **opt)
+    assert np.all(fused[zero] == 0) and np.all(plain[zero] == 0)
+    d = np.abs(parity.bf16_ordered(fused) - parity.bf16_ordered(plain))
+    assert d.max() <= 1, d.max()
     rows = np.random.default_rng(7).choice(w.n_rows, 64, replace=False)
     parity.compare(fused[rows], parity.expected(w, rows), w.dtype, "causal_bf16 fused (rows)")
 
