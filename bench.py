@@ -44,16 +44,31 @@ METRIC = "softmax GB/s and % of GB300 HBM roofline (fp32/bf16) per row-length co
 UNIT = "GB/s"
 L2_FACTOR = 3            # rotating buffer sets cover at least 3x the L2 size
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-# Sources of each path's kernel, hashed to tell whether committed ncu counters
+# The kernel a plan launches (path, and whether it stages rows with bulk
+# copies) and its sources, hashed to tell whether committed ncu counters
 # still describe the kernel being timed.
-KERNEL_SOURCES = {
-    "warp": ["warp_rows.cu", "common.cuh"],
-    "cta": ["row_slices.cu", "common.cuh"],
-    "cluster": ["row_slices.cu", "common.cuh"],
-    "twopass": ["twopass.cu", "common.cuh"],
+KERNELS = {
+    ("warp", 0): ("warp_rows_kernel", ["warp_rows.cu"]),
+    ("warp", 1): ("tile_rows_kernel", ["tile_rows.cu"]),
+    ("cta", 0): ("row_slices_kernel", ["row_slices.cu"]),
+    ("cta", 1): ("row_slices_kernel", ["row_slices.cu"]),
+    ("cluster", 0): ("row_slices_kernel", ["row_slices.cu"]),
+    ("cluster", 1): ("row_slices_kernel", ["row_slices.cu"]),
+    ("twopass", 0): ("twopass_kernel", ["twopass.cu"]),
+    ("twopass", 1): ("stream_rows_kernel", ["stream_rows.cu"]),
 }
-KERNEL_NAMES = {"warp": "warp_rows_kernel", "cta": "row_slices_kernel",
-                "cluster": "row_slices_kernel", "twopass": "twopass_kernel"}
+COMMON_SOURCES = ["common.cuh", "kernels.h"]
+WORKLOAD_DATA = {
+    "small_f32": "synthetic (seeded: N(0,1))",
+    "masked_f32": "synthetic (seeded: N(0,3^2), 41 -inf columns per row, one constant row)",
+    "causal_bf16": "synthetic (seeded: bf16(N(0,1)*8), causal: row r keeps columns <= r mod 1024)",
+    "short_f32": "synthetic (seeded: U[-80,80], input stride 128 with a NaN padding column)",
+    "long_f32": "synthetic (seeded: N(0,1), one +50 spike per row)",
+}
+
+
+def kernel_of(plan):
+    return KERNELS[(plan.path_name, 1 if plan.bulk_copy else 0)]
 
 
 def dist_env():
@@ -81,25 +96,25 @@ def max_over_ranks(value: float, world: int, device: str = "cpu") -> float:
     return float(t.item())
 
 
-def source_hash(path_name: str) -> str:
+def source_hash(plan) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES[path_name]:
+    for f in kernel_of(plan)[1] + COMMON_SOURCES:
         with open(os.path.join(ROOT, "row_wise_softmax_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def committed_traffic(path_name: str, workload: str):
+def committed_traffic(plan, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if still valid."""
-    fn = os.path.join(PROFILE_DIR, "%s.%s.json" % (KERNEL_NAMES[path_name], workload))
+    fn = os.path.join(PROFILE_DIR, "%s.%s.json" % (kernel_of(plan)[0], workload))
     try:
         with open(fn) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None, "no committed ncu summary"
-    if rec.get("source_sha") != source_hash(path_name):
+    if rec.get("source_sha") != source_hash(plan):
         return None, "kernel changed since the ncu capture"
-    return rec.get("dram_bytes_per_launch"), fn
+    return rec.get("dram_bytes_per_launch"), os.path.relpath(fn, ROOT)
 
 
 def measured_peak():
@@ -239,22 +254,33 @@ def copy_calibration(w: wl.Workload, sets, torch, stream, peak):
     return {"GB/s": round(gbs, 1), "mean_ms": round(ms, 5), "frac_of_peak": round(gbs / peak, 4)}
 
 
+FUSED_SCALE = 0.125          # 1/sqrt(64), a head dimension of 64
+
+
+def fused_causal_setup(w: wl.Workload, rws):
+    """Options of the causal workload with its mask computed from indices
+    (query r mod n_cols sees keys 0..r mod n_cols) and a 1/sqrt(64) scale,
+    and its algorithmic bytes: the masked inputs are never read, so the
+    kept inputs plus every output."""
+    period = w.n_cols
+    opt = rws.Options(FUSED_SCALE, 1, period, 0)
+    kept = sum(min(r % period + 1, w.n_cols) for r in range(w.n_rows))
+    return opt, (kept + w.n_rows * w.n_cols) * w.elem_bytes
+
+
 def fused_causal_entry(torch, rws, stream, l2_bytes, peak):
-    """The causal bf16 workload with its mask computed from indices and a
-    1/sqrt(64) scale (softmax_rows_ex): the masked inputs are never read, so
-    the algorithmic bytes are the kept inputs plus every output."""
+    """softmax_rows_ex on the causal bf16 workload with the mask from indices."""
     w = wl.make("causal_bf16")
     period = w.n_cols
-    opt = rws.Options(0.125, 1, period, 0)
-    kept = sum(min(r % period + 1, w.n_cols) for r in range(w.n_rows))
-    algo = (kept + w.n_rows * w.n_cols) * w.elem_bytes
+    opt, algo = fused_causal_setup(w, rws)
     bc = device_buffers(w, torch, l2_bytes)
     tot, launches = time_device(w, bc, 50, 5, torch, rws, stream, options=opt)
     del bc
     med = tot / 50
     gbs = algo / (med * 1e-3) / 1e9
     return {"shape": [w.n_rows, w.n_cols], "dtype": "bf16",
-            "options": {"scale": 0.125, "causal": 1, "causal_period": period, "causal_offset": 0},
+            "options": {"scale": FUSED_SCALE, "causal": 1, "causal_period": period,
+                        "causal_offset": 0},
             "algorithmic_bytes": algo, "mean_ms": round(med, 5), "GB/s": round(gbs, 1),
             "frac_of_measured_peak": round(gbs / peak, 4), "launches": launches,
             "rows_per_s": round(w.n_rows / (med * 1e-3), 1)}
@@ -326,6 +352,11 @@ def run_ours(args):
     w = wl.make(args.workload)
     plan = rws.plan(w.n_rows, w.n_cols, in_row_stride=w.in_row_stride,
                     out_row_stride=w.out_row_stride, dtype=w.dtype)
+    options, bytes_step = None, w.algorithmic_bytes
+    workload_key = args.workload
+    if args.mask_from_indices:
+        options, bytes_step = fused_causal_setup(w, rws)
+        workload_key = "causal_bf16_mask_from_indices"
 
     def barrier():
         if world > 1:
@@ -337,32 +368,34 @@ def run_ours(args):
     barrier()
     with ClockSampler(local) as clk:
         t_wall0 = time.perf_counter()
-        total_ms, launches = time_device(w, bufs, args.steps, args.warmup, torch, rws, stream)
+        total_ms, launches = time_device(w, bufs, args.steps, args.warmup, torch, rws, stream,
+                                         options)
         wall = time.perf_counter() - t_wall0
         # Keep the sampled window at least ~1.5 s: repeat the same step (not
         # counted) if the timed steps were shorter than that.
         extra = 0
         while (not args.no_clock_window and time.perf_counter() - t_wall0 < 1.5
                and extra < 400000):
-            time_device(w, bufs, 2000, 0, torch, rws, stream)
+            time_device(w, bufs, 2000, 0, torch, rws, stream, options)
             extra += 2000
     barrier()
     total_ms = max_over_ranks(total_ms, world, "cuda")
     ms_per_step = total_ms / args.steps
-    bytes_step = w.algorithmic_bytes
     value = world * bytes_step * args.steps / (total_ms * 1e-3) / 1e9
     # One softmax kernel per step: average launch duration = timed region / launches.
     achieved = bytes_step * launches / (total_ms * 1e-3) / 1e9
-    traffic, traffic_src = committed_traffic(plan.path_name, args.workload)
+    traffic, traffic_src = committed_traffic(plan, workload_key)
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded: N(0,3^2), 41 -inf columns per row, one constant row)",
-        "config": {"workload": "%s: %d x %d %s, row strides %d/%d" % (
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32",        # the arithmetic type (bf16 workloads compute in fp32 too)
+        "data": WORKLOAD_DATA[args.workload],
+        "config": {"workload": "%s: %d x %d %s, row strides %d/%d%s" % (
                        args.workload, w.n_rows, w.n_cols, "fp32" if w.dtype == wl.F32 else "bf16",
-                       w.in_row_stride, w.out_row_stride),
+                       w.in_row_stride, w.out_row_stride,
+                       ", mask from indices, scale %g" % FUSED_SCALE if options else ""),
                    "n_rows": w.n_rows, "n_cols": w.n_cols, "bytes_per_step": bytes_step,
                    "l2": "inputs larger than L2: %d rotating input/output sets (%.0f MB, "
                          ">= %dx the %.0f MB L2), steps back to back" % (
@@ -372,7 +405,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": peak_kind, "traffic": traffic,
-                     "kernel": KERNEL_NAMES[plan.path_name],
+                     "kernel": kernel_of(plan)[0],
                      "traffic_source": traffic_src if traffic else traffic_src},
         "gpu_launches": launches,
         "clocks": clk.summary(),
@@ -475,7 +508,15 @@ def main():
                     help="do not extend the clock-sampling window past the timed steps")
     ap.add_argument("--workload", default=HEADLINE, choices=list(wl.NAMES),
                     help="workload timed as the step (default: the headline)")
+    ap.add_argument("--mask-from-indices", action="store_true",
+                    help="with --workload causal_bf16: time softmax_rows_ex with the causal "
+                         "mask computed from indices and a 1/sqrt(64) scale (no end-to-end "
+                         "or CPU legs)")
     args = ap.parse_args()
+    if args.mask_from_indices:
+        if args.workload != "causal_bf16":
+            ap.error("--mask-from-indices applies to --workload causal_bf16")
+        args.no_e2e = args.no_cpu = True
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
