@@ -28,6 +28,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
 F32 = 0
 BF16 = 1
+F16 = 2
 
 # -ffp-contract=off: no fused multiply-add contraction, so x86 and Arm hosts
 # produce the same doubles.  No fast-math: rint() must round ties to even.
@@ -62,6 +63,12 @@ class Oracle:
         lib.oracle_bf16_to_double.restype = dbl
         lib.oracle_double_to_bf16_array.argtypes = [vp, vp, i64]
         lib.oracle_bf16_to_double_array.argtypes = [vp, vp, i64]
+        lib.oracle_double_to_f16.argtypes = [dbl]
+        lib.oracle_double_to_f16.restype = ctypes.c_uint16
+        lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_f16_to_double.restype = dbl
+        lib.oracle_double_to_f16_array.argtypes = [vp, vp, i64]
+        lib.oracle_f16_to_double_array.argtypes = [vp, vp, i64]
         lib.oracle_tiled_row_sum.argtypes = [vp, i64, i64, i64, vp]
         lib.oracle_tiled_row_sum.restype = dbl
         self._lib = lib
@@ -72,8 +79,8 @@ class Oracle:
                      causal_period: int = 0, causal_offset: int = 0) -> np.ndarray:
         """Softmax of each row of a strided row matrix, in double.
 
-        ``buf`` is the flat input buffer: float32 values (dtype F32) or bf16
-        bit patterns as uint16 (dtype BF16).  Row r starts at element
+        ``buf`` is the flat input buffer: float32 values (dtype F32), or bf16
+        (dtype BF16) or fp16 (dtype F16) bit patterns as uint16.  Row r starts at element
         ``r * in_row_stride``.  Returns a dense float64 array [n_rows, n_cols].
         ``tile > 0`` uses the online (m, l) recurrence with that tile width.
         ``scale`` multiplies the inputs (exactly, in double) before the
@@ -106,6 +113,19 @@ class Oracle:
         v = np.ascontiguousarray(values, dtype=np.float64)
         out = np.empty(v.shape, dtype=np.uint16)
         self._lib.oracle_double_to_bf16_array(v.ctypes.data, out.ctypes.data, v.size)
+        return out
+
+    def to_f16(self, values: np.ndarray) -> np.ndarray:
+        """Round doubles to fp16 (ties to even); returns uint16 bit patterns."""
+        v = np.ascontiguousarray(values, dtype=np.float64)
+        out = np.empty(v.shape, dtype=np.uint16)
+        self._lib.oracle_double_to_f16_array(v.ctypes.data, out.ctypes.data, v.size)
+        return out
+
+    def f16_to_double(self, bits: np.ndarray) -> np.ndarray:
+        b = np.ascontiguousarray(bits, dtype=np.uint16)
+        out = np.empty(b.shape, dtype=np.float64)
+        self._lib.oracle_f16_to_double_array(b.ctypes.data, out.ctypes.data, b.size)
         return out
 
     def bf16_to_double(self, bits: np.ndarray) -> np.ndarray:
@@ -144,3 +164,11 @@ def to_bf16(values: np.ndarray) -> np.ndarray:
 
 def bf16_to_double(bits: np.ndarray) -> np.ndarray:
     return load().bf16_to_double(bits)
+
+
+def to_f16(values: np.ndarray) -> np.ndarray:
+    return load().to_f16(values)
+
+
+def f16_to_double(bits: np.ndarray) -> np.ndarray:
+    return load().f16_to_double(bits)

@@ -33,8 +33,10 @@
  *    with no column taking part is the formula over only -inf: all NaN.
  *  - the tiled row sum with one accumulator per lane: lec06 section
  *    "Level 2: Row Sum (tiling)", worked example of 12 elements, BLOCK 4.
- *  - bf16 decoding (exact) and rounding of a double to bf16 with
- *    round-to-nearest-even, for the bf16 comparison.
+ *  - bf16 and fp16 decoding (exact) and rounding of a double to bf16 or
+ *    fp16 with round-to-nearest-even, for the 16-bit comparisons (fp16 I/O
+ *    with fp32 arithmetic: the pages' tuning checklist keeps accumulators in
+ *    fp32 for float16/bfloat16 inputs).
  *
  * Pins: each function here is checked by tests/test_oracle_pins.py against
  * closed forms, invariants, high-precision brute force (mpmath), a library
@@ -45,6 +47,69 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+
+/* ---- fp16 (IEEE 754 binary16) <-> double ------------------------------ */
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 stored mantissa bits.
+ * Exponent field 0: subnormal, m * 2^-24; field 31: infinity (m = 0) or NaN. */
+double oracle_f16_to_double(uint16_t bits)
+{
+    const int neg = (bits >> 15) & 1;
+    const int e = (bits >> 10) & 0x1F;
+    const int m = bits & 0x3FF;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);
+    return neg ? -v : v;
+}
+
+/*
+ * Round a double to the nearest binary16, ties to even, directly from the
+ * double.  As for bf16 below: the spacing q of binary16 values around |v| is
+ * 2^(e-10) for 2^e <= |v| < 2^(e+1), and 2^-24 below 2^-14; rint(|v|/q) * q
+ * is the rounded value (a carry to the next power of two is still exact).
+ * Values from (2 - 2^-11) * 2^15 = 65520 up round to infinity.
+ */
+uint16_t oracle_double_to_f16(double v)
+{
+    if (isnan(v))
+        return (uint16_t)(signbit(v) ? 0xFE00u : 0x7E00u);
+    const uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    const double a = fabs(v);
+    if (a >= 65520.0)
+        return (uint16_t)(sign | 0x7C00u);
+    if (a == 0.0)
+        return sign;
+    int e;
+    frexp(a, &e);                   /* 2^(e-1) <= a < 2^e */
+    int q_exp = (e - 1) - 10;
+    if (q_exp < -24)
+        q_exp = -24;                /* subnormal spacing */
+    const double r = ldexp(rint(ldexp(a, -q_exp)), q_exp);
+    if (r < ldexp(1.0, -14))        /* subnormal (or zero): field 0 */
+        return (uint16_t)(sign | (uint16_t)ldexp(r, 24));
+    int e2;
+    frexp(r, &e2);                  /* 2^(e2-1) <= r < 2^e2 */
+    const int biased = (e2 - 1) + 15;
+    const int mant = (int)(ldexp(r, -(e2 - 1 - 10)) - 1024.0);
+    return (uint16_t)(sign | (uint16_t)(biased << 10) | (uint16_t)mant);
+}
+
+void oracle_double_to_f16_array(const double* v, uint16_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_double_to_f16(v[i]);
+}
+
+void oracle_f16_to_double_array(const uint16_t* b, double* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_f16_to_double(b[i]);
+}
 
 /* ---- bf16 <-> double ------------------------------------------------- */
 
@@ -188,7 +253,8 @@ static int64_t visible_cols(int64_t r, int64_t n_cols, int causal, int64_t perio
 }
 
 /*
- * dtype 0: `in` is binary32; dtype 1: `in` is bf16 bit patterns (uint16).
+ * dtype 0: `in` is binary32; dtype 1: `in` is bf16 bit patterns (uint16);
+ * dtype 2: `in` is binary16 bit patterns (uint16).
  * Row r of the input starts at element r * in_row_stride; row r of the
  * output (double) at element r * out_row_stride.  Only columns [0, n_cols)
  * are written, and only the columns taking part are read.  The softmax is
@@ -203,7 +269,7 @@ int oracle_softmax_rows_ex(const void* in, double* out, int64_t n_rows, int64_t 
                            int64_t tile, double scale, int causal, int64_t period,
                            int64_t offset)
 {
-    if (n_rows < 0 || n_cols < 0 || (dtype != 0 && dtype != 1) || !(scale > 0.0))
+    if (n_rows < 0 || n_cols < 0 || dtype < 0 || dtype > 2 || !(scale > 0.0))
         return -1;
     if (n_rows == 0 || n_cols == 0)
         return 0;
@@ -220,10 +286,14 @@ int oracle_softmax_rows_ex(const void* in, double* out, int64_t n_rows, int64_t 
             const float* src = (const float*)in + r * in_row_stride;
             for (int64_t j = 0; j < vis; ++j)
                 x[j] = scale * (double)src[j];
-        } else {
+        } else if (dtype == 1) {
             const uint16_t* src = (const uint16_t*)in + r * in_row_stride;
             for (int64_t j = 0; j < vis; ++j)
                 x[j] = scale * oracle_bf16_to_double(src[j]);
+        } else {
+            const uint16_t* src = (const uint16_t*)in + r * in_row_stride;
+            for (int64_t j = 0; j < vis; ++j)
+                x[j] = scale * oracle_f16_to_double(src[j]);
         }
         for (int64_t j = vis; j < n_cols; ++j)
             x[j] = -INFINITY;

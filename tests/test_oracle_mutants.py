@@ -44,6 +44,13 @@ MUTANTS = {
     "scale_dropped_bf16": ("x[j] = scale * oracle_bf16_to_double(src[j]);",
                            "x[j] = oracle_bf16_to_double(src[j]);"),
     "scale_divides": ("x[j] = scale * (double)src[j];", "x[j] = (double)src[j] / scale;"),
+    "f16_decode_bias": ("v = ldexp((double)(1024 + m), e - 25);", "v = ldexp((double)(1024 + m), e - 24);"),
+    "f16_round_ties_away": ("const double r = ldexp(rint(ldexp(a, -q_exp)), q_exp);",
+                            "const double r = ldexp(round(ldexp(a, -q_exp)), q_exp);"),
+    "f16_overflow_early": ("if (a >= 65520.0)", "if (a > 65504.0)"),
+    "f16_subnormal_spacing": ("if (q_exp < -24)\n        q_exp = -24;", "if (q_exp < -25)\n        q_exp = -25;"),
+    "f16_input_decoded_as_bf16": ("x[j] = scale * oracle_f16_to_double(src[j]);",
+                                  "x[j] = scale * oracle_bf16_to_double(src[j]);"),
     "tiled_sum_ragged_lane": ("if (t0 + i < n)         /* masked lanes load 0 */",
                               "if (t0 + i <= n)"),
 }

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import oracle
-from oracle import BF16, F32
+from oracle import BF16, F16, F32
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -92,6 +92,81 @@ def test_bf16_round_bruteforce(oracle_lib):
     want = np.array([_nearest_even_bf16(float(v)) for v in vals], dtype=np.uint16)
     assert np.array_equal(got, want), vals[got != want][:5]
     assert oracle_lib.to_bf16(np.array([np.nan]))[0] & 0x7FFF == 0x7FC0
+
+
+# ---------------------------------------------------------------- fp16 codec
+
+def test_f16_decode_exhaustive(oracle_lib):
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    got = oracle_lib.f16_to_double(bits)
+    ref = bits.view(np.float16).astype(np.float64)          # numpy's binary16
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+    assert got[0x0001] == 2.0 ** -24 and got[0x0400] == 2.0 ** -14 and got[0x7BFF] == 65504.0
+
+
+_F16_TABLE = None
+
+
+def _nearest_even_f16(v: float) -> int:
+    """Brute-force RNE among all binary16 values, with exact fractions."""
+    global _F16_TABLE
+    if _F16_TABLE is None:      # every finite non-negative pattern, from its definition
+        _F16_TABLE = [Fraction(m, 1 << 24) if (b >> 10) == 0 else
+                      Fraction(1024 + m) * Fraction(2) ** ((b >> 10) - 25)
+                      for b in range(0x7C00) for m in [b & 0x3FF]]
+    vals = _F16_TABLE
+    if math.isnan(v):
+        return 0x7E00 | (0x8000 if math.copysign(1.0, v) < 0 else 0)
+    sign = 0x8000 if math.copysign(1.0, v) < 0 else 0
+    if not math.isfinite(v) or abs(v) >= 65520.0:
+        return sign | 0x7C00
+    a = Fraction(abs(v))
+    if a >= vals[-1]:
+        return sign | (len(vals) - 1)
+    lo, hi = 0, len(vals) - 1
+    while hi - lo > 1:                      # vals[lo] <= a < vals[hi]
+        mid = (lo + hi) // 2
+        if vals[mid] <= a:
+            lo = mid
+        else:
+            hi = mid
+    dlo, dhi = a - vals[lo], vals[hi] - a
+    pick = lo if dlo < dhi else hi if dhi < dlo else (lo if lo % 2 == 0 else hi)
+    return sign | pick
+
+
+def test_f16_round_bruteforce(oracle_lib):
+    rng = np.random.default_rng(12)
+    vals = list(rng.standard_normal(60) * np.exp2(rng.integers(-26, 16, 60)))
+    for p in list(rng.integers(0, 0x7BFE, 40)) + [0, 1, 0x3FF, 0x400, 0x7BFE]:
+        a = float(np.uint16(p).view(np.float16))
+        b = float(np.uint16(p + 1).view(np.float16))
+        mid = (a + b) / 2.0                 # exact in double
+        vals += [mid, np.nextafter(mid, 0.0), np.nextafter(mid, np.inf), -mid]
+    vals += [0.0, -0.0, np.inf, -np.inf, 65504.0, 65519.99, 65520.0, 2.0 ** -25,
+             3 * 2.0 ** -25, 2.0 ** -26, 1.0, 1.0 / 3.0, 1e-300]
+    vals = np.array(vals, dtype=np.float64)
+    got = oracle_lib.to_f16(vals)
+    want = np.array([_nearest_even_f16(float(v)) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got, want), vals[got != want][:5]
+    # And numpy's own double -> binary16 conversion on a wide random sample.
+    x = rng.standard_normal(20000) * np.exp2(rng.uniform(-28, 16.5, 20000))
+    with np.errstate(over="ignore"):
+        assert np.array_equal(oracle_lib.to_f16(x), x.astype(np.float16).view(np.uint16))
+
+
+def test_f16_input_matches_torch_double(oracle_lib):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(24)
+    xf = (rng.standard_normal((21, 515)) * 6).astype(np.float16)
+    xf[3, 7] = -np.inf
+    bits = xf.view(np.uint16).reshape(-1)
+    y = oracle_lib.softmax_rows(bits, 21, 515, dtype=F16)
+    ref = torch.softmax(torch.from_numpy(xf.astype(np.float64)), dim=-1).numpy()
+    assert np.all(np.abs(y - ref) <= 1e-14 * ref + 1e-300)
 
 
 # --------------------------------------------------- closed forms and invariants
