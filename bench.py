@@ -58,12 +58,14 @@ KERNELS = {
     ("twopass", 1): ("stream_rows_kernel", ["stream_rows.cu"]),
 }
 COMMON_SOURCES = ["common.cuh", "kernels.h"]
+DTYPE_NAMES = {wl.F32: "f32", wl.BF16: "bf16", wl.F16: "f16"}
 WORKLOAD_DATA = {
     "small_f32": "synthetic (seeded: N(0,1))",
     "masked_f32": "synthetic (seeded: N(0,3^2), 41 -inf columns per row, one constant row)",
     "causal_bf16": "synthetic (seeded: bf16(N(0,1)*8), causal: row r keeps columns <= r mod 1024)",
     "short_f32": "synthetic (seeded: U[-80,80], input stride 128 with a NaN padding column)",
     "long_f32": "synthetic (seeded: N(0,1), one +50 spike per row)",
+    "causal_f16": "synthetic (seeded: fp16(N(0,1)*8), causal: row r keeps columns <= r mod 1024)",
 }
 
 
@@ -182,16 +184,20 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- GPU arm
 
+def torch_dtype(dtype: int, torch):
+    return {wl.F32: torch.float32, wl.BF16: torch.bfloat16, wl.F16: torch.float16}[dtype]
+
+
 def to_device(w: wl.Workload, torch):
     if w.dtype == wl.F32:
         return torch.from_numpy(w.data).cuda()
-    return torch.from_numpy(w.data.view(np.int16)).cuda().view(torch.bfloat16)
+    return torch.from_numpy(w.data.view(np.int16)).cuda().view(torch_dtype(w.dtype, torch))
 
 
 def device_buffers(w: wl.Workload, torch, l2_bytes: int):
     """Input/output buffer sets, enough that their total exceeds L2_FACTOR x L2."""
     x = to_device(w, torch)
-    dt = torch.float32 if w.dtype == wl.F32 else torch.bfloat16
+    dt = torch_dtype(w.dtype, torch)
     set_bytes = (x.numel() + max(w.out_elems, 1)) * x.element_size()
     n_sets = max(1, -(-L2_FACTOR * l2_bytes // set_bytes))
     sets = []
@@ -292,11 +298,11 @@ def time_e2e(w: wl.Workload, steps: int, warmup: int, torch, rws, stream, staged
     direct (staged=False): the kernel reads the pinned host input and writes
     the pinned host output over the host link (no device buffers);
     staged: H2D copy into device buffers, kernel, D2H copy, on one stream."""
-    dt = torch.float32 if w.dtype == wl.F32 else torch.bfloat16
+    dt = torch_dtype(w.dtype, torch)
     if w.dtype == wl.F32:
         h_in = torch.from_numpy(w.data).pin_memory()
     else:
-        h_in = torch.from_numpy(w.data.view(np.int16)).view(torch.bfloat16).pin_memory()
+        h_in = torch.from_numpy(w.data.view(np.int16)).view(dt).pin_memory()
     h_out = torch.empty(max(w.out_elems, 1), dtype=dt).pin_memory()
     if staged:
         d_in = torch.empty(w.n_rows * w.n_cols, dtype=dt, device="cuda")
@@ -393,7 +399,7 @@ def run_ours(args):
         "dtype": "f32",        # the arithmetic type (bf16 workloads compute in fp32 too)
         "data": WORKLOAD_DATA[args.workload],
         "config": {"workload": "%s: %d x %d %s, row strides %d/%d%s" % (
-                       args.workload, w.n_rows, w.n_cols, "fp32" if w.dtype == wl.F32 else "bf16",
+                       args.workload, w.n_rows, w.n_cols, DTYPE_NAMES[w.dtype],
                        w.in_row_stride, w.out_row_stride,
                        ", mask from indices, scale %g" % FUSED_SCALE if options else ""),
                    "n_rows": w.n_rows, "n_cols": w.n_cols, "bytes_per_step": bytes_step,
@@ -439,7 +445,7 @@ def run_ours(args):
             "seconds_per_step": round(t, 4)}
     if rank == 0 and not args.no_per_config:
         per = {}
-        for name in wl.NAMES:
+        for name in wl.NAMES + wl.EXTRA_NAMES:
             wc = w if name == args.workload else wl.make(name)
             pc = rws.plan(wc.n_rows, wc.n_cols, in_row_stride=wc.in_row_stride,
                           out_row_stride=wc.out_row_stride, dtype=wc.dtype)
@@ -449,7 +455,7 @@ def run_ours(args):
             del bc
             med = tot / 50
             gbs = wc.algorithmic_bytes / (med * 1e-3) / 1e9
-            per[name] = {"shape": [wc.n_rows, wc.n_cols], "dtype": "f32" if wc.dtype == wl.F32 else "bf16",
+            per[name] = {"shape": [wc.n_rows, wc.n_cols], "dtype": DTYPE_NAMES[wc.dtype],
                          "path": pc.path_name, "plan": str(pc), "mean_ms": round(med, 5),
                          "copy_same_bytes_GB/s": cal["GB/s"] if cal else None,
                          "GB/s": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
@@ -506,7 +512,7 @@ def main():
     ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--no-clock-window", action="store_true",
                     help="do not extend the clock-sampling window past the timed steps")
-    ap.add_argument("--workload", default=HEADLINE, choices=list(wl.NAMES),
+    ap.add_argument("--workload", default=HEADLINE, choices=list(wl.NAMES + wl.EXTRA_NAMES),
                     help="workload timed as the step (default: the headline)")
     ap.add_argument("--mask-from-indices", action="store_true",
                     help="with --workload causal_bf16: time softmax_rows_ex with the causal "

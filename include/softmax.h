@@ -21,8 +21,11 @@
  *    starts at element r * in_row_stride of `in`, row r of the output at
  *    element r * out_row_stride of `out`.  Strides count ELEMENTS, not bytes
  *    (example 2's wrapper passes x.stride(0) and out.stride(0)).
- *  - dtype: SOFTMAX_F32 (binary32 in and out) or SOFTMAX_BF16 (bfloat16 in
- *    and out, rounded to nearest even on output).
+ *  - dtype: SOFTMAX_F32 (binary32 in and out), SOFTMAX_BF16 (bfloat16 in
+ *    and out) or SOFTMAX_F16 (IEEE binary16 in and out); 16-bit outputs
+ *    are rounded to nearest even.  The arithmetic is fp32 for every dtype
+ *    ("Triton: write CUDA-grade GPU operators in Python", tuning checklist:
+ *    fp32 accumulators for float16/bfloat16 data).
  *  - Ownership: every buffer belongs to the caller.  The library never
  *    allocates device or host memory and keeps no workspace.
  *  - Asynchrony: device work is queued on `stream` (a cudaStream_t; NULL is
@@ -52,7 +55,8 @@ extern "C" {
 
 typedef enum {
     SOFTMAX_F32 = 0,
-    SOFTMAX_BF16 = 1
+    SOFTMAX_BF16 = 1,
+    SOFTMAX_F16 = 2
 } softmax_dtype_t;
 
 typedef enum {

@@ -18,7 +18,7 @@ import ctypes
 import os
 
 __all__ = [
-    "F32", "BF16", "PATH_AUTO", "PATH_WARP", "PATH_CTA", "PATH_CLUSTER", "PATH_TWOPASS",
+    "F32", "BF16", "F16", "PATH_AUTO", "PATH_WARP", "PATH_CTA", "PATH_CLUSTER", "PATH_TWOPASS",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_DEVICE_TIMEOUT",
     "SoftmaxError", "DeviceDesc", "Plan", "build", "lib", "library_path",
     "softmax_rows", "softmax_rows_ptr", "softmax_rows_ex_ptr", "softmax_rows_planned_ptr",
@@ -27,7 +27,7 @@ __all__ = [
     "status_string", "device_status", "launch_count", "selftest_wait_timeout", "abi_version", "GB300",
 ]
 
-F32, BF16 = 0, 1
+F32, BF16, F16 = 0, 1, 2
 PATH_AUTO, PATH_WARP, PATH_CTA, PATH_CLUSTER, PATH_TWOPASS = -1, 0, 1, 2, 3
 PATH_NAMES = {PATH_WARP: "warp", PATH_CTA: "cta", PATH_CLUSTER: "cluster", PATH_TWOPASS: "twopass"}
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT = 0, 1, 2, 3, 4
@@ -197,7 +197,9 @@ def _dtype_code(t) -> int:
         return F32
     if t.dtype == torch.bfloat16:
         return BF16
-    raise TypeError("softmax_rows: dtype must be float32 or bfloat16, got %s" % t.dtype)
+    if t.dtype == torch.float16:
+        return F16
+    raise TypeError("softmax_rows: dtype must be float32, bfloat16 or float16, got %s" % t.dtype)
 
 
 def _as_rows(t, name: str):

@@ -174,8 +174,11 @@ __device__ __forceinline__ void warp_ml_merge(float& m, float& l, float k)
 
 // ------------------------------------------------------------ element I/O
 // Elements travel as fp32 in registers.  bf16 is the upper half of a binary32,
-// so widening is a shift; narrowing rounds to nearest even.
+// so widening is a shift; fp16 (binary16) widens exactly with cvt.f32.f16.
+// Narrowing rounds to nearest even.  A 16-bit Elem also provides the pair
+// conversions of one 32-bit word (element 2i in the low half).
 struct BF16Bits { unsigned short b; };
+struct F16Bits { unsigned short b; };
 
 template <typename T> struct Elem;
 
@@ -187,10 +190,14 @@ template <> struct Elem<float> {
 
 template <> struct Elem<BF16Bits> {
     static constexpr int kVec16 = 8;
+    static constexpr unsigned short kNegInfBits = 0xff80u;
+    __device__ static __forceinline__ float widen(unsigned short b)
+    {
+        return __uint_as_float(static_cast<unsigned>(b) << 16);
+    }
     __device__ static __forceinline__ float load1(const BF16Bits* p)
     {
-        const unsigned short b = __ldg(reinterpret_cast<const unsigned short*>(p));
-        return __uint_as_float(static_cast<unsigned>(b) << 16);
+        return widen(__ldg(reinterpret_cast<const unsigned short*>(p)));
     }
     __device__ static __forceinline__ void store1(BF16Bits* p, float v)
     {
@@ -198,20 +205,51 @@ template <> struct Elem<BF16Bits> {
         asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(v));
         *reinterpret_cast<unsigned short*>(p) = h;
     }
+    __device__ static __forceinline__ void unpack2(unsigned w, float& lo, float& hi)
+    {
+        lo = __uint_as_float(w << 16);
+        hi = __uint_as_float(w & 0xffff0000u);
+    }
+    __device__ static __forceinline__ unsigned pack2(float lo, float hi)
+    {
+        unsigned w;   // cvt packs its first source operand into the upper half
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(hi), "f"(lo));
+        return w;
+    }
 };
 
-__device__ __forceinline__ void unpack_bf16x2(unsigned w, float& lo, float& hi)
-{
-    lo = __uint_as_float(w << 16);
-    hi = __uint_as_float(w & 0xffff0000u);
-}
-
-__device__ __forceinline__ unsigned pack_bf16x2(float lo, float hi)
-{
-    unsigned w;   // cvt packs its first source operand into the upper half
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(hi), "f"(lo));
-    return w;
-}
+template <> struct Elem<F16Bits> {
+    static constexpr int kVec16 = 8;
+    static constexpr unsigned short kNegInfBits = 0xfc00u;
+    __device__ static __forceinline__ float widen(unsigned short b)
+    {
+        float f;
+        asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(b));
+        return f;
+    }
+    __device__ static __forceinline__ float load1(const F16Bits* p)
+    {
+        return widen(__ldg(reinterpret_cast<const unsigned short*>(p)));
+    }
+    __device__ static __forceinline__ void store1(F16Bits* p, float v)
+    {
+        unsigned short h;
+        asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(v));
+        *reinterpret_cast<unsigned short*>(p) = h;
+    }
+    __device__ static __forceinline__ void unpack2(unsigned w, float& lo, float& hi)
+    {
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+            "cvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+            : "=f"(lo), "=f"(hi) : "r"(w));
+    }
+    __device__ static __forceinline__ unsigned pack2(float lo, float hi)
+    {
+        unsigned w;   // cvt packs its first source operand into the upper half
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(hi), "f"(lo));
+        return w;
+    }
+};
 
 // Load VEC consecutive elements starting at p (p aligned to VEC elements).
 template <typename T, int VEC>
@@ -231,15 +269,15 @@ __device__ __forceinline__ void load_vec(const T* p, float* v)
     } else {
         if constexpr (VEC == 8) {
             const uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
-            unpack_bf16x2(q.x, v[0], v[1]); unpack_bf16x2(q.y, v[2], v[3]);
-            unpack_bf16x2(q.z, v[4], v[5]); unpack_bf16x2(q.w, v[6], v[7]);
+            Elem<T>::unpack2(q.x, v[0], v[1]); Elem<T>::unpack2(q.y, v[2], v[3]);
+            Elem<T>::unpack2(q.z, v[4], v[5]); Elem<T>::unpack2(q.w, v[6], v[7]);
         } else if constexpr (VEC == 4) {
             const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));
-            unpack_bf16x2(q.x, v[0], v[1]); unpack_bf16x2(q.y, v[2], v[3]);
+            Elem<T>::unpack2(q.x, v[0], v[1]); Elem<T>::unpack2(q.y, v[2], v[3]);
         } else {
-            static_assert(VEC == 2, "bf16 vector width");
+            static_assert(VEC == 2, "16-bit vector width");
             const unsigned q = __ldg(reinterpret_cast<const unsigned*>(p));
-            unpack_bf16x2(q, v[0], v[1]);
+            Elem<T>::unpack2(q, v[0], v[1]);
         }
     }
 }
@@ -260,18 +298,18 @@ __device__ __forceinline__ void store_vec(T* p, const float* v, float scale)
     } else {
         if constexpr (VEC == 8) {
             uint4 q;
-            q.x = pack_bf16x2(v[0] * scale, v[1] * scale);
-            q.y = pack_bf16x2(v[2] * scale, v[3] * scale);
-            q.z = pack_bf16x2(v[4] * scale, v[5] * scale);
-            q.w = pack_bf16x2(v[6] * scale, v[7] * scale);
+            q.x = Elem<T>::pack2(v[0] * scale, v[1] * scale);
+            q.y = Elem<T>::pack2(v[2] * scale, v[3] * scale);
+            q.z = Elem<T>::pack2(v[4] * scale, v[5] * scale);
+            q.w = Elem<T>::pack2(v[6] * scale, v[7] * scale);
             *reinterpret_cast<uint4*>(p) = q;
         } else if constexpr (VEC == 4) {
             uint2 q;
-            q.x = pack_bf16x2(v[0] * scale, v[1] * scale);
-            q.y = pack_bf16x2(v[2] * scale, v[3] * scale);
+            q.x = Elem<T>::pack2(v[0] * scale, v[1] * scale);
+            q.y = Elem<T>::pack2(v[2] * scale, v[3] * scale);
             *reinterpret_cast<uint2*>(p) = q;
         } else {
-            *reinterpret_cast<unsigned*>(p) = pack_bf16x2(v[0] * scale, v[1] * scale);
+            *reinterpret_cast<unsigned*>(p) = Elem<T>::pack2(v[0] * scale, v[1] * scale);
         }
     }
 }
@@ -328,10 +366,10 @@ __device__ __forceinline__ void lds_vec(const T* p, float* v)
         const float4 q = *reinterpret_cast<const float4*>(p);
         v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
     } else {
-        static_assert(VEC == 8, "smem bf16 vector is 16 bytes");
+        static_assert(VEC == 8, "smem 16-bit vector is 16 bytes");
         const uint4 q = *reinterpret_cast<const uint4*>(p);
-        unpack_bf16x2(q.x, v[0], v[1]); unpack_bf16x2(q.y, v[2], v[3]);
-        unpack_bf16x2(q.z, v[4], v[5]); unpack_bf16x2(q.w, v[6], v[7]);
+        Elem<T>::unpack2(q.x, v[0], v[1]); Elem<T>::unpack2(q.y, v[2], v[3]);
+        Elem<T>::unpack2(q.z, v[4], v[5]); Elem<T>::unpack2(q.w, v[6], v[7]);
     }
 }
 
@@ -381,8 +419,8 @@ __device__ __forceinline__ void load16_hint(const T* p, float* v, uint64_t pol)
         v[0] = __uint_as_float(a); v[1] = __uint_as_float(b);
         v[2] = __uint_as_float(c); v[3] = __uint_as_float(d);
     } else {
-        unpack_bf16x2(a, v[0], v[1]); unpack_bf16x2(b, v[2], v[3]);
-        unpack_bf16x2(c, v[4], v[5]); unpack_bf16x2(d, v[6], v[7]);
+        Elem<T>::unpack2(a, v[0], v[1]); Elem<T>::unpack2(b, v[2], v[3]);
+        Elem<T>::unpack2(c, v[4], v[5]); Elem<T>::unpack2(d, v[6], v[7]);
     }
 }
 
@@ -394,8 +432,8 @@ __device__ __forceinline__ void store16_hint(T* p, const float* v, float scale, 
         a = __float_as_uint(v[0] * scale); b = __float_as_uint(v[1] * scale);
         c = __float_as_uint(v[2] * scale); d = __float_as_uint(v[3] * scale);
     } else {
-        a = pack_bf16x2(v[0] * scale, v[1] * scale); b = pack_bf16x2(v[2] * scale, v[3] * scale);
-        c = pack_bf16x2(v[4] * scale, v[5] * scale); d = pack_bf16x2(v[6] * scale, v[7] * scale);
+        a = Elem<T>::pack2(v[0] * scale, v[1] * scale); b = Elem<T>::pack2(v[2] * scale, v[3] * scale);
+        c = Elem<T>::pack2(v[4] * scale, v[5] * scale); d = Elem<T>::pack2(v[6] * scale, v[7] * scale);
     }
     asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;"
                  :: "l"(p), "r"(a), "r"(b), "r"(c), "r"(d), "l"(pol) : "memory");

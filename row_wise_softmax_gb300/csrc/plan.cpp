@@ -115,7 +115,7 @@ bool ranges_intersect(uintptr_t a_lo, uintptr_t a_hi, uintptr_t b_lo, uintptr_t 
 int validate(const void* in, const void* out, int64_t n_rows, int64_t n_cols,
              int64_t ld_in, int64_t ld_out, int dtype)
 {
-    if (dtype != SOFTMAX_F32 && dtype != SOFTMAX_BF16)
+    if (dtype != SOFTMAX_F32 && dtype != SOFTMAX_BF16 && dtype != SOFTMAX_F16)
         return SOFTMAX_ERR_INVALID_ARG;
     if (n_rows < 0 || n_cols < 0)
         return SOFTMAX_ERR_INVALID_ARG;
@@ -230,9 +230,9 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
             return SOFTMAX_ERR_UNSUPPORTED;
         q.threads = 128;
         q.grid = 0;
-        // bf16 rows go through the staged tile kernel; fp32 rows measured
+        // 16-bit rows go through the staged tile kernel; fp32 rows measured
         // faster in the register kernel (its loads are all in flight at once).
-        if (in_al && (p.dtype == SOFTMAX_BF16 || !automatic)) {
+        if (in_al && (p.dtype != SOFTMAX_F32 || !automatic)) {
             // Staged tile kernel: stages of 4 * rows_per_warp rows of
             // row_pad elements (about 16 KB), about 64 KB of ring per CTA.
             const int64_t row_pad = round_up(p.n_cols, vmax);

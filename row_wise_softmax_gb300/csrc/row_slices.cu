@@ -59,7 +59,7 @@ __device__ __forceinline__ void set_neg_inf(T* dst)
     if constexpr (sizeof(T) == 4)
         *reinterpret_cast<float*>(dst) = kNegInf;
     else
-        *reinterpret_cast<unsigned short*>(dst) = 0xff80u;   // bf16 -inf
+        *reinterpret_cast<unsigned short*>(dst) = Elem<T>::kNegInfBits;
 }
 
 // One element from shared memory, widened to fp32.
@@ -69,7 +69,7 @@ __device__ __forceinline__ float lds1(const T* p)
     if constexpr (sizeof(T) == 4)
         return *reinterpret_cast<const float*>(p);
     else
-        return __uint_as_float(static_cast<unsigned>(*reinterpret_cast<const unsigned short*>(p)) << 16);
+        return Elem<T>::widen(*reinterpret_cast<const unsigned short*>(p));
 }
 
 // Cluster-wide reduction of one float per CTA: thread 0 publishes v in its
@@ -497,8 +497,10 @@ cudaError_t launch_threads(const Problem& p, const softmax_plan_t& plan, cudaStr
 #if RWSM_ROW_SLICES_OPTIONS
 cudaError_t launch_row_slices_options(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
 {
-    return p.dtype == SOFTMAX_F32 ? launch_threads<float>(p, plan, s)
-                                  : launch_threads<BF16Bits>(p, plan, s);
+    if (p.dtype == SOFTMAX_F32)
+        return launch_threads<float>(p, plan, s);
+    return p.dtype == SOFTMAX_BF16 ? launch_threads<BF16Bits>(p, plan, s)
+                                   : launch_threads<F16Bits>(p, plan, s);
 }
 #else
 cudaError_t launch_row_slices(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
@@ -507,8 +509,10 @@ cudaError_t launch_row_slices(const Problem& p, const softmax_plan_t& plan, cuda
         return cudaErrorInvalidValue;
     if (has_options(p))
         return launch_row_slices_options(p, plan, s);
-    return p.dtype == SOFTMAX_F32 ? launch_threads<float>(p, plan, s)
-                                  : launch_threads<BF16Bits>(p, plan, s);
+    if (p.dtype == SOFTMAX_F32)
+        return launch_threads<float>(p, plan, s);
+    return p.dtype == SOFTMAX_BF16 ? launch_threads<BF16Bits>(p, plan, s)
+                                   : launch_threads<F16Bits>(p, plan, s);
 }
 
 int max_cluster_size_row_slices()

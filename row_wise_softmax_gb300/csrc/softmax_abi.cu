@@ -214,7 +214,8 @@ int softmax_plan_format(const softmax_plan_t* plan, char* buf, size_t len)
     return std::snprintf(buf, len,
                          "path=%s dtype=%s vec=%d out_vec=%d bulk=%d threads=%d cluster=%d "
                          "rows_per_warp=%d chunks=%d slice_cols=%lld stages=%d smem=%d grid=%lld",
-                         name, plan->dtype == SOFTMAX_F32 ? "f32" : "bf16", plan->vec,
+                         name, plan->dtype == SOFTMAX_F32 ? "f32" : plan->dtype == SOFTMAX_BF16 ? "bf16" : "f16",
+                         plan->vec,
                          plan->out_vec, plan->bulk_copy, plan->threads, plan->cluster,
                          plan->rows_per_warp, plan->chunks,
                          static_cast<long long>(plan->slice_cols), plan->stages, plan->smem_bytes,

@@ -355,9 +355,12 @@ cudaError_t launch_stream_rows(const Problem& p, const softmax_plan_t& plan, cud
     if (p.dtype == SOFTMAX_F32) {
         if (plan.threads == 256) return launch_stream_nv<float, 256>(p, plan, s);
         if (plan.threads == 512) return launch_stream_nv<float, 512>(p, plan, s);
-    } else {
+    } else if (p.dtype == SOFTMAX_BF16) {
         if (plan.threads == 256) return launch_stream_nv<BF16Bits, 256>(p, plan, s);
         if (plan.threads == 512) return launch_stream_nv<BF16Bits, 512>(p, plan, s);
+    } else {
+        if (plan.threads == 256) return launch_stream_nv<F16Bits, 256>(p, plan, s);
+        if (plan.threads == 512) return launch_stream_nv<F16Bits, 512>(p, plan, s);
     }
     return cudaErrorInvalidValue;
 }

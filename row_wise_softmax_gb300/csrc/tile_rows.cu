@@ -44,7 +44,7 @@ __device__ __forceinline__ void lds_any(const T* p, float* v)
         if constexpr (sizeof(T) == 4)
             v[0] = *reinterpret_cast<const float*>(p);
         else
-            v[0] = __uint_as_float(static_cast<unsigned>(*reinterpret_cast<const unsigned short*>(p)) << 16);
+            v[0] = Elem<T>::widen(*reinterpret_cast<const unsigned short*>(p));
     } else {
         lds_vec<T, VEC>(p, v);
     }
@@ -359,9 +359,12 @@ cudaError_t launch_tile_rows(const Problem& p, const softmax_plan_t& plan, cudaS
     if (p.dtype == SOFTMAX_F32) {
         if (plan.vec == 4) return launch_chunks<float, 4>(p, plan, s);
         if (plan.vec == 1) return launch_chunks<float, 1>(p, plan, s);
-    } else {
+    } else if (p.dtype == SOFTMAX_BF16) {
         if (plan.vec == 8) return launch_chunks<BF16Bits, 8>(p, plan, s);
         if (plan.vec == 1) return launch_chunks<BF16Bits, 1>(p, plan, s);
+    } else {
+        if (plan.vec == 8) return launch_chunks<F16Bits, 8>(p, plan, s);
+        if (plan.vec == 1) return launch_chunks<F16Bits, 1>(p, plan, s);
     }
     return cudaErrorInvalidValue;
 }

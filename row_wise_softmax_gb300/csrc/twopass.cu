@@ -234,8 +234,11 @@ cudaError_t launch_twopass(const Problem& p, const softmax_plan_t& plan, cudaStr
     if (p.dtype == SOFTMAX_F32)
         return plan.vec == 4 ? launch_tp_threads<float, 4>(p, plan, s)
                              : launch_tp_threads<float, 1>(p, plan, s);
-    return plan.vec == 8 ? launch_tp_threads<BF16Bits, 8>(p, plan, s)
-                         : launch_tp_threads<BF16Bits, 1>(p, plan, s);
+    if (p.dtype == SOFTMAX_BF16)
+        return plan.vec == 8 ? launch_tp_threads<BF16Bits, 8>(p, plan, s)
+                             : launch_tp_threads<BF16Bits, 1>(p, plan, s);
+    return plan.vec == 8 ? launch_tp_threads<F16Bits, 8>(p, plan, s)
+                         : launch_tp_threads<F16Bits, 1>(p, plan, s);
 }
 
 }  // namespace rwsm

@@ -187,9 +187,12 @@ cudaError_t launch_warp_rows(const Problem& p, const softmax_plan_t& plan, cudaS
     if (p.dtype == SOFTMAX_F32) {
         if (plan.vec == 4) return launch_vec<float, 4>(p, plan, s);
         if (plan.vec == 1) return launch_vec<float, 1>(p, plan, s);
-    } else {
+    } else if (p.dtype == SOFTMAX_BF16) {
         if (plan.vec == 8) return launch_vec<BF16Bits, 8>(p, plan, s);
         if (plan.vec == 1) return launch_vec<BF16Bits, 1>(p, plan, s);
+    } else {
+        if (plan.vec == 8) return launch_vec<F16Bits, 8>(p, plan, s);
+        if (plan.vec == 1) return launch_vec<F16Bits, 1>(p, plan, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -7,7 +7,8 @@ Tolerances (fixed here, used by every parity test):
                even), measured as the distance of the two values in the
                ordered-integer view of bf16 bit patterns.  One ulp allows for
                the double rounding double -> fp32 -> bf16 at near-ties.
-  both:        where the oracle gives exactly 0 (a -inf input in a finite row)
+  fp16 output: the same, with binary16 in place of bf16.
+  all:        where the oracle gives exactly 0 (a -inf input in a finite row)
                the output is exactly +0; where the oracle gives NaN (a row
                with NaN, +inf, or only -inf) the output is NaN.
 """
@@ -23,24 +24,33 @@ F32_ROWSUM_TOL = 1e-5
 BF16_ULP_TOL = 1
 
 
+def decode16(bits: np.ndarray, dtype: int) -> np.ndarray:
+    return oracle.bf16_to_double(bits) if dtype == wl.BF16 else oracle.f16_to_double(bits)
+
+
 def bf16_ordered(bits: np.ndarray) -> np.ndarray:
-    """Map bf16 bit patterns to integers that order like their values (+0 == -0)."""
+    """Map bf16 (or fp16: the same sign-magnitude layout) bit patterns to
+    integers that order like their values (+0 == -0)."""
     b = bits.astype(np.int32)
     mag = b & 0x7FFF
     return np.where(b & 0x8000, -mag, mag)
+
+
+def torch_dtype(dtype: int):
+    import torch
+    return {wl.F32: torch.float32, wl.BF16: torch.bfloat16, wl.F16: torch.float16}[dtype]
 
 
 def device_input(w: wl.Workload):
     import torch
     if w.dtype == wl.F32:
         return torch.from_numpy(w.data).cuda()
-    return torch.from_numpy(w.data.view(np.int16)).cuda().view(torch.bfloat16)
+    return torch.from_numpy(w.data.view(np.int16)).cuda().view(torch_dtype(w.dtype))
 
 
 def empty_output(w: wl.Workload, fill=None):
     import torch
-    dt = torch.float32 if w.dtype == wl.F32 else torch.bfloat16
-    t = torch.empty(max(w.out_elems, 1), dtype=dt, device="cuda")
+    t = torch.empty(max(w.out_elems, 1), dtype=torch_dtype(w.dtype), device="cuda")
     if fill is not None:
         t.fill_(fill)
     return t
@@ -50,7 +60,7 @@ def host_output(t, w: wl.Workload) -> np.ndarray:
     """Dense [n_rows, n_cols] view of a strided device output (float32, or uint16 bf16 bits)."""
     import torch
     flat = t.cpu()
-    if w.dtype == wl.BF16:
+    if w.dtype != wl.F32:
         flat = flat.view(torch.int16).numpy().view(np.uint16)
     else:
         flat = flat.numpy()
@@ -77,10 +87,10 @@ def compare(got: np.ndarray, want: np.ndarray, dtype: int, what: str = "") -> di
     stats = {"rows": int(want.shape[0]), "nan_rows": int(nan_rows.sum())}
     if nan_rows.any():
         g = got[nan_rows]
-        if dtype == wl.BF16:
-            gv = oracle.bf16_to_double(g)
-        else:
+        if dtype == wl.F32:
             gv = g.astype(np.float64)
+        else:
+            gv = decode16(g, dtype)
         assert np.all(np.isnan(gv)), "%s: rows the formula makes NaN are not all NaN" % what
     ok = ~nan_rows
     g, w = got[ok], want[ok]
@@ -100,13 +110,13 @@ def compare(got: np.ndarray, want: np.ndarray, dtype: int, what: str = "") -> di
             what, stats["max_rowsum_err"])
         assert np.all(g.view(np.uint32)[zero] == 0), "%s: masked output not +0" % what
     else:
-        wb = oracle.to_bf16(w)
+        wb = oracle.to_bf16(w) if dtype == wl.BF16 else oracle.to_f16(w)
         d = np.abs(bf16_ordered(g) - bf16_ordered(wb))
         stats["max_ulp"] = int(d.max())
         stats["ulp_gt0"] = int((d > 0).sum())
-        gd = oracle.bf16_to_double(g)
+        gd = decode16(g, dtype)
         stats["max_rowsum_err"] = float(np.abs(gd.sum(axis=1) - 1.0).max())
-        assert stats["max_ulp"] <= BF16_ULP_TOL, "%s: %d bf16 ulp at %s" % (
+        assert stats["max_ulp"] <= BF16_ULP_TOL, "%s: %d ulp (16-bit) at %s" % (
             what, stats["max_ulp"], np.unravel_index(np.argmax(d), d.shape))
         assert np.all(g[zero] == 0), "%s: masked output not +0" % what
     return stats

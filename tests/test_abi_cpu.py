@@ -67,6 +67,16 @@ def test_scheduler_paths_for_the_five_workloads(lib):
     assert (p.path, p.bulk_copy, p.vec, p.threads) == (rws.PATH_TWOPASS, 0, 1, 512)
 
 
+def test_scheduler_fp16_follows_bf16(lib):
+    """fp16 I/O has bf16's element size, so every shape gets bf16's plan."""
+    for shape, kw in (((32768, 1024), {}), ((4096, 4096), {}), ((6, 30000), {}),
+                      ((256, 262144), {}), ((64, 1000), {"out_row_stride": 1001}),
+                      ((9, 5000), {"in_ptr": (1 << 20) + 2})):
+        a = plan(*shape, dtype=rws.BF16, **kw)
+        b = plan(*shape, dtype=rws.F16, **kw)
+        assert str(a).replace("dtype=bf16", "dtype=f16") == str(b), (shape, str(a), str(b))
+
+
 def test_scheduler_boundaries(lib):
     assert plan(1, 1024).path == rws.PATH_WARP
     assert plan(1, 1025).path == rws.PATH_CTA
@@ -143,6 +153,8 @@ def test_validation(lib):
     assert f(A + 2, B, 2, 4, 4, 4, rws.F32) == rws.ERR_INVALID_ARG  # misaligned element
     assert f(A + 2, B + 2, 2, 4, 4, 4, rws.BF16) != rws.ERR_INVALID_ARG or True
     assert f(A, B, 2, 4, 4, 4, 5) == rws.ERR_INVALID_ARG            # dtype
+    assert f(A, B, 2, 4, 4, 4, 3) == rws.ERR_INVALID_ARG
+    assert f(A + 2, B, 2, 4, 4, 4, rws.F16) != rws.ERR_INVALID_ARG   # 2-byte aligned is enough
     assert f(0, 0, 0, 4, 4, 4, rws.F32) == rws.OK                   # empty: no-op
     assert f(0, 0, 4, 0, 4, 4, rws.F32) == rws.OK
     # Overlap: partial overlap rejected, identical (in place) accepted by validation.

@@ -27,7 +27,7 @@ def built():
 def sentinel_run(w: wl.Workload, path):
     """Run into an output surrounded by guard zones, gaps filled with a sentinel."""
     x = parity.device_input(w)
-    dt = torch.float32 if w.dtype == wl.F32 else torch.bfloat16
+    dt = parity.torch_dtype(w.dtype)
     full = torch.full((GUARD + w.out_elems + GUARD,), 7.0, dtype=dt, device="cuda")
     before = full.clone()
     y = full[GUARD:GUARD + w.out_elems]
@@ -39,13 +39,13 @@ def sentinel_run(w: wl.Workload, path):
     idx = (torch.arange(w.n_rows, device="cuda")[:, None] * w.out_row_stride
            + torch.arange(w.n_cols, device="cuda")[None, :]).reshape(-1) + GUARD
     written[idx] = True
-    untouched = (full.view(torch.int16 if w.dtype == wl.BF16 else torch.int32)
-                 == before.view(torch.int16 if w.dtype == wl.BF16 else torch.int32))
+    iv = torch.int32 if w.dtype == wl.F32 else torch.int16
+    untouched = full.view(iv) == before.view(iv)
     assert bool(untouched[~written].all()), "wrote outside the output rows"
     return parity.host_output(y, w)
 
 
-@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
+@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16, wl.F16])
 @pytest.mark.parametrize("path", PATHS, ids=lambda p: rws.PATH_NAMES[p])
 def test_strided_rows_and_guard_zones(dtype, path):
     for n_cols, ld_in, ld_out in ((100, 128, 130), (1000, 1003, 1000), (600, 600, 777),
@@ -61,7 +61,7 @@ def test_strided_rows_and_guard_zones(dtype, path):
 
 @pytest.mark.parametrize("path", PATHS, ids=lambda p: rws.PATH_NAMES[p])
 def test_in_place(path):
-    for dtype in (wl.F32, wl.BF16):
+    for dtype in (wl.F32, wl.BF16, wl.F16):
         n_cols = 900 if path == rws.PATH_WARP else 20000
         w = wl.random_rows(11, n_cols, dtype=dtype, seed=3, scale=5.0)
         x = parity.device_input(w)
@@ -74,7 +74,7 @@ def test_in_place(path):
 
 @pytest.mark.parametrize("path", PATHS, ids=lambda p: rws.PATH_NAMES[p])
 def test_unaligned_pointers_take_scalar_access(path):
-    for dtype in (wl.F32, wl.BF16):
+    for dtype in (wl.F32, wl.BF16, wl.F16):
         n_cols = 333 if path == rws.PATH_WARP else 9001
         w = wl.random_rows(5, n_cols, dtype=dtype, seed=9, scale=2.0)
         x_big = parity.device_input(wl.random_rows(1, w.data.size + 1, dtype=dtype, seed=1))
@@ -95,7 +95,7 @@ def test_unaligned_pointers_take_scalar_access(path):
 @pytest.mark.parametrize("path", PATHS, ids=lambda p: rws.PATH_NAMES[p])
 def test_degenerate_rows(path):
     n_cols = 200 if path == rws.PATH_WARP else 12000
-    for dtype in (wl.F32, wl.BF16):
+    for dtype in (wl.F32, wl.BF16, wl.F16):
         base = np.random.default_rng(4).standard_normal((6, n_cols)).astype(np.float32)
         base[0, :] = -np.inf                       # all masked: NaN row
         base[1, n_cols // 2] = np.nan              # NaN: NaN row
@@ -108,9 +108,12 @@ def test_degenerate_rows(path):
         if dtype == wl.BF16:
             w = wl.Workload("degenerate", 6, n_cols, n_cols, n_cols, wl.BF16,
                             wl._f32_to_bf16_bits(base.reshape(-1)), 0)
+        elif dtype == wl.F16:
+            w = wl.Workload("degenerate", 6, n_cols, n_cols, n_cols, wl.F16,
+                            wl._f32_to_f16_bits(base.reshape(-1)), 0)
         got = sentinel_run(w, path)
         parity.compare(got, parity.expected(w), dtype, "degenerate")
-        one = 1.0 if dtype == wl.F32 else 0x3F80
+        one = {wl.F32: 1.0, wl.BF16: 0x3F80, wl.F16: 0x3C00}[dtype]
         assert got[3, n_cols - 1] == one
 
 
@@ -145,8 +148,13 @@ def test_torch_binding_and_streams():
     yb = rws.softmax_rows(xb, stream=s)
     s.synchronize()
     assert yb.dtype == torch.bfloat16 and yb.shape == xb.shape
+    xh = x.half()
+    yh = rws.softmax_rows(xh)
+    torch.cuda.synchronize()
+    assert yh.dtype == torch.float16
+    assert float((yh.double() - torch.softmax(xh.double(), dim=-1)).abs().max()) <= 1e-3
     with pytest.raises(TypeError):
-        rws.softmax_rows(x.half())
+        rws.softmax_rows(x.double())
     with pytest.raises(ValueError):
         rws.softmax_rows(x.t())                     # column stride != 1
     v = torch.randn(5000, device="cuda")

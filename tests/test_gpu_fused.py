@@ -78,7 +78,7 @@ SHAPES = {
 }
 
 
-@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
+@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16, wl.F16])
 @pytest.mark.parametrize("path", PATHS, ids=lambda p: rws.PATH_NAMES[p])
 def test_scaled_causal_forced_paths(dtype, path):
     for i, (n_rows, n_cols) in enumerate(SHAPES[path]):

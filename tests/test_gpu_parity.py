@@ -85,7 +85,7 @@ def test_forced_cta_beyond_capacity_is_unsupported():
     assert rws.plan(2, CTA_CAPACITY_COLS, path=rws.PATH_CTA).path == rws.PATH_CTA
 
 
-@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
+@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16, wl.F16])
 @pytest.mark.parametrize("path", PATHS, ids=lambda p: rws.PATH_NAMES[p])
 def test_shape_sweep_forced_paths(dtype, path):
     checked = 0
@@ -119,15 +119,27 @@ def test_twopass_long_row_automatic():
     parity.compare(run(w), parity.expected(w), wl.F32, "twopass auto")
 
 
-def test_bf16_long_rows_cluster_and_twopass():
-    w = wl.random_rows(6, 30_000, dtype=wl.BF16, seed=8, scale=6.0)       # 60 KB rows
-    p = rws.plan(w.n_rows, w.n_cols, dtype=wl.BF16)
+@pytest.mark.parametrize("dtype", [wl.BF16, wl.F16])
+def test_16bit_long_rows_cluster_and_twopass(dtype):
+    w = wl.random_rows(6, 30_000, dtype=dtype, seed=8, scale=6.0)       # 60 KB rows
+    p = rws.plan(w.n_rows, w.n_cols, dtype=dtype)
     assert p.path == rws.PATH_CLUSTER
-    parity.compare(run(w), parity.expected(w), wl.BF16, "bf16 cluster")
-    w = wl.random_rows(6, 250_000, dtype=wl.BF16, seed=8, scale=6.0)      # 500 KB rows
-    p = rws.plan(w.n_rows, w.n_cols, dtype=wl.BF16)
+    parity.compare(run(w), parity.expected(w), dtype, "16-bit cluster")
+    w = wl.random_rows(6, 250_000, dtype=dtype, seed=8, scale=6.0)      # 500 KB rows
+    p = rws.plan(w.n_rows, w.n_cols, dtype=dtype)
     assert p.path == rws.PATH_TWOPASS and p.bulk_copy == 1
-    parity.compare(run(w), parity.expected(w), wl.BF16, "bf16 two-pass")
+    parity.compare(run(w), parity.expected(w), dtype, "16-bit two-pass")
+
+
+def test_full_size_f16_causal():
+    """fp16 I/O at the causal workload's size (32768 x 1024, -inf written in)."""
+    w = wl.causal_f16()
+    p = rws.plan(w.n_rows, w.n_cols, dtype=w.dtype)
+    assert p.path == rws.PATH_WARP and p.bulk_copy == 1
+    got = run(w)
+    stats = parity.compare(got, parity.expected(w), w.dtype, "causal_f16")
+    assert np.all(got[0, 1:] == 0) and got[0, 0] == 0x3C00                # exactly [1, 0, ...]
+    print("causal_f16", stats)
 
 
 def test_reduced_workloads_every_path():

@@ -54,3 +54,19 @@ def test_random_rows_exact_extent():
     assert w.data.size == 4 * 9 + 7
     wb = wl.random_rows(3, 4, dtype=wl.BF16)
     assert wb.data.dtype == np.uint16 and wb.data.size == 12
+    wh = wl.random_rows(3, 4, dtype=wl.F16)
+    assert wh.data.dtype == np.uint16 and wh.data.size == 12
+
+
+def test_causal_f16_recipe():
+    w = wl.causal_f16(2100)
+    x = w.data.view(np.float16).reshape(2100, 1024).astype(np.float64)
+    r = np.arange(2100)[:, None] % 1024
+    c = np.arange(1024)[None, :]
+    assert np.all(np.isneginf(x[c > r])) and np.all(np.isfinite(x[c <= r]))
+    # Same draws as the bf16 recipe, rounded to binary16 instead of bfloat16.
+    b = wl.causal_bf16(2100)
+    xb = b.data.view(np.uint16).astype(np.uint32) << 16
+    xb = xb.view(np.float32).reshape(2100, 1024).astype(np.float64)
+    keep = c <= r
+    assert np.max(np.abs(x[keep] - xb[keep]) / (np.abs(xb[keep]) + 1e-3)) < 2 ** -7

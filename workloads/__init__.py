@@ -33,6 +33,7 @@ import numpy as np
 
 F32 = 0
 BF16 = 1
+F16 = 2
 
 
 @dataclass
@@ -78,6 +79,9 @@ COLS = {
 }
 SEEDS = {"small_f32": 1, "masked_f32": 2, "causal_bf16": 3, "short_f32": 4, "long_f32": 5}
 NAMES = tuple(FULL_ROWS)
+# Further workloads (not among the five configurations): fp16 I/O at the
+# causal size.
+EXTRA_NAMES = ("causal_f16",)
 
 
 def _f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -85,6 +89,25 @@ def _f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     import torch
     t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
     return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def _f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to binary16 (numpy, ties to even); uint16 bit patterns."""
+    with np.errstate(over="ignore"):
+        return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def causal_f16(n_rows: int = 32768) -> Workload:
+    """The causal workload's recipe (row r keeps columns c <= r mod n_cols, the
+    rest -inf) with binary16 values: fp16 I/O at the causal size."""
+    n_cols = COLS["causal_bf16"]
+    rng = np.random.default_rng(SEEDS["causal_bf16"])
+    x = rng.standard_normal((n_rows, n_cols), dtype=np.float32) * np.float32(8.0)
+    r = np.arange(n_rows)[:, None] % n_cols
+    c = np.arange(n_cols)[None, :]
+    x = np.where(c > r, np.float32(-np.inf), x).astype(np.float32)
+    return Workload("causal_f16", n_rows, n_cols, n_cols, n_cols, F16,
+                    _f32_to_f16_bits(x).reshape(-1), 3)
 
 
 def small_f32(n_rows: int = 128) -> Workload:
@@ -150,6 +173,7 @@ GENERATORS = {
     "causal_bf16": causal_bf16,
     "short_f32": short_f32,
     "long_f32": long_f32,
+    "causal_f16": causal_f16,
 }
 
 
@@ -173,4 +197,6 @@ def random_rows(n_rows: int, n_cols: int, dtype: int = F32, seed: int = 0,
         flat = flat[: (n_rows - 1) * stride + n_cols]        # exact strided extent
     if dtype == BF16:
         flat = _f32_to_bf16_bits(flat)
+    elif dtype == F16:
+        flat = _f32_to_f16_bits(flat)
     return Workload("random", n_rows, n_cols, stride, n_cols, dtype, np.ascontiguousarray(flat), seed)
