@@ -69,6 +69,9 @@ class Oracle:
         lib.oracle_f16_to_double.restype = dbl
         lib.oracle_double_to_f16_array.argtypes = [vp, vp, i64]
         lib.oracle_f16_to_double_array.argtypes = [vp, vp, i64]
+        lib.oracle_softmax_backward_rows.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64,
+                                                     ctypes.c_int]
+        lib.oracle_softmax_backward_rows.restype = ctypes.c_int
         lib.oracle_tiled_row_sum.argtypes = [vp, i64, i64, i64, vp]
         lib.oracle_tiled_row_sum.restype = dbl
         self._lib = lib
@@ -113,6 +116,29 @@ class Oracle:
         v = np.ascontiguousarray(values, dtype=np.float64)
         out = np.empty(v.shape, dtype=np.uint16)
         self._lib.oracle_double_to_bf16_array(v.ctypes.data, out.ctypes.data, v.size)
+        return out
+
+    def softmax_backward_rows(self, y: np.ndarray, dy: np.ndarray, n_rows: int, n_cols: int,
+                              y_row_stride: int | None = None, dy_row_stride: int | None = None,
+                              dtype: int = F32) -> np.ndarray:
+        """dx = y * (dy - sum(y * dy)) per row, in double, from flat y and dy
+        buffers (float32 values, or 16-bit patterns as uint16); returns a dense
+        float64 array [n_rows, n_cols]."""
+        ys = n_cols if y_row_stride is None else y_row_stride
+        gs = n_cols if dy_row_stride is None else dy_row_stride
+        want = np.float32 if dtype == F32 else np.uint16
+        y = np.ascontiguousarray(y).reshape(-1)
+        dy = np.ascontiguousarray(dy).reshape(-1)
+        for b, st in ((y, ys), (dy, gs)):
+            if b.dtype != want:
+                raise TypeError("oracle: buffer dtype %s, expected %s" % (b.dtype, want))
+            if n_rows > 0 and n_cols > 0 and b.size < (n_rows - 1) * st + n_cols:
+                raise ValueError("oracle: buffer too small for the strided rows")
+        out = np.empty((n_rows, n_cols), dtype=np.float64)
+        rc = self._lib.oracle_softmax_backward_rows(y.ctypes.data, dy.ctypes.data, out.ctypes.data,
+                                                    n_rows, n_cols, ys, gs, n_cols, dtype)
+        if rc != 0:
+            raise ValueError("oracle_softmax_backward_rows rejected its arguments")
         return out
 
     def to_f16(self, values: np.ndarray) -> np.ndarray:
@@ -172,3 +198,7 @@ def to_f16(values: np.ndarray) -> np.ndarray:
 
 def f16_to_double(bits: np.ndarray) -> np.ndarray:
     return load().f16_to_double(bits)
+
+
+def softmax_backward_rows(*args, **kwargs) -> np.ndarray:
+    return load().softmax_backward_rows(*args, **kwargs)

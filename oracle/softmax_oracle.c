@@ -31,6 +31,9 @@
  *    an offset shifts the diagonal; so column c takes part iff
  *    c <= (r mod period) + offset.  A masked column is never read.  A row
  *    with no column taking part is the formula over only -inf: all NaN.
+ *  - the softmax backward (the gradient through the row softmax, by the
+ *    chain rule; the pages name forward-backward fused operators among the
+ *    custom kernels Triton is for, without the formula): see below.
  *  - the tiled row sum with one accumulator per lane: lec06 section
  *    "Level 2: Row Sum (tiling)", worked example of 12 elements, BLOCK 4.
  *  - bf16 and fp16 decoding (exact) and rounding of a double to bf16 or
@@ -344,4 +347,48 @@ double oracle_tiled_row_sum(const double* x, int64_t n, int64_t block,
         s += acc[i];
     free(acc);
     return s;
+}
+
+/* ---- softmax backward --------------------------------------------------- */
+
+/* Element j of row r of a 16-bit or binary32 buffer, exactly, as a double. */
+static double load_elem(const void* base, int64_t idx, int dtype)
+{
+    if (dtype == 0)
+        return (double)((const float*)base)[idx];
+    const uint16_t b = ((const uint16_t*)base)[idx];
+    return dtype == 1 ? oracle_bf16_to_double(b) : oracle_f16_to_double(b);
+}
+
+/*
+ * The gradient of the row softmax y = softmax(x) with respect to x, given y
+ * and the gradient dy of a loss with respect to y.  The Jacobian of the
+ * softmax is dy_j/dx_i = y_j (delta_ij - y_i), so by the chain rule
+ *     dx_i = sum_j dy_j y_j (delta_ij - y_i) = y_i (dy_i - sum_j y_j dy_j).
+ * Computed in double from the exact values of y and dy, the dot product
+ * summed left to right.  Row r of y, dy and dx starts at r times its own
+ * stride (elements); dx is double.  Returns 0, or -1 on a bad argument.
+ */
+int oracle_softmax_backward_rows(const void* y, const void* dy, double* dx, int64_t n_rows,
+                                 int64_t n_cols, int64_t y_row_stride, int64_t dy_row_stride,
+                                 int64_t dx_row_stride, int dtype)
+{
+    if (n_rows < 0 || n_cols < 0 || dtype < 0 || dtype > 2)
+        return -1;
+    if (n_rows == 0 || n_cols == 0)
+        return 0;
+    if (!y || !dy || !dx)
+        return -1;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        double dot = 0.0;
+        for (int64_t j = 0; j < n_cols; ++j)
+            dot += load_elem(y, r * y_row_stride + j, dtype) *
+                   load_elem(dy, r * dy_row_stride + j, dtype);
+        for (int64_t j = 0; j < n_cols; ++j) {
+            const double yj = load_elem(y, r * y_row_stride + j, dtype);
+            const double gj = load_elem(dy, r * dy_row_stride + j, dtype);
+            dx[r * dx_row_stride + j] = yj * (gj - dot);
+        }
+    }
+    return 0;
 }

@@ -51,6 +51,14 @@ MUTANTS = {
     "f16_subnormal_spacing": ("if (q_exp < -24)\n        q_exp = -24;", "if (q_exp < -25)\n        q_exp = -25;"),
     "f16_input_decoded_as_bf16": ("x[j] = scale * oracle_f16_to_double(src[j]);",
                                   "x[j] = scale * oracle_bf16_to_double(src[j]);"),
+    "backward_no_y_factor": ("dx[r * dx_row_stride + j] = yj * (gj - dot);",
+                             "dx[r * dx_row_stride + j] = (gj - dot);"),
+    "backward_sign": ("dx[r * dx_row_stride + j] = yj * (gj - dot);",
+                      "dx[r * dx_row_stride + j] = yj * (gj + dot);"),
+    "backward_dot_without_y": ("dot += load_elem(y, r * y_row_stride + j, dtype) *\n                   load_elem(dy, r * dy_row_stride + j, dtype);",
+                               "dot += load_elem(dy, r * dy_row_stride + j, dtype);"),
+    "backward_dy_stride": ("const double gj = load_elem(dy, r * dy_row_stride + j, dtype);",
+                           "const double gj = load_elem(dy, r * y_row_stride + j, dtype);"),
     "tiled_sum_ragged_lane": ("if (t0 + i < n)         /* masked lanes load 0 */",
                               "if (t0 + i <= n)"),
 }

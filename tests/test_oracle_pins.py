@@ -487,3 +487,79 @@ def test_online_recurrence_causal_equals_definition(oracle_lib, tile):
     assert np.isnan(y[0]).all() and np.isnan(y[6]).all()       # rows with no visible column
     ok = ~np.isnan(y)
     assert np.all(np.abs(yt[ok] - y[ok]) <= 1e-14 * y[ok] + 1e-300)
+
+
+# ------------------------------------------------------------ softmax backward
+# dx_i = y_i (dy_i - sum_j y_j dy_j): the chain rule through the row softmax.
+
+def test_backward_matches_torch_softmax_backward(oracle_lib):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(61)
+    for n_rows, n_cols in ((7, 1), (13, 37), (5, 1000)):
+        x = torch.from_numpy(rng.standard_normal((n_rows, n_cols)) * 3)
+        y = torch.softmax(x, dim=-1).float()
+        dy = torch.from_numpy(rng.standard_normal((n_rows, n_cols))).float()
+        got = oracle_lib.softmax_backward_rows(y.numpy().reshape(-1), dy.numpy().reshape(-1),
+                                               n_rows, n_cols)
+        # torch's own backward of softmax, from the output and the incoming
+        # gradient, in double (the same exact y and dy values).
+        ref = torch._softmax_backward_data(dy.double(), y.double(), -1, torch.float64).numpy()
+        assert np.allclose(got, ref, rtol=1e-12, atol=1e-15)
+
+
+def test_backward_finite_differences(oracle_lib):
+    """The gradient of sum_j dy_j softmax(x)_j by central differences at 40 digits."""
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 40
+    rng = np.random.default_rng(62)
+    for n in (2, 3, 6):
+        x = [mpmath.mpf(float(v)) for v in rng.standard_normal(n) * 2]
+        dy = rng.standard_normal(n).astype(np.float32)
+
+        def loss(xs):
+            e = [mpmath.exp(v) for v in xs]
+            t = mpmath.fsum(e)
+            return mpmath.fsum(float(dy[j]) * e[j] / t for j in range(n))
+
+        e = [mpmath.exp(v) for v in x]
+        t = mpmath.fsum(e)
+        y = np.array([float(v / t) for v in e], dtype=np.float32)
+        got = oracle_lib.softmax_backward_rows(y, dy, 1, n)[0]
+        h = mpmath.mpf(10) ** -15
+        for i in range(n):
+            xp = list(x); xp[i] += h
+            xm = list(x); xm[i] -= h
+            fd = float((loss(xp) - loss(xm)) / (2 * h))
+            assert abs(got[i] - fd) <= 1e-6 * (1 + abs(fd)), (n, i, got[i], fd)
+
+
+def test_backward_exact_dyadic_rows(oracle_lib):
+    """Dyadic y summing to 1 and small-integer dy: every value exact in double."""
+    y = np.array([[0.5, 0.25, 0.125, 0.125], [1.0, 0.0, 0.0, 0.0], [0.25] * 4], np.float32)
+    dy = np.array([[3, -1, 2, 0], [5, 7, -2, 1], [9, 9, 9, 9]], np.float32)
+    got = oracle_lib.softmax_backward_rows(y.reshape(-1), dy.reshape(-1), 3, 4)
+    for r in range(3):
+        dot = sum(Fraction(float(y[r, j])) * Fraction(float(dy[r, j])) for j in range(4))
+        for j in range(4):
+            assert got[r, j] == float(Fraction(float(y[r, j])) * (Fraction(float(dy[r, j])) - dot))
+        assert sum(Fraction(v) for v in got[r]) == 0
+    assert np.all(got[2] == 0.0)                          # constant dy: zero gradient
+
+
+def test_backward_strides_and_16bit(oracle_lib):
+    rng = np.random.default_rng(63)
+    y = rng.random((6, 50)).astype(np.float32)
+    dy = rng.standard_normal((6, 50)).astype(np.float32)
+    dense = oracle_lib.softmax_backward_rows(y.reshape(-1), dy.reshape(-1), 6, 50)
+    yp = np.full((6, 64), np.nan, np.float32); yp[:, :50] = y
+    gp = np.full((6, 57), np.nan, np.float32); gp[:, :50] = dy
+    strided = oracle_lib.softmax_backward_rows(yp.reshape(-1)[:5 * 64 + 50],
+                                               gp.reshape(-1)[:5 * 57 + 50], 6, 50, 64, 57)
+    assert np.array_equal(dense, strided)
+    for dtype, enc, dec in ((BF16, oracle_lib.to_bf16, oracle_lib.bf16_to_double),
+                            (F16, oracle_lib.to_f16, oracle_lib.f16_to_double)):
+        yb, gb = enc(y.astype(np.float64)), enc(dy.astype(np.float64))
+        got = oracle_lib.softmax_backward_rows(yb.reshape(-1), gb.reshape(-1), 6, 50, dtype=dtype)
+        yd, gd = dec(yb).astype(np.float32), dec(gb).astype(np.float32)    # exact in binary32
+        ref = oracle_lib.softmax_backward_rows(yd.reshape(-1), gd.reshape(-1), 6, 50)
+        assert np.array_equal(got, ref)
