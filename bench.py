@@ -292,6 +292,45 @@ def fused_causal_entry(torch, rws, stream, l2_bytes, peak):
             "rows_per_s": round(w.n_rows / (med * 1e-3), 1)}
 
 
+def backward_entry(torch, rws, stream, l2_bytes, peak, n_rows=4096, n_cols=4096, dtype=wl.F32):
+    """softmax_backward_rows over rotating (y, dy, dx) sets: three element
+    transfers per element (read y, read dy, write dx)."""
+    y, g = wl.backward_pair(n_rows, n_cols, dtype)
+    dt = torch_dtype(dtype, torch)
+
+    def dev(a):
+        t = torch.from_numpy(a if dtype == wl.F32 else a.view(np.int16)).cuda()
+        return t if dtype == wl.F32 else t.view(dt)
+
+    ty, tg = dev(y), dev(g)
+    esz = 4 if dtype == wl.F32 else 2
+    algo = 3 * n_rows * n_cols * esz
+    n_sets = max(1, -(-L2_FACTOR * l2_bytes // algo))
+    sets = [(ty if i == 0 else ty.clone(), tg if i == 0 else tg.clone(), torch.empty_like(ty))
+            for i in range(n_sets)]
+    call = rws.lib().softmax_backward_rows
+    args = [(a.data_ptr(), b.data_ptr(), c.data_ptr(), n_rows, n_cols, n_cols, n_cols, n_cols,
+             dtype, stream.cuda_stream) for a, b, c in sets]
+    for i in range(5):
+        if call(*args[i % n_sets]) != rws.OK:
+            raise RuntimeError("softmax_backward_rows failed")
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = rws.launch_count()
+    a.record(stream)
+    for i in range(50):
+        call(*args[i % n_sets])
+    b.record(stream)
+    torch.cuda.synchronize()
+    med = a.elapsed_time(b) / 50
+    gbs = algo / (med * 1e-3) / 1e9
+    return {"shape": [n_rows, n_cols], "dtype": DTYPE_NAMES[dtype],
+            "op": "softmax_backward_rows: dx = y * (dy - sum(y * dy))",
+            "algorithmic_bytes": algo, "mean_ms": round(med, 5), "GB/s": round(gbs, 1),
+            "frac_of_measured_peak": round(gbs / peak, 4),
+            "launches": rws.launch_count() - launches0, "rows_per_s": round(n_rows / (med * 1e-3), 1)}
+
+
 def time_e2e(w: wl.Workload, steps: int, warmup: int, torch, rws, stream, staged: bool):
     """softmax_rows_host on pinned host buffers, timed over `steps` calls.
 
@@ -464,6 +503,9 @@ def run_ours(args):
             del wc
         per["causal_bf16_mask_from_indices"] = fused_causal_entry(torch, rws, stream, l2_bytes,
                                                                   peak)
+        per["backward_f32_4096x4096"] = backward_entry(torch, rws, stream, l2_bytes, peak)
+        per["backward_bf16_32768x1024"] = backward_entry(torch, rws, stream, l2_bytes, peak,
+                                                         32768, 1024, wl.BF16)
         result["per_config"] = per
     if world > 1:
         import torch.distributed as dist

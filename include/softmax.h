@@ -172,6 +172,30 @@ int64_t softmax_visible_cols(const softmax_options_t* options, int64_t n_rows, i
                              int64_t row);
 
 /*
+ * softmax_backward_rows: the gradient through the row softmax.  Given the
+ * forward output y (n_rows x n_cols) and the gradient dy of a loss with
+ * respect to y, writes
+ *     dx_i = y_i * (dy_i - sum_j y_j dy_j)        for every row,
+ * the chain rule through y = softmax(x), whose Jacobian is
+ * dy_j/dx_i = y_j (delta_ij - y_i).  ("Triton: write CUDA-grade GPU operators
+ * in Python" names fused forward-backward operators among what custom
+ * kernels are for; the formula is the derivative of the softmax above.)
+ *
+ *   y, dy, dx    device pointers, rows starting every y_row_stride,
+ *                dy_row_stride and dx_row_stride ELEMENTS; contiguous
+ *                columns; the same dtype for all three; fp32 arithmetic.
+ *   Ownership and asynchrony as for softmax_rows.  dx may be dy or y itself
+ *   (same stride); other overlaps of dx with y or dy are rejected.
+ *   Errors: SOFTMAX_ERR_INVALID_ARG for a null pointer with work to do,
+ *   negative sizes, a stride below n_cols (n_rows > 1), an unknown dtype or
+ *   a partial overlap; SOFTMAX_ERR_UNSUPPORTED without a usable device;
+ *   SOFTMAX_ERR_CUDA if the launch fails.  n_rows == 0 or n_cols == 0: no-op.
+ */
+int softmax_backward_rows(const void* y, const void* dy, void* dx, int64_t n_rows,
+                          int64_t n_cols, int64_t y_row_stride, int64_t dy_row_stride,
+                          int64_t dx_row_stride, int dtype, void* stream);
+
+/*
  * softmax_rows_host: the same operation on HOST buffers.  Two modes:
  *
  *  staged  (d_in and d_out given): queues on `stream` a copy of the strided

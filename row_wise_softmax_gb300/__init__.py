@@ -22,7 +22,7 @@ __all__ = [
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_DEVICE_TIMEOUT",
     "SoftmaxError", "DeviceDesc", "Plan", "build", "lib", "library_path",
     "softmax_rows", "softmax_rows_ptr", "softmax_rows_ex_ptr", "softmax_rows_planned_ptr",
-    "visible_cols",
+    "visible_cols", "softmax_backward", "softmax_backward_rows_ptr",
     "Options", "softmax_rows_host", "plan", "plan_for_device",
     "status_string", "device_status", "launch_count", "selftest_wait_timeout", "abi_version", "GB300",
 ]
@@ -108,6 +108,8 @@ def lib() -> ctypes.CDLL:
         L.softmax_rows_ex.argtypes = [vp, vp, i64, i64, i64, i64, ci, ctypes.POINTER(Options), ci,
                                       vp]
         L.softmax_rows_ex.restype = ci
+        L.softmax_backward_rows.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, ci, vp]
+        L.softmax_backward_rows.restype = ci
         L.softmax_visible_cols.argtypes = [ctypes.POINTER(Options), i64, i64, i64]
         L.softmax_visible_cols.restype = i64
         L.softmax_rows_planned.argtypes = [vp, vp, i64, i64, i64, i64, ci, ctypes.POINTER(Plan), vp]
@@ -173,6 +175,40 @@ def softmax_rows_ex_ptr(in_ptr: int, out_ptr: int, n_rows: int, n_cols: int, in_
     o = Options(scale, 1 if causal else 0, causal_period, causal_offset)
     return lib().softmax_rows_ex(in_ptr, out_ptr, n_rows, n_cols, in_row_stride, out_row_stride,
                                  dtype, ctypes.byref(o), path, stream)
+
+
+def softmax_backward_rows_ptr(y_ptr: int, dy_ptr: int, dx_ptr: int, n_rows: int, n_cols: int,
+                              y_row_stride: int, dy_row_stride: int, dx_row_stride: int,
+                              dtype: int, stream: int = 0) -> int:
+    """C ABI call of the softmax backward; returns the status."""
+    return lib().softmax_backward_rows(y_ptr, dy_ptr, dx_ptr, n_rows, n_cols, y_row_stride,
+                                       dy_row_stride, dx_row_stride, dtype, stream)
+
+
+def softmax_backward(y, dy, out=None, stream=None):
+    """dx = y * (dy - sum(y * dy)) along the last dimension of CUDA tensors
+    (1-D or 2-D, same dtype and shape); ``out`` may be ``dy`` or ``y``."""
+    import torch
+    if y.shape != dy.shape or y.dtype != dy.dtype or y.device != dy.device:
+        raise ValueError("softmax_backward: y and dy must match in shape, dtype and device")
+    if y.dim() not in (1, 2) or not y.is_cuda:
+        raise ValueError("softmax_backward: expects 1-D or 2-D CUDA tensors")
+    y2, g2 = (y.unsqueeze(0), dy.unsqueeze(0)) if y.dim() == 1 else (y, dy)
+    if y2.stride(-1) != 1 or g2.stride(-1) != 1:
+        raise ValueError("softmax_backward: rows must be contiguous (column stride 1)")
+    if out is None:
+        out = torch.empty_like(y)
+    o2 = out.unsqueeze(0) if out.dim() == 1 else out
+    if out.shape != y.shape or out.dtype != y.dtype or o2.stride(-1) != 1:
+        raise ValueError("softmax_backward: out must match y")
+    dt = _dtype_code(y)
+    with torch.cuda.device(y.device):
+        st = softmax_backward_rows_ptr(y2.data_ptr(), g2.data_ptr(), o2.data_ptr(), y2.shape[0],
+                                       y2.shape[1], y2.stride(0), g2.stride(0), o2.stride(0), dt,
+                                       _stream_handle(stream, y.device))
+    if st != OK:
+        raise SoftmaxError(st, "softmax_backward")
+    return out
 
 
 def visible_cols(n_rows: int, n_cols: int, row: int, scale: float = 1.0, causal: bool = False,

@@ -123,6 +123,19 @@ int apply_options(const softmax_options_t* o, Problem* p);
 // Is a caller-supplied plan safe and complete for this problem?
 int check_plan(const softmax_device_desc_t& dev, const Problem& p, const softmax_plan_t& plan);
 
+// Softmax backward (backward_rows.cu): dx = y * (dy - sum(y * dy)) per row.
+struct BackwardProblem {
+    const void* y;
+    const void* dy;
+    void* dx;
+    int64_t n_rows, n_cols;
+    int64_t ld_y, ld_dy, ld_dx;
+    int dtype;
+};
+constexpr int64_t kBackwardWarpMaxCols = 1024;      // warp per row up to here
+// `vec`: y, dy and dx rows all 16-byte aligned (vector access).
+cudaError_t launch_backward_rows(const BackwardProblem& p, bool vec, cudaStream_t s);
+
 // Launchers, one per path (each in its own translation unit).
 cudaError_t launch_warp_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
 cudaError_t launch_tile_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);

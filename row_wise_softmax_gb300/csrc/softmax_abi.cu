@@ -289,6 +289,39 @@ int64_t softmax_visible_cols(const softmax_options_t* options, int64_t n_rows, i
     return rwsm::logits_valid(rwsm::logits_of(p), row, n_cols);
 }
 
+int softmax_backward_rows(const void* y, const void* dy, void* dx, int64_t n_rows,
+                          int64_t n_cols, int64_t y_row_stride, int64_t dy_row_stride,
+                          int64_t dx_row_stride, int dtype, void* stream)
+{
+    // dx against each input: the forward pass's rules (in place allowed,
+    // partial overlap rejected); y and dy are both only read.
+    int st = rwsm::validate(y, dx, n_rows, n_cols, y_row_stride, dx_row_stride, dtype);
+    if (st != SOFTMAX_OK)
+        return st;
+    st = rwsm::validate(dy, dx, n_rows, n_cols, dy_row_stride, dx_row_stride, dtype);
+    if (st != SOFTMAX_OK)
+        return st;
+    if (n_rows == 0 || n_cols == 0)
+        return SOFTMAX_OK;
+    softmax_device_desc_t d;
+    const int ds = rwsm::current_device(&d);
+    if (ds != SOFTMAX_OK)
+        return ds;
+    const int64_t esz = dtype == SOFTMAX_F32 ? 4 : 2;
+    auto aligned = [&](const void* p, int64_t ld) {
+        return reinterpret_cast<uintptr_t>(p) % 16 == 0 && (n_rows == 1 || (ld * esz) % 16 == 0);
+    };
+    const bool vec = aligned(y, y_row_stride) && aligned(dy, dy_row_stride) &&
+                     aligned(dx, dx_row_stride);
+    const rwsm::BackwardProblem p{y, dy, dx, n_rows, n_cols, y_row_stride, dy_row_stride,
+                                  dx_row_stride, dtype};
+    if (rwsm::launch_backward_rows(p, vec, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return SOFTMAX_ERR_CUDA;
+    }
+    return SOFTMAX_OK;
+}
+
 int softmax_rows(const void* in, void* out, int64_t n_rows, int64_t n_cols,
                  int64_t in_row_stride, int64_t out_row_stride, int dtype, void* stream)
 {

@@ -200,3 +200,17 @@ def random_rows(n_rows: int, n_cols: int, dtype: int = F32, seed: int = 0,
     elif dtype == F16:
         flat = _f32_to_f16_bits(flat)
     return Workload("random", n_rows, n_cols, stride, n_cols, dtype, np.ascontiguousarray(flat), seed)
+
+
+def backward_pair(n_rows: int = 4096, n_cols: int = 4096, dtype: int = F32, seed: int = 6):
+    """Inputs of the softmax backward at a given size: y ~ U[0, 2/n_cols) per
+    element (rows of probabilities in scale, without being a softmax output)
+    and dy ~ N(0, 1); flat, dense buffers of the dtype (uint16 bits for 16-bit)."""
+    rng = np.random.default_rng(seed)
+    y = (rng.random((n_rows, n_cols), dtype=np.float32) * np.float32(2.0 / n_cols)).reshape(-1)
+    g = rng.standard_normal(n_rows * n_cols, dtype=np.float32)
+    if dtype == BF16:
+        return _f32_to_bf16_bits(y), _f32_to_bf16_bits(g)
+    if dtype == F16:
+        return _f32_to_f16_bits(y), _f32_to_f16_bits(g)
+    return y, g
