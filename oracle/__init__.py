@@ -72,6 +72,8 @@ class Oracle:
         lib.oracle_softmax_backward_rows.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64,
                                                      ctypes.c_int]
         lib.oracle_softmax_backward_rows.restype = ctypes.c_int
+        lib.oracle_softmax_strided.argtypes = [vp, vp, i64, i64, i64, i64, ctypes.c_int]
+        lib.oracle_softmax_strided.restype = ctypes.c_int
         lib.oracle_tiled_row_sum.argtypes = [vp, i64, i64, i64, vp]
         lib.oracle_tiled_row_sum.restype = dbl
         self._lib = lib
@@ -141,6 +143,26 @@ class Oracle:
             raise ValueError("oracle_softmax_backward_rows rejected its arguments")
         return out
 
+    def softmax_strided(self, buf: np.ndarray, n_rows: int, n_cols: int, in_row_stride: int,
+                        in_col_stride: int, dtype: int = F32) -> np.ndarray:
+        """Softmax over rows whose element c of row r is buf[r * in_row_stride +
+        c * in_col_stride] (non-negative strides); dense float64 [n_rows, n_cols]."""
+        want = np.float32 if dtype == F32 else np.uint16
+        buf = np.ascontiguousarray(buf).reshape(-1)
+        if buf.dtype != want:
+            raise TypeError("oracle: buffer dtype %s, expected %s" % (buf.dtype, want))
+        if in_row_stride < 0 or in_col_stride < 0:
+            raise ValueError("oracle: strides must be non-negative")
+        if n_rows > 0 and n_cols > 0 and \
+                buf.size <= (n_rows - 1) * in_row_stride + (n_cols - 1) * in_col_stride:
+            raise ValueError("oracle: buffer too small for the strided rows")
+        out = np.empty((n_rows, n_cols), dtype=np.float64)
+        rc = self._lib.oracle_softmax_strided(buf.ctypes.data, out.ctypes.data, n_rows, n_cols,
+                                              in_row_stride, in_col_stride, dtype)
+        if rc != 0:
+            raise ValueError("oracle_softmax_strided rejected its arguments")
+        return out
+
     def to_f16(self, values: np.ndarray) -> np.ndarray:
         """Round doubles to fp16 (ties to even); returns uint16 bit patterns."""
         v = np.ascontiguousarray(values, dtype=np.float64)
@@ -202,3 +224,7 @@ def f16_to_double(bits: np.ndarray) -> np.ndarray:
 
 def softmax_backward_rows(*args, **kwargs) -> np.ndarray:
     return load().softmax_backward_rows(*args, **kwargs)
+
+
+def softmax_strided(*args, **kwargs) -> np.ndarray:
+    return load().softmax_strided(*args, **kwargs)

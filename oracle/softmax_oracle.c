@@ -31,6 +31,8 @@
  *    an offset shifts the diagonal; so column c takes part iff
  *    c <= (r mod period) + offset.  A masked column is never read.  A row
  *    with no column taking part is the formula over only -inf: all NaN.
+ *  - softmax over strided rows (column-wise softmax): lec06 "Level 1"
+ *    and its section on strides; see oracle_softmax_strided.
  *  - the softmax backward (the gradient through the row softmax, by the
  *    chain rule; the pages name forward-backward fused operators among the
  *    custom kernels Triton is for, without the formula): see below.
@@ -305,6 +307,45 @@ int oracle_softmax_rows_ex(const void* in, double* out, int64_t n_rows, int64_t 
             online_softmax_row(x, n_cols, tile, y);
         else
             softmax_row(x, n_cols, y);
+    }
+    free(x);
+    return 0;
+}
+
+/*
+ * Softmax over arbitrarily strided rows: element c of row r is
+ * in[r * in_row_stride + c * in_col_stride] (elements).  Column-wise softmax
+ * of a row-major matrix is the case in_row_stride = 1, in_col_stride = its
+ * row length: "Lecture 6: GPU Kernel programming and Triton", section
+ * "Level 1: Softmax", notes that only the strides change to take the softmax
+ * along columns, and its section on strides writes the address of element
+ * [row, col] as ptr + row * stride_row + col * stride_col.  The output is
+ * dense double [n_rows][n_cols]; each row is gathered and then reduced by the
+ * plain definition.  Returns 0, or -1 on a bad argument.
+ */
+int oracle_softmax_strided(const void* in, double* out, int64_t n_rows, int64_t n_cols,
+                           int64_t in_row_stride, int64_t in_col_stride, int dtype)
+{
+    if (n_rows < 0 || n_cols < 0 || dtype < 0 || dtype > 2)
+        return -1;
+    if (n_rows == 0 || n_cols == 0)
+        return 0;
+    if (!in || !out)
+        return -1;
+    double* x = (double*)malloc((size_t)n_cols * sizeof(double));
+    if (!x)
+        return -1;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        for (int64_t c = 0; c < n_cols; ++c) {
+            const int64_t idx = r * in_row_stride + c * in_col_stride;
+            if (dtype == 0)
+                x[c] = (double)((const float*)in)[idx];
+            else if (dtype == 1)
+                x[c] = oracle_bf16_to_double(((const uint16_t*)in)[idx]);
+            else
+                x[c] = oracle_f16_to_double(((const uint16_t*)in)[idx]);
+        }
+        softmax_row(x, n_cols, out + r * n_cols);
     }
     free(x);
     return 0;

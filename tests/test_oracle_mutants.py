@@ -59,6 +59,10 @@ MUTANTS = {
                                "dot += load_elem(dy, r * dy_row_stride + j, dtype);"),
     "backward_dy_stride": ("const double gj = load_elem(dy, r * dy_row_stride + j, dtype);",
                            "const double gj = load_elem(dy, r * y_row_stride + j, dtype);"),
+    "strided_ignores_col_stride": ("const int64_t idx = r * in_row_stride + c * in_col_stride;",
+                                   "const int64_t idx = r * in_row_stride + c;"),
+    "strided_swaps_strides": ("const int64_t idx = r * in_row_stride + c * in_col_stride;",
+                              "const int64_t idx = r * in_col_stride + c * in_row_stride;"),
     "tiled_sum_ragged_lane": ("if (t0 + i < n)         /* masked lanes load 0 */",
                               "if (t0 + i <= n)"),
 }

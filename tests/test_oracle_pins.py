@@ -563,3 +563,43 @@ def test_backward_strides_and_16bit(oracle_lib):
         yd, gd = dec(yb).astype(np.float32), dec(gb).astype(np.float32)    # exact in binary32
         ref = oracle_lib.softmax_backward_rows(yd.reshape(-1), gd.reshape(-1), 6, 50)
         assert np.array_equal(got, ref)
+
+
+# ------------------------------------------------------ strided (column-wise)
+
+def test_strided_column_softmax_matches_transpose(oracle_lib):
+    """Column-wise softmax of a row-major matrix equals the row softmax of its
+    transpose (numpy's transpose, copied dense)."""
+    rng = np.random.default_rng(71)
+    m = (rng.standard_normal((45, 17)) * 4).astype(np.float32)
+    m[3, 5] = -np.inf
+    cols = oracle_lib.softmax_strided(m.reshape(-1), 17, 45, 1, 17)
+    rows_of_t = oracle_lib.softmax_rows(np.ascontiguousarray(m.T).reshape(-1), 17, 45)
+    assert np.array_equal(cols, rows_of_t)
+    # The unit column stride is the row-wise softmax.
+    assert np.array_equal(oracle_lib.softmax_strided(m.reshape(-1), 45, 17, 17, 1),
+                          oracle_lib.softmax_rows(m.reshape(-1), 45, 17))
+
+
+def test_strided_matches_torch_dim0_and_16bit(oracle_lib):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(72)
+    m = (rng.standard_normal((300, 40)) * 2).astype(np.float32)
+    got = oracle_lib.softmax_strided(m.reshape(-1), 40, 300, 1, 40)
+    ref = torch.softmax(torch.from_numpy(m).double(), dim=0).numpy().T
+    assert np.all(np.abs(got - ref) <= 1e-14 * ref + 1e-300)
+    for dtype, enc in ((BF16, oracle_lib.to_bf16), (F16, oracle_lib.to_f16)):
+        b = enc(m.astype(np.float64))
+        got = oracle_lib.softmax_strided(b.reshape(-1), 40, 300, 1, 40, dtype=dtype)
+        ref = oracle_lib.softmax_rows(np.ascontiguousarray(b.T).reshape(-1), 40, 300, dtype=dtype)
+        assert np.array_equal(got, ref)
+
+
+def test_strided_general_gather(oracle_lib):
+    """Row stride 3, column stride 7 over a buffer: each row gathered by index."""
+    rng = np.random.default_rng(73)
+    buf = rng.standard_normal(3 * 9 + 7 * 10 + 1).astype(np.float32)
+    got = oracle_lib.softmax_strided(buf, 10, 11, 3, 7)
+    for r in range(10):
+        row = np.array([buf[r * 3 + c * 7] for c in range(11)], dtype=np.float32)
+        assert np.array_equal(got[r], oracle_lib.softmax_rows(row, 1, 11)[0])
