@@ -331,6 +331,40 @@ def backward_entry(torch, rws, stream, l2_bytes, peak, n_rows=4096, n_cols=4096,
             "launches": rws.launch_count() - launches0, "rows_per_s": round(n_rows / (med * 1e-3), 1)}
 
 
+def columns_entry(torch, rws, stream, l2_bytes, peak, R=4096, C=4096, dtype=wl.F32):
+    """softmax_strided down the columns of a row-major R x C matrix (row
+    strides 1, column strides C), over rotating input/output sets."""
+    w = wl.random_rows(R, C, dtype=dtype, seed=12, scale=3.0)
+    dt = torch_dtype(dtype, torch)
+    x = torch.from_numpy(w.data if dtype == wl.F32 else w.data.view(np.int16)).cuda()
+    x = x if dtype == wl.F32 else x.view(dt)
+    esz = 4 if dtype == wl.F32 else 2
+    algo = 2 * R * C * esz
+    n_sets = max(1, -(-L2_FACTOR * l2_bytes // algo))
+    sets = [(x if i == 0 else x.clone(), torch.empty_like(x)) for i in range(n_sets)]
+    call = rws.lib().softmax_strided
+    args = [(a.data_ptr(), b.data_ptr(), C, R, 1, C, 1, C, dtype, stream.cuda_stream)
+            for a, b in sets]
+    for i in range(5):
+        if call(*args[i % n_sets]) != rws.OK:
+            raise RuntimeError("softmax_strided failed")
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = rws.launch_count()
+    a.record(stream)
+    for i in range(50):
+        call(*args[i % n_sets])
+    b.record(stream)
+    torch.cuda.synchronize()
+    med = a.elapsed_time(b) / 50
+    gbs = algo / (med * 1e-3) / 1e9
+    return {"shape": [R, C], "dtype": DTYPE_NAMES[dtype],
+            "op": "softmax_strided down the columns (rows of the softmax = columns)",
+            "algorithmic_bytes": algo, "mean_ms": round(med, 5), "GB/s": round(gbs, 1),
+            "frac_of_measured_peak": round(gbs / peak, 4),
+            "launches": rws.launch_count() - launches0}
+
+
 def time_e2e(w: wl.Workload, steps: int, warmup: int, torch, rws, stream, staged: bool):
     """softmax_rows_host on pinned host buffers, timed over `steps` calls.
 
@@ -504,6 +538,9 @@ def run_ours(args):
         per["causal_bf16_mask_from_indices"] = fused_causal_entry(torch, rws, stream, l2_bytes,
                                                                   peak)
         per["backward_f32_4096x4096"] = backward_entry(torch, rws, stream, l2_bytes, peak)
+        per["columns_f32_4096x4096"] = columns_entry(torch, rws, stream, l2_bytes, peak)
+        per["columns_bf16_8192x4096"] = columns_entry(torch, rws, stream, l2_bytes, peak,
+                                                      8192, 4096, wl.BF16)
         per["backward_bf16_32768x1024"] = backward_entry(torch, rws, stream, l2_bytes, peak,
                                                          32768, 1024, wl.BF16)
         result["per_config"] = per

@@ -172,6 +172,31 @@ int64_t softmax_visible_cols(const softmax_options_t* options, int64_t n_rows, i
                              int64_t row);
 
 /*
+ * softmax_strided: the softmax of rows whose elements are not contiguous.
+ * Element c of row r is in[r * in_row_stride + c * in_col_stride] and its
+ * result goes to out[r * out_row_stride + c * out_col_stride] (ELEMENTS).
+ * The cs336 lecture 6 notes ("Lecture 6: GPU Kernel programming and Triton",
+ * section "Level 1: Softmax", and its section on strides) take a column-wise
+ * softmax by changing only the strides: the softmax down the columns of a
+ * row-major R x C matrix is n_rows = C, n_cols = R, row strides 1, column
+ * strides C.
+ *
+ *   Unit column strides: the same as softmax_rows.  Unit row strides: the
+ *   columns kernel (128-byte tiles of adjacent rows staged in shared memory,
+ *   one HBM read and one write per element; rows up to 16 x 512 columns per
+ *   cluster of CTAs, longer ones while the tile fits in shared memory).
+ *   Other strides, or longer columns: a general gather kernel (correct for
+ *   any layout, two reads per element).
+ *   Strides must be >= 0; the output elements must be distinct (its rows
+ *   nested within its columns or the reverse); in and out may be the same
+ *   buffer with the same strides, and must not otherwise share bytes.
+ *   Ownership, asynchrony and errors as for softmax_rows.
+ */
+int softmax_strided(const void* in, void* out, int64_t n_rows, int64_t n_cols,
+                    int64_t in_row_stride, int64_t in_col_stride, int64_t out_row_stride,
+                    int64_t out_col_stride, int dtype, void* stream);
+
+/*
  * softmax_backward_rows: the gradient through the row softmax.  Given the
  * forward output y (n_rows x n_cols) and the gradient dy of a loss with
  * respect to y, writes

@@ -22,7 +22,8 @@ __all__ = [
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_DEVICE_TIMEOUT",
     "SoftmaxError", "DeviceDesc", "Plan", "build", "lib", "library_path",
     "softmax_rows", "softmax_rows_ptr", "softmax_rows_ex_ptr", "softmax_rows_planned_ptr",
-    "visible_cols", "softmax_backward", "softmax_backward_rows_ptr",
+    "visible_cols", "softmax_backward", "softmax_backward_rows_ptr", "softmax",
+    "softmax_strided_ptr",
     "Options", "softmax_rows_host", "plan", "plan_for_device",
     "status_string", "device_status", "launch_count", "selftest_wait_timeout", "abi_version", "GB300",
 ]
@@ -108,6 +109,8 @@ def lib() -> ctypes.CDLL:
         L.softmax_rows_ex.argtypes = [vp, vp, i64, i64, i64, i64, ci, ctypes.POINTER(Options), ci,
                                       vp]
         L.softmax_rows_ex.restype = ci
+        L.softmax_strided.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64, ci, vp]
+        L.softmax_strided.restype = ci
         L.softmax_backward_rows.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, ci, vp]
         L.softmax_backward_rows.restype = ci
         L.softmax_visible_cols.argtypes = [ctypes.POINTER(Options), i64, i64, i64]
@@ -175,6 +178,36 @@ def softmax_rows_ex_ptr(in_ptr: int, out_ptr: int, n_rows: int, n_cols: int, in_
     o = Options(scale, 1 if causal else 0, causal_period, causal_offset)
     return lib().softmax_rows_ex(in_ptr, out_ptr, n_rows, n_cols, in_row_stride, out_row_stride,
                                  dtype, ctypes.byref(o), path, stream)
+
+
+def softmax_strided_ptr(in_ptr: int, out_ptr: int, n_rows: int, n_cols: int, in_row_stride: int,
+                       in_col_stride: int, out_row_stride: int, out_col_stride: int, dtype: int,
+                       stream: int = 0) -> int:
+    """C ABI call of the strided softmax; returns the status."""
+    return lib().softmax_strided(in_ptr, out_ptr, n_rows, n_cols, in_row_stride, in_col_stride,
+                                 out_row_stride, out_col_stride, dtype, stream)
+
+
+def softmax(x, dim: int = -1, out=None, stream=None):
+    """softmax(x) along ``dim`` of a 2-D CUDA tensor with any strides (dim 0:
+    column-wise).  ``out`` defaults to a new tensor laid out like ``x``."""
+    import torch
+    if x.dim() != 2 or not x.is_cuda:
+        raise ValueError("softmax: expects a 2-D CUDA tensor")
+    d = dim % 2
+    if out is None:
+        out = torch.empty_like(x)
+    if out.shape != x.shape or out.dtype != x.dtype or out.device != x.device:
+        raise ValueError("softmax: out must match x in dtype, shape and device")
+    # Softmax rows run along `dim`: row index over the other dimension.
+    r, c = (1, 0) if d == 0 else (0, 1)
+    with torch.cuda.device(x.device):
+        st = softmax_strided_ptr(x.data_ptr(), out.data_ptr(), x.shape[r], x.shape[c],
+                                 x.stride(r), x.stride(c), out.stride(r), out.stride(c),
+                                 _dtype_code(x), _stream_handle(stream, x.device))
+    if st != OK:
+        raise SoftmaxError(st, "softmax")
+    return out
 
 
 def softmax_backward_rows_ptr(y_ptr: int, dy_ptr: int, dx_ptr: int, n_rows: int, n_cols: int,

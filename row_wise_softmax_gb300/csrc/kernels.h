@@ -136,6 +136,30 @@ constexpr int64_t kBackwardWarpMaxCols = 1024;      // warp per row up to here
 // `vec`: y, dy and dx rows all 16-byte aligned (vector access).
 cudaError_t launch_backward_rows(const BackwardProblem& p, bool vec, cudaStream_t s);
 
+// Softmax over strided rows (columns.cu): element c of row r at
+// r * row_stride + c * col_stride, in and out each with their own strides.
+struct StridedProblem {
+    const void* in;
+    void* out;
+    int64_t n_rows, n_cols;
+    int64_t in_row_stride, in_col_stride, out_row_stride, out_col_stride;
+    int dtype;
+};
+// Launch shape of the columns kernel (unit row strides): a cluster of
+// `cluster` CTAs per tile of 128 bytes of adjacent rows, `rows_per_cta`
+// memory rows (softmax columns) staged per CTA.  ok = false: use the gather
+// kernel.
+struct ColumnsShape {
+    bool ok;
+    int cluster, rows_per_cta, smem_bytes;
+    int64_t tiles;
+    bool vec_in, vec_out;
+};
+constexpr int64_t kColumnsRowsPerCta = 512;
+constexpr int64_t kColumnsMaxCluster = 16;
+ColumnsShape columns_shape(const StridedProblem& p, int max_smem_per_block);
+cudaError_t launch_strided(const StridedProblem& p, const ColumnsShape& sh, cudaStream_t s);
+
 // Launchers, one per path (each in its own translation unit).
 cudaError_t launch_warp_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
 cudaError_t launch_tile_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);

@@ -289,6 +289,64 @@ int64_t softmax_visible_cols(const softmax_options_t* options, int64_t n_rows, i
     return rwsm::logits_valid(rwsm::logits_of(p), row, n_cols);
 }
 
+int softmax_strided(const void* in, void* out, int64_t n_rows, int64_t n_cols,
+                    int64_t in_row_stride, int64_t in_col_stride, int64_t out_row_stride,
+                    int64_t out_col_stride, int dtype, void* stream)
+{
+    if (dtype != SOFTMAX_F32 && dtype != SOFTMAX_BF16 && dtype != SOFTMAX_F16)
+        return SOFTMAX_ERR_INVALID_ARG;
+    if (n_rows < 0 || n_cols < 0 || in_row_stride < 0 || in_col_stride < 0 ||
+        out_row_stride < 0 || out_col_stride < 0)
+        return SOFTMAX_ERR_INVALID_ARG;
+    if (n_rows == 0 || n_cols == 0)
+        return SOFTMAX_OK;
+    if (in_col_stride == 1 && out_col_stride == 1)          // contiguous rows
+        return softmax_rows(in, out, n_rows, n_cols, in_row_stride, out_row_stride, dtype, stream);
+    if (!in || !out)
+        return SOFTMAX_ERR_INVALID_ARG;
+    const int64_t esz = dtype == SOFTMAX_F32 ? 4 : 2;
+    if (reinterpret_cast<uintptr_t>(in) % esz || reinterpret_cast<uintptr_t>(out) % esz)
+        return SOFTMAX_ERR_INVALID_ARG;
+    // Every output element distinct: rows nested in columns or columns in rows.
+    const int64_t lim = INT64_MAX / 8;
+    auto span = [&](int64_t rs, int64_t cs_) -> int64_t {   // last element index + 1
+        if ((n_rows > 1 && rs > (lim - 1) / (n_rows - 1)) || (n_cols > 1 && cs_ > (lim - 1) / (n_cols - 1)))
+            return -1;
+        const int64_t a = (n_rows - 1) * rs, b = (n_cols - 1) * cs_;
+        return a > lim - b - 1 ? -1 : a + b + 1;
+    };
+    const int64_t in_span = span(in_row_stride, in_col_stride);
+    const int64_t out_span = span(out_row_stride, out_col_stride);
+    if (in_span < 0 || out_span < 0)
+        return SOFTMAX_ERR_INVALID_ARG;
+    const bool distinct = n_rows == 1 || n_cols == 1 ||
+                          (out_col_stride >= 1 && out_row_stride >= n_cols * out_col_stride) ||
+                          (out_row_stride >= 1 && out_col_stride >= n_rows * out_row_stride);
+    if (!distinct)
+        return SOFTMAX_ERR_INVALID_ARG;
+    // In place with the same layout, or no shared bytes at all.
+    const uintptr_t i0 = reinterpret_cast<uintptr_t>(in), o0 = reinterpret_cast<uintptr_t>(out);
+    const uintptr_t i1 = i0 + static_cast<uintptr_t>(in_span * esz);
+    const uintptr_t o1 = o0 + static_cast<uintptr_t>(out_span * esz);
+    const bool same = in == out && in_row_stride == out_row_stride && in_col_stride == out_col_stride;
+    if (!same && i0 < o1 && o0 < i1)
+        return SOFTMAX_ERR_INVALID_ARG;
+    softmax_device_desc_t d;
+    const int ds = rwsm::current_device(&d);
+    if (ds != SOFTMAX_OK)
+        return ds;
+    const rwsm::StridedProblem p{in, out, n_rows, n_cols, in_row_stride, in_col_stride,
+                                 out_row_stride, out_col_stride, dtype};
+    rwsm::ColumnsShape sh{};
+    if ((in_row_stride == 1 && out_row_stride == 1) || n_rows == 1)
+        sh = rwsm::columns_shape(p, d.max_smem_per_block_optin);
+    if (rwsm::launch_strided(p, sh, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return SOFTMAX_ERR_CUDA;
+    }
+    return SOFTMAX_OK;
+}
+
 int softmax_backward_rows(const void* y, const void* dy, void* dx, int64_t n_rows,
                           int64_t n_cols, int64_t y_row_stride, int64_t dy_row_stride,
                           int64_t dx_row_stride, int dtype, void* stream)
