@@ -365,6 +365,48 @@ def columns_entry(torch, rws, stream, l2_bytes, peak, R=4096, C=4096, dtype=wl.F
             "launches": rws.launch_count() - launches0}
 
 
+def tensor_peak():
+    """Measured dense bf16 tensor rate (burst), TFLOP/s, and its kind."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return 1900.0, "fallback"
+
+
+def attention_entry(torch, rws, stream, bh=64, n=4096, d=128, causal=False, dtype=wl.BF16):
+    """softmax_attention_forward on seeded N(0,1) inputs: the (m, l) recurrence
+    inside attention; FLOPs 4 * bh * n * n * d (halved with the causal mask)."""
+    qb, kb, vb = wl.attention_inputs(bh, n, n, d, dtype, seed=21)
+    dt = torch_dtype(dtype, torch)
+    tq, tk, tv = (torch.from_numpy(a.view(np.int16)).cuda().view(dt) for a in (qb, kb, vb))
+    to = torch.empty_like(tq)
+    call = rws.lib().softmax_attention_forward
+    opt = rws.AttentionOptions(1.0 / (d ** 0.5), 1 if causal else 0, 0)
+    import ctypes
+    args = (tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), to.data_ptr(), None, bh, n, n, d, dtype,
+            ctypes.byref(opt), stream.cuda_stream)
+    for _ in range(3):
+        if call(*args) != rws.OK:
+            raise RuntimeError("softmax_attention_forward failed")
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps = 10
+    a.record(stream)
+    for _ in range(steps):
+        call(*args)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    flops = 4.0 * bh * n * n * d * (0.5 if causal else 1.0)
+    tf = flops / (ms * 1e-3) / 1e12
+    peak, kind = tensor_peak()
+    return {"shape": {"batch_heads": bh, "n_q": n, "n_k": n, "head_dim": d},
+            "dtype": DTYPE_NAMES[dtype], "causal": causal,
+            "kernel": "attention_mma_kernel (mma.sync m16n8k16)", "mean_ms": round(ms, 4),
+            "TFLOP/s": round(tf, 1), "frac_of_%s_bf16_peak" % kind: round(tf / peak, 4)}
+
+
 def time_e2e(w: wl.Workload, steps: int, warmup: int, torch, rws, stream, staged: bool):
     """softmax_rows_host on pinned host buffers, timed over `steps` calls.
 
@@ -538,6 +580,10 @@ def run_ours(args):
         per["causal_bf16_mask_from_indices"] = fused_causal_entry(torch, rws, stream, l2_bytes,
                                                                   peak)
         per["backward_f32_4096x4096"] = backward_entry(torch, rws, stream, l2_bytes, peak)
+        per["attention_bf16_64x4096x4096_d128"] = attention_entry(torch, rws, stream)
+        per["attention_bf16_64x4096x4096_d128_causal"] = attention_entry(torch, rws, stream,
+                                                                         causal=True)
+        per["attention_bf16_64x4096x4096_d64"] = attention_entry(torch, rws, stream, d=64)
         per["columns_f32_4096x4096"] = columns_entry(torch, rws, stream, l2_bytes, peak)
         per["columns_bf16_8192x4096"] = columns_entry(torch, rws, stream, l2_bytes, peak,
                                                       8192, 4096, wl.BF16)

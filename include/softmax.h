@@ -172,6 +172,49 @@ int64_t softmax_visible_cols(const softmax_options_t* options, int64_t n_rows, i
                              int64_t row);
 
 /*
+ * Attention with the row softmax inside it ("Triton GPU programming deep
+ * dive", section 3.1: softmax(Q K^T / sqrt(d)) V; section 3.3: the same one
+ * tile of keys at a time with a running max and sum, keys past the query
+ * masked).  The scores never reach memory.
+ *
+ *   scale          multiplies Q K^T before the softmax; 0 < scale <= 2^127.
+ *                  Without options: 1/sqrt(head_dim).
+ *   causal         0: every key.  1: key j is visible to query i iff
+ *                  j <= i + causal_offset (0: the pages' mask; n_k - n_q: a
+ *                  bottom-right aligned mask).  |causal_offset| < 2^62.
+ */
+typedef struct {
+    float scale;
+    int32_t causal;
+    int64_t causal_offset;
+} softmax_attention_options_t;
+
+/*
+ * softmax_attention_forward: O = softmax(scale Q K^T, mask) V for every
+ * (batch, head) pair.
+ *
+ *   q, o   [batch_heads][n_q][head_dim], k, v  [batch_heads][n_k][head_dim],
+ *          dense, device memory, 16-byte aligned, dtype SOFTMAX_BF16 or
+ *          SOFTMAX_F16 (16-bit operands on the tensor cores, fp32 scores,
+ *          softmax and accumulators; the probabilities are rounded to the
+ *          operand type for the P V product).
+ *   lse    optional [batch_heads][n_q] floats: the natural-log logsumexp of
+ *          each query's masked, scaled scores (NULL: not written).
+ *   head_dim 64 or 128.  A query with no visible key (or n_k == 0) gives NaN
+ *          outputs (the softmax of only -inf) and lse = -inf.
+ *   Ownership and asynchrony as for softmax_rows.  o may be q itself; it must
+ *   not otherwise overlap q, k or v.
+ *   Errors: SOFTMAX_ERR_INVALID_ARG (null or misaligned pointers, negative
+ *   sizes, bad options, overlap), SOFTMAX_ERR_UNSUPPORTED (fp32, another
+ *   head_dim, no usable device), SOFTMAX_ERR_CUDA (launch failure).
+ *   batch_heads == 0 or n_q == 0: no-op.
+ */
+int softmax_attention_forward(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int64_t batch_heads, int64_t n_q, int64_t n_k, int64_t head_dim,
+                              int dtype, const softmax_attention_options_t* options,
+                              void* stream);
+
+/*
  * softmax_strided: the softmax of rows whose elements are not contiguous.
  * Element c of row r is in[r * in_row_stride + c * in_col_stride] and its
  * result goes to out[r * out_row_stride + c * out_col_stride] (ELEMENTS).

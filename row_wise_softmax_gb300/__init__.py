@@ -23,7 +23,7 @@ __all__ = [
     "SoftmaxError", "DeviceDesc", "Plan", "build", "lib", "library_path",
     "softmax_rows", "softmax_rows_ptr", "softmax_rows_ex_ptr", "softmax_rows_planned_ptr",
     "visible_cols", "softmax_backward", "softmax_backward_rows_ptr", "softmax",
-    "softmax_strided_ptr",
+    "softmax_strided_ptr", "attention", "attention_forward_ptr", "AttentionOptions",
     "Options", "softmax_rows_host", "plan", "plan_for_device",
     "status_string", "device_status", "launch_count", "selftest_wait_timeout", "abi_version", "GB300",
 ]
@@ -55,6 +55,11 @@ class DeviceDesc(ctypes.Structure):
 class Options(ctypes.Structure):
     _fields_ = [("scale", ctypes.c_float), ("causal", ctypes.c_int32),
                 ("causal_period", ctypes.c_int64), ("causal_offset", ctypes.c_int64)]
+
+
+class AttentionOptions(ctypes.Structure):
+    _fields_ = [("scale", ctypes.c_float), ("causal", ctypes.c_int32),
+                ("causal_offset", ctypes.c_int64)]
 
 
 class Plan(ctypes.Structure):
@@ -109,6 +114,9 @@ def lib() -> ctypes.CDLL:
         L.softmax_rows_ex.argtypes = [vp, vp, i64, i64, i64, i64, ci, ctypes.POINTER(Options), ci,
                                       vp]
         L.softmax_rows_ex.restype = ci
+        L.softmax_attention_forward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ci,
+                                                ctypes.POINTER(AttentionOptions), vp]
+        L.softmax_attention_forward.restype = ci
         L.softmax_strided.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64, ci, vp]
         L.softmax_strided.restype = ci
         L.softmax_backward_rows.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, ci, vp]
@@ -178,6 +186,43 @@ def softmax_rows_ex_ptr(in_ptr: int, out_ptr: int, n_rows: int, n_cols: int, in_
     o = Options(scale, 1 if causal else 0, causal_period, causal_offset)
     return lib().softmax_rows_ex(in_ptr, out_ptr, n_rows, n_cols, in_row_stride, out_row_stride,
                                  dtype, ctypes.byref(o), path, stream)
+
+
+def attention_forward_ptr(q: int, k: int, v: int, o: int, lse: int, batch_heads: int, n_q: int,
+                          n_k: int, head_dim: int, dtype: int, scale: float | None = None,
+                          causal: bool = False, causal_offset: int = 0, stream: int = 0) -> int:
+    """C ABI call of the attention forward; returns the status."""
+    opt = None
+    if scale is not None or causal or causal_offset:
+        sc = scale if scale is not None else 1.0 / (head_dim ** 0.5)
+        opt = ctypes.byref(AttentionOptions(sc, 1 if causal else 0, causal_offset))
+    return lib().softmax_attention_forward(q, k, v, o, lse or None, batch_heads, n_q, n_k,
+                                           head_dim, dtype, opt, stream)
+
+
+def attention(q, k, v, scale: float | None = None, causal: bool = False, causal_offset: int = 0,
+              return_lse: bool = False, stream=None):
+    """softmax(scale q k^T, causal mask) v for CUDA tensors [..., n, head_dim]
+    (bf16 or fp16, contiguous; leading dimensions are batch and heads)."""
+    import torch
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous() or t.dim() < 2:
+            raise ValueError("attention: q, k, v must be contiguous CUDA tensors [..., n, d]")
+    if q.dtype != k.dtype or q.dtype != v.dtype or k.shape != v.shape or \
+            q.shape[:-2] != k.shape[:-2] or q.shape[-1] != k.shape[-1]:
+        raise ValueError("attention: shapes or dtypes do not match")
+    d, n_q, n_k = q.shape[-1], q.shape[-2], k.shape[-2]
+    bh = q.numel() // max(n_q * d, 1) if q.numel() else 0
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device) if return_lse else None
+    with torch.cuda.device(q.device):
+        st = attention_forward_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr() if lse is not None else 0, bh, n_q, n_k, d,
+                                   _dtype_code(q), scale, causal, causal_offset,
+                                   _stream_handle(stream, q.device))
+    if st != OK:
+        raise SoftmaxError(st, "attention")
+    return (o, lse) if return_lse else o
 
 
 def softmax_strided_ptr(in_ptr: int, out_ptr: int, n_rows: int, n_cols: int, in_row_stride: int,

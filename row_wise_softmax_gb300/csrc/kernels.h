@@ -160,6 +160,22 @@ constexpr int64_t kColumnsMaxCluster = 16;
 ColumnsShape columns_shape(const StridedProblem& p, int max_smem_per_block);
 cudaError_t launch_strided(const StridedProblem& p, const ColumnsShape& sh, cudaStream_t s);
 
+// Attention forward (attention_mma.cu): O = softmax(scale Q K^T, mask) V per
+// (batch, head); q, o [bh][n_q][head_dim], k, v [bh][n_k][head_dim], 16-bit.
+struct AttentionProblem {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* o;
+    float* lse;                 // [bh][n_q] natural-log logsumexp, or null
+    int64_t bh, n_q, n_k, head_dim;
+    int dtype;
+    float scale;
+    int causal;
+    int64_t offset;             // key j visible to query i iff j <= i + offset
+};
+cudaError_t launch_attention_mma(const AttentionProblem& p, cudaStream_t s);
+
 // Launchers, one per path (each in its own translation unit).
 cudaError_t launch_warp_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);
 cudaError_t launch_tile_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);

@@ -4,6 +4,8 @@
 // library allocates no memory.
 #include "kernels.h"
 
+#include <cmath>
+
 #include <atomic>
 #include <cstdio>
 #include <cstring>
@@ -287,6 +289,65 @@ int64_t softmax_visible_cols(const softmax_options_t* options, int64_t n_rows, i
     if (rwsm::apply_options(options, &p) != SOFTMAX_OK)
         return -1;
     return rwsm::logits_valid(rwsm::logits_of(p), row, n_cols);
+}
+
+int softmax_attention_forward(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int64_t batch_heads, int64_t n_q, int64_t n_k, int64_t head_dim,
+                              int dtype, const softmax_attention_options_t* options, void* stream)
+{
+    if (batch_heads < 0 || n_q < 0 || n_k < 0 || head_dim < 0)
+        return SOFTMAX_ERR_INVALID_ARG;
+    if (dtype != SOFTMAX_F32 && dtype != SOFTMAX_BF16 && dtype != SOFTMAX_F16)
+        return SOFTMAX_ERR_INVALID_ARG;
+    float scale = head_dim > 0 ? static_cast<float>(1.0 / std::sqrt(static_cast<double>(head_dim)))
+                               : 1.0f;
+    int causal = 0;
+    int64_t offset = 0;
+    if (options) {
+        if (!(options->scale > 0.0f) || !(options->scale <= 0x1p127f))
+            return SOFTMAX_ERR_INVALID_ARG;
+        if (options->causal != 0 && options->causal != 1)
+            return SOFTMAX_ERR_INVALID_ARG;
+        const int64_t big = int64_t{1} << 62;
+        if (options->causal_offset >= big || options->causal_offset <= -big)
+            return SOFTMAX_ERR_INVALID_ARG;
+        scale = options->scale;
+        causal = options->causal;
+        offset = options->causal_offset;
+    }
+    if (batch_heads == 0 || n_q == 0)
+        return SOFTMAX_OK;
+    if (dtype == SOFTMAX_F32 || (head_dim != 64 && head_dim != 128))
+        return SOFTMAX_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !o)
+        return SOFTMAX_ERR_INVALID_ARG;
+    auto a16 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
+    if (!a16(q) || !a16(k) || !a16(v) || !a16(o) || (lse && reinterpret_cast<uintptr_t>(lse) % 4))
+        return SOFTMAX_ERR_INVALID_ARG;
+    // Sizes: every extent in bytes must fit comfortably in int64.
+    const int64_t lim = INT64_MAX / 4;
+    if (n_q > lim / head_dim / batch_heads || (n_k > 0 && n_k > lim / head_dim / batch_heads))
+        return SOFTMAX_ERR_INVALID_ARG;
+    const uintptr_t o0 = reinterpret_cast<uintptr_t>(o);
+    const uintptr_t o1 = o0 + static_cast<uintptr_t>(batch_heads * n_q * head_dim * 2);
+    auto hits = [&](const void* p, int64_t n) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+        const uintptr_t e = a + static_cast<uintptr_t>(batch_heads * n * head_dim * 2);
+        return a < o1 && o0 < e;
+    };
+    if ((q != o && hits(q, n_q)) || hits(k, n_k) || hits(v, n_k))
+        return SOFTMAX_ERR_INVALID_ARG;            // o may be q itself, nothing else
+    softmax_device_desc_t d;
+    const int ds = rwsm::current_device(&d);
+    if (ds != SOFTMAX_OK)
+        return ds;
+    const rwsm::AttentionProblem p{q, k, v, o, lse, batch_heads, n_q, n_k, head_dim, dtype,
+                                   scale, causal, offset};
+    if (rwsm::launch_attention_mma(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return SOFTMAX_ERR_CUDA;
+    }
+    return SOFTMAX_OK;
 }
 
 int softmax_strided(const void* in, void* out, int64_t n_rows, int64_t n_cols,

@@ -214,3 +214,16 @@ def backward_pair(n_rows: int = 4096, n_cols: int = 4096, dtype: int = F32, seed
     if dtype == F16:
         return _f32_to_f16_bits(y), _f32_to_f16_bits(g)
     return y, g
+
+
+def attention_inputs(bh: int, n_q: int, n_k: int, d: int, dtype: int = BF16, seed: int = 7,
+                     scale: float = 1.0):
+    """Q [bh, n_q, d], K and V [bh, n_k, d] with N(0, scale^2) entries, as
+    16-bit bit patterns (uint16) of the dtype."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for n in (n_q, n_k, n_k):
+        x = (rng.standard_normal((bh, n, d), dtype=np.float32) * np.float32(scale)).reshape(-1)
+        bits = _f32_to_bf16_bits(x) if dtype == BF16 else _f32_to_f16_bits(x)
+        out.append(np.ascontiguousarray(bits).reshape(bh, n, d))
+    return out
