@@ -374,7 +374,8 @@ def tensor_peak():
         return 1900.0, "fallback"
 
 
-def attention_entry(torch, rws, stream, bh=64, n=4096, d=128, causal=False, dtype=wl.BF16):
+def attention_entry(torch, rws, stream, bh=64, n=4096, d=128, causal=False, dtype=wl.BF16,
+                    impl=0):
     """softmax_attention_forward on seeded N(0,1) inputs: the (m, l) recurrence
     inside attention; FLOPs 4 * bh * n * n * d (halved with the causal mask)."""
     qb, kb, vb = wl.attention_inputs(bh, n, n, d, dtype, seed=21)
@@ -382,7 +383,7 @@ def attention_entry(torch, rws, stream, bh=64, n=4096, d=128, causal=False, dtyp
     tq, tk, tv = (torch.from_numpy(a.view(np.int16)).cuda().view(dt) for a in (qb, kb, vb))
     to = torch.empty_like(tq)
     call = rws.lib().softmax_attention_forward
-    opt = rws.AttentionOptions(1.0 / (d ** 0.5), 1 if causal else 0, 0)
+    opt = rws.AttentionOptions(1.0 / (d ** 0.5), 1 if causal else 0, 0, impl)
     import ctypes
     args = (tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), to.data_ptr(), None, bh, n, n, d, dtype,
             ctypes.byref(opt), stream.cuda_stream)
@@ -403,7 +404,9 @@ def attention_entry(torch, rws, stream, bh=64, n=4096, d=128, causal=False, dtyp
     peak, kind = tensor_peak()
     return {"shape": {"batch_heads": bh, "n_q": n, "n_k": n, "head_dim": d},
             "dtype": DTYPE_NAMES[dtype], "causal": causal,
-            "kernel": "attention_mma_kernel (mma.sync m16n8k16)", "mean_ms": round(ms, 4),
+            "kernel": ("attention_mma_kernel (mma.sync m16n8k16)" if impl == 1 else
+                       "attention_tc_kernel (tcgen05.mma, TMEM accumulators)"),
+            "mean_ms": round(ms, 4),
             "TFLOP/s": round(tf, 1), "frac_of_%s_bf16_peak" % kind: round(tf / peak, 4)}
 
 
@@ -580,10 +583,13 @@ def run_ours(args):
         per["causal_bf16_mask_from_indices"] = fused_causal_entry(torch, rws, stream, l2_bytes,
                                                                   peak)
         per["backward_f32_4096x4096"] = backward_entry(torch, rws, stream, l2_bytes, peak)
-        per["attention_bf16_64x4096x4096_d128"] = attention_entry(torch, rws, stream)
-        per["attention_bf16_64x4096x4096_d128_causal"] = attention_entry(torch, rws, stream,
-                                                                         causal=True)
-        per["attention_bf16_64x4096x4096_d64"] = attention_entry(torch, rws, stream, d=64)
+        for impl, tag in ((2, "tcgen05"), (1, "mma_sync")):
+            per["attention_%s_bf16_64x4096x4096_d128" % tag] = attention_entry(
+                torch, rws, stream, impl=impl)
+            per["attention_%s_bf16_64x4096x4096_d128_causal" % tag] = attention_entry(
+                torch, rws, stream, causal=True, impl=impl)
+            per["attention_%s_bf16_64x4096x4096_d64" % tag] = attention_entry(
+                torch, rws, stream, d=64, impl=impl)
         per["columns_f32_4096x4096"] = columns_entry(torch, rws, stream, l2_bytes, peak)
         per["columns_bf16_8192x4096"] = columns_entry(torch, rws, stream, l2_bytes, peak,
                                                       8192, 4096, wl.BF16)

@@ -24,6 +24,7 @@ __all__ = [
     "softmax_rows", "softmax_rows_ptr", "softmax_rows_ex_ptr", "softmax_rows_planned_ptr",
     "visible_cols", "softmax_backward", "softmax_backward_rows_ptr", "softmax",
     "softmax_strided_ptr", "attention", "attention_forward_ptr", "AttentionOptions",
+    "ATT_AUTO", "ATT_MMA", "ATT_TCGEN05",
     "Options", "softmax_rows_host", "plan", "plan_for_device",
     "status_string", "device_status", "launch_count", "selftest_wait_timeout", "abi_version", "GB300",
 ]
@@ -59,7 +60,10 @@ class Options(ctypes.Structure):
 
 class AttentionOptions(ctypes.Structure):
     _fields_ = [("scale", ctypes.c_float), ("causal", ctypes.c_int32),
-                ("causal_offset", ctypes.c_int64)]
+                ("causal_offset", ctypes.c_int64), ("impl", ctypes.c_int32)]
+
+
+ATT_AUTO, ATT_MMA, ATT_TCGEN05 = 0, 1, 2
 
 
 class Plan(ctypes.Structure):
@@ -190,18 +194,20 @@ def softmax_rows_ex_ptr(in_ptr: int, out_ptr: int, n_rows: int, n_cols: int, in_
 
 def attention_forward_ptr(q: int, k: int, v: int, o: int, lse: int, batch_heads: int, n_q: int,
                           n_k: int, head_dim: int, dtype: int, scale: float | None = None,
-                          causal: bool = False, causal_offset: int = 0, stream: int = 0) -> int:
-    """C ABI call of the attention forward; returns the status."""
+                          causal: bool = False, causal_offset: int = 0, stream: int = 0,
+                          impl: int = 0) -> int:
+    """C ABI call of the attention forward; returns the status.  ``impl``:
+    0 the library's choice, 1 the mma.sync kernel, 2 the tcgen05 kernel."""
     opt = None
-    if scale is not None or causal or causal_offset:
+    if scale is not None or causal or causal_offset or impl:
         sc = scale if scale is not None else 1.0 / (head_dim ** 0.5)
-        opt = ctypes.byref(AttentionOptions(sc, 1 if causal else 0, causal_offset))
+        opt = ctypes.byref(AttentionOptions(sc, 1 if causal else 0, causal_offset, impl))
     return lib().softmax_attention_forward(q, k, v, o, lse or None, batch_heads, n_q, n_k,
                                            head_dim, dtype, opt, stream)
 
 
 def attention(q, k, v, scale: float | None = None, causal: bool = False, causal_offset: int = 0,
-              return_lse: bool = False, stream=None):
+              return_lse: bool = False, stream=None, impl: int = 0):
     """softmax(scale q k^T, causal mask) v for CUDA tensors [..., n, head_dim]
     (bf16 or fp16, contiguous; leading dimensions are batch and heads)."""
     import torch
@@ -219,7 +225,7 @@ def attention(q, k, v, scale: float | None = None, causal: bool = False, causal_
         st = attention_forward_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                    lse.data_ptr() if lse is not None else 0, bh, n_q, n_k, d,
                                    _dtype_code(q), scale, causal, causal_offset,
-                                   _stream_handle(stream, q.device))
+                                   _stream_handle(stream, q.device), impl)
     if st != OK:
         raise SoftmaxError(st, "attention")
     return (o, lse) if return_lse else o

@@ -20,7 +20,7 @@ LIB = os.path.join(PKG, "libsoftmax.so")
 
 SOURCES = ["softmax_abi.cu", "plan.cpp", "warp_rows.cu", "tile_rows.cu", "row_slices.cu",
            "row_slices_options.cu", "twopass.cu", "stream_rows.cu", "backward_rows.cu",
-           "columns.cu", "attention_mma.cu"]
+           "columns.cu", "attention_mma.cu", "attention_tc.cu"]
 # Sources that include another source file.
 INCLUDED = {"row_slices_options.cu": ["row_slices.cu"]}
 HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "kernels.h")] + [

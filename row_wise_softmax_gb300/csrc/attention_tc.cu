@@ -1,0 +1,486 @@
+// Attention forward on the fifth-generation tensor cores (tcgen05, sm_100
+// family): the same online softmax as attention_mma.cu ("Triton GPU
+// programming deep dive", section 3.3), with both products issued by one
+// thread as tcgen05.mma and accumulated in tensor memory (TMEM).
+//
+//   CTA      128 queries of one (batch, head), 4 warps; thread t of warp w
+//            owns query row 32w + t, which is TMEM lane 32w + t of every
+//            accumulator.
+//   TMEM     256 columns: S (128 keys) at column 0, O (head_dim) at 128.
+//   staging  Q once, K and V tiles of 128 keys by cp.async, double-buffered
+//            (the next tile loads while this one is computed), written in the
+//            tensor cores' canonical layout without swizzle: 8 x 8 "core
+//            matrices" of 128 contiguous bytes.  Q, K and P are K-major (rows
+//            of 8 elements along the reduced dimension in a core matrix);
+//            V is the B operand of P V with its rows along N = head_dim, i.e.
+//            MN-major.
+//   per tile S = Q K^T (head_dim / 16 MMAs of 128 x 128 x 16), committed to
+//            an mbarrier; each thread loads its S row from TMEM, masks it,
+//            updates its running max m and sum l (base-2 domain), writes its
+//            row of P (16-bit) to shared memory in the canonical layout and
+//            rescales its O row in TMEM by 2^(m_old - m_new); then
+//            O += P V (128 / 16 MMAs of 128 x head_dim x 16), committed to a
+//            second mbarrier.
+//   output   O / l from TMEM, and the natural-log logsumexp per query.
+//
+// Every mbarrier wait is bounded; on a timeout the kernel records the error
+// word, stops issuing, waits (bounded) for what it issued and frees TMEM.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace rwsm {
+
+__device__ unsigned g_error_attention_tc = 0;
+
+namespace {
+
+constexpr int kTcBM = 128;          // queries per CTA (MMA M)
+constexpr int kTcBN = 128;          // keys per tile (MMA N of S, K of P V)
+constexpr int kTcThreads = 128;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemO = 128;    // column of the O accumulator
+
+// ---- tcgen05 wrappers -----------------------------------------------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(dst_smem), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                 :: "r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, 16-bit operands, fp32 accumulators.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// Arrive once on the mbarrier when every tcgen05 operation this thread has
+// issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive TMEM columns of this thread's lane (warp w reads lanes
+// 32w..32w+31; `taddr` carries the lane in bits 31..16, the column below).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
+          "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]),
+          "=f"(v[13]), "=f"(v[14]), "=f"(v[15]), "=f"(v[16]), "=f"(v[17]), "=f"(v[18]),
+          "=f"(v[19]), "=f"(v[20]), "=f"(v[21]), "=f"(v[22]), "=f"(v[23]), "=f"(v[24]),
+          "=f"(v[25]), "=f"(v[26]), "=f"(v[27]), "=f"(v[28]), "=f"(v[29]), "=f"(v[30]),
+          "=f"(v[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+        :: "r"(taddr), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]),
+           "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]),
+           "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]),
+           "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]),
+           "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld()
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---- operand layouts and descriptors ---------------------------------------
+//
+// Canonical layout without swizzle: the matrix is cut into 8 x 8 core
+// matrices of 16-bit elements, each 128 contiguous bytes (8 rows of 16
+// bytes).  For a K-major operand a core-matrix row holds 8 consecutive K
+// elements of one M (or N) row; the core matrix of rows 8i.. and K elements
+// 8j.. starts at i * SBO + j * LBO.  For an MN-major operand a core-matrix
+// row holds 8 consecutive MN elements of one K row; the core matrix of MN
+// elements 8i.. and K rows 8j.. starts at i * SBO + j * LBO.  Here LBO is
+// always 128 bytes (core matrices adjacent along K) and SBO the size of one
+// 8-row band.
+
+// Byte offset of the 16-byte chunk holding elements [8c, 8c + 8) of row r of
+// a K-major operand with `kdim` elements per row.
+__device__ __forceinline__ uint32_t kmajor_off(int r, int c, int kdim)
+{
+    return static_cast<uint32_t>((r >> 3) * (kdim / 8) * 128 + c * 128 + (r & 7) * 16);
+}
+
+// Byte offset of the 16-byte chunk holding MN elements [8c, 8c + 8) of K row
+// `kr` of an MN-major operand with `kdim` K rows.
+__device__ __forceinline__ uint32_t mnmajor_off(int kr, int c, int kdim)
+{
+    return static_cast<uint32_t>(c * (kdim / 8) * 128 + (kr >> 3) * 128 + (kr & 7) * 16);
+}
+
+// Shared-memory matrix descriptor: start address, leading (K direction) and
+// stride (8-row band) byte offsets, each in units of 16 bytes; descriptor
+// version 1 at bits 46..47; no swizzle (layout type 0 at bits 61..63).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) |
+           (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) |
+           (static_cast<uint64_t>(1) << 46);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator (bits 4..5 = 1), A
+// and B formats (bits 7..9, 10..12: 0 fp16, 1 bf16), B MN-major flag (bit 16),
+// N / 8 (bits 17..22), M / 16 (bits 24..28); A is K-major.
+__host__ __device__ constexpr uint32_t umma_idesc(int m, int n, bool bf16, bool b_mn_major)
+{
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+           ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// 16-byte global -> shared copy; src_bytes 0 fills the 16 bytes with zeros.
+__device__ __forceinline__ void cp16(uint32_t dst, const void* src, int src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                 :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+// Rows [row0, row0 + ROWS) of a [n][D] matrix into shared memory, K-major
+// (MN_MAJOR = false: rows are M/N, elements along K) or as the MN-major B
+// operand with the rows as K (MN_MAJOR = true).  Rows past n are zero.
+template <int D, int ROWS, bool MN_MAJOR>
+__device__ __forceinline__ void stage(uint32_t base, const unsigned short* g, int64_t row0,
+                                      int64_t n, int tid)
+{
+    constexpr int CH = D / 8;
+    for (int i = tid; i < ROWS * CH; i += kTcThreads) {
+        const int r = i / CH, c = i % CH;
+        const int64_t gr = row0 + r;
+        const bool ok = gr < n;
+        const uint32_t off = MN_MAJOR ? mnmajor_off(r, c, ROWS) : kmajor_off(r, c, D);
+        cp16(base + off, g + (ok ? gr : 0) * D + c * 8, ok ? 16 : 0);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <typename T, int D, int BN, bool CAUSAL>
+__global__ void __launch_bounds__(kTcThreads, 1)
+attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_t bh,
+                    int64_t n_q, int64_t n_k, float scale_log2, int64_t offset)
+{
+    constexpr bool kBF16 = sizeof(T) == 2 && Elem<T>::kNegInfBits == 0xff80u;
+    constexpr uint32_t Q_BYTES = kTcBM * D * 2, KV_BYTES = BN * D * 2, P_BYTES = kTcBM * BN * 2;
+    constexpr uint32_t SBO_QK = (D / 8) * 128;              // 8-row band of Q, K
+    constexpr uint32_t SBO_P = (BN / 8) * 128;              // 8-row band of P
+    constexpr uint32_t SBO_V = (BN / 8) * 128;              // 8-column band of V
+    constexpr uint32_t IDESC_S = umma_idesc(kTcBM, BN, kBF16, false);
+    constexpr uint32_t IDESC_PV = umma_idesc(kTcBM, D, kBF16, true);
+    constexpr int NCH = BN / 32;                             // 32-column S chunks
+    extern __shared__ __align__(1024) unsigned char tc_smem[];
+    __shared__ __align__(8) unsigned long long bar_s, bar_o;
+    __shared__ uint32_t tmem_slot;
+
+    const uint32_t base = (smem_addr(tc_smem) + 1023u) & ~1023u;
+    const uint32_t sQ = base, sK = sQ + Q_BYTES, sV = sK + 2 * KV_BYTES, sP = sV + 2 * KV_BYTES;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int64_t n_qt = (n_q + kTcBM - 1) / kTcBM;
+    const int64_t b = blockIdx.x / n_qt;
+    int64_t qt = blockIdx.x % n_qt;
+    if (CAUSAL)
+        qt = n_qt - 1 - qt;
+    const int64_t q0 = qt * kTcBM, qi = q0 + tid;            // this thread's query
+    const unsigned short* gq = reinterpret_cast<const unsigned short*>(q) + b * n_q * D;
+    const unsigned short* gk = reinterpret_cast<const unsigned short*>(k) + b * n_k * D;
+    const unsigned short* gv = reinterpret_cast<const unsigned short*>(v) + b * n_k * D;
+    int64_t n_kt = (n_k + BN - 1) / BN;
+    if (CAUSAL) {
+        const int64_t last = q0 + kTcBM - 1 + offset;
+        const int64_t lim = last < 0 ? 0 : last / BN + 1;
+        n_kt = lim < n_kt ? lim : n_kt;
+    }
+
+    if (warp == 0) {
+        tmem_alloc(smem_addr(&tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(smem_addr(&bar_s), 1);
+        mbar_init(smem_addr(&bar_o), 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);   // this warp's lanes
+
+    pdl_launch_dependents();
+    pdl_wait();
+    stage<D, kTcBM, false>(sQ, gq, q0, n_q, tid);
+    if (n_kt > 0) {
+        stage<D, BN, false>(sK, gk, 0, n_k, tid);
+        stage<D, BN, true>(sV, gv, 0, n_k, tid);
+    }
+
+    float m = kNegInf, l = 0.0f;
+    bool failed = false;
+    uint32_t issued_s = 0, issued_o = 0;                      // commits to bar_s, bar_o
+    for (int64_t t = 0; t < n_kt; ++t) {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        fence_proxy_async_smem();                            // copies -> tensor cores
+        __syncthreads();
+        if (t + 1 < n_kt) {                                  // prefetch the next tile
+            const uint32_t nb = static_cast<uint32_t>((t + 1) & 1);
+            stage<D, BN, false>(sK + nb * KV_BYTES, gk, (t + 1) * BN, n_k, tid);
+            stage<D, BN, true>(sV + nb * KV_BYTES, gv, (t + 1) * BN, n_k, tid);
+        }
+        const uint32_t cK = sK + static_cast<uint32_t>(t & 1) * KV_BYTES;
+        const uint32_t cV = sV + static_cast<uint32_t>(t & 1) * KV_BYTES;
+
+        // ---- S = Q K^T into TMEM columns [0, BN)
+        if (tid == 0 && !failed) {
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                umma_f16(tmem, smem_desc(sQ + ks * 256, 128, SBO_QK),
+                         smem_desc(cK + ks * 256, 128, SBO_QK), IDESC_S, ks > 0 ? 1u : 0u);
+            umma_commit(smem_addr(&bar_s));
+        }
+        ++issued_s;
+        const bool ok_s = failed ? false : mbar_wait_bounded(smem_addr(&bar_s), t & 1);
+        failed = __syncthreads_or(!ok_s) != 0;
+        if (failed)
+            break;
+        tc_fence_after();
+
+        // ---- this thread's S row: mask, running max, p, P row to shared memory
+        const int64_t k0 = t * BN;
+        float mx = kNegInf;
+        float sv[NCH][32];
+#pragma unroll
+        for (int c = 0; c < NCH; ++c)
+            tmem_ld32(t_row + c * 32, sv[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                float x = sv[c][j] * scale_log2;
+                const int64_t key = k0 + c * 32 + j;
+                if (key >= n_k || (CAUSAL && key > qi + offset))
+                    x = kNegInf;
+                sv[c][j] = x;
+                mx = fmaxf(mx, x);
+            }
+        }
+        const float mn = fmaxf(m, mx);
+        const float ref = mn == kNegInf ? 0.0f : mn;
+        const float alpha = ex2_ftz(m - ref);
+        m = mn;
+        float sum = 0.0f;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {                    // 8 keys per 16-byte chunk
+                float p[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    p[e] = ex2_ftz(sv[c][g * 8 + e] - ref);
+                    sum += p[e];
+                }
+                const uint32_t w0 = Elem<T>::pack2(p[0], p[1]), w1 = Elem<T>::pack2(p[2], p[3]);
+                const uint32_t w2 = Elem<T>::pack2(p[4], p[5]), w3 = Elem<T>::pack2(p[6], p[7]);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                             :: "r"(sP + kmajor_off(tid, c * 4 + g, BN)), "r"(w0), "r"(w1),
+                                "r"(w2), "r"(w3) : "memory");
+            }
+        }
+        l = l * alpha + sum;
+        // ---- rescale this thread's O row (the previous P V has completed)
+        if (t > 0) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                float ov[32];
+                tmem_ld32(t_row + kTmemO + c * 32, ov);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    ov[j] *= alpha;
+                tmem_st32(t_row + kTmemO + c * 32, ov);
+            }
+            tmem_wait_st();
+        }
+        fence_proxy_async_smem();                            // P -> tensor cores
+        tc_fence_before();
+        __syncthreads();
+
+        // ---- O += P V into TMEM columns [128, 128 + D)
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < BN / 16; ++ks)
+                umma_f16(tmem + kTmemO, smem_desc(sP + ks * 256, 128, SBO_P),
+                         smem_desc(cV + ks * 256, 128, SBO_V), IDESC_PV,
+                         (t > 0 || ks > 0) ? 1u : 0u);
+            umma_commit(smem_addr(&bar_o));
+        }
+        ++issued_o;
+        const bool ok_o = mbar_wait_bounded(smem_addr(&bar_o), t & 1);
+        failed = __syncthreads_or(!ok_o) != 0;
+        if (failed)
+            break;
+        tc_fence_after();
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+
+    if (!failed) {
+        // ---- O / l to global (this thread's row), logsumexp
+        const float inv = 1.0f / l;
+        unsigned short* go = reinterpret_cast<unsigned short*>(o) + b * n_q * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            float ov[32];
+            tmem_ld32(t_row + kTmemO + c * 32, ov);
+            tmem_wait_ld();
+            if (qi < n_q) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    uint4 w;
+                    w.x = Elem<T>::pack2(ov[g * 8 + 0] * inv, ov[g * 8 + 1] * inv);
+                    w.y = Elem<T>::pack2(ov[g * 8 + 2] * inv, ov[g * 8 + 3] * inv);
+                    w.z = Elem<T>::pack2(ov[g * 8 + 4] * inv, ov[g * 8 + 5] * inv);
+                    w.w = Elem<T>::pack2(ov[g * 8 + 6] * inv, ov[g * 8 + 7] * inv);
+                    *reinterpret_cast<uint4*>(go + qi * D + c * 32 + g * 8) = w;
+                }
+            }
+        }
+        if (n_kt == 0 && qi < n_q) {                         // no key at all: NaN rows
+            const float nan = __int_as_float(0x7fc00000);
+            for (int d0 = 0; d0 < D; d0 += 2)
+                *reinterpret_cast<uint32_t*>(go + qi * D + d0) = Elem<T>::pack2(nan, nan);
+        }
+        if (lse && qi < n_q)
+            lse[b * n_q + qi] = l > 0.0f ? (m + __log2f(l)) * 0.69314718055994531f : kNegInf;
+    } else {
+        if (tid == 0) {
+            atomicOr(&g_error_attention_tc, kErrMbarrierTimeout);
+            // Wait (bounded) for what was issued before freeing TMEM.
+            if (issued_s)
+                mbar_wait_bounded(smem_addr(&bar_s), (issued_s - 1) & 1u);
+            if (issued_o)
+                mbar_wait_bounded(smem_addr(&bar_o), (issued_o - 1) & 1u);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0)
+        tmem_dealloc(tmem, kTmemCols);
+}
+
+template <typename T, int D, int BN, bool CAUSAL>
+cudaError_t launch_tc(const AttentionProblem& p, cudaStream_t s)
+{
+    auto* kern = attention_tc_kernel<T, D, BN, CAUSAL>;
+    const int smem = (kTcBM * D + 4 * BN * D + kTcBM * BN) * 2 + 1024;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess)
+            return e;
+        attr_set[dev] = true;
+    }
+    const int64_t n_qt = (p.n_q + kTcBM - 1) / kTcBM;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(n_qt * p.bh), 1, 1);
+    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = static_cast<unsigned>(launch_attrs(attr, 1));
+    const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, kern, static_cast<const T*>(p.q),
+                                               static_cast<const T*>(p.k),
+                                               static_cast<const T*>(p.v), static_cast<T*>(p.o),
+                                               p.lse, p.bh, p.n_q, p.n_k, scale_log2, p.offset);
+    note_launch();
+    return err;
+}
+
+template <typename T, int D>
+cudaError_t launch_tc_d(const AttentionProblem& p, cudaStream_t s)
+{
+    return p.causal ? launch_tc<T, D, 128, true>(p, s) : launch_tc<T, D, 128, false>(p, s);
+}
+
+template <typename T>
+cudaError_t launch_tc_t(const AttentionProblem& p, cudaStream_t s)
+{
+    if (p.head_dim == 64) return launch_tc_d<T, 64>(p, s);
+    if (p.head_dim == 128) return launch_tc_d<T, 128>(p, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_attention_tc(const AttentionProblem& p, cudaStream_t s)
+{
+    if (p.bh * ((p.n_q + kTcBM - 1) / kTcBM) > 0x7fffffff)
+        return cudaErrorInvalidValue;
+    return p.dtype == SOFTMAX_BF16 ? launch_tc_t<BF16Bits>(p, s) : launch_tc_t<F16Bits>(p, s);
+}
+
+unsigned read_error_attention_tc(bool clear)
+{
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_error_attention_tc, sizeof v) != cudaSuccess)
+        return 0;
+    if (clear && v) {
+        const unsigned zero = 0;
+        cudaMemcpyToSymbol(g_error_attention_tc, &zero, sizeof zero);
+    }
+    return v;
+}
+
+}  // namespace rwsm

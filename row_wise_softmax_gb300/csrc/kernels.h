@@ -174,7 +174,9 @@ struct AttentionProblem {
     int causal;
     int64_t offset;             // key j visible to query i iff j <= i + offset
 };
-cudaError_t launch_attention_mma(const AttentionProblem& p, cudaStream_t s);
+cudaError_t launch_attention_mma(const AttentionProblem& p, cudaStream_t s);   // mma.sync
+cudaError_t launch_attention_tc(const AttentionProblem& p, cudaStream_t s);    // tcgen05
+unsigned read_error_attention_tc(bool clear);
 
 // Launchers, one per path (each in its own translation unit).
 cudaError_t launch_warp_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s);

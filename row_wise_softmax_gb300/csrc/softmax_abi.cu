@@ -301,7 +301,7 @@ int softmax_attention_forward(const void* q, const void* k, const void* v, void*
         return SOFTMAX_ERR_INVALID_ARG;
     float scale = head_dim > 0 ? static_cast<float>(1.0 / std::sqrt(static_cast<double>(head_dim)))
                                : 1.0f;
-    int causal = 0;
+    int causal = 0, impl = 0;
     int64_t offset = 0;
     if (options) {
         if (!(options->scale > 0.0f) || !(options->scale <= 0x1p127f))
@@ -311,9 +311,12 @@ int softmax_attention_forward(const void* q, const void* k, const void* v, void*
         const int64_t big = int64_t{1} << 62;
         if (options->causal_offset >= big || options->causal_offset <= -big)
             return SOFTMAX_ERR_INVALID_ARG;
+        if (options->impl < 0 || options->impl > 2)
+            return SOFTMAX_ERR_INVALID_ARG;
         scale = options->scale;
         causal = options->causal;
         offset = options->causal_offset;
+        impl = options->impl;
     }
     if (batch_heads == 0 || n_q == 0)
         return SOFTMAX_OK;
@@ -343,7 +346,9 @@ int softmax_attention_forward(const void* q, const void* k, const void* v, void*
         return ds;
     const rwsm::AttentionProblem p{q, k, v, o, lse, batch_heads, n_q, n_k, head_dim, dtype,
                                    scale, causal, offset};
-    if (rwsm::launch_attention_mma(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    const cudaError_t err = impl == 1 ? rwsm::launch_attention_mma(p, static_cast<cudaStream_t>(stream))
+                                      : rwsm::launch_attention_tc(p, static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) {
         cudaGetLastError();
         return SOFTMAX_ERR_CUDA;
     }
@@ -543,7 +548,8 @@ int softmax_device_status(int clear)
     }
     const unsigned e = rwsm::read_error_row_slices(clear != 0) |
                        rwsm::read_error_tile_rows(clear != 0) |
-                       rwsm::read_error_stream_rows(clear != 0);
+                       rwsm::read_error_stream_rows(clear != 0) |
+                       rwsm::read_error_attention_tc(clear != 0);
     return e ? SOFTMAX_ERR_DEVICE_TIMEOUT : SOFTMAX_OK;
 }
 

@@ -32,7 +32,7 @@ def built():
     rws.lib()
 
 
-def run(bh, n_q, n_k, d, dtype, seed, scale=None, causal=False, offset=0, qscale=1.0):
+def run(bh, n_q, n_k, d, dtype, seed, scale=None, causal=False, offset=0, qscale=1.0, impl=0):
     qb, kb, vb = wl.attention_inputs(bh, n_q, n_k, d, dtype, seed, qscale)
     dt = parity.torch_dtype(dtype)
     tq, tk, tv = (torch.from_numpy(a.view(np.int16)).cuda().view(dt) for a in (qb, kb, vb))
@@ -40,7 +40,8 @@ def run(bh, n_q, n_k, d, dtype, seed, scale=None, causal=False, offset=0, qscale
     lse = torch.full((bh, n_q), 123.0, device="cuda")
     before = rws.launch_count()
     st = rws.attention_forward_ptr(tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), to.data_ptr(),
-                                   lse.data_ptr(), bh, n_q, n_k, d, dtype, scale, causal, offset)
+                                   lse.data_ptr(), bh, n_q, n_k, d, dtype, scale, causal, offset,
+                                   impl=impl)
     assert st == rws.OK, rws.status_string(st)
     torch.cuda.synchronize()
     assert rws.launch_count() - before == 1
@@ -77,23 +78,45 @@ CASES = [  # bh, n_q, n_k, d, causal, offset
 ]
 
 
+IMPLS = [rws.ATT_MMA, rws.ATT_TCGEN05]
+
+
+@pytest.mark.parametrize("impl", IMPLS, ids=["mma_sync", "tcgen05"])
 @pytest.mark.parametrize("dtype", [wl.BF16, wl.F16])
-def test_attention_cases(dtype):
+def test_attention_cases(dtype, impl):
     for i, (bh, n_q, n_k, d, causal, offset) in enumerate(CASES):
-        o, lse, q, k, v = run(bh, n_q, n_k, d, dtype, 40 + i, causal=causal, offset=offset)
+        o, lse, q, k, v = run(bh, n_q, n_k, d, dtype, 40 + i, causal=causal, offset=offset,
+                              impl=impl)
         check(o, lse, q, k, v, dtype, None, causal, offset, "case %d" % i)
 
 
-def test_attention_scale_and_large_scores():
+def test_attention_kernels_agree():
+    """The tcgen05 and mma.sync kernels on the same inputs agree within the
+    P-rounding error bound (both are checked against the oracle elsewhere;
+    their fp32 sums run in different orders): |a - b| <= 2^-7 (1 + |a|) for
+    N(0, 1) values."""
+    for causal in (False, True):
+        a = run(4, 300, 300, 128, wl.BF16, 71, causal=causal, impl=rws.ATT_MMA)[0]
+        b = run(4, 300, 300, 128, wl.BF16, 71, causal=causal, impl=rws.ATT_TCGEN05)[0]
+        assert np.array_equal(np.isnan(a), np.isnan(b))
+        ok = ~np.isnan(a)
+        excess = np.abs(a[ok] - b[ok]) - 2.0 ** -7 * (1.0 + np.abs(a[ok]))
+        assert np.all(excess <= 0), float(excess.max())
+        assert np.mean(a[ok] == b[ok]) > 0.5            # mostly the same bf16 values
+
+
+@pytest.mark.parametrize("impl", IMPLS, ids=["mma_sync", "tcgen05"])
+def test_attention_scale_and_large_scores(impl):
     """An explicit scale, and scores spread over +-100 (queries scaled by 8)."""
-    o, lse, q, k, v = run(2, 64, 256, 64, wl.BF16, 9, scale=0.3, qscale=8.0)
+    o, lse, q, k, v = run(2, 64, 256, 64, wl.BF16, 9, scale=0.3, qscale=8.0, impl=impl)
     check(o, lse, q, k, v, wl.BF16, 0.3, False, 0, "scaled")
 
 
-def test_attention_full_size_sampled():
+@pytest.mark.parametrize("impl", IMPLS, ids=["mma_sync", "tcgen05"])
+def test_attention_full_size_sampled(impl):
     """8 heads x 2048 x 2048, d = 128, causal: sampled query rows of 2 heads."""
     bh, n, d = 8, 2048, 128
-    o, lse, q, k, v = run(bh, n, n, d, wl.BF16, 11, causal=True)
+    o, lse, q, k, v = run(bh, n, n, d, wl.BF16, 11, causal=True, impl=impl)
     rows = np.random.default_rng(2).choice(n, 64, replace=False)
     for b in (0, 5):
         # Causal rows: each sampled query i sees keys 0..i; compare one at a time.
@@ -120,3 +143,4 @@ def test_attention_binding_and_errors():
     assert rws.attention_forward_ptr(q.data_ptr() + 2, k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                      0, 6, 200, 150, 64, wl.BF16) == rws.ERR_INVALID_ARG
     assert rws.launch_count() == before
+    assert rws.device_status(clear=True) == rws.OK
