@@ -6,21 +6,25 @@
 //   CTA      128 queries of one (batch, head), 4 warps; thread t of warp w
 //            owns query row 32w + t, which is TMEM lane 32w + t of every
 //            accumulator.
-//   TMEM     256 columns: S (128 keys) at column 0, O (head_dim) at 128.
-//   staging  Q once, K and V tiles of 128 keys by cp.async, double-buffered
+//   TMEM     256 columns: S (one tile of keys) at column 0, O (head_dim) at
+//            128.
+//   staging  Q once, K and V tiles of 64 keys by cp.async, double-buffered
 //            (the next tile loads while this one is computed), written in the
 //            tensor cores' canonical layout without swizzle: 8 x 8 "core
 //            matrices" of 128 contiguous bytes.  Q, K and P are K-major (rows
 //            of 8 elements along the reduced dimension in a core matrix);
 //            V is the B operand of P V with its rows along N = head_dim, i.e.
 //            MN-major.
-//   per tile S = Q K^T (head_dim / 16 MMAs of 128 x 128 x 16), committed to
+//   per tile S = Q K^T (head_dim / 16 MMAs of 128 x 64 x 16), committed to
 //            an mbarrier; each thread loads its S row from TMEM, masks it,
 //            updates its running max m and sum l (base-2 domain), writes its
 //            row of P (16-bit) to shared memory in the canonical layout and
-//            rescales its O row in TMEM by 2^(m_old - m_new); then
-//            O += P V (128 / 16 MMAs of 128 x head_dim x 16), committed to a
-//            second mbarrier.
+//            rescales its O row in TMEM by 2^(m_old - m_new) (a warp whose
+//            rows all kept their maximum skips it); then O += P V (64 / 16
+//            MMAs of 128 x head_dim x 16), committed to a second mbarrier.
+//   SM       112 KB of shared memory and 256 TMEM columns per CTA at
+//            head_dim 128: two CTAs share an SM, so one's softmax overlaps
+//            the other's tensor-core work.
 //   output   O / l from TMEM, and the natural-log logsumexp per query.
 //
 // Every mbarrier wait is bounded; on a timeout the kernel records the error
@@ -35,7 +39,6 @@ __device__ unsigned g_error_attention_tc = 0;
 namespace {
 
 constexpr int kTcBM = 128;          // queries per CTA (MMA M)
-constexpr int kTcBN = 128;          // keys per tile (MMA N of S, K of P V)
 constexpr int kTcThreads = 128;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kTmemO = 128;    // column of the O accumulator
@@ -201,7 +204,7 @@ __device__ __forceinline__ void stage(uint32_t base, const unsigned short* g, in
 }
 
 template <typename T, int D, int BN, bool CAUSAL>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, BN == 64 ? 2 : 1)
 attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_t bh,
                     int64_t n_q, int64_t n_k, float scale_log2, int64_t offset)
 {
@@ -213,11 +216,11 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
     constexpr uint32_t IDESC_S = umma_idesc(kTcBM, BN, kBF16, false);
     constexpr uint32_t IDESC_PV = umma_idesc(kTcBM, D, kBF16, true);
     constexpr int NCH = BN / 32;                             // 32-column S chunks
-    extern __shared__ __align__(1024) unsigned char tc_smem[];
+    extern __shared__ __align__(128) unsigned char tc_smem[];
     __shared__ __align__(8) unsigned long long bar_s, bar_o;
     __shared__ uint32_t tmem_slot;
 
-    const uint32_t base = (smem_addr(tc_smem) + 1023u) & ~1023u;
+    const uint32_t base = (smem_addr(tc_smem) + 127u) & ~127u;
     const uint32_t sQ = base, sK = sQ + Q_BYTES, sV = sK + 2 * KV_BYTES, sP = sV + 2 * KV_BYTES;
     const int tid = threadIdx.x, warp = tid >> 5;
     const int64_t n_qt = (n_q + kTcBM - 1) / kTcBM;
@@ -333,8 +336,9 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
             }
         }
         l = l * alpha + sum;
-        // ---- rescale this thread's O row (the previous P V has completed)
-        if (t > 0) {
+        // ---- rescale this thread's O row (the previous P V has completed);
+        // skipped by a warp whose rows all kept their maximum (alpha = 1).
+        if (t > 0 && !__all_sync(0xffffffffu, alpha == 1.0f)) {
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 float ov[32];
@@ -418,7 +422,10 @@ template <typename T, int D, int BN, bool CAUSAL>
 cudaError_t launch_tc(const AttentionProblem& p, cudaStream_t s)
 {
     auto* kern = attention_tc_kernel<T, D, BN, CAUSAL>;
-    const int smem = (kTcBM * D + 4 * BN * D + kTcBM * BN) * 2 + 1024;
+    // At most two CTAs per SM (each holds 256 TMEM columns of 512): the
+    // request is at least a third of an SM's shared memory.
+    int smem = (kTcBM * D + 4 * BN * D + kTcBM * BN) * 2 + 128;
+    smem = smem < 80 * 1024 ? 80 * 1024 : smem;
     static bool attr_set[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
@@ -451,7 +458,9 @@ cudaError_t launch_tc(const AttentionProblem& p, cudaStream_t s)
 template <typename T, int D>
 cudaError_t launch_tc_d(const AttentionProblem& p, cudaStream_t s)
 {
-    return p.causal ? launch_tc<T, D, 128, true>(p, s) : launch_tc<T, D, 128, false>(p, s);
+    // 64-key tiles: 112 KB of shared memory at d = 128, so two CTAs share an
+    // SM and one's softmax overlaps the other's tensor-core work.
+    return p.causal ? launch_tc<T, D, 64, true>(p, s) : launch_tc<T, D, 64, false>(p, s);
 }
 
 template <typename T>
