@@ -7,11 +7,11 @@
 //                 registers (VEC-wide loads at columns (c*32 + lane)*VEC), the
 //                 dot product reduced with __shfl_xor, dx stored from the same
 //                 registers.  Persistent grid, warps stride over rows.
-//   CTA kernel    longer rows: one CTA per row.  A row of up to
-//                 THREADS * NV * VEC elements stays in registers (one HBM
-//                 pass); a longer row is streamed twice, the first pass
-//                 computing the dot product with its loads kept in L2
-//                 (evict_last), the second reading them back for dx.
+//   CTA kernel    longer rows: one CTA of 512 threads per row.  A row of up
+//                 to THREADS * NV * VEC = 8192 elements stays in registers
+//                 (one HBM pass); a longer row is streamed twice, the first
+//                 pass computing the dot product, the second reading y and
+//                 dy again (mostly from L2) for dx.
 //
 // Both read y and dy through the same masked vector loads as the forward
 // kernels (element loads when a row is not 16-byte aligned).
@@ -199,8 +199,10 @@ cudaError_t launch_warp(const BackwardProblem& p, cudaStream_t s)
 template <typename T, int VEC>
 cudaError_t launch_cta(const BackwardProblem& p, cudaStream_t s)
 {
-    constexpr int THREADS = 256;
-    constexpr int NV = 32 / VEC > 8 ? 8 : 32 / VEC;           // up to 32 elements a thread
+    // 512 threads x 16 elements: 4 CTAs of 16 warps per SM (a row in flight
+    // per CTA, so resident warps hide the load latency).
+    constexpr int THREADS = 512;
+    constexpr int NV = 16 / VEC > 8 ? 8 : 16 / VEC;           // up to 16 elements a thread
     auto* k = backward_cta_kernel<T, THREADS, VEC, NV>;
     return launch_pdl(k, persistent_grid(k, THREADS, p.n_rows), THREADS, s,
                       static_cast<const T*>(p.y), static_cast<const T*>(p.dy),
