@@ -28,6 +28,8 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <atomic>
+
 namespace rwsm {
 
 namespace {
@@ -298,16 +300,16 @@ cudaError_t launch_att(const AttentionProblem& p, cudaStream_t s)
 {
     auto* kern = attention_mma_kernel<T, D, CAUSAL>;
     const int smem = (kAttBM + 4 * kAttBN) * D * 2;
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
+    if (!attr_set[dev].load()) {
         const cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return e;
-        attr_set[dev] = true;
+        attr_set[dev].store(true);
     }
     const int64_t n_qt = (p.n_q + kAttBM - 1) / kAttBM;
     cudaLaunchAttribute attr[2];

@@ -32,6 +32,8 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <atomic>
+
 namespace rwsm {
 
 __device__ unsigned g_error_attention_tc = 0;
@@ -426,16 +428,16 @@ cudaError_t launch_tc(const AttentionProblem& p, cudaStream_t s)
     // request is at least a third of an SM's shared memory.
     int smem = (kTcBM * D + 4 * BN * D + kTcBM * BN) * 2 + 128;
     smem = smem < 80 * 1024 ? 80 * 1024 : smem;
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
+    if (!attr_set[dev].load()) {
         const cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return e;
-        attr_set[dev] = true;
+        attr_set[dev].store(true);
     }
     const int64_t n_qt = (p.n_q + kTcBM - 1) / kTcBM;
     cudaLaunchAttribute attr[2];
