@@ -187,6 +187,18 @@ __device__ __forceinline__ void cp16(uint32_t dst, const void* src, int src_byte
                  :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 
+// Wait until at most n (0, 1 or 2) of this thread's cp.async groups are
+// still pending (the most recent ones).
+__device__ __forceinline__ void cp_async_wait_pending(int n)
+{
+    if (n <= 0)
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+    else if (n == 1)
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else
+        asm volatile("cp.async.wait_group 2;" ::: "memory");
+}
+
 // Rows [row0, row0 + ROWS) of a [n][D] matrix into shared memory, K-major
 // (MN_MAJOR = false: rows are M/N, elements along K) or as the MN-major B
 // operand with the rows as K (MN_MAJOR = true).  Rows past n are zero.
@@ -267,20 +279,22 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
     float m = kNegInf, l = 0.0f;
     bool failed = false;
     uint32_t issued_s = 0, issued_o = 0;                      // commits to bar_s, bar_o
+    // One tensor-core wait per tile: P V(t - 1) is issued at the end of tile
+    // t - 1 and S(t) right after it, so S(t) completing (bar_s) also means
+    // P V(t - 1) has completed (a commit covers every earlier tcgen05 op of
+    // the issuing thread).  K(t + 1) is prefetched as soon as S(t) is issued
+    // (its buffer held K(t - 1)), V(t + 1) once S(t) has completed (its
+    // buffer held V(t - 1)).
     for (int64_t t = 0; t < n_kt; ++t) {
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        // (a) K(t) has landed; V(t), issued after it, may still be in flight
+        cp_async_wait_pending(t == 0 ? 0 : 1);
         fence_proxy_async_smem();                            // copies -> tensor cores
         __syncthreads();
-        if (t + 1 < n_kt) {                                  // prefetch the next tile
-            const uint32_t nb = static_cast<uint32_t>((t + 1) & 1);
-            stage<D, BN, false>(sK + nb * KV_BYTES, gk, (t + 1) * BN, n_k, tid);
-            stage<D, BN, true>(sV + nb * KV_BYTES, gv, (t + 1) * BN, n_k, tid);
-        }
         const uint32_t cK = sK + static_cast<uint32_t>(t & 1) * KV_BYTES;
         const uint32_t cV = sV + static_cast<uint32_t>(t & 1) * KV_BYTES;
 
-        // ---- S = Q K^T into TMEM columns [0, BN)
-        if (tid == 0 && !failed) {
+        // (b) S = Q K^T into TMEM columns [0, BN), queued behind P V(t - 1)
+        if (tid == 0) {
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
@@ -289,13 +303,22 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
             umma_commit(smem_addr(&bar_s));
         }
         ++issued_s;
-        const bool ok_s = failed ? false : mbar_wait_bounded(smem_addr(&bar_s), t & 1);
+        // (c) K(t + 1) into the buffer S(t - 1) finished with
+        if (t + 1 < n_kt)
+            stage<D, BN, false>(sK + static_cast<uint32_t>((t + 1) & 1) * KV_BYTES, gk,
+                                (t + 1) * BN, n_k, tid);
+        // (d) S(t), and with it P V(t - 1), has completed
+        const bool ok_s = mbar_wait_bounded(smem_addr(&bar_s), static_cast<uint32_t>(t & 1));
         failed = __syncthreads_or(!ok_s) != 0;
         if (failed)
             break;
         tc_fence_after();
+        // (e) V(t + 1) into the buffer P V(t - 1) finished with
+        if (t + 1 < n_kt)
+            stage<D, BN, true>(sV + static_cast<uint32_t>((t + 1) & 1) * KV_BYTES, gv,
+                               (t + 1) * BN, n_k, tid);
 
-        // ---- this thread's S row: mask, running max, p, P row to shared memory
+        // (f) this thread's S row: mask, running max, p, P row to shared memory
         const int64_t k0 = t * BN;
         float mx = kNegInf;
         float sv[NCH][32];
@@ -338,8 +361,8 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
             }
         }
         l = l * alpha + sum;
-        // ---- rescale this thread's O row (the previous P V has completed);
-        // skipped by a warp whose rows all kept their maximum (alpha = 1).
+        // rescale this thread's O row; skipped by a warp whose rows all kept
+        // their maximum (alpha = 1)
         if (t > 0 && !__all_sync(0xffffffffu, alpha == 1.0f)) {
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -353,11 +376,14 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
             }
             tmem_wait_st();
         }
-        fence_proxy_async_smem();                            // P -> tensor cores
+        // (g) V(t) has landed: only the two copies of this tile may be pending
+        cp_async_wait_pending(t + 1 < n_kt ? 2 : 0);
+        fence_proxy_async_smem();                            // P, V -> tensor cores
         tc_fence_before();
         __syncthreads();
 
-        // ---- O += P V into TMEM columns [128, 128 + D)
+        // (h) O += P V(t) into TMEM columns [128, 128 + D); waited for through
+        // the next S (or after the loop)
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
@@ -368,10 +394,11 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
             umma_commit(smem_addr(&bar_o));
         }
         ++issued_o;
-        const bool ok_o = mbar_wait_bounded(smem_addr(&bar_o), t & 1);
+    }
+    if (!failed && n_kt > 0) {
+        const bool ok_o = mbar_wait_bounded(smem_addr(&bar_o),
+                                            static_cast<uint32_t>((n_kt - 1) & 1));
         failed = __syncthreads_or(!ok_o) != 0;
-        if (failed)
-            break;
         tc_fence_after();
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
