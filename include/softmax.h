@@ -182,9 +182,9 @@ int64_t softmax_visible_cols(const softmax_options_t* options, int64_t n_rows, i
  *   causal         0: every key.  1: key j is visible to query i iff
  *                  j <= i + causal_offset (0: the pages' mask; n_k - n_q: a
  *                  bottom-right aligned mask).  |causal_offset| < 2^62.
- *   impl           0: the library's choice (the tcgen05 kernel at head_dim
- *                  128, the mma.sync kernel at 64, the faster of the two on
- *                  GB300); 1: the warp-level mma.sync kernel; 2: tcgen05.
+ *   impl           0: the library's choice (the tcgen05 kernel, the faster
+ *                  of the two on GB300); 1: the warp-level mma.sync kernel;
+ *                  2: the tcgen05 kernel.
  */
 typedef struct {
     float scale;

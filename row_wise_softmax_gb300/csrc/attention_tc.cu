@@ -318,7 +318,11 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
             stage<D, BN, true>(sV + static_cast<uint32_t>((t + 1) & 1) * KV_BYTES, gv,
                                (t + 1) * BN, n_k, tid);
 
-        // (f) this thread's S row: mask, running max, p, P row to shared memory
+        // (f) this thread's S row: mask, running max, p, P row to shared memory.
+        // The max is taken on the raw scores (the scale is positive) and the
+        // scale folds into p = 2^(S * scale * log2 e - m).  Only a tile that
+        // reaches past the last key or (causal) past the diagonal of the
+        // CTA's first query is masked, with one integer compare per score.
         const int64_t k0 = t * BN;
         float mx = kNegInf;
         float sv[NCH][32];
@@ -326,19 +330,25 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
         for (int c = 0; c < NCH; ++c)
             tmem_ld32(t_row + c * 32, sv[c]);
         tmem_wait_ld();
+        const bool edge = k0 + BN > n_k || (CAUSAL && k0 + BN - 1 > q0 + offset);
+        if (edge) {
+            int64_t lim = n_k - k0;                          // keys of the tile kept
+            if (CAUSAL && qi + offset + 1 - k0 < lim)
+                lim = qi + offset + 1 - k0;
+            const int keep = static_cast<int>(lim < 0 ? 0 : (lim > BN ? BN : lim));
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) {
+            for (int c = 0; c < NCH; ++c)
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                float x = sv[c][j] * scale_log2;
-                const int64_t key = k0 + c * 32 + j;
-                if (key >= n_k || (CAUSAL && key > qi + offset))
-                    x = kNegInf;
-                sv[c][j] = x;
-                mx = fmaxf(mx, x);
-            }
+                for (int j = 0; j < 32; ++j)
+                    if (c * 32 + j >= keep)
+                        sv[c][j] = kNegInf;
         }
-        const float mn = fmaxf(m, mx);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c)
+#pragma unroll
+            for (int j = 0; j < 32; j += 2)
+                mx = max3(mx, sv[c][j], sv[c][j + 1]);
+        const float mn = fmaxf(m, mx * scale_log2);
         const float ref = mn == kNegInf ? 0.0f : mn;
         const float alpha = ex2_ftz(m - ref);
         m = mn;
@@ -350,7 +360,7 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
                 float p[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    p[e] = ex2_ftz(sv[c][g * 8 + e] - ref);
+                    p[e] = ex2_ftz(fmaf(sv[c][g * 8 + e], scale_log2, -ref));
                     sum += p[e];
                 }
                 const uint32_t w0 = Elem<T>::pack2(p[0], p[1]), w1 = Elem<T>::pack2(p[2], p[3]);

@@ -346,10 +346,10 @@ int softmax_attention_forward(const void* q, const void* k, const void* v, void*
         return ds;
     const rwsm::AttentionProblem p{q, k, v, o, lse, batch_heads, n_q, n_k, head_dim, dtype,
                                    scale, causal, offset};
-    // The library's choice (measured on GB300): tcgen05 at head_dim 128,
-    // mma.sync at 64.
+    // The library's choice: the tcgen05 kernel (faster at both head
+    // dimensions on GB300).
     if (impl == 0)
-        impl = head_dim == 128 ? 2 : 1;
+        impl = 2;
     const cudaError_t err = impl == 1 ? rwsm::launch_attention_mma(p, static_cast<cudaStream_t>(stream))
                                       : rwsm::launch_attention_tc(p, static_cast<cudaStream_t>(stream));
     if (err != cudaSuccess) {
