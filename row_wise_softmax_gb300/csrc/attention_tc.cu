@@ -44,6 +44,7 @@ constexpr int kTcBM = 128;          // queries per CTA (MMA M)
 constexpr int kTcThreads = 128;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kTmemO = 128;    // column of the O accumulator
+constexpr float kLazyRescaleLog2 = 8.0f;    // p <= 2^8 between rescales
 
 // ---- tcgen05 wrappers -----------------------------------------------------
 
@@ -348,10 +349,17 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
 #pragma unroll
             for (int j = 0; j < 32; j += 2)
                 mx = max3(mx, sv[c][j], sv[c][j + 1]);
-        const float mn = fmaxf(m, mx * scale_log2);
-        const float ref = mn == kNegInf ? 0.0f : mn;
-        const float alpha = ex2_ftz(m - ref);
-        m = mn;
+        // Lazy rescaling: the reference m (base 2) moves only when the tile's
+        // max exceeds it by more than 2^8, so p stays below 2^8 and most
+        // tiles leave O alone; O / l and the logsumexp only need m and l to
+        // agree.
+        const float mx_s = mx * scale_log2;
+        float alpha = 1.0f;
+        if (mx_s > m + kLazyRescaleLog2) {
+            alpha = ex2_ftz(m - mx_s);                      // 0 while m is -inf
+            m = mx_s;
+        }
+        const float ref = m == kNegInf ? 0.0f : m;
         float sum = 0.0f;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
