@@ -410,6 +410,43 @@ def attention_entry(torch, rws, stream, bh=64, n=4096, d=128, causal=False, dtyp
             "TFLOP/s": round(tf, 1), "frac_of_%s_bf16_peak" % kind: round(tf / peak, 4)}
 
 
+def graph_entry(torch, rws, stream, l2_bytes, peak, name="small_f32", calls=200):
+    """A launch-bound workload replayed from a CUDA graph of `calls`
+    softmax_rows calls over rotating input/output sets (launch overhead paid
+    once per replay instead of once per call)."""
+    w = wl.make(name)
+    sets = device_buffers(w, torch, l2_bytes)
+    call = rws.lib().softmax_rows
+    for x, y in sets[:3]:                                  # first calls outside capture
+        call(x.data_ptr(), y.data_ptr(), w.n_rows, w.n_cols, w.in_row_stride,
+             w.out_row_stride, w.dtype, stream.cuda_stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=cap):
+        h = torch.cuda.current_stream().cuda_stream
+        for i in range(calls):
+            x, y = sets[i % len(sets)]
+            if call(x.data_ptr(), y.data_ptr(), w.n_rows, w.n_cols, w.in_row_stride,
+                    w.out_row_stride, w.dtype, h) != rws.OK:
+                raise RuntimeError("softmax_rows failed under capture")
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    reps = 10
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    per_call = a.elapsed_time(b) / (reps * calls)
+    gbs = w.algorithmic_bytes / (per_call * 1e-3) / 1e9
+    return {"shape": [w.n_rows, w.n_cols], "calls_per_graph": calls,
+            "mean_ms_per_call": round(per_call, 5), "GB/s": round(gbs, 1),
+            "frac_of_measured_peak": round(gbs / peak, 4)}
+
+
 def time_e2e(w: wl.Workload, steps: int, warmup: int, torch, rws, stream, staged: bool):
     """softmax_rows_host on pinned host buffers, timed over `steps` calls.
 
@@ -583,6 +620,7 @@ def run_ours(args):
         per["causal_bf16_mask_from_indices"] = fused_causal_entry(torch, rws, stream, l2_bytes,
                                                                   peak)
         per["backward_f32_4096x4096"] = backward_entry(torch, rws, stream, l2_bytes, peak)
+        per["small_f32_cuda_graph"] = graph_entry(torch, rws, stream, l2_bytes, peak)
         for impl, tag in ((2, "tcgen05"), (1, "mma_sync")):
             per["attention_%s_bf16_64x4096x4096_d128" % tag] = attention_entry(
                 torch, rws, stream, impl=impl)
