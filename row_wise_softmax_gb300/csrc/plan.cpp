@@ -13,10 +13,11 @@
 //   CLUSTER  rows of 32..64 KB: one HBM pass, a cluster of CTAs holding
 //            <= 32 KB slices, max and sum exchanged through distributed shared
 //            memory.  (When forced: slices up to 128 KB fp32 / 64 KB bf16.)
-//   TWOPASS  longer rows: a cluster of 1..8 CTAs (about 128 KB of row per
-//            CTA) streams the row twice through a cp.async.bulk chunk ring;
-//            the second read mostly hits L2.  Unaligned input: the register
-//            two-pass kernel (about 256 KB per CTA).
+//   TWOPASS  longer rows: a cluster of 1..4 CTAs (about 256 KB of fp32 row
+//            or 1 MB of 16-bit row per CTA) streams the row twice through a
+//            cp.async.bulk chunk ring fed by a producer warp; the second read
+//            mostly hits L2.  Unaligned input: the register two-pass kernel
+//            (about 256 KB per CTA, clusters of up to 8).
 //
 // Whole waves (the "Block Occupancy: tail effect" rule of the cs336 lecture
 // 6 notes): every grid is persistent, sized at launch to the number of CTAs
@@ -36,10 +37,19 @@ constexpr int kSliceStages = 2;                    // ring stages of the slice k
 constexpr int64_t kTileRingBudgetBytes = 16 * 1024; // shared memory for the tile ring, per CTA
 constexpr int64_t kClusterMaxRowBytes = 64 * 1024;  // longer rows take TWOPASS
 constexpr int64_t kTwoPassBytesPerCta = 256 * 1024;      // register two-pass
-constexpr int64_t kStreamBytesPerCta = 128 * 1024;       // staged two-pass
-constexpr int kStreamThreads = 256;                      // staged two-pass: 16 KB chunks
-constexpr int kStreamStages = 2;
+// Staged two-pass (measured on GB300 over rows of 128 KB to 16 MB): 512
+// consumer threads x 4 vectors (32 KB chunks); slices of about 256 KB fp32
+// or 1 MB 16-bit; clusters of at most 4; ring stages by CTAs per SM.
+constexpr int64_t kStreamSliceBytesF32 = 256 * 1024;
+constexpr int64_t kStreamSliceBytes16 = 1024 * 1024;
+constexpr int kStreamThreads = 512;
+constexpr int kStreamVectors = 4;
+constexpr int kStreamStagesOneCta = 6;       // 192 KB: one CTA per SM
+constexpr int kStreamStagesTwoCtas = 3;      // 96 KB: two CTAs per SM
+constexpr int kStreamStagesLongSlice = 4;    // fp32 slices beyond 256 KB
+constexpr int64_t kStreamMaxClusterAuto = 4;
 constexpr int64_t kTwoPassMaxCluster = 8;
+constexpr int64_t kTwoPassMinSliceBytes = 64 * 1024;     // when clusters grow for few rows
 constexpr int kMaxStages = 8;                       // must match row_slices.cu
 constexpr int kMaxSliceThreads = 1024;
 constexpr int kSmemReserve = 2048;                  // static smem + slack
@@ -291,27 +301,44 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
         break;
     }
     case SOFTMAX_PATH_TWOPASS: {
-        // About 128 KB of row per CTA when staged, 256 KB (and at least two
-        // CTAs) for the register kernel; a single CTA when forced on short rows.
-        int64_t cs = pow2_ceil(ceil_div(row_bytes, in_al ? kStreamBytesPerCta : kTwoPassBytesPerCta));
+        // Staged: 512 consumer threads stream 32 KB chunks; slices of about
+        // 256 KB (fp32) or 1 MB (16-bit) on clusters of up to 4 CTAs, with a
+        // 192 KB ring when one CTA holds the SM and 96-128 KB for two.  The
+        // register kernel (unaligned input): about 256 KB and at least two
+        // CTAs.  A single CTA when forced on short rows.
+        const int64_t per_cta = in_al ? (esz == 4 ? kStreamSliceBytesF32 : kStreamSliceBytes16)
+                                      : kTwoPassBytesPerCta;
+        int64_t cs = pow2_ceil(ceil_div(row_bytes, per_cta));
         if (automatic && !in_al && cs < 2)
             cs = 2;
-        if (automatic && cs > kTwoPassMaxCluster)
-            cs = kTwoPassMaxCluster;       // 16-CTA clusters pack onto 74% of the SMs
+        if (automatic && cs > (in_al ? kStreamMaxClusterAuto : kTwoPassMaxCluster))
+            cs = in_al ? kStreamMaxClusterAuto : kTwoPassMaxCluster;
+        // Few rows: larger clusters (up to 8, slices of at least 64 KB) so
+        // that more SMs take part.
+        while (automatic && cs < kTwoPassMaxCluster && p.n_rows * cs < dev.sm_count &&
+               row_bytes / (2 * cs) >= kTwoPassMinSliceBytes)
+            cs *= 2;
         if (cs > max_cluster)
             cs = pow2_floor(max_cluster);
         q.cluster = static_cast<int>(cs);
         q.slice_cols = round_up(ceil_div(p.n_cols, cs), vmax);
         q.grid = 0;
         if (in_al) {
-            // Staged: the slice streams twice through a ring of 16 KB chunks.
+            // Staged: the slice streams twice through a ring of 32 KB chunks.
             q.bulk_copy = 1;
             q.vec = vmax;
             q.out_vec = out_al ? vmax : 1;
             q.threads = kStreamThreads;
-            q.chunks = esz == 4 ? 8 : 4;          // 32 KB fp32 / 16 KB bf16 chunks
-            q.stages = kStreamStages;
-            q.smem_bytes = q.stages * q.threads * q.chunks * 16;
+            q.chunks = kStreamVectors;
+            const int64_t slice_bytes = q.slice_cols * esz;
+            int stages = (esz != 4 || cs == 1) ? kStreamStagesOneCta
+                         : (slice_bytes > kStreamSliceBytesF32 ? kStreamStagesLongSlice
+                                                               : kStreamStagesTwoCtas);
+            const int64_t chunk_bytes = int64_t{q.threads} * q.chunks * 16;
+            while (stages > 1 && stages * chunk_bytes > smem_cap)
+                --stages;
+            q.stages = stages;
+            q.smem_bytes = static_cast<int>(stages * chunk_bytes);
         } else {
             q.vec = (in_vec && out_al) ? vmax : 1;
             q.out_vec = q.vec;

@@ -1,28 +1,36 @@
 // TWOPASS path, staged: rows too long to keep on chip, with 16-byte aligned
-// input.  A cluster of cs CTAs owns a row; each CTA streams its slice of the
-// row twice through a ring of `stages` shared-memory chunks:
+// input.  A cluster of cs CTAs owns a row; each CTA owns a slice of it and
+// streams the slice twice through a shared-memory ring: once from HBM, once
+// more mostly from L2.
 //
-//   ring    one elected thread keeps `stages` chunk copies in flight
-//           (cp.async.bulk, global -> shared, one mbarrier per stage) along
-//           the fixed sequence (row, pass, chunk).  Pass-1 copies carry an
-//           L2 evict-last policy so the lines stay for the second read;
-//           pass-2 copies and the output stores carry evict-first.
-//   pass 1  each thread folds its vectors of every chunk into an online
-//           (m, l): m_new = max(m, chunk max), l = l * e^(m - m_new) +
-//           sum e^(x - m_new) — the running-max rescale of "Triton GPU
-//           programming deep dive", section 3.3, over the chunks of the
-//           "Level 2: Row Sum (tiling)" loop of the cs336 lecture 6 notes.
-//   merge   warp (__shfl_xor), CTA (shared memory), cluster (distributed
-//           shared memory after a cluster barrier): every thread gets the
-//           row's (M, L).
-//   pass 2  the slice streams again (mostly from L2): y = e^(x - M) / L.
+//   producer  the last warp of the CTA (one elected lane) keeps `stages`
+//             chunk copies in flight (cp.async.bulk, global -> shared, one
+//             "full" mbarrier per stage) along the fixed sequence
+//             (row, pass, chunk).  First-pass copies carry an L2 evict-last
+//             policy so the lines stay for the second read; second-pass
+//             copies and the output stores carry evict-first.  It refills a
+//             stage as soon as its "empty" mbarrier shows every consumer warp
+//             has the chunk in registers: no CTA-wide barrier per chunk.
+//   pass 1    the consumer warps fold each chunk into an online (m, l):
+//             m_new = max(m, chunk max), l = l * e^(m - m_new) +
+//             sum e^(x - m_new) — the running-max rescale of "Triton GPU
+//             programming deep dive", section 3.3, over the chunks of the
+//             "Level 2: Row Sum (tiling)" loop of the cs336 lecture 6 notes.
+//   merge     warp (__shfl_xor), consumer warps (shared memory, a named
+//             barrier), cluster: each CTA stores its (m, l) into every peer's
+//             shared memory and arrives on the peer's exchange mbarrier
+//             (release at cluster scope); each CTA waits on its own.  No
+//             cluster-wide barrier per row, so the producer never stops.
+//   pass 2    the slice's chunks again: y = e^(x - M) / L.
 //
-// In-flight data lives in shared memory, not registers (a thread holds one
-// chunk's 16 floats), so each SM keeps several ring stages of HBM reads
-// outstanding while its warps reduce.  A stage is refilled after a CTA
-// barrier shows every thread has its vectors in registers.  The last chunk of
-// a slice may be ragged: its final < 16 bytes are read with plain loads by
-// the lane that owns them.
+// Exchange slots and mbarriers are double-buffered by row parity: a CTA can
+// run at most one row ahead of a peer (it needs the peer's partial of the
+// row in between), so a slot is rewritten only after its reader is done.
+// In place (in == out) is safe: each element is re-read by the thread that
+// then writes it, and every first-pass read of a row precedes the exchange
+// that any write of the row waits for.  The last chunk of a slice may be
+// ragged: its final < 16 bytes are read with plain loads by the lane that
+// owns them.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -32,25 +40,112 @@ namespace rwsm {
 
 __device__ unsigned g_error_stream_rows = 0;
 
+// Position in a ring of stages walked in order: the stage and the parity of
+// the number of completed trips around the ring (the mbarrier phase parity
+// of that stage's next use), advanced without divisions.
+struct RingPos {
+    int slot = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next(int stages)
+    {
+        if (++slot == stages) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// ------------------------------------ distributed shared memory, barriers
+// Address of the same shared-memory variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_f2(uint32_t addr, float a, float b)
+{
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" :: "r"(addr), "f"(a), "f"(b)
+                 : "memory");
+}
+
+// Arrive on an mbarrier of any CTA of the cluster, releasing this thread's
+// earlier writes (distributed shared memory included) at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+                 :: "r"(cluster_addr) : "memory");
+}
+
+// Bounded wait (as mbar_wait_bounded) with acquire at cluster scope: writes
+// released by peers' mbar_arrive_cluster are visible after it returns true.
+// Polls without a suspend-time hint.
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity)
+{
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 0; it < (1u << 30); ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+        if (ok)
+            return true;
+        if ((it & 255u) == 255u && global_ns() - t0 > kWaitLimitNs)
+            return false;
+    }
+    return false;
+}
+
+// Barrier over the first `count` threads of the CTA (a multiple of 32) on
+// hardware barrier `id` (1..15; __syncthreads uses 0).
+__device__ __forceinline__ void named_barrier(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
+}
+
+// Cluster-wide barrier for every thread of every CTA (release / acquire);
+// the non-.aligned form, so it may follow divergent code.
+__device__ __forceinline__ void cluster_barrier()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 constexpr int kStreamMaxStages = 8;
 constexpr int kStreamRingAlign = 128;
+constexpr int kStreamMaxCluster = 16;
+
+// CTAs per SM the register budget is set for: a consumer thread holds one
+// chunk of E = NV * 16 / sizeof(T) floats plus about 40 registers of
+// addresses and state (measured with -Xptxas -v).
+template <typename T, int THREADS, int NV>
+__host__ __device__ constexpr int stream_min_blocks()
+{
+    constexpr int b = 65536 / ((THREADS + 32) * (NV * Elem<T>::kVec16 + 40));
+    return b < 1 ? 1 : b;
+}
 
 template <typename T, int THREADS, int NV, bool OUTVEC, bool OPTS>
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(THREADS + 32, (stream_min_blocks<T, THREADS, NV>()))
 stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t ld_in,
                    int64_t ld_out, int64_t slice_cols, int cs, int stages, LogitsArg lg)
 {
     constexpr int VEC = Elem<T>::kVec16;
-    constexpr int NW = THREADS / 32;
+    constexpr int NW = THREADS / 32;                    // consumer warps; warp NW produces
     constexpr int E = NV * VEC;
     constexpr int CHUNK = THREADS * E;                  // elements per chunk
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    __shared__ float red_m[NW], red_l[NW];
-    __shared__ float2 part[2];
+    __shared__ float red_m[2][NW], red_l[2][NW];
+    __shared__ __align__(8) float2 xpart[2][kStreamMaxCluster];
     __shared__ __align__(8) unsigned long long full[kStreamMaxStages];
+    __shared__ __align__(8) unsigned long long empty[kStreamMaxStages];
+    __shared__ __align__(8) unsigned long long xbar[2];
     __shared__ unsigned issued[kStreamMaxStages];
+    __shared__ int s_failed;
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float kk = OPTS ? lg.k : kLog2e;       // exponent multiplier, scale * log2 e
     const int rank = static_cast<int>(blockIdx.x % cs);
     const int64_t cluster_id = blockIdx.x / cs;
@@ -60,48 +155,29 @@ stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t 
     len = len < 0 ? 0 : (len > slice_cols ? slice_cols : len);
     const int64_t K = (len + CHUNK - 1) / CHUNK;        // chunks per pass
     const int64_t my_rows = cluster_id < n_rows ? (n_rows - 1 - cluster_id) / n_clusters + 1 : 0;
-    const int64_t total_q = my_rows * 2 * K;            // chunk copies this CTA consumes
 
     T* ring = reinterpret_cast<T*>((reinterpret_cast<uintptr_t>(smem_raw) + (kStreamRingAlign - 1)) &
                                    ~static_cast<uintptr_t>(kStreamRingAlign - 1));
     auto stage_ptr = [&](int s) { return ring + static_cast<int64_t>(s) * CHUNK; };
-    // Chunk q of the sequence: row i = q / 2K, pass = (q / K) & 1, chunk q % K.
     auto chunk_len = [&](int64_t chunk) {
         const int64_t rest = len - chunk * CHUNK;
         return static_cast<int>(rest < CHUNK ? rest : CHUNK);
     };
     // Columns of this slice that take part in `row` (all of them unless a
     // causal mask stops the row inside or before the slice), and of `chunk`
-    // given that count (masked columns are never copied).
+    // given that count (masked columns are never read).
     auto row_keep = [&](int64_t row) -> int64_t { return kept_cols<OPTS>(lg, row, n_cols) - c0; };
     auto chunk_lim = [&](int64_t keep, int64_t chunk) {
         const int64_t rest = keep - chunk * CHUNK;
         const int clen = chunk_len(chunk);
         return static_cast<int>(rest < 0 ? 0 : (rest > clen ? clen : rest));
     };
-    const uint64_t keep = policy_evict_last();
-    const uint64_t stream = policy_evict_first();
-    auto issue = [&](int64_t q) {                       // thread 0 only
-        const int s = static_cast<int>(q % stages);
-        const int64_t i = q / (2 * K);
-        const bool second = ((q / K) & 1) != 0;
-        const int64_t chunk = q % K;
-        const int64_t row = cluster_id + i * n_clusters;
-        uint32_t bytes;
+    // Bytes of `chunk` of `row` the bulk copy moves (whole 16-byte granules).
+    auto copy_bytes = [&](int64_t row, int64_t chunk) -> uint32_t {
         if constexpr (OPTS)
-            bytes = span_copy_bytes<T>(chunk_lim(row_keep(row), chunk), n_cols - c0 - chunk * CHUNK);
+            return span_copy_bytes<T>(chunk_lim(row_keep(row), chunk), n_cols - c0 - chunk * CHUNK);
         else
-            bytes = static_cast<uint32_t>(chunk_len(chunk) * sizeof(T)) & ~15u;
-        const uint32_t bar = smem_addr(&full[s]);
-        fence_proxy_async_smem();
-        issued[s] += 1;
-        if (bytes) {
-            mbar_arrive_expect_tx(bar, bytes);
-            bulk_g2s_hint(smem_addr(stage_ptr(s)), in + row * ld_in + c0 + chunk * CHUNK, bytes,
-                          bar, second ? stream : keep);
-        } else {
-            mbar_arrive(bar);
-        }
+            return static_cast<uint32_t>(chunk_len(chunk) * sizeof(T)) & ~15u;
     };
 
     // Cluster launches let the next grid start only after the row loop:
@@ -112,120 +188,213 @@ stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t 
     if (tid == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
+            mbar_init(smem_addr(&empty[s]), NW);
             issued[s] = 0;
         }
+        mbar_init(smem_addr(&xbar[0]), static_cast<uint32_t>(cs));
+        mbar_init(smem_addr(&xbar[1]), static_cast<uint32_t>(cs));
+        s_failed = 0;
         fence_mbar_init();
     }
-    __syncthreads();
+    // Peers arrive on this CTA's exchange mbarriers: they must be initialised
+    // cluster-wide first.
+    if (cs > 1)
+        cluster_barrier();
+    else
+        __syncthreads();
     pdl_wait();
-    if (tid == 0)
-        for (int64_t q = 0; q < stages && q < total_q; ++q)
-            issue(q);
 
-    bool failed = false;                                 // CTA-uniform
-    int64_t q = 0;
-    // Wait for chunk q, copy this thread's vectors into registers (ragged
-    // tail from HBM), release the stage and start the copy `stages` ahead.
-    auto take = [&](int64_t keep, const T* src_row, int64_t chunk, float (&x)[E]) {
-        const int s = static_cast<int>(q % stages);
-        const uint32_t parity = static_cast<uint32_t>((q / stages) & 1);
-        const bool ok = failed ? true : mbar_wait_bounded(smem_addr(&full[s]), parity);
-        int clen, bulk;                              // kept columns, copied columns
-        if constexpr (OPTS) {
-            clen = chunk_lim(keep, chunk);
-            bulk = static_cast<int>(span_copy_bytes<T>(clen, n_cols - c0 - chunk * CHUNK) / sizeof(T));
-            bulk = bulk < clen ? bulk : clen;
-        } else {
-            clen = chunk_len(chunk);
-            bulk = static_cast<int>((clen * sizeof(T)) & ~size_t{15}) / static_cast<int>(sizeof(T));
-        }
-        const T* st = stage_ptr(s);
-        const T* g = src_row + chunk * CHUNK;
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const int e0 = (tid + k * THREADS) * VEC;
-            if (e0 + VEC <= bulk) {
-                lds_vec<T, VEC>(st + e0, &x[k * VEC]);
-            } else if (OPTS && e0 >= clen) {
-#pragma unroll
-                for (int j = 0; j < VEC; ++j)
-                    x[k * VEC + j] = kNegInf;
-            } else {
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    const int e = e0 + j;
-                    x[k * VEC + j] = e < clen ? Elem<T>::load1(g + e) : kNegInf;
+    if (warp == NW) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            const uint64_t keep_pol = policy_evict_last();
+            const uint64_t stream_pol = policy_evict_first();
+            const int64_t total_q = my_rows * 2 * K;
+            RingPos pos;
+            int64_t chunk = 0, row = cluster_id;
+            bool second = false;
+            // The sequence: for each row, pass 1's K chunks, then pass 2's.
+            for (int64_t q = 0; q < total_q; ++q) {
+                const int s = pos.slot;
+                // The stage's previous use (one trip earlier) must be released.
+                if (q >= stages && !mbar_wait_bounded(smem_addr(&empty[s]), pos.phase ^ 1u)) {
+                    *reinterpret_cast<volatile int*>(&s_failed) = 1;
+                    break;
+                }
+                if (*reinterpret_cast<volatile int*>(&s_failed))
+                    break;
+                const uint32_t bytes = copy_bytes(row, chunk);
+                const uint32_t bar = smem_addr(&full[s]);
+                fence_proxy_async_smem();
+                issued[s] += 1;
+                if (bytes) {
+                    mbar_arrive_expect_tx(bar, bytes);
+                    bulk_g2s_hint(smem_addr(stage_ptr(s)), in + row * ld_in + c0 + chunk * CHUNK,
+                                  bytes, bar, second ? stream_pol : keep_pol);
+                } else {
+                    mbar_arrive(bar);
+                }
+                pos.next(stages);
+                if (++chunk == K) {
+                    chunk = 0;
+                    second = !second;
+                    if (!second)
+                        row += n_clusters;
                 }
             }
         }
-        if (__syncthreads_or(!ok))
-            failed = true;
-        if (tid == 0 && !failed && q + stages < total_q)
-            issue(q + stages);
-        ++q;
-    };
-
-    int slot = 0;
-    for (int64_t row = cluster_id; row < n_rows; row += n_clusters, slot ^= 1) {
-        const T* src = in + row * ld_in + c0;
-        const int64_t keep = row_keep(row);
-        // ---- pass 1: online (m, l)
-        float m = kNegInf, l = 0.0f;
-        for (int64_t chunk = 0; chunk < K; ++chunk) {
-            float x[E];
-            take(keep, src, chunk, x);
-            float bm = kNegInf;
-#pragma unroll
-            for (int e = 0; e < E; ++e)
-                bm = fmaxf(bm, x[e]);
-            const float mn = fmaxf(m, bm);
-            const float ref = (mn == kNegInf) ? 0.0f : mn;
-            float sum = 0.0f;
-#pragma unroll
-            for (int e = 0; e < E; ++e)
-                sum += exp_biased(x[e] - ref, kk);
-            l = l * exp_ftz(m - ref, kk) + sum;
-            m = mn;
-        }
-        cta_ml_reduce<THREADS>(m, l, red_m, red_l, kk);
-        if (cs > 1)
-            cluster_ml_reduce(m, l, part, slot, cs, kk);
-        const float inv = 1.0f / l;
-        // ---- pass 2: normalise and store
-        T* dst = out + row * ld_out + c0;
-        for (int64_t chunk = 0; chunk < K; ++chunk) {
-            float x[E];
-            take(keep, src, chunk, x);
-            const int clen = chunk_len(chunk);
-            T* d = dst + chunk * CHUNK;
+        __syncwarp();
+    } else {
+        // --------------------------------------------------------- consumers
+        const uint64_t stream_pol = policy_evict_first();
+        bool failed = false;                             // warp-uniform
+        RingPos cpos;                                    // next chunk's stage and phase
+        // Wait for the next chunk of the sequence, copy this thread's vectors
+        // into registers (the ragged tail from global memory, masked columns
+        // as -inf) and hand the stage back to the producer.
+        auto take = [&](int64_t keep, const T* src_row, int64_t chunk, float (&x)[E]) {
+            const int s = cpos.slot;
+            const bool ok = failed || mbar_wait_bounded(smem_addr(&full[s]), cpos.phase);
+            cpos.next(stages);
+            if (__any_sync(0xffffffffu, !ok) && !failed) {
+                failed = true;
+                *reinterpret_cast<volatile int*>(&s_failed) = 1;
+            }
+            int clen, bulk;                              // kept columns, copied columns
+            if constexpr (OPTS) {
+                clen = chunk_lim(keep, chunk);
+                bulk = static_cast<int>(span_copy_bytes<T>(clen, n_cols - c0 - chunk * CHUNK) /
+                                        sizeof(T));
+                bulk = bulk < clen ? bulk : clen;
+            } else {
+                clen = chunk_len(chunk);
+                bulk = static_cast<int>((clen * sizeof(T)) & ~size_t{15}) / static_cast<int>(sizeof(T));
+            }
+            const T* st = stage_ptr(s);
+            const T* g = src_row + chunk * CHUNK;
 #pragma unroll
             for (int k = 0; k < NV; ++k) {
                 const int e0 = (tid + k * THREADS) * VEC;
-                if (e0 < clen) {
+                if (e0 + VEC <= bulk) {
+                    lds_vec<T, VEC>(st + e0, &x[k * VEC]);
+                } else if (e0 >= clen) {
 #pragma unroll
                     for (int j = 0; j < VEC; ++j)
-                        x[k * VEC + j] = exp_biased(x[k * VEC + j] - m, kk);
-                    if constexpr (OUTVEC) {
-                        if (e0 + VEC <= clen)
-                            store16_hint<T>(d + e0, &x[k * VEC], inv, stream);
-                        else
-                            store_vec_masked<T, VEC>(d, e0, clen, &x[k * VEC], inv);
-                    } else {
+                        x[k * VEC + j] = kNegInf;
+                } else {
 #pragma unroll
-                        for (int j = 0; j < VEC; ++j)
-                            if (e0 + j < clen)
-                                Elem<T>::store1(d + e0 + j, x[k * VEC + j] * inv);
+                    for (int j = 0; j < VEC; ++j) {
+                        const int e = e0 + j;
+                        x[k * VEC + j] = e < clen ? Elem<T>::load1(g + e) : kNegInf;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_addr(&empty[s]));       // stage free for the producer
+        };
+        int64_t i = 0;                                   // this cluster's row counter
+        for (int64_t row = cluster_id; row < n_rows; row += n_clusters, ++i) {
+            const T* src = in + row * ld_in + c0;
+            T* dst = out + row * ld_out + c0;
+            const int64_t keep = row_keep(row);
+            // ---- pass 1: online (m, l) over the staged chunks
+            float m = kNegInf, l = 0.0f;
+            for (int64_t chunk = 0; chunk < K; ++chunk) {
+                float x[E];
+                take(keep, src, chunk, x);
+                // Paired fp32 instructions (two results each, rounded as
+                // the scalar ones) and a three-input max.
+                const float mn = frag_max<E>(x, m);
+                const float ref = (mn == kNegInf) ? 0.0f : mn;
+                float s0 = 0.0f, s1 = 0.0f;
+                frag_exp_acc<E>(x, ref, kk, s0, s1);
+                l = l * exp_ftz(m - ref, kk) + (s0 + s1);
+                m = mn;
+            }
+            // ---- merge over the consumer warps
+            const int p = static_cast<int>(i & 1);
+            warp_ml_merge(m, l, kk);
+            if (lane == 0) {
+                red_m[p][warp] = m;
+                red_l[p][warp] = l;
+            }
+            named_barrier(1, THREADS);
+            m = lane < NW ? red_m[p][lane] : kNegInf;
+            l = lane < NW ? red_l[p][lane] : 0.0f;
+            warp_ml_merge(m, l, kk);
+            // ---- merge over the cluster (distributed shared memory)
+            if (cs > 1) {
+                if (tid == 0) {
+                    const uint32_t slot = smem_addr(&xpart[p][rank]);
+                    const uint32_t bar = smem_addr(&xbar[p]);
+                    for (int r = 0; r < cs; ++r) {
+                        st_cluster_f2(cluster_map(slot, static_cast<uint32_t>(r)), m, l);
+                        mbar_arrive_cluster(cluster_map(bar, static_cast<uint32_t>(r)));
+                    }
+                }
+                const bool ok = failed ||
+                                mbar_wait_cluster_bounded(smem_addr(&xbar[p]),
+                                                          static_cast<uint32_t>((i >> 1) & 1));
+                if (__any_sync(0xffffffffu, !ok) && !failed) {
+                    failed = true;
+                    *reinterpret_cast<volatile int*>(&s_failed) = 1;
+                }
+                float pm = kNegInf, pl = 0.0f;
+                if (lane < cs) {
+                    const float2 v = xpart[p][lane];
+                    pm = v.x;
+                    pl = v.y;
+                }
+                warp_ml_merge(pm, pl, kk);
+                m = pm;
+                l = pl;
+            }
+            const float inv = 1.0f / l;
+            // ---- pass 2: the staged chunks again (mostly L2 hits): normalise, store
+            for (int64_t chunk = 0; chunk < K; ++chunk) {
+                float x[E];
+                take(keep, src, chunk, x);
+                const int clen = chunk_len(chunk);
+                T* d = dst + chunk * CHUNK;
+#pragma unroll
+                for (int k = 0; k < NV; ++k) {
+                    const int e0 = (tid + k * THREADS) * VEC;
+                    if (e0 < clen) {
+                        // y = exp_biased(x - M) * (1 / L), two elements per
+                        // instruction.
+                        float* v = &x[k * VEC];
+#pragma unroll
+                        for (int j = 0; j < VEC; j += 2) {
+                            float d0, d1;
+                            add2(d0, d1, v[j], v[j + 1], -m, -m);
+                            fma2(d0, d1, d0, d1, kk, kk, kExpBias, kExpBias);
+                            mul2(v[j], v[j + 1], ex2_ftz(d0), ex2_ftz(d1), inv, inv);
+                        }
+                        if constexpr (OUTVEC) {
+                            if (e0 + VEC <= clen)
+                                store16_hint<T>(d + e0, v, 1.0f, stream_pol);
+                            else
+                                store_vec_masked<T, VEC>(d, e0, clen, v, 1.0f);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < VEC; ++j)
+                                if (e0 + j < clen)
+                                    Elem<T>::store1(d + e0 + j, v[j]);
+                        }
                     }
                 }
             }
         }
-        __syncthreads();        // red_* are rewritten by the next row's reduction
     }
     if (cs > 1)
         pdl_launch_dependents();
+    // No CTA may exit while a peer can still write its shared memory.
     if (cs > 1)
-        cooperative_groups::this_cluster().sync();       // peers may still read `part`
-    if (failed && tid == 0) {
+        cluster_barrier();
+    else
+        __syncthreads();
+    if (tid == THREADS && *reinterpret_cast<volatile int*>(&s_failed)) {
         atomicOr(&g_error_stream_rows, kErrMbarrierTimeout);
         for (int s = 0; s < stages; ++s)                  // copies possibly still in flight
             if (issued[s])
@@ -291,7 +460,7 @@ cudaError_t launch_stream_opts(const Problem& p, const softmax_plan_t& plan, cud
         if (cs > 1) {
             cudaLaunchConfig_t q = {};
             q.gridDim = dim3(static_cast<unsigned>(cs), 1, 1);
-            q.blockDim = dim3(THREADS, 1, 1);
+            q.blockDim = dim3(THREADS + 32, 1, 1);
             q.dynamicSmemBytes = static_cast<size_t>(smem);
             q.attrs = attr;
             q.numAttrs = 1;
@@ -300,7 +469,7 @@ cudaError_t launch_stream_opts(const Problem& p, const softmax_plan_t& plan, cud
                 active = 0;
             }
         } else {
-            active = resident_ctas(reinterpret_cast<const void*>(k), THREADS, smem);
+            active = resident_ctas(reinterpret_cast<const void*>(k), THREADS + 32, smem);
         }
         if (active < 1)
             active = 1;
@@ -308,7 +477,7 @@ cudaError_t launch_stream_opts(const Problem& p, const softmax_plan_t& plan, cud
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * cs), 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.blockDim = dim3(THREADS + 32, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = s;
     cfg.attrs = attr;
@@ -350,7 +519,8 @@ cudaError_t launch_stream_nv(const Problem& p, const softmax_plan_t& plan, cudaS
 
 cudaError_t launch_stream_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
 {
-    if (plan.stages < 1 || plan.stages > kStreamMaxStages)
+    if (plan.stages < 1 || plan.stages > kStreamMaxStages || plan.cluster < 1 ||
+        plan.cluster > kStreamMaxCluster)
         return cudaErrorInvalidValue;
     if (p.dtype == SOFTMAX_F32) {
         if (plan.threads == 256) return launch_stream_nv<float, 256>(p, plan, s);

@@ -49,7 +49,7 @@ int main(void)
     CHECK(softmax_plan_format(&plan, text, sizeof text) > 0 && strstr(text, "path=cta"));
     CHECK(softmax_plan(&gb300, (void*)0x10000, (void*)0x20000000, 256, 262144, 262144, 262144,
                        SOFTMAX_F32, SOFTMAX_PATH_AUTO, &plan) == SOFTMAX_OK);
-    CHECK(plan.path == SOFTMAX_PATH_TWOPASS && plan.cluster == 8 && plan.stages == 2);
+    CHECK(plan.path == SOFTMAX_PATH_TWOPASS && plan.cluster == 4 && plan.stages == 3);
     gb300.cc_minor = 0;
     CHECK(softmax_plan(&gb300, (void*)0x10000, (void*)0x20000000, 4, 4, 4, 4, SOFTMAX_F32,
                        SOFTMAX_PATH_AUTO, &plan) == SOFTMAX_ERR_UNSUPPORTED);

@@ -60,9 +60,13 @@ def test_scheduler_paths_for_the_five_workloads(lib):
     assert (p.stages, p.smem_bytes) == (2, 16384)
     p = plan(262144, 127, in_row_stride=128, out_row_stride=127)
     assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 0, 1, 4, 4)
-    p = plan(256, 262144)                                 # staged two-pass, 16 KB chunks
-    assert (p.path, p.cluster, p.slice_cols, p.threads, p.grid) == (rws.PATH_TWOPASS, 8, 32768, 256, 0)
-    assert (p.vec, p.out_vec, p.bulk_copy, p.chunks, p.stages, p.smem_bytes) == (4, 4, 1, 8, 2, 65536)
+    p = plan(256, 262144)                                 # staged two-pass, 32 KB chunks
+    assert (p.path, p.cluster, p.slice_cols, p.threads, p.grid) == (rws.PATH_TWOPASS, 4, 65536, 512, 0)
+    assert (p.vec, p.out_vec, p.bulk_copy, p.chunks, p.stages, p.smem_bytes) == (4, 4, 1, 4, 3, 98304)
+    p = plan(1024, 65536)                                 # one CTA per row: a 192 KB ring
+    assert (p.cluster, p.stages, p.smem_bytes) == (1, 6, 196608)
+    p = plan(256, 262144, dtype=rws.BF16)                 # 16-bit: slices up to 1 MB
+    assert (p.path, p.cluster, p.threads, p.chunks, p.stages) == (rws.PATH_TWOPASS, 1, 512, 4, 6)
     p = plan(256, 262144, in_ptr=(1 << 20) + 4)           # unaligned: register two-pass
     assert (p.path, p.bulk_copy, p.vec, p.threads) == (rws.PATH_TWOPASS, 0, 1, 512)
 
@@ -86,9 +90,11 @@ def test_scheduler_boundaries(lib):
     assert plan(1, 16384).path == rws.PATH_CLUSTER         # single pass up to 64 KB rows
     p = plan(1, 16388)
     assert p.path == rws.PATH_TWOPASS and p.cluster == 1 and p.bulk_copy == 1
-    assert plan(1, 32768).cluster == 1 and plan(1, 32772).cluster == 2
-    assert plan(1, 131072).cluster == 4 and plan(1, 262144).cluster == 8
+    # Few rows: clusters grow (slices of at least 64 KB) up to 8 CTAs.
+    assert plan(1, 32768).cluster == 2 and plan(1, 32772).cluster == 2
+    assert plan(1, 131072).cluster == 8 and plan(1, 262144).cluster == 8
     assert plan(1, 4 << 20).cluster == 8                  # capped: 16-CTA clusters pack poorly
+    assert plan(64, 1 << 20).cluster == 4                 # many rows: about 256 KB slices, <= 4
     assert plan(1, 16384, dtype=rws.BF16).path == rws.PATH_CTA
     assert plan(1, 16392, dtype=rws.BF16).path == rws.PATH_CLUSTER
     assert plan(1, 32768, dtype=rws.BF16).path == rws.PATH_CLUSTER
