@@ -10,11 +10,13 @@
 //   CTA      row <= 32 KB: a persistent CTA per row at a time, the row staged
 //            by cp.async.bulk and held in registers (one ring stage: the
 //            register copy is the second buffer).
-//   CLUSTER  rows of 32..64 KB: one HBM pass, a cluster of CTAs holding
-//            <= 32 KB slices, max and sum exchanged through distributed shared
-//            memory.  (When forced: slices up to 128 KB fp32 / 64 KB bf16.)
-//   TWOPASS  longer rows: a cluster of 1..4 CTAs (about 256 KB of fp32 row
-//            or 1 MB of 16-bit row per CTA) streams the row twice through a
+//   CLUSTER  rows of 32..64 KB whose input is not 16-byte aligned: one HBM
+//            pass, a cluster of CTAs holding <= 32 KB slices, max and sum
+//            exchanged through distributed shared memory.  (When forced:
+//            slices up to 128 KB fp32 / 64 KB bf16.)
+//   TWOPASS  longer rows (every row beyond 32 KB when the input is 16-byte
+//            aligned): a cluster of 1..4 CTAs (about 256 KB of fp32 row or
+//            1 MB of 16-bit row per CTA) streams the row twice through a
 //            cp.async.bulk chunk ring fed by a producer warp; the second read
 //            mostly hits L2.  Unaligned input: the register two-pass kernel
 //            (about 256 KB per CTA, clusters of up to 8).
@@ -215,15 +217,17 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
         return 0;
     };
 
-    // Rows whose slices would exceed 32 KB even on 16 SMs go to the two-pass
-    // kernel: on-chip staging would then hold too few rows in flight, while
-    // the second pass re-reads the row mostly from L2.
+    // Rows beyond 32 KB go to the staged two-pass kernel when the input
+    // allows bulk copies: its deep ring and producer warp measured faster than
+    // a cluster holding the row on chip from 48 KB up (e.g. 64 KB fp32 rows
+    // 6.2 against 5.0 TB/s), while the second pass re-reads the row mostly
+    // from L2.  Unaligned input keeps the cluster kernel up to 64 KB rows.
     if (path == SOFTMAX_PATH_AUTO) {
         if (p.n_cols <= kWarpMaxCols)
             path = SOFTMAX_PATH_WARP;
         else if (row_bytes <= kSliceTargetBytes)
             path = SOFTMAX_PATH_CTA;
-        else if (cluster_for(false) && row_bytes <= kClusterMaxRowBytes)
+        else if (!in_al && cluster_for(false) && row_bytes <= kClusterMaxRowBytes)
             path = SOFTMAX_PATH_CLUSTER;
         else
             path = SOFTMAX_PATH_TWOPASS;

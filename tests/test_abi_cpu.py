@@ -85,9 +85,12 @@ def test_scheduler_boundaries(lib):
     assert plan(1, 1024).path == rws.PATH_WARP
     assert plan(1, 1025).path == rws.PATH_CTA
     assert plan(1, 8192).path == rws.PATH_CTA             # 32 KB row
-    p = plan(1, 8196)
-    assert p.path == rws.PATH_CLUSTER and p.cluster == 2 and p.stages == 2
-    assert plan(1, 16384).path == rws.PATH_CLUSTER         # single pass up to 64 KB rows
+    p = plan(1, 8196)                                      # aligned rows beyond 32 KB: staged two-pass
+    assert p.path == rws.PATH_TWOPASS and p.cluster == 1 and p.bulk_copy == 1
+    p = plan(1, 8196, in_ptr=(1 << 20) + 4)                # unaligned: the cluster kernel to 64 KB
+    assert p.path == rws.PATH_CLUSTER and p.cluster == 2 and p.bulk_copy == 0
+    assert plan(1, 16384, in_ptr=(1 << 20) + 4).path == rws.PATH_CLUSTER
+    assert plan(1, 16388, in_ptr=(1 << 20) + 4).path == rws.PATH_TWOPASS
     p = plan(1, 16388)
     assert p.path == rws.PATH_TWOPASS and p.cluster == 1 and p.bulk_copy == 1
     # Few rows: clusters grow (slices of at least 64 KB) up to 8 CTAs.
@@ -96,9 +99,10 @@ def test_scheduler_boundaries(lib):
     assert plan(1, 4 << 20).cluster == 8                  # capped: 16-CTA clusters pack poorly
     assert plan(64, 1 << 20).cluster == 4                 # many rows: about 256 KB slices, <= 4
     assert plan(1, 16384, dtype=rws.BF16).path == rws.PATH_CTA
-    assert plan(1, 16392, dtype=rws.BF16).path == rws.PATH_CLUSTER
-    assert plan(1, 32768, dtype=rws.BF16).path == rws.PATH_CLUSTER
-    assert plan(1, 32776, dtype=rws.BF16).path == rws.PATH_TWOPASS
+    assert plan(1, 16392, dtype=rws.BF16).path == rws.PATH_TWOPASS
+    assert plan(1, 16392, dtype=rws.BF16, in_ptr=(1 << 20) + 2).path == rws.PATH_CLUSTER
+    assert plan(1, 32768, dtype=rws.BF16, in_ptr=(1 << 20) + 2).path == rws.PATH_CLUSTER
+    assert plan(1, 32776, dtype=rws.BF16, in_ptr=(1 << 20) + 2).path == rws.PATH_TWOPASS
     forced = plan(1, 16 * 32768, path=rws.PATH_CLUSTER)    # forced: 128 KB slices
     assert forced.cluster == 16 and forced.threads == 1024 and forced.chunks == 8
     assert forced.smem_bytes == 131072

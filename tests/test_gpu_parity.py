@@ -123,8 +123,10 @@ def test_twopass_long_row_automatic():
 def test_16bit_long_rows_cluster_and_twopass(dtype):
     w = wl.random_rows(6, 30_000, dtype=dtype, seed=8, scale=6.0)       # 60 KB rows
     p = rws.plan(w.n_rows, w.n_cols, dtype=dtype)
-    assert p.path == rws.PATH_CLUSTER
-    parity.compare(run(w), parity.expected(w), dtype, "16-bit cluster")
+    assert p.path == rws.PATH_TWOPASS and p.bulk_copy == 1 and p.cluster == 1
+    parity.compare(run(w), parity.expected(w), dtype, "16-bit two-pass, one CTA")
+    assert rws.plan(w.n_rows, w.n_cols, dtype=dtype, path=rws.PATH_CLUSTER).cluster == 2
+    parity.compare(run(w, rws.PATH_CLUSTER), parity.expected(w), dtype, "16-bit cluster")
     w = wl.random_rows(6, 250_000, dtype=dtype, seed=8, scale=6.0)      # 500 KB rows
     p = rws.plan(w.n_rows, w.n_cols, dtype=dtype)
     assert p.path == rws.PATH_TWOPASS and p.bulk_copy == 1
