@@ -55,7 +55,7 @@ KERNELS = {
     ("cluster", 0): ("row_slices_kernel", ["row_slices.cu"]),
     ("cluster", 1): ("row_slices_kernel", ["row_slices.cu"]),
     ("twopass", 0): ("twopass_kernel", ["twopass.cu"]),
-    ("twopass", 1): ("stream_rows_kernel", ["stream_rows.cu"]),
+    ("twopass", 1): ("stream_rows_kernel", ["stream_rows.cu", "cluster_ring.cuh"]),
 }
 COMMON_SOURCES = ["common.cuh", "kernels.h"]
 DTYPE_NAMES = {wl.F32: "f32", wl.BF16: "bf16", wl.F16: "f16"}

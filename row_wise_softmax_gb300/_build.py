@@ -20,10 +20,10 @@ LIB = os.path.join(PKG, "libsoftmax.so")
 
 SOURCES = ["softmax_abi.cu", "plan.cpp", "warp_rows.cu", "tile_rows.cu", "row_slices.cu",
            "row_slices_options.cu", "twopass.cu", "stream_rows.cu", "backward_rows.cu",
-           "columns.cu", "attention_mma.cu", "attention_tc.cu"]
+           "columns.cu", "columns_stream.cu", "attention_mma.cu", "attention_tc.cu"]
 # Sources that include another source file.
 INCLUDED = {"row_slices_options.cu": ["row_slices.cu"]}
-HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "kernels.h")] + [
+HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "kernels.h", "cluster_ring.cuh")] + [
     os.path.join(INCLUDE, "softmax.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -349,6 +349,8 @@ ColumnsShape columns_shape(const StridedProblem& p, int max_smem_per_block)
 
 cudaError_t launch_strided(const StridedProblem& p, const ColumnsShape& sh, cudaStream_t s)
 {
+    if (sh.ok && sh.stream)
+        return launch_columns_stream(p, sh, s);
     if (sh.ok) {
         if (p.dtype == SOFTMAX_F32) return launch_columns<float>(p, sh, s);
         if (p.dtype == SOFTMAX_BF16) return launch_columns<BF16Bits>(p, sh, s);

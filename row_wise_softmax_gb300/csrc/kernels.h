@@ -151,7 +151,9 @@ struct StridedProblem {
 // kernel.
 struct ColumnsShape {
     bool ok;
-    int cluster, rows_per_cta, smem_bytes;
+    bool stream;            // the staged (tensor-copy) columns kernel
+    int row_bytes;          // staged kernel: tile width in bytes of a memory row
+    int cluster, rows_per_cta, smem_bytes, stages;
     int64_t tiles;
     bool vec_in, vec_out;
 };
@@ -159,6 +161,12 @@ constexpr int64_t kColumnsRowsPerCta = 512;
 constexpr int64_t kColumnsMaxCluster = 16;
 ColumnsShape columns_shape(const StridedProblem& p, int max_smem_per_block);
 cudaError_t launch_strided(const StridedProblem& p, const ColumnsShape& sh, cudaStream_t s);
+// Staged columns kernel (columns_stream.cu): 16 KB boxes of a tile's memory
+// row segments by the tensor memory accelerator, two passes, clusters split
+// the memory rows.  ok = false when the input layout does not allow it.
+ColumnsShape columns_stream_shape(const StridedProblem& p, int sm_count, int max_smem_per_sm);
+cudaError_t launch_columns_stream(const StridedProblem& p, const ColumnsShape& sh, cudaStream_t s);
+unsigned read_error_columns_stream(bool clear);
 
 // Attention forward (attention_mma.cu): O = softmax(scale Q K^T, mask) V per
 // (batch, head); q, o [bh][n_q][head_dim], k, v [bh][n_k][head_dim], 16-bit.

@@ -408,7 +408,9 @@ int softmax_strided(const void* in, void* out, int64_t n_rows, int64_t n_cols,
     const rwsm::StridedProblem p{in, out, n_rows, n_cols, in_row_stride, in_col_stride,
                                  out_row_stride, out_col_stride, dtype};
     rwsm::ColumnsShape sh{};
-    if ((in_row_stride == 1 && out_row_stride == 1) || n_rows == 1)
+    if (in_row_stride == 1 && out_row_stride == 1)
+        sh = rwsm::columns_stream_shape(p, d.sm_count, d.max_smem_per_sm);
+    if (!sh.ok && ((in_row_stride == 1 && out_row_stride == 1) || n_rows == 1))
         sh = rwsm::columns_shape(p, d.max_smem_per_block_optin);
     if (rwsm::launch_strided(p, sh, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
@@ -553,6 +555,7 @@ int softmax_device_status(int clear)
     const unsigned e = rwsm::read_error_row_slices(clear != 0) |
                        rwsm::read_error_tile_rows(clear != 0) |
                        rwsm::read_error_stream_rows(clear != 0) |
+                       rwsm::read_error_columns_stream(clear != 0) |
                        rwsm::read_error_attention_tc(clear != 0);
     return e ? SOFTMAX_ERR_DEVICE_TIMEOUT : SOFTMAX_OK;
 }

@@ -67,6 +67,46 @@ def test_column_softmax(dtype):
         parity.compare(got, want, dtype, "columns %dx%d" % (R, C))
 
 
+# Staged columns kernel (16-byte aligned memory-row pitch): boxes of 128
+# memory rows, tiles of 128 bytes of softmax rows.  R (the softmax length)
+# covers one partial box, exact boxes, a box plus one, several CTAs of a
+# cluster with ragged slices; C covers partial tiles and many tiles.
+STAGED_SHAPES = [(1, 32), (127, 36), (128, 64), (129, 96), (1000, 100), (4097, 64),
+                 (20000, 48), (300, 4096)]
+
+
+@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16, wl.F16])
+def test_column_softmax_staged(dtype):
+    esz = 4 if dtype == wl.F32 else 2
+    for i, (R, C) in enumerate(STAGED_SHAPES):
+        if (C * esz) % 16:
+            C += (16 - C * esz % 16) // esz
+        buf = matrix(R, C, dtype, seed=700 + i)
+        got = run_strided(buf, dtype, C, R, 1, C, 1, C, R * C)
+        want = oracle.softmax_strided(buf, C, R, 1, C, dtype)
+        parity.compare(got, want, dtype, "staged columns %dx%d" % (R, C))
+    # A padded input pitch (only C of every ld elements are softmax rows) and
+    # an output pitch that is odd: element stores instead of pairs.
+    R, C, ld = 3000, 40, 48
+    buf = matrix(R, ld, dtype, seed=801)
+    ocs = C + 1
+    got = run_strided(buf, dtype, C, R, 1, ld, 1, ocs, (R - 1) * ocs + C)
+    want = oracle.softmax_strided(buf, C, R, 1, ld, dtype)
+    parity.compare(got, want, dtype, "staged columns padded in, odd out")
+
+
+def test_column_softmax_staged_in_place_bf16():
+    R, C = 5000, 64
+    buf = matrix(R, C, wl.BF16, seed=802)
+    x = torch.from_numpy(buf.view(np.int16)).cuda().view(torch.bfloat16)
+    st = rws.softmax_strided_ptr(x.data_ptr(), x.data_ptr(), C, R, 1, C, 1, C, wl.BF16)
+    assert st == rws.OK
+    torch.cuda.synchronize()
+    flat = x.cpu().view(torch.int16).numpy().view(np.uint16)
+    got = np.ascontiguousarray(flat.reshape(R, C).T)
+    parity.compare(got, oracle.softmax_strided(buf, C, R, 1, C, wl.BF16), wl.BF16, "in place")
+
+
 @pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
 def test_general_strides_gather(dtype):
     # Row stride 3, column stride 7 (rows interleaved); output dense rows.
