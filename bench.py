@@ -600,7 +600,8 @@ def run_ours(args):
             "seconds_per_step": round(t, 4)}
     if rank == 0 and not args.no_per_config:
         per = {}
-        for name in wl.NAMES + wl.EXTRA_NAMES:
+
+        def workload_entry(name):
             wc = w if name == args.workload else wl.make(name)
             pc = rws.plan(wc.n_rows, wc.n_cols, in_row_stride=wc.in_row_stride,
                           out_row_stride=wc.out_row_stride, dtype=wc.dtype)
@@ -610,29 +611,45 @@ def run_ours(args):
             del bc
             med = tot / 50
             gbs = wc.algorithmic_bytes / (med * 1e-3) / 1e9
-            per[name] = {"shape": [wc.n_rows, wc.n_cols], "dtype": DTYPE_NAMES[wc.dtype],
-                         "path": pc.path_name, "plan": str(pc), "mean_ms": round(med, 5),
-                         "copy_same_bytes_GB/s": cal["GB/s"] if cal else None,
-                         "GB/s": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
-                         "frac_of_8000": round(gbs / 8000.0, 4),
-                         "rows_per_s": round(wc.n_rows / (med * 1e-3), 1)}
-            del wc
-        per["causal_bf16_mask_from_indices"] = fused_causal_entry(torch, rws, stream, l2_bytes,
-                                                                  peak)
-        per["backward_f32_4096x4096"] = backward_entry(torch, rws, stream, l2_bytes, peak)
-        per["small_f32_cuda_graph"] = graph_entry(torch, rws, stream, l2_bytes, peak)
+            return {"shape": [wc.n_rows, wc.n_cols], "dtype": DTYPE_NAMES[wc.dtype],
+                    "path": pc.path_name, "plan": str(pc), "mean_ms": round(med, 5),
+                    "copy_same_bytes_GB/s": cal["GB/s"] if cal else None,
+                    "GB/s": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
+                    "frac_of_8000": round(gbs / 8000.0, 4),
+                    "rows_per_s": round(wc.n_rows / (med * 1e-3), 1)}
+
+        entries = [(name, lambda name=name: workload_entry(name))
+                   for name in wl.NAMES + wl.EXTRA_NAMES]
+        entries.append(("causal_bf16_mask_from_indices",
+                        lambda: fused_causal_entry(torch, rws, stream, l2_bytes, peak)))
+        entries.append(("backward_f32_4096x4096",
+                        lambda: backward_entry(torch, rws, stream, l2_bytes, peak)))
+        entries.append(("small_f32_cuda_graph",
+                        lambda: graph_entry(torch, rws, stream, l2_bytes, peak)))
         for impl, tag in ((2, "tcgen05"), (1, "mma_sync")):
-            per["attention_%s_bf16_64x4096x4096_d128" % tag] = attention_entry(
-                torch, rws, stream, impl=impl)
-            per["attention_%s_bf16_64x4096x4096_d128_causal" % tag] = attention_entry(
-                torch, rws, stream, causal=True, impl=impl)
-            per["attention_%s_bf16_64x4096x4096_d64" % tag] = attention_entry(
-                torch, rws, stream, d=64, impl=impl)
-        per["columns_f32_4096x4096"] = columns_entry(torch, rws, stream, l2_bytes, peak)
-        per["columns_bf16_8192x4096"] = columns_entry(torch, rws, stream, l2_bytes, peak,
-                                                      8192, 4096, wl.BF16)
-        per["backward_bf16_32768x1024"] = backward_entry(torch, rws, stream, l2_bytes, peak,
-                                                         32768, 1024, wl.BF16)
+            entries.append(("attention_%s_bf16_64x4096x4096_d128" % tag,
+                            lambda impl=impl: attention_entry(torch, rws, stream, impl=impl)))
+            entries.append(("attention_%s_bf16_64x4096x4096_d128_causal" % tag,
+                            lambda impl=impl: attention_entry(torch, rws, stream, causal=True,
+                                                              impl=impl)))
+            entries.append(("attention_%s_bf16_64x4096x4096_d64" % tag,
+                            lambda impl=impl: attention_entry(torch, rws, stream, d=64,
+                                                              impl=impl)))
+        entries.append(("columns_f32_4096x4096",
+                        lambda: columns_entry(torch, rws, stream, l2_bytes, peak)))
+        entries.append(("columns_bf16_8192x4096",
+                        lambda: columns_entry(torch, rws, stream, l2_bytes, peak, 8192, 4096,
+                                              wl.BF16)))
+        entries.append(("backward_bf16_32768x1024",
+                        lambda: backward_entry(torch, rws, stream, l2_bytes, peak, 32768, 1024,
+                                               wl.BF16)))
+        only = set(args.per_config_only.split(",")) if args.per_config_only else None
+        if only is not None and not only <= {k for k, _ in entries}:
+            raise SystemExit("--per-config-only: unknown entries %s" %
+                             sorted(only - {k for k, _ in entries}))
+        for key, fn in entries:
+            if only is None or key in only:
+                per[key] = fn()
         result["per_config"] = per
     if world > 1:
         import torch.distributed as dist
@@ -679,6 +696,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--per-config-only", default="",
+                    help="comma-separated per_config entries to time (default: all)")
     ap.add_argument("--no-clock-window", action="store_true",
                     help="do not extend the clock-sampling window past the timed steps")
     ap.add_argument("--workload", default=HEADLINE, choices=list(wl.NAMES + wl.EXTRA_NAMES),
