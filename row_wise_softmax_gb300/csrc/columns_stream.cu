@@ -71,6 +71,7 @@ columns_stream_kernel(const __grid_constant__ CUtensorMap map, T* out, int64_t n
     constexpr int B = kColBoxBytes / ROW_BYTES; // memory rows per box
     constexpr int RPW = B / NW;                 // memory rows of a box per warp
     static_assert(LB == 4 || LB == 8 || LB == 16, "lane vector");
+    static_assert(RPW % 2 == 0, "paired arithmetic over a box's rows");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ float red_m[NW][W], red_l[NW][W];
     __shared__ __align__(8) unsigned long long full[kColMaxStages];
@@ -219,18 +220,19 @@ columns_stream_kernel(const __grid_constant__ CUtensorMap map, T* out, int64_t n
                     }
                 }
                 release(s);
+                // Per softmax row: the box's RPW values, two per paired fp32
+                // instruction (rounded as the scalar ones), three-input max.
 #pragma unroll
                 for (int c = 0; c < CPT; ++c) {
-                    float bm = m[c];
+                    float v[RPW];
 #pragma unroll
                     for (int k = 0; k < RPW; ++k)
-                        bm = fmaxf(bm, x[k][c]);
+                        v[k] = x[k][c];
+                    const float bm = frag_max<RPW>(v, m[c]);
                     const float ref = (bm == kNegInf) ? 0.0f : bm;
-                    float sum = 0.0f;
-#pragma unroll
-                    for (int k = 0; k < RPW; ++k)
-                        sum += exp_biased(x[k][c] - ref, kLog2e);
-                    l[c] = l[c] * exp_ftz(m[c] - ref, kLog2e) + sum;
+                    float s0 = 0.0f, s1 = 0.0f;
+                    frag_exp_acc<RPW>(v, ref, kLog2e, s0, s1);
+                    l[c] = l[c] * exp_ftz(m[c] - ref, kLog2e) + (s0 + s1);
                     m[c] = bm;
                 }
             }
@@ -295,9 +297,19 @@ columns_stream_kernel(const __grid_constant__ CUtensorMap map, T* out, int64_t n
                         continue;
                     T* dst = out + (r0 + b * B + row) * ld_out + col0;
                     float y[CPT];
+                    if constexpr (CPT % 2 == 0) {
 #pragma unroll
-                    for (int c = 0; c < CPT; ++c)
-                        y[c] = exp_biased(x[k][c] - m[c], kLog2e) * inv[c];
+                        for (int c = 0; c < CPT; c += 2) {
+                            float d0, d1;
+                            add2(d0, d1, x[k][c], x[k][c + 1], -m[c], -m[c + 1]);
+                            fma2(d0, d1, d0, d1, kLog2e, kLog2e, kExpBias, kExpBias);
+                            mul2(y[c], y[c + 1], ex2_ftz(d0), ex2_ftz(d1), inv[c], inv[c + 1]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < CPT; ++c)
+                            y[c] = exp_biased(x[k][c] - m[c], kLog2e) * inv[c];
+                    }
                     if (VEC_STORES && col0 + CPT <= n_s) {
                         // LB bytes in one store, evict-first.
                         uint32_t w[LB / 4];

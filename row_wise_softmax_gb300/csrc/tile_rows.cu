@@ -135,10 +135,11 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
         }
 
     bool failed = false;                         // CTA-uniform
-    int64_t k = 0;
-    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++k) {
-        const int s = static_cast<int>(k % stages);
-        const uint32_t parity = static_cast<uint32_t>((k / stages) & 1);
+    // Ring stage of the current tile and its phase parity, advanced per tile
+    // (no 64-bit division).
+    int s = 0;
+    uint32_t parity = 0;
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
         const bool ok = failed ? true : mbar_wait_bounded(smem_addr(&full[s]), parity);
         for (int rr = 0; rr < rows_per_warp; ++rr) {
             const int r = warp * rows_per_warp + rr;
@@ -246,6 +247,10 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
             const int64_t next = tile + static_cast<int64_t>(stages) * gridDim.x;
             if (next < n_tiles)
                 issue(s, next);
+        }
+        if (++s == stages) {
+            s = 0;
+            parity ^= 1u;
         }
     }
     if (failed && tid == 0) {
