@@ -210,14 +210,16 @@ columns_stream_kernel(const __grid_constant__ CUtensorMap map, T* out, int64_t n
                 const int64_t valid = len - b * B;       // rows of this box in the slice
                 float x[RPW][CPT];
 #pragma unroll
-                for (int k = 0; k < RPW; ++k) {
-                    const int row = warp + k * NW;
-                    read_row(s, row, x[k]);
-                    if (row >= valid) {
+                for (int k = 0; k < RPW; ++k)
+                    read_row(s, warp + k * NW, x[k]);
+                if (valid < B) {                         // CTA-uniform: only a slice's last box
 #pragma unroll
-                        for (int c = 0; c < CPT; ++c)
-                            x[k][c] = kNegInf;
-                    }
+                    for (int k = 0; k < RPW; ++k)
+                        if (warp + k * NW >= valid) {
+#pragma unroll
+                            for (int c = 0; c < CPT; ++c)
+                                x[k][c] = kNegInf;
+                        }
                 }
                 release(s);
                 // Per softmax row: the box's RPW values, two per paired fp32
@@ -290,12 +292,13 @@ columns_stream_kernel(const __grid_constant__ CUtensorMap map, T* out, int64_t n
                 for (int k = 0; k < RPW; ++k)
                     read_row(s, warp + k * NW, x[k]);
                 release(s);
+                // Memory row warp + k * NW of the box: advance by NW rows.
+                T* dst = out + (r0 + b * B + warp) * ld_out + col0;
+                const int64_t step = static_cast<int64_t>(NW) * ld_out;
 #pragma unroll
-                for (int k = 0; k < RPW; ++k) {
-                    const int row = warp + k * NW;
-                    if (row >= valid)
+                for (int k = 0; k < RPW; ++k, dst += step) {
+                    if (valid < B && warp + k * NW >= valid)
                         continue;
-                    T* dst = out + (r0 + b * B + row) * ld_out + col0;
                     float y[CPT];
                     if constexpr (CPT % 2 == 0) {
 #pragma unroll

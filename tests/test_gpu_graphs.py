@@ -4,7 +4,7 @@ Every kernel is launched with programmatic dependent launch on the caller's
 stream; under stream capture those launches become graph nodes (with their
 programmatic edges).  A graph of many softmax calls replays to the same bits
 as the calls made one by one, for the row path, the options path, the
-backward and the attention forward.
+backward, the attention forward and the column-wise softmax.
 """
 import numpy as np
 import pytest
@@ -101,3 +101,35 @@ def test_graph_of_attention_and_backward():
     torch.cuda.synchronize()
     assert torch.equal(o.view(torch.int16), o_eager.view(torch.int16))
     assert torch.equal(dx, dx_eager)
+
+
+def test_graph_of_column_softmax():
+    """softmax_strided down the columns (the tensor-copy kernel, whose tensor
+    map is a kernel parameter captured with the launch) and the staged-tile
+    kernel (an unaligned memory-row pitch) replay to the eager bits."""
+    cases = []
+    for R, C, dtype in ((3000, 96, wl.F32), (5000, 64, wl.BF16), (700, 33, wl.F32)):
+        w = wl.random_rows(R, C, dtype=dtype, seed=R + C, scale=3.0)
+        x = torch.from_numpy(w.data if dtype == wl.F32 else w.data.view(np.int16)).cuda()
+        if dtype != wl.F32:
+            x = x.view(parity.torch_dtype(dtype))
+        cases.append((R, C, dtype, x))
+    eager = []
+    for R, C, dtype, x in cases:
+        y = torch.empty_like(x)
+        assert rws.softmax_strided_ptr(x.data_ptr(), y.data_ptr(), C, R, 1, C, 1, C, dtype) == rws.OK
+        eager.append(y)
+    torch.cuda.synchronize()
+    outs = [torch.zeros_like(y) for y in eager]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+        h = torch.cuda.current_stream().cuda_stream
+        for (R, C, dtype, x), y in zip(cases, outs):
+            assert rws.softmax_strided_ptr(x.data_ptr(), y.data_ptr(), C, R, 1, C, 1, C, dtype,
+                                           h) == rws.OK
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager, outs):
+        iv = torch.int32 if a.dtype == torch.float32 else torch.int16
+        assert torch.equal(a.view(iv), b.view(iv))
