@@ -200,20 +200,26 @@ stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t 
             }
             const T* st = stage_ptr(s);
             const T* g = src_row + chunk * CHUNK;
+            if (bulk == CHUNK) {                         // CTA-uniform: a whole chunk
 #pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                const int e0 = (tid + k * THREADS) * VEC;
-                if (e0 + VEC <= bulk) {
-                    lds_vec<T, VEC>(st + e0, &x[k * VEC]);
-                } else if (e0 >= clen) {
+                for (int k = 0; k < NV; ++k)
+                    lds_vec<T, VEC>(st + (tid + k * THREADS) * VEC, &x[k * VEC]);
+            } else {
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j)
-                        x[k * VEC + j] = kNegInf;
-                } else {
+                for (int k = 0; k < NV; ++k) {
+                    const int e0 = (tid + k * THREADS) * VEC;
+                    if (e0 + VEC <= bulk) {
+                        lds_vec<T, VEC>(st + e0, &x[k * VEC]);
+                    } else if (e0 >= clen) {
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j) {
-                        const int e = e0 + j;
-                        x[k * VEC + j] = e < clen ? Elem<T>::load1(g + e) : kNegInf;
+                        for (int j = 0; j < VEC; ++j)
+                            x[k * VEC + j] = kNegInf;
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) {
+                            const int e = e0 + j;
+                            x[k * VEC + j] = e < clen ? Elem<T>::load1(g + e) : kNegInf;
+                        }
                     }
                 }
             }
@@ -285,10 +291,11 @@ stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t 
                 take(keep, src, chunk, x);
                 const int clen = chunk_len(chunk);
                 T* d = dst + chunk * CHUNK;
+                const bool whole = OUTVEC && clen == CHUNK;   // CTA-uniform
 #pragma unroll
                 for (int k = 0; k < NV; ++k) {
                     const int e0 = (tid + k * THREADS) * VEC;
-                    if (e0 < clen) {
+                    if (whole || e0 < clen) {
                         // y = exp_biased(x - M) * (1 / L), two elements per
                         // instruction.
                         float* v = &x[k * VEC];
@@ -300,7 +307,7 @@ stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t 
                             mul2(v[j], v[j + 1], ex2_ftz(d0), ex2_ftz(d1), inv, inv);
                         }
                         if constexpr (OUTVEC) {
-                            if (e0 + VEC <= clen)
+                            if (whole || e0 + VEC <= clen)
                                 store16_hint<T>(d + e0, v, 1.0f, stream_pol);
                             else
                                 store_vec_masked<T, VEC>(d, e0, clen, v, 1.0f);
