@@ -35,6 +35,7 @@ __device__ unsigned g_error_tile_rows = 0;
 constexpr int kTileWarps = 4;
 constexpr int kTileThreads = kTileWarps * 32;
 constexpr int kTileMaxStages = 8;
+constexpr int kTileMaxRows = 64;             // rows per tile: 4 warps x up to 16 rows
 constexpr int kTileRingAlign = 128;
 
 template <typename T, int VEC>
@@ -61,6 +62,9 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ __align__(8) unsigned long long full[kTileMaxStages];
     __shared__ unsigned issued[kTileMaxStages];
+    // Options build: each row's kept columns, written by the issuing thread
+    // with the tile's copies (read after the stage's mbarrier completes).
+    __shared__ int row_keep[OPTS ? kTileMaxStages : 1][OPTS ? kTileMaxRows : 1];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float kk = OPTS ? lg.k : kLog2e;       // exponent multiplier, scale * log2 e
@@ -93,7 +97,9 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
             // One pass: each copy raises the phase's byte count before it
             // starts; the single arrival comes after the last copy.
             for (int r = 0; r < nr; ++r) {
-                const uint32_t n = copy_bytes(r0 + r, logits_valid(lg, r0 + r, n_cols));
+                const int64_t lim = logits_valid(lg, r0 + r, n_cols);
+                row_keep[s][r] = static_cast<int>(lim);
+                const uint32_t n = copy_bytes(r0 + r, lim);
                 if (n) {
                     mbar_expect_tx(bar, n);
                     bulk_g2s(smem_addr(row_ptr(s, r)), in + (r0 + r) * ld_in, n, bar);
@@ -151,7 +157,11 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
             // Columns [0, avail) are in shared memory, [avail, lim) is a
             // < 16-byte tail read from HBM, and from lim on the row is masked
             // or padding (-inf).
-            const int lim = static_cast<int>(kept_cols<OPTS>(lg, row, n_cols));
+            int lim;
+            if constexpr (OPTS)
+                lim = row_keep[s][r];
+            else
+                lim = n_cols;
             const int copied = static_cast<int>(copy_bytes(row, lim) / sizeof(T));
             const int avail = copied < lim ? copied : lim;
             // Whole vectors first: a vector that starts below `avail` is read
@@ -171,14 +181,17 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
                 }
             }
             if (OPTS && avail == lim && lim % VEC != 0) {              // warp-uniform
-                // Only the vector holding column lim - 1 straddles the edge:
-                // its copied elements past lim are masked.
+                // Only the vector holding column lim - 1 straddles the edge
+                // (one lane, one chunk): its copied elements past lim are
+                // masked; vectors wholly past lim are already -inf.
 #pragma unroll
                 for (int c = 0; c < CHUNKS; ++c) {
                     const int keep_n = lim - (c * 32 + lane) * VEC;
+                    if (keep_n > 0 && keep_n < VEC) {
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j)
-                        x[c * VEC + j] = j < keep_n ? x[c * VEC + j] : kNegInf;
+                        for (int j = 0; j < VEC; ++j)
+                            x[c * VEC + j] = j < keep_n ? x[c * VEC + j] : kNegInf;
+                    }
                 }
             } else if ((avail | lim) % VEC != 0 || avail < lim) {   // warp-uniform
 #pragma unroll
@@ -359,7 +372,8 @@ cudaError_t launch_chunks(const Problem& p, const softmax_plan_t& plan, cudaStre
 
 cudaError_t launch_tile_rows(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
 {
-    if (plan.stages < 1 || plan.stages > kTileMaxStages)
+    if (plan.stages < 1 || plan.stages > kTileMaxStages || plan.rows_per_warp < 1 ||
+        plan.rows_per_warp * kTileWarps > kTileMaxRows)
         return cudaErrorInvalidValue;
     if (p.dtype == SOFTMAX_F32) {
         if (plan.vec == 4) return launch_chunks<float, 4>(p, plan, s);
