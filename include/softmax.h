@@ -228,12 +228,16 @@ int softmax_attention_forward(const void* q, const void* k, const void* v, void*
  * row-major R x C matrix is n_rows = C, n_cols = R, row strides 1, column
  * strides C.
  *
- *   Unit column strides: the same as softmax_rows.  Unit row strides: the
- *   columns kernel (128-byte tiles of adjacent rows staged in shared memory,
- *   one HBM read and one write per element; rows up to 16 x 512 columns per
- *   cluster of CTAs, longer ones while the tile fits in shared memory).
- *   Other strides, or longer columns: a general gather kernel (correct for
- *   any layout, two reads per element).
+ *   Unit column strides: the same as softmax_rows.  Unit row strides with a
+ *   16-byte aligned input and memory-row pitch: the tensor-copy columns
+ *   kernel (tiles of 128 or 256 bytes of adjacent rows streamed twice in
+ *   16 KB boxes, the second read mostly from L2; clusters of up to 8 CTAs
+ *   split long rows).  Other unit-row-stride layouts: the staged-tile
+ *   columns kernel (128-byte tiles staged in shared memory, one HBM read
+ *   and one write per element; rows up to 16 x 512 columns per cluster of
+ *   CTAs, longer ones while the tile fits in shared memory).  Other
+ *   strides, or longer rows: a general gather kernel (correct for any
+ *   layout, two reads per element).
  *   Strides must be >= 0; the output elements must be distinct (its rows
  *   nested within its columns or the reverse); in and out may be the same
  *   buffer with the same strides, and must not otherwise share bytes.
@@ -321,13 +325,16 @@ typedef struct {
     int vec;             /* elements per global vector access (1 = scalar) */
     int out_vec;         /* elements per global vector store */
     int bulk_copy;       /* 1: rows staged by cp.async.bulk into shared memory */
-    int threads;         /* threads per CTA */
+    int threads;         /* threads per CTA (TWOPASS staged: consumer threads;
+                            the CTA also has one producer warp) */
     int cluster;         /* CTAs per cluster (1: no cluster) */
     int rows_per_warp;   /* WARP path: rows a warp holds at once */
     int chunks;          /* vectors per thread (WARP: per lane per row; CTA and
-                            CLUSTER: 16-byte vectors of the slice) */
+                            CLUSTER: 16-byte vectors of the slice; TWOPASS
+                            staged: 16-byte vectors per thread per ring chunk) */
     int64_t slice_cols;  /* CTA/CLUSTER/TWOPASS: columns owned by one CTA */
-    int stages;          /* CTA/CLUSTER: slices in flight per CTA (ring depth) */
+    int stages;          /* CTA/CLUSTER: slices in flight per CTA; TWOPASS
+                            staged: chunks in the ring (ring depth) */
     int smem_bytes;      /* dynamic shared memory per CTA */
     int64_t grid;        /* CTAs launched; 0 = sized at launch from occupancy
                             (whole waves of resident CTAs, persistent) */
