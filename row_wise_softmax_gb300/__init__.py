@@ -24,7 +24,7 @@ __all__ = [
     "softmax_rows", "softmax_rows_ptr", "softmax_rows_ex_ptr", "softmax_rows_planned_ptr",
     "visible_cols", "softmax_backward", "softmax_backward_rows_ptr", "softmax",
     "softmax_strided_ptr", "attention", "attention_forward_ptr", "AttentionOptions",
-    "ATT_AUTO", "ATT_MMA", "ATT_TCGEN05",
+    "ATT_AUTO", "ATT_MMA", "ATT_TCGEN05", "ATT_TCGEN05_PINGPONG",
     "Options", "softmax_rows_host", "plan", "plan_for_device",
     "status_string", "device_status", "launch_count", "selftest_wait_timeout", "abi_version", "GB300",
 ]
@@ -63,7 +63,7 @@ class AttentionOptions(ctypes.Structure):
                 ("causal_offset", ctypes.c_int64), ("impl", ctypes.c_int32)]
 
 
-ATT_AUTO, ATT_MMA, ATT_TCGEN05 = 0, 1, 2
+ATT_AUTO, ATT_MMA, ATT_TCGEN05, ATT_TCGEN05_PINGPONG = 0, 1, 2, 3
 
 
 class Plan(ctypes.Structure):

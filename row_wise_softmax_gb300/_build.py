@@ -23,7 +23,8 @@ SOURCES = ["softmax_abi.cu", "plan.cpp", "warp_rows.cu", "tile_rows.cu", "row_sl
            "columns.cu", "columns_stream.cu", "attention_mma.cu", "attention_tc.cu"]
 # Sources that include another source file.
 INCLUDED = {"row_slices_options.cu": ["row_slices.cu"]}
-HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "kernels.h", "cluster_ring.cuh")] + [
+HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "kernels.h", "cluster_ring.cuh",
+                                            "tensor_map.h", "attention_pp.h")] + [
     os.path.join(INCLUDE, "softmax.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -29,8 +29,10 @@
 //
 // Every mbarrier wait is bounded; on a timeout the kernel records the error
 // word, stops issuing, waits (bounded) for what it issued and frees TMEM.
+#include "attention_pp.h"
 #include "common.cuh"
 #include "kernels.h"
+#include "tensor_map.h"
 
 #include <atomic>
 
@@ -224,7 +226,7 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
                     int64_t n_q, int64_t n_k, float scale_log2, int64_t offset)
 {
     constexpr bool kBF16 = sizeof(T) == 2 && Elem<T>::kNegInfBits == 0xff80u;
-    constexpr uint32_t Q_BYTES = kTcBM * D * 2, KV_BYTES = BN * D * 2, P_BYTES = kTcBM * BN * 2;
+    constexpr uint32_t Q_BYTES = kTcBM * D * 2, KV_BYTES = BN * D * 2;
     constexpr uint32_t SBO_QK = (D / 8) * 128;              // 8-row band of Q, K
     constexpr uint32_t SBO_P = (BN / 8) * 128;              // 8-row band of P
     constexpr uint32_t SBO_V = (BN / 8) * 128;              // 8-column band of V
@@ -465,6 +467,457 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
         tmem_dealloc(tmem, kTmemCols);
 }
 
+// ---- two query tiles per CTA in ping-pong ---------------------------------
+//
+//   CTA      256 queries of one (batch, head): tile A (queries 0..127) and
+//            tile B (128..255).  Warps 0-3 run tile A's softmax, warps 4-7
+//            tile B's (thread t of a warpgroup owns query row t = TMEM lane
+//            t); warp 8 stages Q, K and V with cp.async and its lane 0 issues
+//            every tcgen05.mma.
+//   TMEM     S_A at column 0, S_B at BN, O_A at 2 BN, O_B at 2 BN + D.
+//   order    per key tile t the control lane waits for P_A(t) (bar_p[A]),
+//            issues O_A += P_A V(t) and S_A(t+1) = Q_A K(t+1)^T, commits
+//            (bar_s[A]); then the same for B.  So the tensor cores compute
+//            one tile's products while the other tile's warpgroup runs its
+//            softmax, and every K/V tile staged serves 256 queries.  A
+//            warpgroup's wait on S_X(t+1) also covers O_X += P_X V(t) (one
+//            commit covers every earlier operation of the issuing thread), so
+//            P_X and O_X are free for it when S_X(t+1) has landed.
+//   buffers  K and V double-buffered: K(t+2) refills the buffer of K(t) once
+//            both S(t) have been read by the warpgroups (bar_p), V(t+2) once
+//            S_B(t+1) (issued after both P V(t)) has completed.
+//
+// Every wait is bounded; a timed-out wait records the error word and the
+// kernel stops issuing, waits (bounded) for what it issued and frees TMEM.
+constexpr int kPpWarpgroups = 2;
+constexpr int kPpThreads = kPpWarpgroups * 128 + 32;
+
+template <int D>
+__host__ __device__ constexpr uint32_t pp_tmem_cols(int bn)
+{
+    return 2 * bn + 2 * D <= 256 ? 256u : 512u;
+}
+
+template <typename T, int D, int BN, bool CAUSAL>
+__global__ void __launch_bounds__(kPpThreads, 1)
+attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
+                    const __grid_constant__ CUtensorMap map_k,
+                    const __grid_constant__ CUtensorMap map_v, T* o, float* lse, int64_t bh,
+                    int64_t n_q, int64_t n_k, float scale_log2, int64_t offset)
+{
+    constexpr bool kBF16 = sizeof(T) == 2 && Elem<T>::kNegInfBits == 0xff80u;
+    constexpr uint32_t QT_BYTES = kTcBM * D * 2, KV_BYTES = BN * D * 2, P_BYTES = kTcBM * BN * 2;
+    constexpr uint32_t SBO_P = (BN / 8) * 128;
+    constexpr uint32_t SBO_V = (BN / 8) * 128;
+    constexpr uint32_t IDESC_S = umma_idesc(kTcBM, BN, kBF16, false);
+    constexpr uint32_t IDESC_PV = umma_idesc(kTcBM, D, kBF16, true);
+    constexpr uint32_t TMEM_COLS = pp_tmem_cols<D>(BN);
+    constexpr int NCH = BN / 32;
+    constexpr int CTRL = kPpWarpgroups * 4;                  // the control warp
+    extern __shared__ __align__(128) unsigned char tc_smem[];
+    __shared__ __align__(8) unsigned long long bar_s[2], bar_p[2], bar_fin[2], bar_drain;
+    __shared__ __align__(8) unsigned long long q_full, k_full[2], v_full[2];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int s_failed;
+
+    const uint32_t base = (smem_addr(tc_smem) + 127u) & ~127u;
+    const uint32_t sQ = base, sK = sQ + 2 * QT_BYTES, sV = sK + 2 * KV_BYTES,
+                   sP = sV + 2 * KV_BYTES;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t n_qt = (n_q + 2 * kTcBM - 1) / (2 * kTcBM);
+    const int64_t b = blockIdx.x / n_qt;
+    int64_t qt = blockIdx.x % n_qt;
+    if (CAUSAL)
+        qt = n_qt - 1 - qt;
+    const int64_t q0 = qt * 2 * kTcBM;
+    int64_t n_kt = (n_k + BN - 1) / BN;
+    if (CAUSAL) {
+        const int64_t last = q0 + 2 * kTcBM - 1 + offset;    // the CTA's last query
+        const int64_t lim = last < 0 ? 0 : last / BN + 1;
+        n_kt = lim < n_kt ? lim : n_kt;
+    }
+
+    if (warp == 0) {
+        tmem_alloc(smem_addr(&tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(smem_addr(&bar_s[x]), 1);
+            mbar_init(smem_addr(&bar_p[x]), 128);
+            mbar_init(smem_addr(&bar_fin[x]), 1);
+        }
+        mbar_init(smem_addr(&bar_drain), 1);
+        mbar_init(smem_addr(&q_full), 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(smem_addr(&k_full[x]), 1);
+            mbar_init(smem_addr(&v_full[x]), 1);
+        }
+        s_failed = 0;
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    pdl_launch_dependents();
+    pdl_wait();
+
+    if (warp == CTRL) {
+        // ------------------------------------------------------ control warp
+        // Lane 0 issues every copy (the tensor memory accelerator) and every
+        // product.  An operand tile lands as D/8 boxes of 8 elements x ROWS
+        // rows: box c (elements 8c..8c+7 of every row) is ROWS contiguous
+        // 16-byte rows, i.e. ROWS/8 core matrices; so core matrix (row band i,
+        // element chunk c) sits at c * ROWS * 16 + i * 128.  For Q and K
+        // (K-major) that is LBO = ROWS * 16 between K-adjacent core matrices
+        // and SBO = 128 between row bands; for V (MN-major, rows = keys) it is
+        // the canonical layout already used for P V.  Rows past a head's end
+        // are zero-filled by the copy engine (the tensor maps are 3-D:
+        // element, row, head).
+        if (lane == 0) {
+            bool failed = false;
+            auto wait1 = [&](uint32_t bar, uint32_t parity) {
+                if (!failed && !mbar_wait_bounded(bar, parity)) {
+                    failed = true;
+                    *reinterpret_cast<volatile int*>(&s_failed) = 1;
+                }
+            };
+            auto tma3 = [&](uint32_t dst, const CUtensorMap* map, int xe, int64_t row, uint32_t bar) {
+                asm volatile(
+                    "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                    " [%0], [%1, {%2, %3, %4}], [%5];"
+                    :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(xe),
+                       "r"(static_cast<int>(row)), "r"(static_cast<int>(b)), "r"(bar)
+                    : "memory");
+            };
+            auto load_rows = [&](uint32_t dst, const CUtensorMap* map, int rows, int64_t row0,
+                                 uint32_t bar, uint32_t bytes) {
+                mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c)
+                    tma3(dst + static_cast<uint32_t>(c * rows * 16), map, c * 8, row0, bar);
+            };
+            // Copies issued and waited for, so that a failed wait can still
+            // drain what is in flight before the CTA exits.
+            int64_t k_issued = 0, v_issued = 0, k_waited = 0, v_waited = 0;
+            bool q_issued = false;
+            auto load_k = [&](int64_t t) {
+                load_rows(sK + static_cast<uint32_t>(t & 1) * KV_BYTES, &map_k, BN, t * BN,
+                          smem_addr(&k_full[t & 1]), KV_BYTES);
+                k_issued = t + 1;
+            };
+            auto load_v = [&](int64_t t) {
+                load_rows(sV + static_cast<uint32_t>(t & 1) * KV_BYTES, &map_v, BN, t * BN,
+                          smem_addr(&v_full[t & 1]), KV_BYTES);
+                v_issued = t + 1;
+            };
+            auto issue_s = [&](int x, int64_t t) {
+                const uint32_t cK = sK + static_cast<uint32_t>(t & 1) * KV_BYTES;
+                const uint32_t qx = sQ + static_cast<uint32_t>(x) * QT_BYTES;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                    umma_f16(tmem + static_cast<uint32_t>(x * BN),
+                             smem_desc(qx + ks * 2 * (kTcBM * 16), kTcBM * 16, 128),
+                             smem_desc(cK + ks * 2 * (BN * 16), BN * 16, 128), IDESC_S,
+                             ks > 0 ? 1u : 0u);
+            };
+            auto issue_pv = [&](int x, int64_t t) {
+                const uint32_t cV = sV + static_cast<uint32_t>(t & 1) * KV_BYTES;
+                const uint32_t px = sP + static_cast<uint32_t>(x) * P_BYTES;
+#pragma unroll
+                for (int ks = 0; ks < BN / 16; ++ks)
+                    umma_f16(tmem + static_cast<uint32_t>(2 * BN + x * D),
+                             smem_desc(px + ks * 256, 128, SBO_P),
+                             smem_desc(cV + ks * 256, 128, SBO_V), IDESC_PV,
+                             (t > 0 || ks > 0) ? 1u : 0u);
+            };
+            asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&map_q)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&map_k)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&map_v)) : "memory");
+            if (n_kt > 0) {
+                load_rows(sQ, &map_q, kTcBM, q0, smem_addr(&q_full), 2 * QT_BYTES);
+                q_issued = true;
+                // (the second Q tile completes on the same barrier)
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c)
+                    tma3(sQ + QT_BYTES + static_cast<uint32_t>(c * kTcBM * 16), &map_q, c * 8,
+                         q0 + kTcBM, smem_addr(&q_full));
+                load_k(0);
+                load_v(0);
+                if (n_kt > 1) {
+                    load_k(1);
+                    load_v(1);
+                }
+                wait1(smem_addr(&q_full), 0u);
+                wait1(smem_addr(&k_full[0]), 0u);
+                if (!failed) {
+                    q_issued = false;
+                    k_waited = 1;
+                    tc_fence_after();
+                    issue_s(0, 0);
+                    umma_commit(smem_addr(&bar_s[0]));
+                    issue_s(1, 0);
+                    umma_commit(smem_addr(&bar_s[1]));
+                }
+            }
+            for (int64_t t = 0; t < n_kt && !failed; ++t) {
+                const bool more = t + 1 < n_kt;
+                if (more) {
+                    wait1(smem_addr(&k_full[(t + 1) & 1]), static_cast<uint32_t>(((t + 1) >> 1) & 1));
+                    k_waited = failed ? k_waited : t + 2;
+                }
+                wait1(smem_addr(&v_full[t & 1]), static_cast<uint32_t>((t >> 1) & 1));
+                v_waited = failed ? v_waited : t + 1;
+                for (int x = 0; x < 2 && !failed; ++x) {
+                    wait1(smem_addr(&bar_p[x]), static_cast<uint32_t>(t & 1));   // P_X(t) written
+                    if (failed)
+                        break;
+                    tc_fence_after();
+                    issue_pv(x, t);
+                    if (more)
+                        issue_s(x, t + 1);
+                    umma_commit(smem_addr(more ? &bar_s[x] : &bar_fin[x]));
+                }
+                if (failed || t + 2 >= n_kt)
+                    continue;
+                // K(t + 2) into K(t)'s buffer: both S(t) were read (bar_p).
+                fence_proxy_async_smem();
+                load_k(t + 2);
+                // V(t + 2) into V(t)'s buffer once both P V(t) have completed:
+                // S_B(t + 1), committed after them, has.
+                wait1(smem_addr(&bar_s[1]), static_cast<uint32_t>((t + 1) & 1));
+                if (!failed)
+                    load_v(t + 2);
+            }
+            if (failed) {
+                // Let the copies still in flight land (each wait bounded).
+                if (q_issued)
+                    mbar_wait_bounded(smem_addr(&q_full), 0u);
+                for (; k_waited < k_issued; ++k_waited)
+                    mbar_wait_bounded(smem_addr(&k_full[k_waited & 1]),
+                                      static_cast<uint32_t>((k_waited >> 1) & 1));
+                for (; v_waited < v_issued; ++v_waited)
+                    mbar_wait_bounded(smem_addr(&v_full[v_waited & 1]),
+                                      static_cast<uint32_t>((v_waited >> 1) & 1));
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- softmax warpgroups
+        const int x = warp >> 2;                             // 0: tile A, 1: tile B
+        const int r = tid & 127;                             // row of the tile = TMEM lane
+        const int64_t qx0 = q0 + static_cast<int64_t>(x) * kTcBM;
+        const int64_t qi = qx0 + r;                          // this thread's query
+        const uint32_t t_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const uint32_t s_col = static_cast<uint32_t>(x * BN);
+        const uint32_t o_col = static_cast<uint32_t>(2 * BN + x * D);
+        const uint32_t px = sP + static_cast<uint32_t>(x) * P_BYTES;
+        float m = kNegInf, l = 0.0f;
+        bool failed = false;                                 // warp-uniform
+        for (int64_t t = 0; t < n_kt; ++t) {
+            const bool ok = failed || mbar_wait_bounded(smem_addr(&bar_s[x]), static_cast<uint32_t>(t & 1));
+            if (__any_sync(0xffffffffu, !ok) && !failed) {
+                failed = true;
+                *reinterpret_cast<volatile int*>(&s_failed) = 1;
+            }
+            tc_fence_after();
+            const int64_t k0 = t * BN;
+            float mx = kNegInf;
+            float sv[NCH][32];
+#pragma unroll
+            for (int c = 0; c < NCH; ++c)
+                tmem_ld32(t_row + s_col + c * 32, sv[c]);
+            tmem_wait_ld();
+            const bool edge = k0 + BN > n_k || (CAUSAL && k0 + BN - 1 > qx0 + offset);
+            if (edge) {
+                int64_t lim = n_k - k0;                      // keys of the tile kept
+                if (CAUSAL && qi + offset + 1 - k0 < lim)
+                    lim = qi + offset + 1 - k0;
+                const int keep = static_cast<int>(lim < 0 ? 0 : (lim > BN ? BN : lim));
+#pragma unroll
+                for (int c = 0; c < NCH; ++c)
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (c * 32 + j >= keep)
+                            sv[c][j] = kNegInf;
+            }
+#pragma unroll
+            for (int c = 0; c < NCH; ++c)
+#pragma unroll
+                for (int j = 0; j < 32; j += 2)
+                    mx = max3(mx, sv[c][j], sv[c][j + 1]);
+            // Lazy rescaling as in attention_tc_kernel: the reference m moves
+            // only when a tile's max exceeds it by more than 2^8.
+            const float mx_s = mx * scale_log2;
+            float alpha = 1.0f;
+            if (mx_s > m + kLazyRescaleLog2) {
+                alpha = ex2_ftz(m - mx_s);
+                m = mx_s;
+            }
+            const float ref = m == kNegInf ? 0.0f : m;
+            float sum = 0.0f;
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    float p[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        p[e] = ex2_ftz(fmaf(sv[c][g * 8 + e], scale_log2, -ref));
+                        sum += p[e];
+                    }
+                    const uint32_t w0 = Elem<T>::pack2(p[0], p[1]), w1 = Elem<T>::pack2(p[2], p[3]);
+                    const uint32_t w2 = Elem<T>::pack2(p[4], p[5]), w3 = Elem<T>::pack2(p[6], p[7]);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                                 :: "r"(px + kmajor_off(r, c * 4 + g, BN)), "r"(w0), "r"(w1),
+                                    "r"(w2), "r"(w3) : "memory");
+                }
+            }
+            l = l * alpha + sum;
+            if (t > 0 && !__all_sync(0xffffffffu, alpha == 1.0f)) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    float ov[32];
+                    tmem_ld32(t_row + o_col + c * 32, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        ov[j] *= alpha;
+                    tmem_st32(t_row + o_col + c * 32, ov);
+                }
+                tmem_wait_st();
+            }
+            fence_proxy_async_smem();                        // P -> tensor cores
+            tc_fence_before();
+            mbar_arrive(smem_addr(&bar_p[x]));               // release: P_X(t), O_X rescaled
+        }
+        if (n_kt > 0) {
+            const bool ok = failed || mbar_wait_bounded(smem_addr(&bar_fin[x]), 0u);
+            if (__any_sync(0xffffffffu, !ok) && !failed) {
+                failed = true;
+                *reinterpret_cast<volatile int*>(&s_failed) = 1;
+            }
+            tc_fence_after();
+        }
+        if (!failed) {
+            const float inv = 1.0f / l;
+            unsigned short* go = reinterpret_cast<unsigned short*>(o) + b * n_q * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                float ov[32];
+                tmem_ld32(t_row + o_col + c * 32, ov);
+                tmem_wait_ld();
+                if (qi < n_q && n_kt > 0) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        uint4 w;
+                        w.x = Elem<T>::pack2(ov[g * 8 + 0] * inv, ov[g * 8 + 1] * inv);
+                        w.y = Elem<T>::pack2(ov[g * 8 + 2] * inv, ov[g * 8 + 3] * inv);
+                        w.z = Elem<T>::pack2(ov[g * 8 + 4] * inv, ov[g * 8 + 5] * inv);
+                        w.w = Elem<T>::pack2(ov[g * 8 + 6] * inv, ov[g * 8 + 7] * inv);
+                        *reinterpret_cast<uint4*>(go + qi * D + c * 32 + g * 8) = w;
+                    }
+                }
+            }
+            if (n_kt == 0 && qi < n_q) {                     // no key at all: NaN rows
+                const float nan = __int_as_float(0x7fc00000);
+                for (int d0 = 0; d0 < D; d0 += 2)
+                    *reinterpret_cast<uint32_t*>(go + qi * D + d0) = Elem<T>::pack2(nan, nan);
+            }
+            if (lse && qi < n_q)
+                lse[b * n_q + qi] = l > 0.0f ? (m + __log2f(l)) * 0.69314718055994531f : kNegInf;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == CTRL * 32 && *reinterpret_cast<volatile int*>(&s_failed)) {
+        // One more commit: it arrives once every tensor-core operation this
+        // thread issued has completed; wait for it (bounded) before TMEM is
+        // freed.
+        atomicOr(&g_error_attention_tc, kErrMbarrierTimeout);
+        tc_fence_after();
+        umma_commit(smem_addr(&bar_drain));
+        mbar_wait_bounded(smem_addr(&bar_drain), 0u);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// 3-D tensor map of a [bh][n][D] operand (element, row, head) with boxes of
+// 8 elements x `rows` rows of one head: rows past a head's end read as zero.
+inline bool pp_tensor_map(CUtensorMap* map, const void* ptr, int64_t bh, int64_t n, int d,
+                          int rows, int dtype)
+{
+    auto encode = tensor_map_encoder();
+    if (!encode || bh >= (int64_t{1} << 31) || n >= (int64_t{1} << 31))
+        return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n),
+                                static_cast<cuuint64_t>(bh)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(n) * d * 2};
+    const cuuint32_t box[3] = {8u, static_cast<cuuint32_t>(rows), 1u};
+    const cuuint32_t estride[3] = {1u, 1u, 1u};
+    return encode(map, dtype == SOFTMAX_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  3, const_cast<void*>(ptr), dims, strides, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+template <typename T, int D, bool CAUSAL>
+cudaError_t launch_pp(const AttentionProblem& p, cudaStream_t s)
+{
+    constexpr int BN = 64;
+    auto* kern = attention_pp_kernel<T, D, BN, CAUSAL>;
+    const int smem = (2 * kTcBM * D + 4 * BN * D + 2 * kTcBM * BN) * 2 + 128;
+    static std::atomic<bool> attr_set[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    if (!attr_set[dev].load()) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess)
+            return e;
+        attr_set[dev].store(true);
+    }
+    CUtensorMap mq, mk, mv;
+    if (!pp_tensor_map(&mq, p.q, p.bh, p.n_q, D, kTcBM, p.dtype) ||
+        !pp_tensor_map(&mk, p.k, p.bh, p.n_k, D, BN, p.dtype) ||
+        !pp_tensor_map(&mv, p.v, p.bh, p.n_k, D, BN, p.dtype))
+        return cudaErrorNotSupported;                    // nothing launched
+    const int64_t n_qt = (p.n_q + 2 * kTcBM - 1) / (2 * kTcBM);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(n_qt * p.bh), 1, 1);
+    cfg.blockDim = dim3(kPpThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = static_cast<unsigned>(launch_attrs(attr, 1));
+    const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, static_cast<T*>(p.o),
+                                               p.lse, p.bh, p.n_q, p.n_k, scale_log2, p.offset);
+    note_launch();
+    return err;
+}
+
+template <typename T>
+cudaError_t launch_pp_t(const AttentionProblem& p, cudaStream_t s)
+{
+    if (p.head_dim == 64)
+        return p.causal ? launch_pp<T, 64, true>(p, s) : launch_pp<T, 64, false>(p, s);
+    if (p.head_dim == 128)
+        return p.causal ? launch_pp<T, 128, true>(p, s) : launch_pp<T, 128, false>(p, s);
+    return cudaErrorInvalidValue;
+}
+
 template <typename T, int D, int BN, bool CAUSAL>
 cudaError_t launch_tc(const AttentionProblem& p, cudaStream_t s)
 {
@@ -525,6 +978,13 @@ cudaError_t launch_attention_tc(const AttentionProblem& p, cudaStream_t s)
     if (p.bh * ((p.n_q + kTcBM - 1) / kTcBM) > 0x7fffffff)
         return cudaErrorInvalidValue;
     return p.dtype == SOFTMAX_BF16 ? launch_tc_t<BF16Bits>(p, s) : launch_tc_t<F16Bits>(p, s);
+}
+
+cudaError_t launch_attention_pp(const AttentionProblem& p, cudaStream_t s)
+{
+    if (p.bh * ((p.n_q + 2 * kTcBM - 1) / (2 * kTcBM)) > 0x7fffffff)
+        return cudaErrorInvalidValue;
+    return p.dtype == SOFTMAX_BF16 ? launch_pp_t<BF16Bits>(p, s) : launch_pp_t<F16Bits>(p, s);
 }
 
 unsigned read_error_attention_tc(bool clear)

@@ -31,8 +31,7 @@
 #include "cluster_ring.cuh"
 #include "common.cuh"
 #include "kernels.h"
-
-#include <cudaTypedefs.h>
+#include "tensor_map.h"
 
 #include <atomic>
 
@@ -355,23 +354,6 @@ columns_stream_kernel(const __grid_constant__ CUtensorMap map, T* out, int64_t n
             if (issued[s])
                 mbar_wait_bounded(smem_addr(&full[s]), (issued[s] - 1) & 1u);
     }
-}
-
-// The driver's tensor-map encoder, looked up once through the runtime.
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess) {
-            cudaGetLastError();
-            return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
-        }
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }();
-    return fn;
 }
 
 constexpr int kMaxDevices = 64;

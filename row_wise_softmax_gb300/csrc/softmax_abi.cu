@@ -2,6 +2,7 @@
 // device description cache, dispatch to the path launchers, host-buffer
 // staging, status strings.  No C++ exception crosses this boundary and the
 // library allocates no memory.
+#include "attention_pp.h"
 #include "kernels.h"
 
 #include <cmath>
@@ -311,7 +312,7 @@ int softmax_attention_forward(const void* q, const void* k, const void* v, void*
         const int64_t big = int64_t{1} << 62;
         if (options->causal_offset >= big || options->causal_offset <= -big)
             return SOFTMAX_ERR_INVALID_ARG;
-        if (options->impl < 0 || options->impl > 2)
+        if (options->impl < 0 || options->impl > 3)
             return SOFTMAX_ERR_INVALID_ARG;
         scale = options->scale;
         causal = options->causal;
@@ -346,12 +347,24 @@ int softmax_attention_forward(const void* q, const void* k, const void* v, void*
         return ds;
     const rwsm::AttentionProblem p{q, k, v, o, lse, batch_heads, n_q, n_k, head_dim, dtype,
                                    scale, causal, offset};
-    // The library's choice: the tcgen05 kernel (faster at both head
-    // dimensions on GB300).
-    if (impl == 0)
-        impl = 2;
-    const cudaError_t err = impl == 1 ? rwsm::launch_attention_mma(p, static_cast<cudaStream_t>(stream))
-                                      : rwsm::launch_attention_tc(p, static_cast<cudaStream_t>(stream));
+    // The library's choice (measured on GB300, 64 heads x 4096 queries and
+    // keys): the ping-pong kernel at head dimension 64, the single-tile one
+    // at 128; the single-tile one also wherever the ping-pong kernel cannot
+    // run (no tensor-map encoder, sizes past its 32-bit copy coordinates).
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t err;
+    if (impl == 1) {
+        err = rwsm::launch_attention_mma(p, st);
+    } else if (impl == 3 || (impl == 0 && head_dim == 64)) {
+        err = rwsm::launch_attention_pp(p, st);
+        if (err == cudaErrorNotSupported) {
+            if (impl == 3)
+                return SOFTMAX_ERR_UNSUPPORTED;
+            err = rwsm::launch_attention_tc(p, st);
+        }
+    } else {
+        err = rwsm::launch_attention_tc(p, st);
+    }
     if (err != cudaSuccess) {
         cudaGetLastError();
         return SOFTMAX_ERR_CUDA;

@@ -78,10 +78,11 @@ CASES = [  # bh, n_q, n_k, d, causal, offset
 ]
 
 
-IMPLS = [rws.ATT_MMA, rws.ATT_TCGEN05]
+IMPLS = [rws.ATT_MMA, rws.ATT_TCGEN05, rws.ATT_TCGEN05_PINGPONG]
+IMPL_IDS = ["mma_sync", "tcgen05", "tcgen05_pingpong"]
 
 
-@pytest.mark.parametrize("impl", IMPLS, ids=["mma_sync", "tcgen05"])
+@pytest.mark.parametrize("impl", IMPLS, ids=IMPL_IDS)
 @pytest.mark.parametrize("dtype", [wl.BF16, wl.F16])
 def test_attention_cases(dtype, impl):
     for i, (bh, n_q, n_k, d, causal, offset) in enumerate(CASES):
@@ -91,28 +92,29 @@ def test_attention_cases(dtype, impl):
 
 
 def test_attention_kernels_agree():
-    """The tcgen05 and mma.sync kernels on the same inputs agree within the
+    """The tcgen05 kernels and the mma.sync kernel on the same inputs agree within the
     P-rounding error bound (both are checked against the oracle elsewhere;
     their fp32 sums run in different orders): |a - b| <= 2^-7 (1 + |a|) for
     N(0, 1) values."""
     for causal in (False, True):
         a = run(4, 300, 300, 128, wl.BF16, 71, causal=causal, impl=rws.ATT_MMA)[0]
-        b = run(4, 300, 300, 128, wl.BF16, 71, causal=causal, impl=rws.ATT_TCGEN05)[0]
-        assert np.array_equal(np.isnan(a), np.isnan(b))
-        ok = ~np.isnan(a)
-        excess = np.abs(a[ok] - b[ok]) - 2.0 ** -7 * (1.0 + np.abs(a[ok]))
-        assert np.all(excess <= 0), float(excess.max())
-        assert np.mean(a[ok] == b[ok]) > 0.5            # mostly the same bf16 values
+        for other in (rws.ATT_TCGEN05, rws.ATT_TCGEN05_PINGPONG):
+            b = run(4, 300, 300, 128, wl.BF16, 71, causal=causal, impl=other)[0]
+            assert np.array_equal(np.isnan(a), np.isnan(b))
+            ok = ~np.isnan(a)
+            excess = np.abs(a[ok] - b[ok]) - 2.0 ** -7 * (1.0 + np.abs(a[ok]))
+            assert np.all(excess <= 0), float(excess.max())
+            assert np.mean(a[ok] == b[ok]) > 0.5        # mostly the same bf16 values
 
 
-@pytest.mark.parametrize("impl", IMPLS, ids=["mma_sync", "tcgen05"])
+@pytest.mark.parametrize("impl", IMPLS, ids=IMPL_IDS)
 def test_attention_scale_and_large_scores(impl):
     """An explicit scale, and scores spread over +-100 (queries scaled by 8)."""
     o, lse, q, k, v = run(2, 64, 256, 64, wl.BF16, 9, scale=0.3, qscale=8.0, impl=impl)
     check(o, lse, q, k, v, wl.BF16, 0.3, False, 0, "scaled")
 
 
-@pytest.mark.parametrize("impl", IMPLS, ids=["mma_sync", "tcgen05"])
+@pytest.mark.parametrize("impl", IMPLS, ids=IMPL_IDS)
 def test_attention_full_size_sampled(impl):
     """8 heads x 2048 x 2048, d = 128, causal: sampled query rows of 2 heads."""
     bh, n, d = 8, 2048, 128
