@@ -404,8 +404,10 @@ def attention_entry(torch, rws, stream, bh=64, n=4096, d=128, causal=False, dtyp
     peak, kind = tensor_peak()
     return {"shape": {"batch_heads": bh, "n_q": n, "n_k": n, "head_dim": d},
             "dtype": DTYPE_NAMES[dtype], "causal": causal,
-            "kernel": ("attention_mma_kernel (mma.sync m16n8k16)" if impl == 1 else
-                       "attention_tc_kernel (tcgen05.mma, TMEM accumulators)"),
+            "kernel": {1: "attention_mma_kernel (mma.sync m16n8k16)",
+                       2: "attention_tc_kernel (tcgen05.mma, TMEM accumulators)"}.get(
+                           impl, "attention_pp_kernel (tcgen05.mma, two query tiles ping-pong, "
+                                 "TMA operands with 128-byte swizzle)"),
             "mean_ms": round(ms, 4),
             "TFLOP/s": round(tf, 1), "frac_of_%s_bf16_peak" % kind: round(tf / peak, 4)}
 
@@ -626,7 +628,9 @@ def run_ours(args):
                         lambda: backward_entry(torch, rws, stream, l2_bytes, peak)))
         entries.append(("small_f32_cuda_graph",
                         lambda: graph_entry(torch, rws, stream, l2_bytes, peak)))
-        for impl, tag in ((2, "tcgen05"), (1, "mma_sync")):
+        entries.append(("attention_tcgen05_pingpong_bf16_64x4096x4096_d64_causal",
+                        lambda: attention_entry(torch, rws, stream, d=64, causal=True, impl=3)))
+        for impl, tag in ((3, "tcgen05_pingpong"), (2, "tcgen05"), (1, "mma_sync")):
             entries.append(("attention_%s_bf16_64x4096x4096_d128" % tag,
                             lambda impl=impl: attention_entry(torch, rws, stream, impl=impl)))
             entries.append(("attention_%s_bf16_64x4096x4096_d128_causal" % tag,

@@ -182,9 +182,9 @@ int64_t softmax_visible_cols(const softmax_options_t* options, int64_t n_rows, i
  *   causal         0: every key.  1: key j is visible to query i iff
  *                  j <= i + causal_offset (0: the pages' mask; n_k - n_q: a
  *                  bottom-right aligned mask).  |causal_offset| < 2^62.
- *   impl           0: the library's choice (the ping-pong kernel at
- *                  head_dim 64, the single-tile tcgen05 kernel at 128: the
- *                  faster one at each on GB300); 1: the warp-level mma.sync
+ *   impl           0: the library's choice (the ping-pong kernel, the
+ *                  fastest on GB300; the single-tile tcgen05 kernel where
+ *                  the ping-pong one cannot run); 1: the warp-level mma.sync
  *                  kernel; 2: the tcgen05 kernel, one 128-query tile per
  *                  CTA; 3: the ping-pong tcgen05 kernel, two 128-query
  *                  tiles per CTA, one tile's softmax overlapping the other's

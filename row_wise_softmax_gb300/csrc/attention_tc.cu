@@ -173,6 +173,14 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
            (static_cast<uint64_t>(1) << 46);
 }
 
+// Same, for operands stored with the 128-byte swizzle (layout type 2 in
+// bits 61..63): 8-row atoms of 128-byte rows whose 16-byte chunks are
+// permuted by row % 8, atoms 1024-byte aligned.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    return smem_desc(addr, lbo, sbo) | (static_cast<uint64_t>(2) << 61);
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulator (bits 4..5 = 1), A
 // and B formats (bits 7..9, 10..12: 0 fp16, 1 bf16), B MN-major flag (bit 16),
 // N / 8 (bits 17..22), M / 16 (bits 24..28); A is K-major.
@@ -508,7 +516,6 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
     constexpr bool kBF16 = sizeof(T) == 2 && Elem<T>::kNegInfBits == 0xff80u;
     constexpr uint32_t QT_BYTES = kTcBM * D * 2, KV_BYTES = BN * D * 2, P_BYTES = kTcBM * BN * 2;
     constexpr uint32_t SBO_P = (BN / 8) * 128;
-    constexpr uint32_t SBO_V = (BN / 8) * 128;
     constexpr uint32_t IDESC_S = umma_idesc(kTcBM, BN, kBF16, false);
     constexpr uint32_t IDESC_PV = umma_idesc(kTcBM, D, kBF16, true);
     constexpr uint32_t TMEM_COLS = pp_tmem_cols<D>(BN);
@@ -520,7 +527,7 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
     __shared__ uint32_t tmem_slot;
     __shared__ int s_failed;
 
-    const uint32_t base = (smem_addr(tc_smem) + 127u) & ~127u;
+    const uint32_t base = (smem_addr(tc_smem) + 1023u) & ~1023u;   // swizzle atoms
     const uint32_t sQ = base, sK = sQ + 2 * QT_BYTES, sV = sK + 2 * KV_BYTES,
                    sP = sV + 2 * KV_BYTES;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -567,14 +574,15 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
     if (warp == CTRL) {
         // ------------------------------------------------------ control warp
         // Lane 0 issues every copy (the tensor memory accelerator) and every
-        // product.  An operand tile lands as D/8 boxes of 8 elements x ROWS
-        // rows: box c (elements 8c..8c+7 of every row) is ROWS contiguous
-        // 16-byte rows, i.e. ROWS/8 core matrices; so core matrix (row band i,
-        // element chunk c) sits at c * ROWS * 16 + i * 128.  For Q and K
-        // (K-major) that is LBO = ROWS * 16 between K-adjacent core matrices
-        // and SBO = 128 between row bands; for V (MN-major, rows = keys) it is
-        // the canonical layout already used for P V.  Rows past a head's end
-        // are zero-filled by the copy engine (the tensor maps are 3-D:
+        // product.  An operand tile lands as D/64 boxes of 64 elements x ROWS
+        // rows, each row 128 bytes with the copy engine's 128-byte swizzle,
+        // so box c is ROWS/8 swizzle atoms of 1024 bytes.  Q and K are
+        // K-major: a 16-element step of the contraction is 32 bytes into the
+        // atom row (the tensor cores apply the same swizzle to the address),
+        // SBO = 1024 between 8-row bands.  V is MN-major (rows = keys, the
+        // output dimension contiguous): SBO = 1024 between 8-key bands, LBO =
+        // one box between the 64-element halves of D.  Rows past a head's
+        // end are zero-filled by the copy engine (the tensor maps are 3-D:
         // element, row, head).
         if (lane == 0) {
             bool failed = false;
@@ -596,8 +604,8 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                                  uint32_t bar, uint32_t bytes) {
                 mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
-                for (int c = 0; c < D / 8; ++c)
-                    tma3(dst + static_cast<uint32_t>(c * rows * 16), map, c * 8, row0, bar);
+                for (int c = 0; c < D / 64; ++c)
+                    tma3(dst + static_cast<uint32_t>(c * rows * 128), map, c * 64, row0, bar);
             };
             // Copies issued and waited for, so that a failed wait can still
             // drain what is in flight before the CTA exits.
@@ -619,8 +627,9 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
                     umma_f16(tmem + static_cast<uint32_t>(x * BN),
-                             smem_desc(qx + ks * 2 * (kTcBM * 16), kTcBM * 16, 128),
-                             smem_desc(cK + ks * 2 * (BN * 16), BN * 16, 128), IDESC_S,
+                             smem_desc_sw128(qx + (ks >> 2) * (kTcBM * 128) + (ks & 3) * 32, 16, 1024),
+                             smem_desc_sw128(cK + (ks >> 2) * (BN * 128) + (ks & 3) * 32, 16, 1024),
+                             IDESC_S,
                              ks > 0 ? 1u : 0u);
             };
             auto issue_pv = [&](int x, int64_t t) {
@@ -630,7 +639,7 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                 for (int ks = 0; ks < BN / 16; ++ks)
                     umma_f16(tmem + static_cast<uint32_t>(2 * BN + x * D),
                              smem_desc(px + ks * 256, 128, SBO_P),
-                             smem_desc(cV + ks * 256, 128, SBO_V), IDESC_PV,
+                             smem_desc_sw128(cV + ks * 2048, BN * 128, 1024), IDESC_PV,
                              (t > 0 || ks > 0) ? 1u : 0u);
             };
             asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&map_q)) : "memory");
@@ -641,8 +650,8 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                 q_issued = true;
                 // (the second Q tile completes on the same barrier)
 #pragma unroll
-                for (int c = 0; c < D / 8; ++c)
-                    tma3(sQ + QT_BYTES + static_cast<uint32_t>(c * kTcBM * 16), &map_q, c * 8,
+                for (int c = 0; c < D / 64; ++c)
+                    tma3(sQ + QT_BYTES + static_cast<uint32_t>(c * kTcBM * 128), &map_q, c * 64,
                          q0 + kTcBM, smem_addr(&q_full));
                 load_k(0);
                 load_v(0);
@@ -850,7 +859,8 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
 }
 
 // 3-D tensor map of a [bh][n][D] operand (element, row, head) with boxes of
-// 8 elements x `rows` rows of one head: rows past a head's end read as zero.
+// 64 elements (128 bytes, 128-byte swizzle) x `rows` rows of one head: rows
+// past a head's end read as zero.
 inline bool pp_tensor_map(CUtensorMap* map, const void* ptr, int64_t bh, int64_t n, int d,
                           int rows, int dtype)
 {
@@ -860,12 +870,12 @@ inline bool pp_tensor_map(CUtensorMap* map, const void* ptr, int64_t bh, int64_t
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n),
                                 static_cast<cuuint64_t>(bh)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(n) * d * 2};
-    const cuuint32_t box[3] = {8u, static_cast<cuuint32_t>(rows), 1u};
+    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(rows), 1u};
     const cuuint32_t estride[3] = {1u, 1u, 1u};
     return encode(map, dtype == SOFTMAX_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                   3, const_cast<void*>(ptr), dims, strides, box, estride,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }
@@ -875,7 +885,7 @@ cudaError_t launch_pp(const AttentionProblem& p, cudaStream_t s)
 {
     constexpr int BN = 64;
     auto* kern = attention_pp_kernel<T, D, BN, CAUSAL>;
-    const int smem = (2 * kTcBM * D + 4 * BN * D + 2 * kTcBM * BN) * 2 + 128;
+    const int smem = (2 * kTcBM * D + 4 * BN * D + 2 * kTcBM * BN) * 2 + 1024;
     static std::atomic<bool> attr_set[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)

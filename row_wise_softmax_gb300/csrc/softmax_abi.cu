@@ -347,15 +347,15 @@ int softmax_attention_forward(const void* q, const void* k, const void* v, void*
         return ds;
     const rwsm::AttentionProblem p{q, k, v, o, lse, batch_heads, n_q, n_k, head_dim, dtype,
                                    scale, causal, offset};
-    // The library's choice (measured on GB300, 64 heads x 4096 queries and
-    // keys): the ping-pong kernel at head dimension 64, the single-tile one
-    // at 128; the single-tile one also wherever the ping-pong kernel cannot
-    // run (no tensor-map encoder, sizes past its 32-bit copy coordinates).
+    // The library's choice: the ping-pong kernel (the fastest of the three
+    // on GB300 at both head dimensions, causal or not); the single-tile
+    // tcgen05 kernel wherever the ping-pong one cannot run (no tensor-map
+    // encoder, sizes past its 32-bit copy coordinates).
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t err;
     if (impl == 1) {
         err = rwsm::launch_attention_mma(p, st);
-    } else if (impl == 3 || (impl == 0 && head_dim == 64)) {
+    } else if (impl == 0 || impl == 3) {
         err = rwsm::launch_attention_pp(p, st);
         if (err == cudaErrorNotSupported) {
             if (impl == 3)

@@ -75,6 +75,8 @@ CASES = [  # bh, n_q, n_k, d, causal, offset
     (1, 70, 70, 64, True, -5),              # first queries see nothing: NaN
     (4, 33, 1, 64, False, 0),               # one key
     (1, 1, 300, 128, False, 0),
+    (2, 515, 517, 128, True, 2),            # several 256-query CTAs, ragged tails
+    (1, 300, 1000, 64, False, 0),
 ]
 
 
