@@ -197,7 +197,8 @@ def attention_forward_ptr(q: int, k: int, v: int, o: int, lse: int, batch_heads:
                           causal: bool = False, causal_offset: int = 0, stream: int = 0,
                           impl: int = 0) -> int:
     """C ABI call of the attention forward; returns the status.  ``impl``:
-    0 the library's choice, 1 the mma.sync kernel, 2 the tcgen05 kernel."""
+    0 the library's choice, 1 the mma.sync kernel, 2 the single-tile tcgen05
+    kernel, 3 the ping-pong tcgen05 kernel."""
     opt = None
     if scale is not None or causal or causal_offset or impl:
         sc = scale if scale is not None else 1.0 / (head_dim ** 0.5)

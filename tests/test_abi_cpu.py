@@ -215,6 +215,19 @@ def test_visible_cols_division_by_invariant_period(lib):
     assert rws.visible_cols(10, 8, 1, scale=0.0) == -1
 
 
+def test_attention_options_validation(lib):
+    """Options are checked before any device work: impl outside 0..3, a bad
+    scale or offset is rejected; valid options on no queries are a no-op."""
+    g = lambda **kw: rws.attention_forward_ptr(1 << 20, 1 << 21, 1 << 22, 1 << 23, 0, 2, 64, 64,
+                                               64, rws.BF16, **kw)
+    for bad in (dict(impl=4), dict(impl=-1), dict(scale=0.0), dict(scale=float("nan")),
+                dict(causal=True, causal_offset=1 << 62)):
+        assert g(**bad) == rws.ERR_INVALID_ARG, bad
+    for impl in (0, 1, 2, 3):
+        assert rws.attention_forward_ptr(0, 0, 0, 0, 0, 0, 64, 64, 64, rws.BF16,
+                                         impl=impl) == rws.OK
+
+
 def test_no_gpu_means_loud_failure(lib):
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():
@@ -223,6 +236,9 @@ def test_no_gpu_means_loud_failure(lib):
     assert rws.softmax_rows_ptr(1 << 20, 1 << 30, 2, 8, 8, 8, rws.F32) == rws.ERR_UNSUPPORTED
     assert rws.softmax_rows_ex_ptr(1 << 20, 1 << 30, 2, 8, 8, 8, rws.F32, scale=0.5,
                                    causal=True) == rws.ERR_UNSUPPORTED
+    for impl in (0, 3):
+        assert rws.attention_forward_ptr(1 << 20, 1 << 21, 1 << 22, 1 << 23, 0, 2, 64, 64, 64,
+                                         rws.BF16, impl=impl) == rws.ERR_UNSUPPORTED
 
 
 def test_c_only_caller(lib, tmp_path):
