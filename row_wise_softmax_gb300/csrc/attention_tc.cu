@@ -500,6 +500,15 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
 constexpr int kPpWarpgroups = 2;
 constexpr int kPpThreads = kPpWarpgroups * 128 + 32;
 
+// Key/value ring depth of the ping-pong kernel: three slots at d = 128 (one
+// CTA per SM; the third slot hides the copy latency of the next key tile),
+// two at d = 64 so that two CTAs fit in one SM's shared memory.
+template <int D>
+__host__ __device__ constexpr int pp_kv_stages()
+{
+    return D == 128 ? 3 : 2;
+}
+
 template <int D>
 __host__ __device__ constexpr uint32_t pp_tmem_cols(int bn)
 {
@@ -515,6 +524,7 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
 {
     constexpr bool kBF16 = sizeof(T) == 2 && Elem<T>::kNegInfBits == 0xff80u;
     constexpr uint32_t QT_BYTES = kTcBM * D * 2, KV_BYTES = BN * D * 2, P_BYTES = kTcBM * BN * 2;
+    constexpr int KVS = pp_kv_stages<D>();
     constexpr uint32_t SBO_P = (BN / 8) * 128;
     constexpr uint32_t IDESC_S = umma_idesc(kTcBM, BN, kBF16, false);
     constexpr uint32_t IDESC_PV = umma_idesc(kTcBM, D, kBF16, true);
@@ -523,13 +533,13 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
     constexpr int CTRL = kPpWarpgroups * 4;                  // the control warp
     extern __shared__ __align__(128) unsigned char tc_smem[];
     __shared__ __align__(8) unsigned long long bar_s[2], bar_p[2], bar_fin[2], bar_drain;
-    __shared__ __align__(8) unsigned long long q_full, k_full[2], v_full[2];
+    __shared__ __align__(8) unsigned long long q_full, k_full[KVS], v_full[KVS], bar_pv;
     __shared__ uint32_t tmem_slot;
     __shared__ int s_failed;
 
     const uint32_t base = (smem_addr(tc_smem) + 1023u) & ~1023u;   // swizzle atoms
-    const uint32_t sQ = base, sK = sQ + 2 * QT_BYTES, sV = sK + 2 * KV_BYTES,
-                   sP = sV + 2 * KV_BYTES;
+    const uint32_t sQ = base, sK = sQ + 2 * QT_BYTES, sV = sK + KVS * KV_BYTES,
+                   sP = sV + KVS * KV_BYTES;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t n_qt = (n_q + 2 * kTcBM - 1) / (2 * kTcBM);
     const int64_t b = blockIdx.x / n_qt;
@@ -556,7 +566,8 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
         }
         mbar_init(smem_addr(&bar_drain), 1);
         mbar_init(smem_addr(&q_full), 1);
-        for (int x = 0; x < 2; ++x) {
+        mbar_init(smem_addr(&bar_pv), 1);
+        for (int x = 0; x < KVS; ++x) {
             mbar_init(smem_addr(&k_full[x]), 1);
             mbar_init(smem_addr(&v_full[x]), 1);
         }
@@ -607,22 +618,34 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                 for (int c = 0; c < D / 64; ++c)
                     tma3(dst + static_cast<uint32_t>(c * rows * 128), map, c * 64, row0, bar);
             };
-            // Copies issued and waited for, so that a failed wait can still
-            // drain what is in flight before the CTA exits.
+            // Key tile t lives in ring slot t % KVS; its barrier phase is
+            // t / KVS.  Copies issued and waited for are counted, so that a
+            // failed wait can still drain what is in flight before the CTA
+            // exits.
+            auto slot = [](int64_t t) { return static_cast<uint32_t>(t) % KVS; };
+            auto phase = [](int64_t t) { return (static_cast<uint32_t>(t) / KVS) & 1u; };
             int64_t k_issued = 0, v_issued = 0, k_waited = 0, v_waited = 0;
             bool q_issued = false;
             auto load_k = [&](int64_t t) {
-                load_rows(sK + static_cast<uint32_t>(t & 1) * KV_BYTES, &map_k, BN, t * BN,
-                          smem_addr(&k_full[t & 1]), KV_BYTES);
+                load_rows(sK + slot(t) * KV_BYTES, &map_k, BN, t * BN, smem_addr(&k_full[slot(t)]),
+                          KV_BYTES);
                 k_issued = t + 1;
             };
             auto load_v = [&](int64_t t) {
-                load_rows(sV + static_cast<uint32_t>(t & 1) * KV_BYTES, &map_v, BN, t * BN,
-                          smem_addr(&v_full[t & 1]), KV_BYTES);
+                load_rows(sV + slot(t) * KV_BYTES, &map_v, BN, t * BN, smem_addr(&v_full[slot(t)]),
+                          KV_BYTES);
                 v_issued = t + 1;
             };
+            auto wait_k = [&](int64_t t) {
+                wait1(smem_addr(&k_full[slot(t)]), phase(t));
+                k_waited = failed ? k_waited : t + 1;
+            };
+            auto wait_v = [&](int64_t t) {
+                wait1(smem_addr(&v_full[slot(t)]), phase(t));
+                v_waited = failed ? v_waited : t + 1;
+            };
             auto issue_s = [&](int x, int64_t t) {
-                const uint32_t cK = sK + static_cast<uint32_t>(t & 1) * KV_BYTES;
+                const uint32_t cK = sK + slot(t) * KV_BYTES;
                 const uint32_t qx = sQ + static_cast<uint32_t>(x) * QT_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
@@ -633,7 +656,7 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                              ks > 0 ? 1u : 0u);
             };
             auto issue_pv = [&](int x, int64_t t) {
-                const uint32_t cV = sV + static_cast<uint32_t>(t & 1) * KV_BYTES;
+                const uint32_t cV = sV + slot(t) * KV_BYTES;
                 const uint32_t px = sP + static_cast<uint32_t>(x) * P_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < BN / 16; ++ks)
@@ -653,17 +676,14 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                 for (int c = 0; c < D / 64; ++c)
                     tma3(sQ + QT_BYTES + static_cast<uint32_t>(c * kTcBM * 128), &map_q, c * 64,
                          q0 + kTcBM, smem_addr(&q_full));
-                load_k(0);
-                load_v(0);
-                if (n_kt > 1) {
-                    load_k(1);
-                    load_v(1);
+                for (int64_t t = 0; t < KVS && t < n_kt; ++t) {
+                    load_k(t);
+                    load_v(t);
                 }
                 wait1(smem_addr(&q_full), 0u);
-                wait1(smem_addr(&k_full[0]), 0u);
+                wait_k(0);
                 if (!failed) {
                     q_issued = false;
-                    k_waited = 1;
                     tc_fence_after();
                     issue_s(0, 0);
                     umma_commit(smem_addr(&bar_s[0]));
@@ -671,45 +691,47 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                     umma_commit(smem_addr(&bar_s[1]));
                 }
             }
+            // Per key tile t: P_A V(t) and S_A(t+1) once the softmax of A
+            // has written P_A(t), then the same for B; one commit after
+            // P_B V(t) tells when V(t)'s slot is free, and K(t)'s slot is
+            // free once both softmaxes have read S(t) (both P(t) written).
+            // K(t + KVS) and V(t + KVS) go into those slots.
             for (int64_t t = 0; t < n_kt && !failed; ++t) {
                 const bool more = t + 1 < n_kt;
-                if (more) {
-                    wait1(smem_addr(&k_full[(t + 1) & 1]), static_cast<uint32_t>(((t + 1) >> 1) & 1));
-                    k_waited = failed ? k_waited : t + 2;
-                }
-                wait1(smem_addr(&v_full[t & 1]), static_cast<uint32_t>((t >> 1) & 1));
-                v_waited = failed ? v_waited : t + 1;
+                wait_v(t);
                 for (int x = 0; x < 2 && !failed; ++x) {
                     wait1(smem_addr(&bar_p[x]), static_cast<uint32_t>(t & 1));   // P_X(t) written
                     if (failed)
                         break;
                     tc_fence_after();
                     issue_pv(x, t);
-                    if (more)
+                    if (x == 1)
+                        umma_commit(smem_addr(&bar_pv));           // phase t: P V(t) done
+                    if (more) {
+                        if (x == 0)
+                            wait_k(t + 1);
+                        if (failed)
+                            break;
                         issue_s(x, t + 1);
+                    }
                     umma_commit(smem_addr(more ? &bar_s[x] : &bar_fin[x]));
                 }
-                if (failed || t + 2 >= n_kt)
+                if (failed || t + KVS >= n_kt)
                     continue;
-                // K(t + 2) into K(t)'s buffer: both S(t) were read (bar_p).
                 fence_proxy_async_smem();
-                load_k(t + 2);
-                // V(t + 2) into V(t)'s buffer once both P V(t) have completed:
-                // S_B(t + 1), committed after them, has.
-                wait1(smem_addr(&bar_s[1]), static_cast<uint32_t>((t + 1) & 1));
+                load_k(t + KVS);
+                wait1(smem_addr(&bar_pv), static_cast<uint32_t>(t & 1));
                 if (!failed)
-                    load_v(t + 2);
+                    load_v(t + KVS);
             }
             if (failed) {
                 // Let the copies still in flight land (each wait bounded).
                 if (q_issued)
                     mbar_wait_bounded(smem_addr(&q_full), 0u);
                 for (; k_waited < k_issued; ++k_waited)
-                    mbar_wait_bounded(smem_addr(&k_full[k_waited & 1]),
-                                      static_cast<uint32_t>((k_waited >> 1) & 1));
+                    mbar_wait_bounded(smem_addr(&k_full[slot(k_waited)]), phase(k_waited));
                 for (; v_waited < v_issued; ++v_waited)
-                    mbar_wait_bounded(smem_addr(&v_full[v_waited & 1]),
-                                      static_cast<uint32_t>((v_waited >> 1) & 1));
+                    mbar_wait_bounded(smem_addr(&v_full[slot(v_waited)]), phase(v_waited));
             }
         }
         __syncwarp();
@@ -885,7 +907,7 @@ cudaError_t launch_pp(const AttentionProblem& p, cudaStream_t s)
 {
     constexpr int BN = 64;
     auto* kern = attention_pp_kernel<T, D, BN, CAUSAL>;
-    const int smem = (2 * kTcBM * D + 4 * BN * D + 2 * kTcBM * BN) * 2 + 1024;
+    const int smem = (2 * kTcBM * D + 2 * pp_kv_stages<D>() * BN * D + 2 * kTcBM * BN) * 2 + 1024;
     static std::atomic<bool> attr_set[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
