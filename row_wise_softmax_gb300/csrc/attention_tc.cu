@@ -515,8 +515,11 @@ __host__ __device__ constexpr uint32_t pp_tmem_cols(int bn)
     return 2 * bn + 2 * D <= 256 ? 256u : 512u;
 }
 
+// At d = 64 two CTAs share an SM: the bound keeps every instantiation at or
+// below 96 registers a thread (9 warps a CTA; the fifth warp on a
+// sub-partition must still fit its register file).
 template <typename T, int D, int BN, bool CAUSAL>
-__global__ void __launch_bounds__(kPpThreads, 1)
+__global__ void __launch_bounds__(kPpThreads, D == 64 ? 2 : 1)
 attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, T* o, float* lse, int64_t bh,
@@ -1015,7 +1018,7 @@ cudaError_t launch_attention_tc(const AttentionProblem& p, cudaStream_t s)
 cudaError_t launch_attention_pp(const AttentionProblem& p, cudaStream_t s)
 {
     if (p.bh * ((p.n_q + 2 * kTcBM - 1) / (2 * kTcBM)) > 0x7fffffff)
-        return cudaErrorInvalidValue;
+        return cudaErrorNotSupported;                    // grid too large: nothing launched
     return p.dtype == SOFTMAX_BF16 ? launch_pp_t<BF16Bits>(p, s) : launch_pp_t<F16Bits>(p, s);
 }
 
