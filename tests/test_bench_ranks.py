@@ -42,7 +42,7 @@ def _rank_main(rank, world, port, out):
 
 def test_max_over_ranks_gloo_world2():
     world = 2
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:   # no fork of a threaded process
         out = mgr.dict()
         mp.spawn(_rank_main, args=(world, _free_port(), out), nprocs=world, join=True)
         assert dict(out) == {0: 15.0, 1: 15.0}
