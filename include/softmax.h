@@ -216,7 +216,8 @@ typedef struct {
  *   not otherwise overlap q, k or v.
  *   Errors: SOFTMAX_ERR_INVALID_ARG (null or misaligned pointers, negative
  *   sizes, bad options, overlap), SOFTMAX_ERR_UNSUPPORTED (fp32, another
- *   head_dim, no usable device), SOFTMAX_ERR_CUDA (launch failure).
+ *   head_dim, no usable device, impl 3 outside its limits), SOFTMAX_ERR_CUDA
+ *   (launch failure).
  *   batch_heads == 0 or n_q == 0: no-op.
  */
 int softmax_attention_forward(const void* q, const void* k, const void* v, void* o, float* lse,
