@@ -497,6 +497,48 @@ def cpu_oracle_time(w: wl.Workload, reps: int):
     return statistics.median(ts)
 
 
+def cpu_model() -> str:
+    """The host CPU's name from /proc/cpuinfo (x86 "model name"; on Arm the
+    implementer and part numbers), else the platform's machine string."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return platform.machine()
+    fields = {}
+    for line in info.splitlines():
+        k, _, v = line.partition(":")
+        fields.setdefault(k.strip(), v.strip())
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU part" in fields:
+        return "%s, CPU implementer %s, part %s" % (platform.machine(),
+                                                    fields.get("CPU implementer", "?"),
+                                                    fields["CPU part"])
+    return platform.machine()
+
+
+def torch_cpu_time(w: wl.Workload, reps: int):
+    """Median time of torch.softmax over the workload's rows on the host, fp32,
+    with every intra-op thread torch has (the library's own CPU kernel, a
+    context figure beside the single-threaded oracle).  None for 16-bit
+    workloads (torch's CPU bf16 softmax is not the fp32 figure asked for)."""
+    import torch
+    if w.dtype != wl.F32 or w.n_rows == 0:
+        return None
+    item = w.data.itemsize
+    x = torch.from_numpy(np.lib.stride_tricks.as_strided(
+        w.data, shape=(w.n_rows, w.n_cols), strides=(w.in_row_stride * item, item)).copy())
+    torch.softmax(x, dim=-1)                             # warm-up
+    ts = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        torch.softmax(x, dim=-1)
+        ts.append(time.perf_counter() - t0)
+    return statistics.median(ts)
+
+
 def run_ours(args):
     import torch
     import row_wise_softmax_gb300 as rws
@@ -600,6 +642,17 @@ def run_ours(args):
             "sample": "the full %d x %d workload, median of %d runs of the double-precision "
                       "single-threaded oracle" % (w.n_rows, w.n_cols, reps),
             "seconds_per_step": round(t, 4)}
+        try:
+            import torch as _t
+            tt = torch_cpu_time(w, 5)
+            if tt is not None:
+                result["cpu_baseline"]["torch_cpu_all_cores"] = {
+                    "value": round(bytes_step / tt / 1e9, 3), "unit": UNIT,
+                    "threads": _t.get_num_threads(), "cpu_count": os.cpu_count(),
+                    "cpu": cpu_model(), "seconds_per_step": round(tt, 5),
+                    "what": "torch.softmax(x, dim=-1), fp32, on the host, median of 5"}
+        except Exception as e:                       # context figure only: never fatal
+            result["cpu_baseline"]["torch_cpu_all_cores"] = {"unavailable": str(e)[:200]}
     if rank == 0 and not args.no_per_config:
         per = {}
 

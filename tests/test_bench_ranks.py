@@ -47,3 +47,14 @@ def test_max_over_ranks_gloo_world2():
         mp.spawn(_rank_main, args=(world, _free_port(), out), nprocs=world, join=True)
         assert dict(out) == {0: 15.0, 1: 15.0}
     assert bench.max_over_ranks(3.5, 1) == 3.5
+
+
+def test_torch_cpu_context_figure():
+    """The optional all-core torch.softmax timing runs on an fp32 workload and
+    is skipped (None) for 16-bit ones; the CPU name is a non-empty string."""
+    import workloads as wl
+    t = bench.torch_cpu_time(wl.make("small_f32"), 2)
+    assert t is not None and t > 0
+    assert bench.torch_cpu_time(wl.make("short_f32"), 1) > 0        # in-stride 128, 127 columns
+    assert bench.torch_cpu_time(wl.make("causal_bf16"), 1) is None
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
