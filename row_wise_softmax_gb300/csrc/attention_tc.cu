@@ -1,7 +1,18 @@
 // Attention forward on the fifth-generation tensor cores (tcgen05, sm_100
 // family): the same online softmax as attention_mma.cu ("Triton GPU
 // programming deep dive", section 3.3), with both products issued by one
-// thread as tcgen05.mma and accumulated in tensor memory (TMEM).
+// thread as tcgen05.mma and accumulated in tensor memory (TMEM).  Two
+// kernels:
+//
+// attention_pp_kernel (the library's choice): a CTA owns two 128-query tiles
+// A and B and ping-pongs them, so that one tile's softmax runs while the
+// tensor cores compute the other's products.  A control warp's lane 0 issues
+// every tensor-map copy (Q once; K and V tiles of 64 keys through a ring of
+// 3 slots at head_dim 128, 2 at 64, all with the 128-byte swizzle) and every
+// product; two warpgroups run the softmax, one per tile.  The protocol is
+// described beside the kernel.
+//
+// attention_tc_kernel, one tile per CTA:
 //
 //   CTA      128 queries of one (batch, head), 4 warps; thread t of warp w
 //            owns query row 32w + t, which is TMEM lane 32w + t of every
@@ -480,20 +491,26 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
 //   CTA      256 queries of one (batch, head): tile A (queries 0..127) and
 //            tile B (128..255).  Warps 0-3 run tile A's softmax, warps 4-7
 //            tile B's (thread t of a warpgroup owns query row t = TMEM lane
-//            t); warp 8 stages Q, K and V with cp.async and its lane 0 issues
-//            every tcgen05.mma.
+//            t); lane 0 of warp 8 issues every tensor-map copy and every
+//            tcgen05.mma.
+//   operands Q, K and V land by cp.async.bulk.tensor (3-D maps: element,
+//            row, head; rows past a head's end read as zero) in boxes of 64
+//            elements with the 128-byte swizzle, read by the tensor cores
+//            through swizzled descriptors; P is written by the softmax
+//            threads in the plain core-matrix layout.
 //   TMEM     S_A at column 0, S_B at BN, O_A at 2 BN, O_B at 2 BN + D.
 //   order    per key tile t the control lane waits for P_A(t) (bar_p[A]),
 //            issues O_A += P_A V(t) and S_A(t+1) = Q_A K(t+1)^T, commits
 //            (bar_s[A]); then the same for B.  So the tensor cores compute
 //            one tile's products while the other tile's warpgroup runs its
-//            softmax, and every K/V tile staged serves 256 queries.  A
+//            softmax, and every K/V tile copied serves 256 queries.  A
 //            warpgroup's wait on S_X(t+1) also covers O_X += P_X V(t) (one
 //            commit covers every earlier operation of the issuing thread), so
 //            P_X and O_X are free for it when S_X(t+1) has landed.
-//   buffers  K and V double-buffered: K(t+2) refills the buffer of K(t) once
-//            both S(t) have been read by the warpgroups (bar_p), V(t+2) once
-//            S_B(t+1) (issued after both P V(t)) has completed.
+//   ring     K and V in KVS slots (tile t in slot t % KVS): K(t+KVS) refills
+//            K(t)'s slot once both S(t) were read (both P(t) written), V(t+KVS)
+//            refills V(t)'s once a commit issued right after P_B V(t) has
+//            arrived (bar_pv).
 //
 // Every wait is bounded; a timed-out wait records the error word and the
 // kernel stops issuing, waits (bounded) for what it issued and frees TMEM.
