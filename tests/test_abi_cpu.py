@@ -249,3 +249,44 @@ def test_c_only_caller(lib, tmp_path):
                    check=True)
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
+
+
+def test_strided_validation(lib):
+    """softmax_strided checks its arguments before any device work."""
+    A, B = 1 << 20, 1 << 30                           # fake, far-apart device addresses
+    s = lambda *a, dtype=rws.F32: rws.softmax_strided_ptr(*a, dtype)
+    # Column softmax of a 64 x 32 row-major matrix: 32 rows of 64, strides (1, 32).
+    ok = (A, B, 32, 64, 1, 32, 1, 32)
+    assert s(*ok, dtype=7) == rws.ERR_INVALID_ARG                     # unknown dtype
+    assert s(A, B, -1, 64, 1, 32, 1, 32) == rws.ERR_INVALID_ARG       # negative size
+    assert s(A, B, 32, 64, 1, -32, 1, 32) == rws.ERR_INVALID_ARG      # negative stride
+    assert s(0, B, 32, 64, 1, 32, 1, 32) == rws.ERR_INVALID_ARG       # null input
+    assert s(A + 2, B, 32, 64, 1, 32, 1, 32) == rws.ERR_INVALID_ARG   # misaligned f32
+    assert s(A, B, 32, 64, 1, 32, 1, 16) == rws.ERR_INVALID_ARG       # outputs alias each other
+    assert s(A, A + 64, 32, 64, 1, 32, 1, 32) == rws.ERR_INVALID_ARG  # partial in/out overlap
+    assert s(A, B, 0, 64, 1, 32, 1, 32) == rws.OK                     # empty: no-op
+    assert s(A, B, 1 << 40, 1 << 40, 1, 1 << 40, 1, 1 << 40) == rws.ERR_INVALID_ARG  # span overflow
+
+
+def test_backward_validation(lib):
+    """softmax_backward_rows checks y, dy and dx like the forward call checks
+    in and out: dx may be y or dy in place, never partly overlap them."""
+    A, B, C = 1 << 20, 1 << 28, 1 << 30
+    g = lambda *a, dtype=rws.F32: rws.softmax_backward_rows_ptr(*a, dtype)
+    assert g(A, B, C, 8, 100, 100, 100, 100, dtype=9) == rws.ERR_INVALID_ARG
+    assert g(A, B, C, -1, 100, 100, 100, 100) == rws.ERR_INVALID_ARG
+    assert g(A, B, C, 8, 100, 50, 100, 100) == rws.ERR_INVALID_ARG      # stride < n_cols
+    assert g(0, B, C, 8, 100, 100, 100, 100) == rws.ERR_INVALID_ARG     # null y
+    assert g(A, B, A + 40, 8, 100, 100, 100, 100) == rws.ERR_INVALID_ARG  # dx partly over y
+    assert g(A, B, B + 40, 8, 100, 100, 100, 100) == rws.ERR_INVALID_ARG  # dx partly over dy
+    assert g(A, B, C, 0, 100, 100, 100, 100) == rws.OK                  # empty: no-op
+
+
+def test_strided_and_backward_without_a_device(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    A, B, C = 1 << 20, 1 << 28, 1 << 30
+    assert rws.softmax_strided_ptr(A, B, 32, 64, 1, 32, 1, 32, rws.F32) == rws.ERR_UNSUPPORTED
+    assert rws.softmax_backward_rows_ptr(A, B, C, 8, 100, 100, 100, 100,
+                                         rws.F32) == rws.ERR_UNSUPPORTED
