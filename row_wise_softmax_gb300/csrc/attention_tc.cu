@@ -562,10 +562,11 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                    sP = sV + KVS * KV_BYTES;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t n_qt = (n_q + 2 * kTcBM - 1) / (2 * kTcBM);
-    const int64_t b = blockIdx.x / n_qt;
-    int64_t qt = blockIdx.x % n_qt;
-    if (CAUSAL)
-        qt = n_qt - 1 - qt;
+    // Causal: query tiles of every head, longest (last) first, so that the
+    // CTAs dispatched last are the short ones and the tail is short.
+    const int64_t b = CAUSAL ? static_cast<int64_t>(blockIdx.x) % bh : blockIdx.x / n_qt;
+    const int64_t qt = CAUSAL ? n_qt - 1 - static_cast<int64_t>(blockIdx.x) / bh
+                              : static_cast<int64_t>(blockIdx.x) % n_qt;
     const int64_t q0 = qt * 2 * kTcBM;
     int64_t n_kt = (n_k + BN - 1) / BN;
     if (CAUSAL) {
