@@ -69,8 +69,25 @@ WORKLOAD_DATA = {
 }
 
 
+# The five configurations' short tags, in the order the configurations are listed.
+CONFIG_TAGS = {"small_f32": "C1", "masked_f32": "C2", "causal_bf16": "C3", "short_f32": "C4",
+               "long_f32": "C5"}
+
+
 def kernel_of(plan):
     return KERNELS[(plan.path_name, 1 if plan.bulk_copy else 0)]
+
+
+def workload_label(w: wl.Workload, options: bool = False) -> str:
+    """The workload as both arms name it in config.workload."""
+    return "%s: %d x %d %s, row strides %d/%d%s" % (
+        w.name, w.n_rows, w.n_cols, DTYPE_NAMES[w.dtype], w.in_row_stride, w.out_row_stride,
+        ", mask from indices, scale %g" % FUSED_SCALE if options else "")
+
+
+def sig(x: float, digits: int = 4) -> float:
+    """x rounded to `digits` significant digits (keeps the JSON line short)."""
+    return float("%.*g" % (digits, x))
 
 
 def dist_env():
@@ -106,8 +123,10 @@ def source_hash(plan) -> str:
     return h.hexdigest()[:16]
 
 
-def committed_traffic(plan, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if still valid."""
+def committed_record(plan, workload: str):
+    """The committed one-launch ncu record (DRAM bytes, duration) of the
+    kernel this plan launches on this workload, if the kernel's sources still
+    hash to the captured value: (record or None, its path or why not)."""
     fn = os.path.join(PROFILE_DIR, "%s.%s.json" % (kernel_of(plan)[0], workload))
     try:
         with open(fn) as f:
@@ -116,7 +135,13 @@ def committed_traffic(plan, workload: str):
         return None, "no committed ncu summary"
     if rec.get("source_sha") != source_hash(plan):
         return None, "kernel changed since the ncu capture"
-    return rec.get("dram_bytes_per_launch"), os.path.relpath(fn, ROOT)
+    return rec, os.path.relpath(fn, ROOT)
+
+
+def committed_traffic(plan, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if still valid."""
+    rec, src = committed_record(plan, workload)
+    return (rec.get("dram_bytes_per_launch") if rec else None), src
 
 
 def measured_peak():
@@ -207,6 +232,14 @@ def device_buffers(w: wl.Workload, torch, l2_bytes: int):
     return sets
 
 
+def hold_stream(torch, steps: int):
+    """Keep the stream busy (torch's sleep kernel) while the host enqueues the
+    timed launches, so that the timed region starts with the whole batch
+    queued: it then measures the device back to back, not the host's launch
+    rate or the latency of the first launch after an idle GPU."""
+    torch.cuda._sleep(int(min(20e-3, 30e-6 * steps + 100e-6) * 2.0e9))
+
+
 def time_device(w: wl.Workload, sets, steps: int, warmup: int, torch, rws, stream,
                 options=None):
     """softmax_rows (softmax_rows_ex with ``options``, a rws.Options) over
@@ -230,12 +263,41 @@ def time_device(w: wl.Workload, sets, steps: int, warmup: int, torch, rws, strea
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = rws.launch_count()
+    hold_stream(torch, steps)
     a.record(stream)
     for i in range(steps):
         call(*calls[(warmup + i) % len(calls)])
     b.record(stream)
     torch.cuda.synchronize()
     return a.elapsed_time(b), rws.launch_count() - launches0
+
+
+def time_each_step(w: wl.Workload, sets, steps: int, torch, rws, stream):
+    """softmax_rows over the rotating sets with every step bracketed by its own
+    pair of CUDA events (each launch's ramp and drain included, no overlap
+    with its neighbours): the per-step times in ms."""
+    calls = [(x.data_ptr(), y.data_ptr(), w.n_rows, w.n_cols, w.in_row_stride,
+              w.out_row_stride, w.dtype, stream.cuda_stream) for x, y in sets]
+    call = rws.lib().softmax_rows
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    hold_stream(torch, steps)
+    for i, (a, b) in enumerate(ev):
+        a.record(stream)
+        call(*calls[i % len(calls)])
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def percentile(xs, q: float) -> float:
+    """The q-quantile of xs by linear interpolation between order statistics."""
+    ys = sorted(xs)
+    pos = q * (len(ys) - 1)
+    lo = int(pos)
+    hi = min(lo + 1, len(ys) - 1)
+    return ys[lo] + (ys[hi] - ys[lo]) * (pos - lo)
 
 
 def copy_calibration(w: wl.Workload, sets, torch, stream, peak):
@@ -249,6 +311,7 @@ def copy_calibration(w: wl.Workload, sets, torch, stream, peak):
         src, dst = pairs[i % len(pairs)]
         dst.copy_(src)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    hold_stream(torch, 30)
     a.record(stream)
     for i in range(30):
         src, dst = pairs[i % len(pairs)]
@@ -317,6 +380,7 @@ def backward_entry(torch, rws, stream, l2_bytes, peak, n_rows=4096, n_cols=4096,
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = rws.launch_count()
+    hold_stream(torch, 50)
     a.record(stream)
     for i in range(50):
         call(*args[i % n_sets])
@@ -351,6 +415,7 @@ def columns_entry(torch, rws, stream, l2_bytes, peak, R=4096, C=4096, dtype=wl.F
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = rws.launch_count()
+    hold_stream(torch, 50)
     a.record(stream)
     for i in range(50):
         call(*args[i % n_sets])
@@ -393,6 +458,7 @@ def attention_entry(torch, rws, stream, bh=64, n=4096, d=128, causal=False, dtyp
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     steps = 10
+    hold_stream(torch, steps)
     a.record(stream)
     for _ in range(steps):
         call(*args)
@@ -437,6 +503,7 @@ def graph_entry(torch, rws, stream, l2_bytes, peak, name="small_f32", calls=200)
     torch.cuda.synchronize()
     reps = 10
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    hold_stream(torch, reps)
     a.record()
     for _ in range(reps):
         g.replay()
@@ -597,10 +664,7 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32",        # the arithmetic type (bf16 workloads compute in fp32 too)
         "data": WORKLOAD_DATA[args.workload],
-        "config": {"workload": "%s: %d x %d %s, row strides %d/%d%s" % (
-                       args.workload, w.n_rows, w.n_cols, DTYPE_NAMES[w.dtype],
-                       w.in_row_stride, w.out_row_stride,
-                       ", mask from indices, scale %g" % FUSED_SCALE if options else ""),
+        "config": {"workload": workload_label(w, options is not None),
                    "n_rows": w.n_rows, "n_cols": w.n_cols, "bytes_per_step": bytes_step,
                    "l2": "inputs larger than L2: %d rotating input/output sets (%.0f MB, "
                          ">= %dx the %.0f MB L2), steps back to back" % (
@@ -656,22 +720,47 @@ def run_ours(args):
     if rank == 0 and not args.no_per_config:
         per = {}
 
+        cpu_oracle = {}
+
         def workload_entry(name):
             wc = w if name == args.workload else wl.make(name)
             pc = rws.plan(wc.n_rows, wc.n_cols, in_row_stride=wc.in_row_stride,
                           out_row_stride=wc.out_row_stride, dtype=wc.dtype)
             bc = bufs if name == args.workload else device_buffers(wc, torch, l2_bytes)
             tot, _ = time_device(wc, bc, 50, 5, torch, rws, stream)
+            each = time_each_step(wc, bc, 50, torch, rws, stream)
             cal = copy_calibration(wc, bc, torch, stream, peak)
             del bc
-            med = tot / 50
-            gbs = wc.algorithmic_bytes / (med * 1e-3) / 1e9
-            return {"shape": [wc.n_rows, wc.n_cols], "dtype": DTYPE_NAMES[wc.dtype],
-                    "path": pc.path_name, "plan": str(pc), "mean_ms": round(med, 5),
-                    "copy_same_bytes_GB/s": cal["GB/s"] if cal else None,
-                    "GB/s": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
-                    "frac_of_8000": round(gbs / 8000.0, 4),
-                    "rows_per_s": round(wc.n_rows / (med * 1e-3), 1)}
+            mean = tot / 50
+            gbs = wc.algorithmic_bytes / (mean * 1e-3) / 1e9
+            entry = {"shape": [wc.n_rows, wc.n_cols], "dtype": DTYPE_NAMES[wc.dtype],
+                     "workload": workload_label(wc),
+                     "path": pc.path_name, "kernel": kernel_of(pc)[0], "plan": str(pc),
+                     "mean_ms": round(mean, 5),
+                     "median_ms_single": round(statistics.median(each), 5),
+                     "p95_ms_single": round(percentile(each, 0.95), 5),
+                     "copy_same_bytes_GB/s": cal["GB/s"] if cal else None,
+                     "GB/s": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
+                     "frac_of_8000": round(gbs / 8000.0, 4),
+                     "rows_per_s": sig(wc.n_rows / (mean * 1e-3))}
+            rec, src = committed_record(pc, name)
+            if rec and rec.get("gpu_time_us"):
+                ncu_gbs = wc.algorithmic_bytes / (rec["gpu_time_us"] * 1e-6) / 1e9
+                entry["ncu_one_launch"] = {
+                    "gpu_time_us": rec["gpu_time_us"], "GB/s": round(ncu_gbs, 1),
+                    "frac_of_measured_peak": round(ncu_gbs / peak, 4),
+                    "traffic_over_algorithmic": round(
+                        rec["dram_bytes_per_launch"] / wc.algorithmic_bytes, 4),
+                    "source": src}
+            else:
+                entry["ncu_one_launch"] = {"unavailable": src}
+            if name in CONFIG_TAGS and not args.no_cpu:
+                t = cpu_oracle_time(wc, 3)
+                cpu_oracle[name] = t
+                entry["cpu_oracle"] = {"seconds": round(t, 4), "cores": 1, "runs": 3,
+                                       "GB/s": sig(wc.algorithmic_bytes / t / 1e9),
+                                       "rows_per_s": sig(wc.n_rows / t)}
+            return entry
 
         entries = [(name, lambda name=name: workload_entry(name))
                    for name in wl.NAMES + wl.EXTRA_NAMES]
@@ -708,12 +797,41 @@ def run_ours(args):
             if only is None or key in only:
                 per[key] = fn()
         result["per_config"] = per
+        # The five configurations again, compactly, as the line's last key
+        # (a reader that keeps only the end of the line still sees them).
+        result["configs"] = configs_block(per, peak)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def configs_block(per, peak):
+    """C1..C5 in a few keys each: GB/s and rows/s of the back-to-back steps,
+    their fraction of the measured copy peak and of 8000 GB/s, the median and
+    95th percentile of singly timed steps, the committed one-launch ncu
+    figures (fraction of the peak, DRAM traffic over algorithmic bytes) and
+    the single-threaded CPU oracle's time."""
+    out = {"peak_GB/s": peak, "cpu": "oracle, double, 1 thread, median of 3"}
+    for name, tag in CONFIG_TAGS.items():
+        e = per.get(name)
+        if e is None:
+            continue
+        c = {"w": "%s %dx%d %s" % (name, e["shape"][0], e["shape"][1], e["dtype"]),
+             "GB/s": e["GB/s"], "frac": e["frac_of_measured_peak"],
+             "frac8000": e["frac_of_8000"], "rows/s": e["rows_per_s"],
+             "med_ms": e["median_ms_single"], "p95_ms": e["p95_ms_single"]}
+        n = e.get("ncu_one_launch", {})
+        if "frac_of_measured_peak" in n:
+            c["ncu_frac"] = n["frac_of_measured_peak"]
+            c["traffic"] = n["traffic_over_algorithmic"]
+        if "cpu_oracle" in e:
+            c["cpu_s"] = e["cpu_oracle"]["seconds"]
+            c["cpu_GB/s"] = e["cpu_oracle"]["GB/s"]
+        out[tag] = c
+    return out
 
 
 def run_reference(args):
@@ -736,7 +854,7 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * total / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "%s: %d x %d fp32" % (HEADLINE, w.n_rows, w.n_cols)},
+        "config": {"workload": workload_label(w)},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,

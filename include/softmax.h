@@ -211,13 +211,16 @@ typedef struct {
  *   lse    optional [batch_heads][n_q] floats: the natural-log logsumexp of
  *          each query's masked, scaled scores (NULL: not written).
  *   head_dim 64 or 128.  A query with no visible key (or n_k == 0) gives NaN
- *          outputs (the softmax of only -inf) and lse = -inf.
+ *          outputs (the softmax of only -inf) and lse = -inf.  n_k == 0 is
+ *          served by the single-tile tcgen05 kernel whatever impl asks for;
+ *          k and v may then be NULL.
  *   Ownership and asynchrony as for softmax_rows.  o may be q itself; it must
- *   not otherwise overlap q, k or v.
+ *   not otherwise overlap q, k or v; lse must overlap none of q, k, v, o.
  *   Errors: SOFTMAX_ERR_INVALID_ARG (null or misaligned pointers, negative
  *   sizes, bad options, overlap), SOFTMAX_ERR_UNSUPPORTED (fp32, another
- *   head_dim, no usable device, impl 3 outside its limits), SOFTMAX_ERR_CUDA
- *   (launch failure).
+ *   head_dim, no usable device, impl 3 outside its limits, a grid of more
+ *   than 2^31 - 1 CTAs: batch_heads x the query tiles of the chosen kernel,
+ *   64, 128 or 256 queries each), SOFTMAX_ERR_CUDA (launch failure).
  *   batch_heads == 0 or n_q == 0: no-op.
  */
 int softmax_attention_forward(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -375,6 +378,25 @@ int softmax_rows_planned(const void* in, void* out, int64_t n_rows, int64_t n_co
 /* Writes a one-line text form of *plan into buf (always NUL-terminated when
  * len > 0).  Returns the number of characters the full text needs. */
 int softmax_plan_format(const softmax_plan_t* plan, char* buf, size_t len);
+
+/*
+ * softmax_plan_describe: the scheduler's decision, as text, for softmax_rows
+ * on n_rows contiguous rows of n_cols elements (strides n_cols, 16-byte
+ * aligned device buffers) on the current device.  The launch wrapper of
+ * "Triton: write CUDA-grade GPU operators in Python", Example 2 (Fused
+ * Softmax), fixes one program per row; this call reports how this library
+ * maps the same rows instead (path, threads, cluster, slices, stages, grid).
+ *
+ *   buf, len  receives the one-line text of softmax_plan_format, truncated
+ *             to len - 1 characters and NUL-terminated (len == 0: nothing is
+ *             written; buf may then be NULL).
+ *   Returns SOFTMAX_OK, SOFTMAX_ERR_INVALID_ARG (bad sizes or dtype, or
+ *   buf == NULL with len > 0), SOFTMAX_ERR_UNSUPPORTED (no usable device).
+ *   Launches nothing.  A composition of softmax_plan and
+ *   softmax_plan_format, which also take other strides and alignments, and
+ *   a device description in place of the current device.
+ */
+int softmax_plan_describe(int64_t n_rows, int64_t n_cols, int dtype, char* buf, size_t len);
 
 /*
  * softmax_device_status: synchronises the current device, then reports

@@ -16,7 +16,8 @@ m_i = m_ij; finally acc / l_i.
 ``attention_online`` follows section 3.3's steps in their order.  Shapes:
 q [BH, n_q, d], k and v [BH, n_k, d], float64; the causal mask keeps key j
 for query i iff j <= i + offset (offset 0: the page's mask).  A query row with
-no visible key is the softmax of only -inf: NaN.
+no visible key (every key masked, or no key at all) is the softmax of only
+-inf: NaN, and its logsumexp is -inf.
 """
 from __future__ import annotations
 
@@ -41,10 +42,11 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float | None =
         for b in range(q.shape[0]):
             s = scale * (q[b] @ k[b].T)
             s = np.where(keep, s, -np.inf)
-            m = s.max(axis=1, keepdims=True)
+            # The max of no score is -inf; the weights' sum then is 0 and the
+            # weighted sum of V over no key, divided by it, is 0/0 = NaN.
+            m = s.max(axis=1, keepdims=True, initial=-np.inf)
             e = np.exp(s - m)
-            p = e / e.sum(axis=1, keepdims=True)
-            out[b] = p @ v[b]
+            out[b] = (e @ v[b]) / e.sum(axis=1, keepdims=True)
     return out
 
 
@@ -91,7 +93,7 @@ def logsumexp(q: np.ndarray, k: np.ndarray, scale: float | None = None, causal: 
     with np.errstate(invalid="ignore", divide="ignore"):
         for b in range(q.shape[0]):
             s = np.where(keep, scale * (q[b] @ k[b].T), -np.inf)
-            m = s.max(axis=1)
+            m = s.max(axis=1, initial=-np.inf)
             ref = np.where(m > -np.inf, m, 0.0)
             out[b] = ref + np.log(np.exp(s - ref[:, None]).sum(axis=1))
     return out

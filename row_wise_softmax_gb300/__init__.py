@@ -138,6 +138,8 @@ def lib() -> ctypes.CDLL:
         L.softmax_plan.restype = ci
         L.softmax_plan_format.argtypes = [ctypes.POINTER(Plan), ctypes.c_char_p, ctypes.c_size_t]
         L.softmax_plan_format.restype = ci
+        L.softmax_plan_describe.argtypes = [i64, i64, ci, ctypes.c_char_p, ctypes.c_size_t]
+        L.softmax_plan_describe.restype = ci
         L.softmax_device_status.argtypes = [ci]
         L.softmax_device_status.restype = ci
         L.softmax_selftest_wait_timeout.argtypes = [vp]
@@ -441,3 +443,13 @@ def plan_for_device(desc: dict | DeviceDesc | None, n_rows: int, n_cols: int,
 def plan(n_rows: int, n_cols: int, **kw) -> Plan:
     """Scheduler decision on the current GPU."""
     return plan_for_device(None, n_rows, n_cols, **kw)
+
+
+def plan_describe(n_rows: int, n_cols: int, dtype: int = F32) -> str:
+    """The scheduler's decision for contiguous, aligned rows on the current
+    GPU, as the library's one-line text (softmax_plan_describe)."""
+    buf = ctypes.create_string_buffer(256)
+    st = lib().softmax_plan_describe(n_rows, n_cols, dtype, buf, 256)
+    if st != OK:
+        raise SoftmaxError(st, "softmax_plan_describe")
+    return buf.value.decode()

@@ -1036,7 +1036,7 @@ cudaError_t launch_attention_tc(const AttentionProblem& p, cudaStream_t s)
 cudaError_t launch_attention_pp(const AttentionProblem& p, cudaStream_t s)
 {
     if (p.bh * ((p.n_q + 2 * kTcBM - 1) / (2 * kTcBM)) > 0x7fffffff)
-        return cudaErrorNotSupported;                    // grid too large: nothing launched
+        return cudaErrorInvalidValue;                    // grid too large: nothing launched
     return p.dtype == SOFTMAX_BF16 ? launch_pp_t<BF16Bits>(p, s) : launch_pp_t<F16Bits>(p, s);
 }
 

@@ -225,6 +225,25 @@ int softmax_plan_format(const softmax_plan_t* plan, char* buf, size_t len)
                          static_cast<long long>(plan->grid));
 }
 
+int softmax_plan_describe(int64_t n_rows, int64_t n_cols, int dtype, char* buf, size_t len)
+{
+    if (len > 0 && !buf)
+        return SOFTMAX_ERR_INVALID_ARG;
+    if (len > 0)
+        buf[0] = '\0';
+    // Contiguous rows at a 256-byte aligned address, as a device allocator
+    // returns them; the same buffer for input and output (in place), which
+    // the scheduler treats like separate buffers.
+    const void* at = reinterpret_cast<const void*>(uintptr_t{256});
+    softmax_plan_t plan;
+    const int st = softmax_plan(nullptr, at, at, n_rows, n_cols, n_cols, n_cols, dtype,
+                                SOFTMAX_PATH_AUTO, &plan);
+    if (st != SOFTMAX_OK)
+        return st;
+    softmax_plan_format(&plan, buf, len);
+    return SOFTMAX_OK;
+}
+
 int softmax_rows_path(const void* in, void* out, int64_t n_rows, int64_t n_cols,
                       int64_t in_row_stride, int64_t out_row_stride, int dtype,
                       void* stream, int path)
@@ -323,7 +342,7 @@ int softmax_attention_forward(const void* q, const void* k, const void* v, void*
         return SOFTMAX_OK;
     if (dtype == SOFTMAX_F32 || (head_dim != 64 && head_dim != 128))
         return SOFTMAX_ERR_UNSUPPORTED;
-    if (!q || !k || !v || !o)
+    if (!q || !o || (n_k > 0 && (!k || !v)))           // no key: k and v may be NULL
         return SOFTMAX_ERR_INVALID_ARG;
     auto a16 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
     if (!a16(q) || !a16(k) || !a16(v) || !a16(o) || (lse && reinterpret_cast<uintptr_t>(lse) % 4))
@@ -341,6 +360,31 @@ int softmax_attention_forward(const void* q, const void* k, const void* v, void*
     };
     if ((q != o && hits(q, n_q)) || hits(k, n_k) || hits(v, n_k))
         return SOFTMAX_ERR_INVALID_ARG;            // o may be q itself, nothing else
+    if (lse) {
+        // The logsumexp rows are written while other CTAs still read q, k
+        // and v and write o: lse may overlap none of them.
+        const uintptr_t l0 = reinterpret_cast<uintptr_t>(lse);
+        const uintptr_t l1 = l0 + static_cast<uintptr_t>(batch_heads * n_q) * sizeof(float);
+        auto meets = [&](const void* a, int64_t n) {
+            const uintptr_t a0 = reinterpret_cast<uintptr_t>(a);
+            const uintptr_t a1 = a0 + static_cast<uintptr_t>(batch_heads * n * head_dim * 2);
+            return a0 < l1 && l0 < a1;
+        };
+        if (meets(q, n_q) || meets(k, n_k) || meets(v, n_k) || meets(o, n_q))
+            return SOFTMAX_ERR_INVALID_ARG;
+    }
+    // Grid sizes: one CTA per 64 queries of a head (mma.sync kernel), per 128
+    // (single-tile tcgen05) or per 256 (ping-pong); a grid past 2^31 - 1 CTAs
+    // cannot be launched.  With no key at all every kernel choice takes the
+    // single-tile kernel (the ping-pong kernel's copy descriptors cannot
+    // describe an empty K and V): rows of NaN, logsumexp -inf.
+    auto grid_fits = [&](int64_t rows_per_cta) {
+        return batch_heads <= 0x7fffffff / ((n_q + rows_per_cta - 1) / rows_per_cta);
+    };
+    if (n_k == 0 && (impl == 0 || impl == 3))
+        impl = 2;
+    if (!grid_fits(impl == 1 ? 64 : impl == 2 ? 128 : 256))
+        return SOFTMAX_ERR_UNSUPPORTED;
     softmax_device_desc_t d;
     const int ds = rwsm::current_device(&d);
     if (ds != SOFTMAX_OK)
@@ -349,8 +393,8 @@ int softmax_attention_forward(const void* q, const void* k, const void* v, void*
                                    scale, causal, offset};
     // The library's choice: the ping-pong kernel (the fastest of the three
     // on GB300 at both head dimensions, causal or not); the single-tile
-    // tcgen05 kernel wherever the ping-pong one cannot run (no tensor-map
-    // encoder, sizes past its 32-bit copy coordinates).
+    // tcgen05 kernel where the ping-pong one's copy descriptors cannot be
+    // made (no tensor-map encoder, sizes past their 32-bit coordinates).
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t err;
     if (impl == 1) {
@@ -358,7 +402,7 @@ int softmax_attention_forward(const void* q, const void* k, const void* v, void*
     } else if (impl == 0 || impl == 3) {
         err = rwsm::launch_attention_pp(p, st);
         if (err == cudaErrorNotSupported) {
-            if (impl == 3)
+            if (impl == 3 || !grid_fits(128))
                 return SOFTMAX_ERR_UNSUPPORTED;
             err = rwsm::launch_attention_tc(p, st);
         }

@@ -50,6 +50,16 @@ int main(void)
     CHECK(softmax_plan(&gb300, (void*)0x10000, (void*)0x20000000, 256, 262144, 262144, 262144,
                        SOFTMAX_F32, SOFTMAX_PATH_AUTO, &plan) == SOFTMAX_OK);
     CHECK(plan.path == SOFTMAX_PATH_TWOPASS && plan.cluster == 4 && plan.stages == 3);
+    /* softmax_plan_describe: the same decision on the current device (none
+     * here: UNSUPPORTED, never a made-up plan); its arguments are checked
+     * first. */
+    CHECK(softmax_plan_describe(4096, 4096, 7, text, sizeof text) == SOFTMAX_ERR_INVALID_ARG);
+    CHECK(softmax_plan_describe(-1, 4096, SOFTMAX_F32, text, sizeof text) == SOFTMAX_ERR_INVALID_ARG);
+    CHECK(softmax_plan_describe(4096, 4096, SOFTMAX_F32, NULL, 16) == SOFTMAX_ERR_INVALID_ARG);
+    {
+        const int st = softmax_plan_describe(4096, 4096, SOFTMAX_F32, text, sizeof text);
+        CHECK(st == SOFTMAX_OK ? strstr(text, "path=cta") != NULL : st == SOFTMAX_ERR_UNSUPPORTED);
+    }
     gb300.cc_minor = 0;
     CHECK(softmax_plan(&gb300, (void*)0x10000, (void*)0x20000000, 4, 4, 4, 4, SOFTMAX_F32,
                        SOFTMAX_PATH_AUTO, &plan) == SOFTMAX_ERR_UNSUPPORTED);

@@ -228,6 +228,20 @@ def test_attention_options_validation(lib):
                                          impl=impl) == rws.OK
 
 
+def test_attention_grid_and_lse_checks(lib):
+    """A grid past 2^31 - 1 CTAs is refused for every kernel choice as
+    UNSUPPORTED before any device work; an lse buffer overlapping q, k, v or o
+    is an invalid argument."""
+    Q, K, V, O = 1 << 50, 2 << 50, 3 << 50, 4 << 50       # fake, far-apart device addresses
+    bh = (1 << 31) - 1
+    for impl in (0, 1, 2, 3):
+        assert rws.attention_forward_ptr(Q, K, V, O, 0, bh, 512, 64, 64, rws.BF16,
+                                         impl=impl) == rws.ERR_UNSUPPORTED, impl
+    for lse in (Q + 64, K, V + 4096, O, O + 2 * 64 * 100 * 2 - 4):
+        assert rws.attention_forward_ptr(Q, K, V, O, lse, 2, 100, 64, 64,
+                                         rws.BF16) == rws.ERR_INVALID_ARG, hex(lse)
+
+
 def test_no_gpu_means_loud_failure(lib):
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():

@@ -72,6 +72,16 @@ def pin_closed_forms(m):
     assert np.allclose(causal[0, 2], v[0, :3].T @ _softmax(q[0, 2] @ k[0, :3].T / 2.0))
     empty = m.attention(q, k, v, causal=True, offset=-1)  # query 0 sees nothing
     assert np.all(np.isnan(empty[0, 0])) and np.all(np.isfinite(empty[0, 1:]))
+    # No key at all is the same as every key masked: the softmax of only -inf
+    # (NaN outputs), whose logsumexp is log 0 = -inf.
+    none = np.zeros((1, 0, 4))
+    hidden = m.attention(q, k, v, causal=True, offset=-10)
+    assert np.all(np.isnan(hidden)) and np.all(np.isneginf(m.logsumexp(q, k, causal=True,
+                                                                       offset=-10)))
+    for fn in (m.attention, m.attention_online):
+        out = fn(q, none, none)
+        assert out.shape == (1, 6, 4) and np.all(np.isnan(out))
+    assert np.all(np.isneginf(m.logsumexp(q, none)))
 
 
 def _softmax(z):
@@ -101,11 +111,13 @@ MUTANTS = {
     "no_scale": ("s = scale * (q[b] @ k[b].T)", "s = (q[b] @ k[b].T)"),
     "mask_off_by_one": ("return np.arange(n_k)[None, :] <= np.arange(n_q)[:, None] + offset",
                         "return np.arange(n_k)[None, :] < np.arange(n_q)[:, None] + offset"),
-    "no_normalise": ("p = e / e.sum(axis=1, keepdims=True)", "p = e"),
+    "no_normalise": ("out[b] = (e @ v[b]) / e.sum(axis=1, keepdims=True)", "out[b] = e @ v[b]"),
+    "empty_keys_give_zero": ("out[b] = (e @ v[b]) / e.sum(axis=1, keepdims=True)",
+                             "out[b] = (e / e.sum(axis=1, keepdims=True)) @ v[b]"),
     "online_no_rescale": ("acc = acc * alpha[:, None] + p @ vt", "acc = acc + p @ vt"),
     "online_l_no_rescale": ("                l_i = l_i * alpha + l_ij",
                             "                l_i = l_i + l_ij"),
-    "transposed_v": ("out[b] = p @ v[b]", "out[b] = (v[b].T @ p.T).T[:, ::-1]"),
+    "transposed_v": ("out[b] = (e @ v[b])", "out[b] = (v[b].T @ e.T).T[:, ::-1]"),
     "lse_no_ref": ("out[b] = ref + np.log(", "out[b] = np.log("),
 }
 

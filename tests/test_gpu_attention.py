@@ -77,6 +77,9 @@ CASES = [  # bh, n_q, n_k, d, causal, offset
     (1, 1, 300, 128, False, 0),
     (2, 515, 517, 128, True, 2),            # several 256-query CTAs, ragged tails
     (1, 300, 1000, 64, False, 0),
+    (2, 50, 0, 64, False, 0),               # no key at all: NaN rows, lse -inf
+    (7, 600, 600, 64, True, 0),             # many heads, several query tiles each
+    (7, 600, 600, 128, True, 0),
 ]
 
 

@@ -224,3 +224,17 @@ def test_planned_rejects_unsafe_plans():
         st, _ = _planned(w, q)
         assert st == rws.ERR_INVALID_ARG, str(q)
     assert rws.launch_count() == before
+
+
+def test_plan_describe_matches_plan():
+    """softmax_plan_describe is softmax_plan on contiguous aligned rows,
+    formatted: the same text as the plan of real device buffers."""
+    for name in wl.NAMES:
+        w = wl.make(name, n_rows=4)
+        n_rows = wl.FULL_ROWS[name]
+        want = str(rws.plan(n_rows, w.n_cols, dtype=w.dtype))
+        assert rws.plan_describe(n_rows, w.n_cols, w.dtype) == want, name
+    before = rws.launch_count()
+    with pytest.raises(rws.SoftmaxError):
+        rws.plan_describe(4, 4, 9)
+    assert rws.launch_count() == before
