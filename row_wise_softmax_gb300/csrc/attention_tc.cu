@@ -6,9 +6,9 @@
 //
 // attention_pp_kernel (the library's choice): a CTA owns two 128-query tiles
 // A and B and ping-pongs them, so that one tile's softmax runs while the
-// tensor cores compute the other's products.  A control warp's lane 0 issues
-// every tensor-map copy (Q once; K and V tiles of 64 keys through a ring of
-// 3 slots at head_dim 128, 2 at 64, all with the 128-byte swizzle) and every
+// tensor cores compute the other's products.  One warp's lane 0 issues every
+// tensor-map copy (Q once; K and V tiles of 64 keys through a ring of 3 slots
+// at head_dim 128, 2 at 64, all with the 128-byte swizzle), another's every
 // product; two warpgroups run the softmax, one per tile.  The protocol is
 // described beside the kernel.
 //
@@ -491,15 +491,15 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
 //   CTA      256 queries of one (batch, head): tile A (queries 0..127) and
 //            tile B (128..255).  Warps 0-3 run tile A's softmax, warps 4-7
 //            tile B's (thread t of a warpgroup owns query row t = TMEM lane
-//            t); lane 0 of warp 8 issues every tensor-map copy and every
-//            tcgen05.mma.
+//            t); lane 0 of warp 8 issues every tcgen05.mma, lane 0 of warp 9
+//            every tensor-map copy.
 //   operands Q, K and V land by cp.async.bulk.tensor (3-D maps: element,
 //            row, head; rows past a head's end read as zero) in boxes of 64
 //            elements with the 128-byte swizzle, read by the tensor cores
 //            through swizzled descriptors; P is written by the softmax
 //            threads in the plain core-matrix layout.
 //   TMEM     S_A at column 0, S_B at BN, O_A at 2 BN, O_B at 2 BN + D.
-//   order    per key tile t the control lane waits for P_A(t) (bar_p[A]),
+//   order    per key tile t the MMA lane waits for P_A(t) (bar_p[A]),
 //            issues O_A += P_A V(t) and S_A(t+1) = Q_A K(t+1)^T, commits
 //            (bar_s[A]); then the same for B.  So the tensor cores compute
 //            one tile's products while the other tile's warpgroup runs its
@@ -507,15 +507,19 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
 //            warpgroup's wait on S_X(t+1) also covers O_X += P_X V(t) (one
 //            commit covers every earlier operation of the issuing thread), so
 //            P_X and O_X are free for it when S_X(t+1) has landed.
-//   ring     K and V in KVS slots (tile t in slot t % KVS): K(t+KVS) refills
-//            K(t)'s slot once both S(t) were read (both P(t) written), V(t+KVS)
-//            refills V(t)'s once a commit issued right after P_B V(t) has
-//            arrived (bar_pv).
+//   ring     K and V in KVS slots (tile t in slot t % KVS): the copy lane
+//            refills K(t)'s slot with K(t+KVS) once a commit issued right
+//            after S_B(t) has arrived (k_free), V(t)'s with V(t+KVS) once one
+//            issued after P_B V(t) has (v_free).  Its waits never hold up the
+//            MMA lane, which only waits for operands and for P: with one lane
+//            doing both, a time-stamped build showed it reacting to a written
+//            P about 1700 cycles late (blocked on the P V wait and the
+//            copies), in a 3600-cycle period per key tile.
 //
 // Every wait is bounded; a timed-out wait records the error word and the
 // kernel stops issuing, waits (bounded) for what it issued and frees TMEM.
 constexpr int kPpWarpgroups = 2;
-constexpr int kPpThreads = kPpWarpgroups * 128 + 32;
+constexpr int kPpThreads = kPpWarpgroups * 128 + 64;     // + the MMA warp and the copy warp
 
 // Key/value ring depth of the ping-pong kernel: three slots at d = 128 (one
 // CTA per SM; the third slot hides the copy latency of the next key tile),
@@ -533,8 +537,8 @@ __host__ __device__ constexpr uint32_t pp_tmem_cols(int bn)
 }
 
 // At d = 64 two CTAs share an SM: the bound keeps every instantiation at or
-// below 96 registers a thread (9 warps a CTA; the fifth warp on a
-// sub-partition must still fit its register file).
+// below 96 registers a thread (10 warps a CTA, five on each sub-partition,
+// must fit its register file).
 template <typename T, int D, int BN, bool CAUSAL>
 __global__ void __launch_bounds__(kPpThreads, D == 64 ? 2 : 1)
 attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
@@ -550,10 +554,12 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
     constexpr uint32_t IDESC_PV = umma_idesc(kTcBM, D, kBF16, true);
     constexpr uint32_t TMEM_COLS = pp_tmem_cols<D>(BN);
     constexpr int NCH = BN / 32;
-    constexpr int CTRL = kPpWarpgroups * 4;                  // the control warp
+    constexpr int CTRL = kPpWarpgroups * 4;                  // the MMA warp
+    constexpr int LOADW = CTRL + 1;                          // the copy warp
     extern __shared__ __align__(128) unsigned char tc_smem[];
     __shared__ __align__(8) unsigned long long bar_s[2], bar_p[2], bar_fin[2], bar_drain;
-    __shared__ __align__(8) unsigned long long q_full, k_full[KVS], v_full[KVS], bar_pv;
+    __shared__ __align__(8) unsigned long long q_full, k_full[KVS], v_full[KVS];
+    __shared__ __align__(8) unsigned long long k_free[KVS], v_free[KVS];
     __shared__ uint32_t tmem_slot;
     __shared__ int s_failed;
 
@@ -587,10 +593,11 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
         }
         mbar_init(smem_addr(&bar_drain), 1);
         mbar_init(smem_addr(&q_full), 1);
-        mbar_init(smem_addr(&bar_pv), 1);
         for (int x = 0; x < KVS; ++x) {
             mbar_init(smem_addr(&k_full[x]), 1);
             mbar_init(smem_addr(&v_full[x]), 1);
+            mbar_init(smem_addr(&k_free[x]), 1);
+            mbar_init(smem_addr(&v_free[x]), 1);
         }
         s_failed = 0;
         fence_mbar_init();
@@ -603,19 +610,20 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
     pdl_launch_dependents();
     pdl_wait();
 
-    if (warp == CTRL) {
-        // ------------------------------------------------------ control warp
-        // Lane 0 issues every copy (the tensor memory accelerator) and every
-        // product.  An operand tile lands as D/64 boxes of 64 elements x ROWS
-        // rows, each row 128 bytes with the copy engine's 128-byte swizzle,
-        // so box c is ROWS/8 swizzle atoms of 1024 bytes.  Q and K are
-        // K-major: a 16-element step of the contraction is 32 bytes into the
-        // atom row (the tensor cores apply the same swizzle to the address),
-        // SBO = 1024 between 8-row bands.  V is MN-major (rows = keys, the
-        // output dimension contiguous): SBO = 1024 between 8-key bands, LBO =
-        // one box between the 64-element halves of D.  Rows past a head's
-        // end are zero-filled by the copy engine (the tensor maps are 3-D:
-        // element, row, head).
+    // Key tile t lives in ring slot t % KVS; its barriers' phase is t / KVS.
+    auto slot = [](int64_t t) { return static_cast<uint32_t>(t) % KVS; };
+    auto phase = [](int64_t t) { return (static_cast<uint32_t>(t) / KVS) & 1u; };
+    if (warp == LOADW) {
+        // --------------------------------------------------------- copy warp
+        // Lane 0 issues every copy (the tensor memory accelerator).  An
+        // operand tile lands as D/64 boxes of 64 elements x ROWS rows, each
+        // row 128 bytes with the copy engine's 128-byte swizzle, so box c is
+        // ROWS/8 swizzle atoms of 1024 bytes.  Rows past a head's end are
+        // zero-filled by the copy engine (the tensor maps are 3-D: element,
+        // row, head).  K(t + KVS) goes into K(t)'s slot once both S(t) have
+        // completed (k_free), V(t + KVS) into V(t)'s once both P V(t) have
+        // (v_free): the MMA warp commits those barriers, so neither of its
+        // waits holds up the products.
         if (lane == 0) {
             bool failed = false;
             auto wait1 = [&](uint32_t bar, uint32_t parity) {
@@ -639,14 +647,7 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                 for (int c = 0; c < D / 64; ++c)
                     tma3(dst + static_cast<uint32_t>(c * rows * 128), map, c * 64, row0, bar);
             };
-            // Key tile t lives in ring slot t % KVS; its barrier phase is
-            // t / KVS.  Copies issued and waited for are counted, so that a
-            // failed wait can still drain what is in flight before the CTA
-            // exits.
-            auto slot = [](int64_t t) { return static_cast<uint32_t>(t) % KVS; };
-            auto phase = [](int64_t t) { return (static_cast<uint32_t>(t) / KVS) & 1u; };
-            int64_t k_issued = 0, v_issued = 0, k_waited = 0, v_waited = 0;
-            bool q_issued = false;
+            int64_t k_issued = 0, v_issued = 0;
             auto load_k = [&](int64_t t) {
                 load_rows(sK + slot(t) * KV_BYTES, &map_k, BN, t * BN, smem_addr(&k_full[slot(t)]),
                           KV_BYTES);
@@ -657,13 +658,59 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                           KV_BYTES);
                 v_issued = t + 1;
             };
-            auto wait_k = [&](int64_t t) {
-                wait1(smem_addr(&k_full[slot(t)]), phase(t));
-                k_waited = failed ? k_waited : t + 1;
-            };
-            auto wait_v = [&](int64_t t) {
-                wait1(smem_addr(&v_full[slot(t)]), phase(t));
-                v_waited = failed ? v_waited : t + 1;
+            asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&map_q)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&map_k)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&map_v)) : "memory");
+            if (n_kt > 0) {
+                load_rows(sQ, &map_q, kTcBM, q0, smem_addr(&q_full), 2 * QT_BYTES);
+                // (the second Q tile completes on the same barrier)
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tma3(sQ + QT_BYTES + static_cast<uint32_t>(c * kTcBM * 128), &map_q, c * 64,
+                         q0 + kTcBM, smem_addr(&q_full));
+                for (int64_t t = 0; t < KVS && t < n_kt; ++t) {
+                    load_k(t);
+                    load_v(t);
+                }
+                for (int64_t t = 0; t + KVS < n_kt && !failed; ++t) {
+                    wait1(smem_addr(&k_free[slot(t)]), phase(t));      // both S(t) done
+                    if (failed || *reinterpret_cast<volatile int*>(&s_failed))
+                        break;
+                    load_k(t + KVS);
+                    wait1(smem_addr(&v_free[slot(t)]), phase(t));      // both P V(t) done
+                    if (failed || *reinterpret_cast<volatile int*>(&s_failed))
+                        break;
+                    load_v(t + KVS);
+                }
+                if (failed || *reinterpret_cast<volatile int*>(&s_failed)) {
+                    // Let the copies still in flight land (each wait bounded):
+                    // Q, and the last KVS tiles issued into each ring (an
+                    // earlier tile of a slot was consumed before its slot
+                    // was refilled).
+                    mbar_wait_bounded(smem_addr(&q_full), 0u);
+                    for (int64_t t = k_issued > KVS ? k_issued - KVS : 0; t < k_issued; ++t)
+                        mbar_wait_bounded(smem_addr(&k_full[slot(t)]), phase(t));
+                    for (int64_t t = v_issued > KVS ? v_issued - KVS : 0; t < v_issued; ++t)
+                        mbar_wait_bounded(smem_addr(&v_full[slot(t)]), phase(t));
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == CTRL) {
+        // ---------------------------------------------------------- MMA warp
+        // Lane 0 issues every product.  Q and K are K-major: a 16-element
+        // step of the contraction is 32 bytes into the swizzle atom row (the
+        // tensor cores apply the same swizzle to the address), SBO = 1024
+        // between 8-row bands.  V is MN-major (rows = keys, the output
+        // dimension contiguous): SBO = 1024 between 8-key bands, LBO = one
+        // box between the 64-element halves of D.
+        if (lane == 0) {
+            bool failed = false;
+            auto wait1 = [&](uint32_t bar, uint32_t parity) {
+                if (!failed && !mbar_wait_bounded(bar, parity)) {
+                    failed = true;
+                    *reinterpret_cast<volatile int*>(&s_failed) = 1;
+                }
             };
             auto issue_s = [&](int x, int64_t t) {
                 const uint32_t cK = sK + slot(t) * KV_BYTES;
@@ -686,40 +733,24 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                              smem_desc_sw128(cV + ks * 2048, BN * 128, 1024), IDESC_PV,
                              (t > 0 || ks > 0) ? 1u : 0u);
             };
-            asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&map_q)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&map_k)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&map_v)) : "memory");
             if (n_kt > 0) {
-                load_rows(sQ, &map_q, kTcBM, q0, smem_addr(&q_full), 2 * QT_BYTES);
-                q_issued = true;
-                // (the second Q tile completes on the same barrier)
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    tma3(sQ + QT_BYTES + static_cast<uint32_t>(c * kTcBM * 128), &map_q, c * 64,
-                         q0 + kTcBM, smem_addr(&q_full));
-                for (int64_t t = 0; t < KVS && t < n_kt; ++t) {
-                    load_k(t);
-                    load_v(t);
-                }
                 wait1(smem_addr(&q_full), 0u);
-                wait_k(0);
+                wait1(smem_addr(&k_full[0]), 0u);
                 if (!failed) {
-                    q_issued = false;
                     tc_fence_after();
                     issue_s(0, 0);
                     umma_commit(smem_addr(&bar_s[0]));
                     issue_s(1, 0);
                     umma_commit(smem_addr(&bar_s[1]));
+                    umma_commit(smem_addr(&k_free[0]));           // both S(0) done
                 }
             }
             // Per key tile t: P_A V(t) and S_A(t+1) once the softmax of A
-            // has written P_A(t), then the same for B; one commit after
-            // P_B V(t) tells when V(t)'s slot is free, and K(t)'s slot is
-            // free once both softmaxes have read S(t) (both P(t) written).
-            // K(t + KVS) and V(t + KVS) go into those slots.
+            // has written P_A(t), then the same for B.  After P_B V(t) a
+            // commit frees V(t)'s slot, after S_B(t+1) one frees K(t+1)'s.
             for (int64_t t = 0; t < n_kt && !failed; ++t) {
                 const bool more = t + 1 < n_kt;
-                wait_v(t);
+                wait1(smem_addr(&v_full[slot(t)]), phase(t));
                 for (int x = 0; x < 2 && !failed; ++x) {
                     wait1(smem_addr(&bar_p[x]), static_cast<uint32_t>(t & 1));   // P_X(t) written
                     if (failed)
@@ -727,32 +758,18 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                     tc_fence_after();
                     issue_pv(x, t);
                     if (x == 1)
-                        umma_commit(smem_addr(&bar_pv));           // phase t: P V(t) done
+                        umma_commit(smem_addr(&v_free[slot(t)]));   // both P V(t) done
                     if (more) {
                         if (x == 0)
-                            wait_k(t + 1);
+                            wait1(smem_addr(&k_full[slot(t + 1)]), phase(t + 1));
                         if (failed)
                             break;
                         issue_s(x, t + 1);
+                        if (x == 1)
+                            umma_commit(smem_addr(&k_free[slot(t + 1)]));   // both S(t+1) done
                     }
                     umma_commit(smem_addr(more ? &bar_s[x] : &bar_fin[x]));
                 }
-                if (failed || t + KVS >= n_kt)
-                    continue;
-                fence_proxy_async_smem();
-                load_k(t + KVS);
-                wait1(smem_addr(&bar_pv), static_cast<uint32_t>(t & 1));
-                if (!failed)
-                    load_v(t + KVS);
-            }
-            if (failed) {
-                // Let the copies still in flight land (each wait bounded).
-                if (q_issued)
-                    mbar_wait_bounded(smem_addr(&q_full), 0u);
-                for (; k_waited < k_issued; ++k_waited)
-                    mbar_wait_bounded(smem_addr(&k_full[slot(k_waited)]), phase(k_waited));
-                for (; v_waited < v_issued; ++v_waited)
-                    mbar_wait_bounded(smem_addr(&v_full[slot(v_waited)]), phase(v_waited));
             }
         }
         __syncwarp();
