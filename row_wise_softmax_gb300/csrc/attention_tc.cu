@@ -7,10 +7,11 @@
 // attention_pp_kernel (the library's choice): a CTA owns two 128-query tiles
 // A and B and ping-pongs them, so that one tile's softmax runs while the
 // tensor cores compute the other's products.  One warp's lane 0 issues every
-// tensor-map copy (Q once; K and V tiles of 64 keys through a ring of 3 slots
-// at head_dim 128, 2 at 64, all with the 128-byte swizzle), another's every
-// product; two warpgroups run the softmax, one per tile.  The protocol is
-// described beside the kernel.
+// tensor-map copy (Q once; K and V tiles of 128 keys through a ring of 2
+// slots at head_dim 128, of 64 keys through 4 slots at 64, all with the
+// 128-byte swizzle), another's
+// every product; two warpgroups run the softmax, one per tile, and keep P in
+// tensor memory.  The protocol is described beside the kernel.
 //
 // attention_tc_kernel, one tile per CTA:
 //
@@ -88,6 +89,18 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
                  : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T: A (M x 16) read from tensor memory, lane
+// = row, each 32-bit column two consecutive 16-bit K elements (the lower
+// index in the low half).
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
 // Arrive once on the mbarrier when every tcgen05 operation this thread has
 // issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar)
@@ -134,6 +147,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
            "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]),
            "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]),
            "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+        : "memory");
+}
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+        :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+           "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
+           "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
 
@@ -496,9 +521,14 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
 //   operands Q, K and V land by cp.async.bulk.tensor (3-D maps: element,
 //            row, head; rows past a head's end read as zero) in boxes of 64
 //            elements with the 128-byte swizzle, read by the tensor cores
-//            through swizzled descriptors; P is written by the softmax
-//            threads in the plain core-matrix layout.
-//   TMEM     S_A at column 0, S_B at BN, O_A at 2 BN, O_B at 2 BN + D.
+//            through swizzled descriptors.  Key tiles hold BN keys (128 at
+//            d = 128, 64 at d = 64).
+//   TMEM     S_A at column 0, S_B at BN, O_A at 2 BN, O_B at 2 BN + D (512
+//            columns at d = 128, 256 at d = 64).  A softmax thread reads its S row twice (the max,
+//            then the exponentials) and writes its P row, rounded to the
+//            operand type, over the first BN / 2 columns of S: P V takes its
+//            A operand from tensor memory, so P never passes through shared
+//            memory.
 //   order    per key tile t the MMA lane waits for P_A(t) (bar_p[A]),
 //            issues O_A += P_A V(t) and S_A(t+1) = Q_A K(t+1)^T, commits
 //            (bar_s[A]); then the same for B.  So the tensor cores compute
@@ -506,7 +536,9 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
 //            softmax, and every K/V tile copied serves 256 queries.  A
 //            warpgroup's wait on S_X(t+1) also covers O_X += P_X V(t) (one
 //            commit covers every earlier operation of the issuing thread), so
-//            P_X and O_X are free for it when S_X(t+1) has landed.
+//            O_X is free for it when S_X(t+1) has landed; S_X(t+1) overwrites
+//            P_X(t) only after P_X V(t) has read it (the tensor cores perform
+//            one thread's products in the order issued).
 //   ring     K and V in KVS slots (tile t in slot t % KVS): the copy lane
 //            refills K(t)'s slot with K(t+KVS) once a commit issued right
 //            after S_B(t) has arrived (k_free), V(t)'s with V(t+KVS) once one
@@ -521,24 +553,28 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
 constexpr int kPpWarpgroups = 2;
 constexpr int kPpThreads = kPpWarpgroups * 128 + 64;     // + the MMA warp and the copy warp
 
-// Key/value ring depth of the ping-pong kernel: three slots at d = 128 (one
-// CTA per SM; the third slot hides the copy latency of the next key tile),
-// two at d = 64 so that two CTAs fit in one SM's shared memory.
+// Keys per tile of the ping-pong kernel.  d = 128: 128, so that S = Q K^T
+// is a 128 x 128 product (a 128 x 64 x 16 product reads 6 KB of operands
+// from shared memory for 32 cycles of arithmetic; a time-stamped build saw
+// about 90 cycles per such product issued), one CTA per SM (S_A, S_B, O_A,
+// O_B fill the 512 TMEM columns).  d = 64: 64 keys and two CTAs per SM (256
+// columns each): the exponentials, not the products, bound it there (one
+// exponential per 2 x 64 multiply-adds), and two CTAs keep four softmax
+// warpgroups on each SM.
+template <int D>
+__host__ __device__ constexpr int pp_bn()
+{
+    return D == 128 ? 128 : 64;
+}
+
+// Key/value ring depth: two slots at d = 128 (Q, K and V fill 192 KB), four
+// at d = 64 (96 KB a CTA).
 template <int D>
 __host__ __device__ constexpr int pp_kv_stages()
 {
-    return D == 128 ? 3 : 2;
+    return D == 128 ? 2 : 4;
 }
 
-template <int D>
-__host__ __device__ constexpr uint32_t pp_tmem_cols(int bn)
-{
-    return 2 * bn + 2 * D <= 256 ? 256u : 512u;
-}
-
-// At d = 64 two CTAs share an SM: the bound keeps every instantiation at or
-// below 96 registers a thread (10 warps a CTA, five on each sub-partition,
-// must fit its register file).
 template <typename T, int D, int BN, bool CAUSAL>
 __global__ void __launch_bounds__(kPpThreads, D == 64 ? 2 : 1)
 attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
@@ -547,12 +583,12 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                     int64_t n_q, int64_t n_k, float scale_log2, int64_t offset)
 {
     constexpr bool kBF16 = sizeof(T) == 2 && Elem<T>::kNegInfBits == 0xff80u;
-    constexpr uint32_t QT_BYTES = kTcBM * D * 2, KV_BYTES = BN * D * 2, P_BYTES = kTcBM * BN * 2;
+    constexpr uint32_t QT_BYTES = kTcBM * D * 2, KV_BYTES = BN * D * 2;
     constexpr int KVS = pp_kv_stages<D>();
-    constexpr uint32_t SBO_P = (BN / 8) * 128;
     constexpr uint32_t IDESC_S = umma_idesc(kTcBM, BN, kBF16, false);
     constexpr uint32_t IDESC_PV = umma_idesc(kTcBM, D, kBF16, true);
-    constexpr uint32_t TMEM_COLS = pp_tmem_cols<D>(BN);
+    constexpr uint32_t TMEM_COLS = 2 * BN + 2 * D <= 256 ? 256u : 512u;
+    static_assert(2 * BN + 2 * D <= 512, "S_A, S_B, O_A and O_B fill at most 512 columns");
     constexpr int NCH = BN / 32;
     constexpr int CTRL = kPpWarpgroups * 4;                  // the MMA warp
     constexpr int LOADW = CTRL + 1;                          // the copy warp
@@ -564,8 +600,7 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
     __shared__ int s_failed;
 
     const uint32_t base = (smem_addr(tc_smem) + 1023u) & ~1023u;   // swizzle atoms
-    const uint32_t sQ = base, sK = sQ + 2 * QT_BYTES, sV = sK + KVS * KV_BYTES,
-                   sP = sV + KVS * KV_BYTES;
+    const uint32_t sQ = base, sK = sQ + 2 * QT_BYTES, sV = sK + KVS * KV_BYTES;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t n_qt = (n_q + 2 * kTcBM - 1) / (2 * kTcBM);
     // Causal: query tiles of every head, longest (last) first, so that the
@@ -723,15 +758,16 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                              IDESC_S,
                              ks > 0 ? 1u : 0u);
             };
+            // P_X (16-bit) sits in the first BN / 2 columns of S_X: a
+            // 16-key step of the product reads 8 of them.
             auto issue_pv = [&](int x, int64_t t) {
                 const uint32_t cV = sV + slot(t) * KV_BYTES;
-                const uint32_t px = sP + static_cast<uint32_t>(x) * P_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < BN / 16; ++ks)
-                    umma_f16(tmem + static_cast<uint32_t>(2 * BN + x * D),
-                             smem_desc(px + ks * 256, 128, SBO_P),
-                             smem_desc_sw128(cV + ks * 2048, BN * 128, 1024), IDESC_PV,
-                             (t > 0 || ks > 0) ? 1u : 0u);
+                    umma_f16_ta(tmem + static_cast<uint32_t>(2 * BN + x * D),
+                                tmem + static_cast<uint32_t>(x * BN + ks * 8),
+                                smem_desc_sw128(cV + ks * 2048, BN * 128, 1024), IDESC_PV,
+                                (t > 0 || ks > 0) ? 1u : 0u);
             };
             if (n_kt > 0) {
                 wait1(smem_addr(&q_full), 0u);
@@ -782,7 +818,6 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
         const uint32_t t_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const uint32_t s_col = static_cast<uint32_t>(x * BN);
         const uint32_t o_col = static_cast<uint32_t>(2 * BN + x * D);
-        const uint32_t px = sP + static_cast<uint32_t>(x) * P_BYTES;
         float m = kNegInf, l = 0.0f;
         bool failed = false;                                 // warp-uniform
         for (int64_t t = 0; t < n_kt; ++t) {
@@ -793,30 +828,38 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
             }
             tc_fence_after();
             const int64_t k0 = t * BN;
-            float mx = kNegInf;
-            float sv[NCH][32];
-#pragma unroll
-            for (int c = 0; c < NCH; ++c)
-                tmem_ld32(t_row + s_col + c * 32, sv[c]);
-            tmem_wait_ld();
             const bool edge = k0 + BN > n_k || (CAUSAL && k0 + BN - 1 > qx0 + offset);
+            int keep = BN;                                   // keys of the tile kept
             if (edge) {
-                int64_t lim = n_k - k0;                      // keys of the tile kept
+                int64_t lim = n_k - k0;
                 if (CAUSAL && qi + offset + 1 - k0 < lim)
                     lim = qi + offset + 1 - k0;
-                const int keep = static_cast<int>(lim < 0 ? 0 : (lim > BN ? BN : lim));
-#pragma unroll
-                for (int c = 0; c < NCH; ++c)
+                keep = static_cast<int>(lim < 0 ? 0 : (lim > BN ? BN : lim));
+            }
+            // 64-key tiles: the row's scores stay in registers.  128-key
+            // tiles: two passes over S in tensor memory (the maximum, then the
+            // exponentials), 32 scores at a time.
+            constexpr int HOLD = NCH <= 2 ? NCH : 1;
+            float sv[HOLD][32];
+            auto load_chunk = [&](int c, float (&v)[32]) {
+                tmem_ld32(t_row + s_col + c * 32, v);
+                tmem_wait_ld();
+                if (edge) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         if (c * 32 + j >= keep)
-                            sv[c][j] = kNegInf;
-            }
+                            v[j] = kNegInf;
+                }
+            };
+            float mx = kNegInf;
 #pragma unroll
-            for (int c = 0; c < NCH; ++c)
+            for (int c = 0; c < NCH; ++c) {
+                float (&v)[32] = sv[HOLD == NCH ? c : 0];
+                load_chunk(c, v);
 #pragma unroll
                 for (int j = 0; j < 32; j += 2)
-                    mx = max3(mx, sv[c][j], sv[c][j + 1]);
+                    mx = max3(mx, v[j], v[j + 1]);
+            }
             // Lazy rescaling as in attention_tc_kernel: the reference m moves
             // only when a tile's max exceeds it by more than 2^8.
             const float mx_s = mx * scale_log2;
@@ -826,24 +869,28 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                 m = mx_s;
             }
             const float ref = m == kNegInf ? 0.0f : m;
-            float sum = 0.0f;
+            // p = 2^(S scale log2 e - m), summed, rounded to the operand type
+            // in pairs and stored over S's first columns (P chunk c takes
+            // columns [16c, 16c + 16), whose scores are already read).
+            float sum0 = 0.0f, sum1 = 0.0f;
 #pragma unroll
             for (int c = 0; c < NCH; ++c) {
+                float (&v)[32] = sv[HOLD == NCH ? c : 0];
+                if (HOLD != NCH)
+                    load_chunk(c, v);
+                uint32_t w[16];
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    float p[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        p[e] = ex2_ftz(fmaf(sv[c][g * 8 + e], scale_log2, -ref));
-                        sum += p[e];
-                    }
-                    const uint32_t w0 = Elem<T>::pack2(p[0], p[1]), w1 = Elem<T>::pack2(p[2], p[3]);
-                    const uint32_t w2 = Elem<T>::pack2(p[4], p[5]), w3 = Elem<T>::pack2(p[6], p[7]);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                                 :: "r"(px + kmajor_off(r, c * 4 + g, BN)), "r"(w0), "r"(w1),
-                                    "r"(w2), "r"(w3) : "memory");
+                for (int j = 0; j < 16; ++j) {
+                    const float p0 = ex2_ftz(fmaf(v[2 * j], scale_log2, -ref));
+                    const float p1 = ex2_ftz(fmaf(v[2 * j + 1], scale_log2, -ref));
+                    sum0 += p0;
+                    sum1 += p1;
+                    w[j] = Elem<T>::pack2(p0, p1);
                 }
+                tmem_st16(t_row + s_col + c * 16, w);
             }
+            tmem_wait_st();
+            const float sum = sum0 + sum1;
             l = l * alpha + sum;
             if (t > 0 && !__all_sync(0xffffffffu, alpha == 1.0f)) {
 #pragma unroll
@@ -858,7 +905,6 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                 }
                 tmem_wait_st();
             }
-            fence_proxy_async_smem();                        // P -> tensor cores
             tc_fence_before();
             mbar_arrive(smem_addr(&bar_p[x]));               // release: P_X(t), O_X rescaled
         }
@@ -943,9 +989,9 @@ inline bool pp_tensor_map(CUtensorMap* map, const void* ptr, int64_t bh, int64_t
 template <typename T, int D, bool CAUSAL>
 cudaError_t launch_pp(const AttentionProblem& p, cudaStream_t s)
 {
-    constexpr int BN = 64;
+    constexpr int BN = pp_bn<D>();
     auto* kern = attention_pp_kernel<T, D, BN, CAUSAL>;
-    const int smem = (2 * kTcBM * D + 2 * pp_kv_stages<D>() * BN * D + 2 * kTcBM * BN) * 2 + 1024;
+    const int smem = (2 * kTcBM * D + 2 * pp_kv_stages<D>() * BN * D) * 2 + 1024;
     static std::atomic<bool> attr_set[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
