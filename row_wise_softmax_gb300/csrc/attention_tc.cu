@@ -839,26 +839,36 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
             // 64-key tiles: the row's scores stay in registers.  128-key
             // tiles: two passes over S in tensor memory (the maximum, then the
             // exponentials), 32 scores at a time.
-            constexpr int HOLD = NCH <= 2 ? NCH : 1;
-            float sv[HOLD][32];
-            auto load_chunk = [&](int c, float (&v)[32]) {
-                tmem_ld32(t_row + s_col + c * 32, v);
+            // The row's scores in groups of G chunks of 32: each group's
+            // tensor-memory loads are issued together and waited for once
+            // (all of them at BN = 64, held through both steps; two of four
+            // at BN = 128, read twice: the maximum, then the exponentials).
+            constexpr int G = NCH <= 2 ? NCH : 2;
+            constexpr bool HOLD = G == NCH;
+            float sv[G][32];
+            auto load_group = [&](int c0) {
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    tmem_ld32(t_row + s_col + (c0 + g) * 32, sv[g]);
                 tmem_wait_ld();
                 if (edge) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (c * 32 + j >= keep)
-                            v[j] = kNegInf;
+                    for (int g = 0; g < G; ++g)
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if ((c0 + g) * 32 + j >= keep)
+                                sv[g][j] = kNegInf;
                 }
             };
             float mx = kNegInf;
 #pragma unroll
-            for (int c = 0; c < NCH; ++c) {
-                float (&v)[32] = sv[HOLD == NCH ? c : 0];
-                load_chunk(c, v);
+            for (int c0 = 0; c0 < NCH; c0 += G) {
+                load_group(c0);
 #pragma unroll
-                for (int j = 0; j < 32; j += 2)
-                    mx = max3(mx, v[j], v[j + 1]);
+                for (int g = 0; g < G; ++g)
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2)
+                        mx = max3(mx, sv[g][j], sv[g][j + 1]);
             }
             // Lazy rescaling as in attention_tc_kernel: the reference m moves
             // only when a tile's max exceeds it by more than 2^8.
@@ -873,37 +883,38 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
             // in pairs and stored over S's first columns (P chunk c takes
             // columns [16c, 16c + 16), whose scores are already read).  The
             // loop is written out twice, for tiles with and without masked
-            // keys: the same arithmetic, but compiled this way the kernel
-            // holds 86-89 registers a thread instead of 140 and measured
-            // faster (1217 against 1137 TFLOP/s at d = 128, 828 against 832
-            // at d = 64).
+            // keys: the same arithmetic, but compiled apart it keeps fewer
+            // registers live and measured faster.
             float sum0 = 0.0f, sum1 = 0.0f;
 #pragma unroll
-            for (int c = 0; c < NCH; ++c) {
-                float (&v)[32] = sv[HOLD == NCH ? c : 0];
-                if (HOLD != NCH)
-                    load_chunk(c, v);
-                uint32_t w[16];
-                if (edge) {                                  // masked scores are -inf: p = 0
+            for (int c0 = 0; c0 < NCH; c0 += G) {
+                if (!HOLD)
+                    load_group(c0);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float p0 = ex2_ftz(fmaf(v[2 * j], scale_log2, -ref));
-                        const float p1 = ex2_ftz(fmaf(v[2 * j + 1], scale_log2, -ref));
-                        sum0 += p0;
-                        sum1 += p1;
-                        w[j] = Elem<T>::pack2(p0, p1);
-                    }
-                } else {
+                for (int g = 0; g < G; ++g) {
+                    const float (&v)[32] = sv[g];
+                    uint32_t w[16];
+                    if (edge) {                              // masked scores are -inf: p = 0
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float p0 = ex2_ftz(fmaf(v[2 * j], scale_log2, -ref));
-                        const float p1 = ex2_ftz(fmaf(v[2 * j + 1], scale_log2, -ref));
-                        sum0 += p0;
-                        sum1 += p1;
-                        w[j] = Elem<T>::pack2(p0, p1);
+                        for (int j = 0; j < 16; ++j) {
+                            const float p0 = ex2_ftz(fmaf(v[2 * j], scale_log2, -ref));
+                            const float p1 = ex2_ftz(fmaf(v[2 * j + 1], scale_log2, -ref));
+                            sum0 += p0;
+                            sum1 += p1;
+                            w[j] = Elem<T>::pack2(p0, p1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float p0 = ex2_ftz(fmaf(v[2 * j], scale_log2, -ref));
+                            const float p1 = ex2_ftz(fmaf(v[2 * j + 1], scale_log2, -ref));
+                            sum0 += p0;
+                            sum1 += p1;
+                            w[j] = Elem<T>::pack2(p0, p1);
+                        }
                     }
+                    tmem_st16(t_row + s_col + (c0 + g) * 16, w);
                 }
-                tmem_st16(t_row + s_col + c * 16, w);
             }
             tmem_wait_st();
             const float sum = sum0 + sum1;
