@@ -609,11 +609,17 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
     const int64_t qt = CAUSAL ? n_qt - 1 - static_cast<int64_t>(blockIdx.x) / bh
                               : static_cast<int64_t>(blockIdx.x) % n_qt;
     const int64_t q0 = qt * 2 * kTcBM;
-    int64_t n_kt = (n_k + BN - 1) / BN;
+    // Key tiles the CTA visits (n_kt, all of them for tile B) and tile A's
+    // share: under the causal mask tile A stops where its own last query
+    // does (at 128-key tiles one tile before B when the mask is the pages').
+    int64_t n_kt = (n_k + BN - 1) / BN, n_kt_a = n_kt;
     if (CAUSAL) {
-        const int64_t last = q0 + 2 * kTcBM - 1 + offset;    // the CTA's last query
-        const int64_t lim = last < 0 ? 0 : last / BN + 1;
-        n_kt = lim < n_kt ? lim : n_kt;
+        auto tiles_to = [&](int64_t last) {                  // through query `last`
+            const int64_t lim = last < 0 ? 0 : last / BN + 1;
+            return lim < n_kt ? lim : n_kt;
+        };
+        n_kt_a = tiles_to(q0 + kTcBM - 1 + offset);
+        n_kt = tiles_to(q0 + 2 * kTcBM - 1 + offset);
     }
 
     if (warp == 0) {
@@ -774,35 +780,40 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                 wait1(smem_addr(&k_full[0]), 0u);
                 if (!failed) {
                     tc_fence_after();
-                    issue_s(0, 0);
-                    umma_commit(smem_addr(&bar_s[0]));
+                    if (n_kt_a > 0) {
+                        issue_s(0, 0);
+                        umma_commit(smem_addr(&bar_s[0]));
+                    }
                     issue_s(1, 0);
                     umma_commit(smem_addr(&bar_s[1]));
-                    umma_commit(smem_addr(&k_free[0]));           // both S(0) done
+                    umma_commit(smem_addr(&k_free[0]));           // S(0) done
                 }
             }
             // Per key tile t: P_A V(t) and S_A(t+1) once the softmax of A
-            // has written P_A(t), then the same for B.  After P_B V(t) a
-            // commit frees V(t)'s slot, after S_B(t+1) one frees K(t+1)'s.
+            // has written P_A(t) (while A has tiles left), then the same for
+            // B.  After P_B V(t) a commit frees V(t)'s slot, after S_B(t+1)
+            // one frees K(t+1)'s (B visits every tile the CTA loads).
             for (int64_t t = 0; t < n_kt && !failed; ++t) {
-                const bool more = t + 1 < n_kt;
                 wait1(smem_addr(&v_full[slot(t)]), phase(t));
                 for (int x = 0; x < 2 && !failed; ++x) {
+                    const int64_t tiles = x == 0 ? n_kt_a : n_kt;
+                    if (t >= tiles)
+                        continue;
+                    const bool more = t + 1 < tiles;
                     wait1(smem_addr(&bar_p[x]), static_cast<uint32_t>(t & 1));   // P_X(t) written
                     if (failed)
                         break;
                     tc_fence_after();
                     issue_pv(x, t);
                     if (x == 1)
-                        umma_commit(smem_addr(&v_free[slot(t)]));   // both P V(t) done
+                        umma_commit(smem_addr(&v_free[slot(t)]));   // P V(t) done
                     if (more) {
-                        if (x == 0)
-                            wait1(smem_addr(&k_full[slot(t + 1)]), phase(t + 1));
+                        wait1(smem_addr(&k_full[slot(t + 1)]), phase(t + 1));
                         if (failed)
                             break;
                         issue_s(x, t + 1);
                         if (x == 1)
-                            umma_commit(smem_addr(&k_free[slot(t + 1)]));   // both S(t+1) done
+                            umma_commit(smem_addr(&k_free[slot(t + 1)]));   // S(t+1) done
                     }
                     umma_commit(smem_addr(more ? &bar_s[x] : &bar_fin[x]));
                 }
@@ -818,9 +829,10 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
         const uint32_t t_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const uint32_t s_col = static_cast<uint32_t>(x * BN);
         const uint32_t o_col = static_cast<uint32_t>(2 * BN + x * D);
+        const int64_t my_kt = x == 0 ? n_kt_a : n_kt;         // key tiles of this query tile
         float m = kNegInf, l = 0.0f;
         bool failed = false;                                 // warp-uniform
-        for (int64_t t = 0; t < n_kt; ++t) {
+        for (int64_t t = 0; t < my_kt; ++t) {
             const bool ok = failed || mbar_wait_bounded(smem_addr(&bar_s[x]), static_cast<uint32_t>(t & 1));
             if (__any_sync(0xffffffffu, !ok) && !failed) {
                 failed = true;
@@ -935,7 +947,7 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
             tc_fence_before();
             mbar_arrive(smem_addr(&bar_p[x]));               // release: P_X(t), O_X rescaled
         }
-        if (n_kt > 0) {
+        if (my_kt > 0) {
             const bool ok = failed || mbar_wait_bounded(smem_addr(&bar_fin[x]), 0u);
             if (__any_sync(0xffffffffu, !ok) && !failed) {
                 failed = true;
@@ -951,7 +963,7 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                 float ov[32];
                 tmem_ld32(t_row + o_col + c * 32, ov);
                 tmem_wait_ld();
-                if (qi < n_q && n_kt > 0) {
+                if (qi < n_q && my_kt > 0) {
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
                         uint4 w;
@@ -963,7 +975,7 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                     }
                 }
             }
-            if (n_kt == 0 && qi < n_q) {                     // no key at all: NaN rows
+            if (my_kt == 0 && qi < n_q) {                    // no key at all: NaN rows
                 const float nan = __int_as_float(0x7fc00000);
                 for (int d0 = 0; d0 < D; d0 += 2)
                     *reinterpret_cast<uint32_t*>(go + qi * D + d0) = Elem<T>::pack2(nan, nan);
