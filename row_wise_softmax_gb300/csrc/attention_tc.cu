@@ -42,6 +42,7 @@
 // Every mbarrier wait is bounded; on a timeout the kernel records the error
 // word, stops issuing, waits (bounded) for what it issued and frees TMEM.
 #include "attention_pp.h"
+#include "cluster_ring.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "tensor_map.h"
@@ -550,8 +551,23 @@ attention_tc_kernel(const T* q, const T* k, const T* v, T* o, float* lse, int64_
 //
 // Every wait is bounded; a timed-out wait records the error word and the
 // kernel stops issuing, waits (bounded) for what it issued and frees TMEM.
-constexpr int kPpWarpgroups = 2;
-constexpr int kPpThreads = kPpWarpgroups * 128 + 64;     // + the MMA warp and the copy warp
+constexpr int kPpWarpgroups = 2;                          // query tiles per CTA
+
+// Warps that share a row of S (each takes BN / split of its keys): two at
+// d = 128, so a query tile's softmax runs on eight warps; one at d = 64
+// (two CTAs share an SM there and their registers would not fit twice).
+template <int D>
+__host__ __device__ constexpr int pp_split()
+{
+    return D == 128 ? 2 : 1;
+}
+
+// Softmax warps, plus the MMA warp and the copy warp.
+template <int D>
+__host__ __device__ constexpr int pp_threads()
+{
+    return kPpWarpgroups * 4 * pp_split<D>() * 32 + 64;
+}
 
 // Keys per tile of the ping-pong kernel.  d = 128: 128, so that S = Q K^T
 // is a 128 x 128 product (a 128 x 64 x 16 product reads 6 KB of operands
@@ -576,7 +592,7 @@ __host__ __device__ constexpr int pp_kv_stages()
 }
 
 template <typename T, int D, int BN, bool CAUSAL>
-__global__ void __launch_bounds__(kPpThreads, D == 64 ? 2 : 1)
+__global__ void __launch_bounds__(pp_threads<D>(), D == 64 ? 2 : 1)
 attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, T* o, float* lse, int64_t bh,
@@ -590,7 +606,9 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
     constexpr uint32_t TMEM_COLS = 2 * BN + 2 * D <= 256 ? 256u : 512u;
     static_assert(2 * BN + 2 * D <= 512, "S_A, S_B, O_A and O_B fill at most 512 columns");
     constexpr int NCH = BN / 32;
-    constexpr int CTRL = kPpWarpgroups * 4;                  // the MMA warp
+    constexpr int HS = pp_split<D>();                        // warps per row group
+    constexpr int CW = BN / HS;                              // keys of S per softmax warp
+    constexpr int CTRL = kPpWarpgroups * 4 * HS;             // the MMA warp
     constexpr int LOADW = CTRL + 1;                          // the copy warp
     extern __shared__ __align__(128) unsigned char tc_smem[];
     __shared__ __align__(8) unsigned long long bar_s[2], bar_p[2], bar_fin[2], bar_drain;
@@ -598,6 +616,9 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
     __shared__ __align__(8) unsigned long long k_free[KVS], v_free[KVS];
     __shared__ uint32_t tmem_slot;
     __shared__ int s_failed;
+    // Row maxima (by tile parity) and final sums of the warps sharing a row.
+    __shared__ float xmax[HS > 1 ? 2 : 1][kPpWarpgroups][HS][kTcBM];
+    __shared__ float xsum[kPpWarpgroups][HS][kTcBM];
 
     const uint32_t base = (smem_addr(tc_smem) + 1023u) & ~1023u;   // swizzle atoms
     const uint32_t sQ = base, sK = sQ + 2 * QT_BYTES, sV = sK + KVS * KV_BYTES;
@@ -629,7 +650,7 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
     if (tid == 0) {
         for (int x = 0; x < 2; ++x) {
             mbar_init(smem_addr(&bar_s[x]), 1);
-            mbar_init(smem_addr(&bar_p[x]), 128);
+            mbar_init(smem_addr(&bar_p[x]), 128 * HS);
             mbar_init(smem_addr(&bar_fin[x]), 1);
         }
         mbar_init(smem_addr(&bar_drain), 1);
@@ -764,14 +785,17 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
                              IDESC_S,
                              ks > 0 ? 1u : 0u);
             };
-            // P_X (16-bit) sits in the first BN / 2 columns of S_X: a
-            // 16-key step of the product reads 8 of them.
+            // P_X (16-bit) sits over S_X: each softmax warp's CW keys in the
+            // first CW / 2 columns of its own CW-column part of S_X, so a
+            // 16-key step of the product reads 8 columns, CW / 2 further on
+            // in the second part.
             auto issue_pv = [&](int x, int64_t t) {
                 const uint32_t cV = sV + slot(t) * KV_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < BN / 16; ++ks)
                     umma_f16_ta(tmem + static_cast<uint32_t>(2 * BN + x * D),
-                                tmem + static_cast<uint32_t>(x * BN + ks * 8),
+                                tmem + static_cast<uint32_t>(x * BN + ks * 8 +
+                                                             (ks * 16 / CW) * (CW / 2)),
                                 smem_desc_sw128(cV + ks * 2048, BN * 128, 1024), IDESC_PV,
                                 (t > 0 || ks > 0) ? 1u : 0u);
             };
@@ -821,16 +845,22 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
         }
         __syncwarp();
     } else {
-        // ---------------------------------------------------- softmax warpgroups
-        const int x = warp >> 2;                             // 0: tile A, 1: tile B
-        const int r = tid & 127;                             // row of the tile = TMEM lane
+        // ---------------------------------------------------- softmax warps
+        // Warp w: query tile x, TMEM lane group w % 4 (rows 32 (w % 4) ..),
+        // and part h of the tile's keys and of O's columns when HS warps
+        // share a row (h = 0 at d = 64).
+        const int x = warp / (4 * HS);                       // 0: tile A, 1: tile B
+        const int h = (warp / 4) % HS;
+        const int r = (warp & 3) * 32 + lane;                // row of the tile = TMEM lane
         const int64_t qx0 = q0 + static_cast<int64_t>(x) * kTcBM;
         const int64_t qi = qx0 + r;                          // this thread's query
         const uint32_t t_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-        const uint32_t s_col = static_cast<uint32_t>(x * BN);
-        const uint32_t o_col = static_cast<uint32_t>(2 * BN + x * D);
+        const uint32_t s_col = static_cast<uint32_t>(x * BN + h * CW);   // this warp's keys
+        constexpr int OW = D / HS;                           // O columns per warp
+        const uint32_t o_col = static_cast<uint32_t>(2 * BN + x * D + h * OW);
         const int64_t my_kt = x == 0 ? n_kt_a : n_kt;         // key tiles of this query tile
-        float m = kNegInf, l = 0.0f;
+        constexpr int NCH = CW / 32;                         // 32-column chunks per warp
+        float m = kNegInf, l = 0.0f;                         // l: this warp's part of the sum
         bool failed = false;                                 // warp-uniform
         for (int64_t t = 0; t < my_kt; ++t) {
             const bool ok = failed || mbar_wait_bounded(smem_addr(&bar_s[x]), static_cast<uint32_t>(t & 1));
@@ -841,46 +871,45 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
             tc_fence_after();
             const int64_t k0 = t * BN;
             const bool edge = k0 + BN > n_k || (CAUSAL && k0 + BN - 1 > qx0 + offset);
-            int keep = BN;                                   // keys of the tile kept
+            int keep = CW;                                   // this warp's keys kept
             if (edge) {
                 int64_t lim = n_k - k0;
                 if (CAUSAL && qi + offset + 1 - k0 < lim)
                     lim = qi + offset + 1 - k0;
-                keep = static_cast<int>(lim < 0 ? 0 : (lim > BN ? BN : lim));
+                lim -= h * CW;
+                keep = static_cast<int>(lim < 0 ? 0 : (lim > CW ? CW : lim));
             }
-            // 64-key tiles: the row's scores stay in registers.  128-key
-            // tiles: two passes over S in tensor memory (the maximum, then the
-            // exponentials), 32 scores at a time.
-            // The row's scores in groups of G chunks of 32: each group's
-            // tensor-memory loads are issued together and waited for once
-            // (all of them at BN = 64, held through both steps; two of four
-            // at BN = 128, read twice: the maximum, then the exponentials).
-            constexpr int G = NCH <= 2 ? NCH : 2;
-            constexpr bool HOLD = G == NCH;
-            float sv[G][32];
-            auto load_group = [&](int c0) {
+            // This warp's CW scores stay in registers: loaded together,
+            // waited for once.
+            float sv[NCH][32];
 #pragma unroll
-                for (int g = 0; g < G; ++g)
-                    tmem_ld32(t_row + s_col + (c0 + g) * 32, sv[g]);
-                tmem_wait_ld();
-                if (edge) {
+            for (int c = 0; c < NCH; ++c)
+                tmem_ld32(t_row + s_col + c * 32, sv[c]);
+            tmem_wait_ld();
+            if (edge) {
 #pragma unroll
-                    for (int g = 0; g < G; ++g)
+                for (int c = 0; c < NCH; ++c)
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if ((c0 + g) * 32 + j >= keep)
-                                sv[g][j] = kNegInf;
-                }
-            };
+                    for (int j = 0; j < 32; ++j)
+                        if (c * 32 + j >= keep)
+                            sv[c][j] = kNegInf;
+            }
             float mx = kNegInf;
 #pragma unroll
-            for (int c0 = 0; c0 < NCH; c0 += G) {
-                load_group(c0);
+            for (int c = 0; c < NCH; ++c)
 #pragma unroll
-                for (int g = 0; g < G; ++g)
+                for (int j = 0; j < 32; j += 2)
+                    mx = max3(mx, sv[c][j], sv[c][j + 1]);
+            if constexpr (HS > 1) {
+                // The row's maximum over the warps that share it (named
+                // barrier of the tile's warps; slots by tile parity, so a
+                // slot is rewritten only after the next barrier).
+                const int par = static_cast<int>(t & 1);
+                xmax[par][x][h][r] = mx;
+                named_barrier(1 + x, 128 * HS);
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2)
-                        mx = max3(mx, sv[g][j], sv[g][j + 1]);
+                for (int o = 0; o < HS; ++o)
+                    mx = fmaxf(mx, xmax[par][x][o][r]);
             }
             // Lazy rescaling as in attention_tc_kernel: the reference m moves
             // only when a tile's max exceeds it by more than 2^8.
@@ -892,48 +921,42 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
             }
             const float ref = m == kNegInf ? 0.0f : m;
             // p = 2^(S scale log2 e - m), summed, rounded to the operand type
-            // in pairs and stored over S's first columns (P chunk c takes
-            // columns [16c, 16c + 16), whose scores are already read).  The
+            // in pairs and stored over the first CW / 2 columns of this
+            // warp's part of S (its own scores, already in registers).  The
             // loop is written out twice, for tiles with and without masked
             // keys: the same arithmetic, but compiled apart it keeps fewer
             // registers live and measured faster.
             float sum0 = 0.0f, sum1 = 0.0f;
 #pragma unroll
-            for (int c0 = 0; c0 < NCH; c0 += G) {
-                if (!HOLD)
-                    load_group(c0);
+            for (int c = 0; c < NCH; ++c) {
+                const float (&v)[32] = sv[c];
+                uint32_t w[16];
+                if (edge) {                                  // masked scores are -inf: p = 0
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float (&v)[32] = sv[g];
-                    uint32_t w[16];
-                    if (edge) {                              // masked scores are -inf: p = 0
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float p0 = ex2_ftz(fmaf(v[2 * j], scale_log2, -ref));
-                            const float p1 = ex2_ftz(fmaf(v[2 * j + 1], scale_log2, -ref));
-                            sum0 += p0;
-                            sum1 += p1;
-                            w[j] = Elem<T>::pack2(p0, p1);
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float p0 = ex2_ftz(fmaf(v[2 * j], scale_log2, -ref));
-                            const float p1 = ex2_ftz(fmaf(v[2 * j + 1], scale_log2, -ref));
-                            sum0 += p0;
-                            sum1 += p1;
-                            w[j] = Elem<T>::pack2(p0, p1);
-                        }
+                    for (int j = 0; j < 16; ++j) {
+                        const float p0 = ex2_ftz(fmaf(v[2 * j], scale_log2, -ref));
+                        const float p1 = ex2_ftz(fmaf(v[2 * j + 1], scale_log2, -ref));
+                        sum0 += p0;
+                        sum1 += p1;
+                        w[j] = Elem<T>::pack2(p0, p1);
                     }
-                    tmem_st16(t_row + s_col + (c0 + g) * 16, w);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float p0 = ex2_ftz(fmaf(v[2 * j], scale_log2, -ref));
+                        const float p1 = ex2_ftz(fmaf(v[2 * j + 1], scale_log2, -ref));
+                        sum0 += p0;
+                        sum1 += p1;
+                        w[j] = Elem<T>::pack2(p0, p1);
+                    }
                 }
+                tmem_st16(t_row + s_col + c * 16, w);
             }
             tmem_wait_st();
-            const float sum = sum0 + sum1;
-            l = l * alpha + sum;
+            l = l * alpha + (sum0 + sum1);
             if (t > 0 && !__all_sync(0xffffffffu, alpha == 1.0f)) {
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < OW / 32; ++c) {
                     float ov[32];
                     tmem_ld32(t_row + o_col + c * 32, ov);
                     tmem_wait_ld();
@@ -955,11 +978,20 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
             }
             tc_fence_after();
         }
+        if constexpr (HS > 1) {
+            // The row's sum over the warps that share it.
+            xsum[x][h][r] = l;
+            named_barrier(1 + x, 128 * HS);
+            l = 0.0f;
+#pragma unroll
+            for (int o = 0; o < HS; ++o)
+                l += xsum[x][o][r];
+        }
         if (!failed) {
             const float inv = 1.0f / l;
-            unsigned short* go = reinterpret_cast<unsigned short*>(o) + b * n_q * D;
+            unsigned short* go = reinterpret_cast<unsigned short*>(o) + b * n_q * D + h * OW;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < OW / 32; ++c) {
                 float ov[32];
                 tmem_ld32(t_row + o_col + c * 32, ov);
                 tmem_wait_ld();
@@ -977,10 +1009,10 @@ attention_pp_kernel(const __grid_constant__ CUtensorMap map_q,
             }
             if (my_kt == 0 && qi < n_q) {                    // no key at all: NaN rows
                 const float nan = __int_as_float(0x7fc00000);
-                for (int d0 = 0; d0 < D; d0 += 2)
+                for (int d0 = 0; d0 < OW; d0 += 2)
                     *reinterpret_cast<uint32_t*>(go + qi * D + d0) = Elem<T>::pack2(nan, nan);
             }
-            if (lse && qi < n_q)
+            if (lse && qi < n_q && h == 0)
                 lse[b * n_q + qi] = l > 0.0f ? (m + __log2f(l)) * 0.69314718055994531f : kNegInf;
         }
     }
@@ -1051,7 +1083,7 @@ cudaError_t launch_pp(const AttentionProblem& p, cudaStream_t s)
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(n_qt * p.bh), 1, 1);
-    cfg.blockDim = dim3(kPpThreads, 1, 1);
+    cfg.blockDim = dim3(pp_threads<D>(), 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = s;
     cfg.attrs = attr;
