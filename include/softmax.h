@@ -347,7 +347,10 @@ typedef struct {
                             staged: chunks in the ring (ring depth) */
     int smem_bytes;      /* dynamic shared memory per CTA */
     int64_t grid;        /* CTAs launched; 0 = sized at launch from occupancy
-                            (whole waves of resident CTAs, persistent) */
+                            in waves of resident CTAs: CTA path up to ten
+                            (4-byte elements) or two (2-byte), at least 1.5
+                            rows per CTA; WARP path up to four; cluster and
+                            two-pass paths one persistent wave */
 } softmax_plan_t;
 
 /*

@@ -37,6 +37,7 @@ constexpr int kTileThreads = kTileWarps * 32;
 constexpr int kTileMaxStages = 8;
 constexpr int kTileMaxRows = 64;             // rows per tile: 4 warps x up to 16 rows
 constexpr int kTileRingAlign = 128;
+constexpr int64_t kTileGridWaves = 4;       // most waves of resident CTAs launched
 
 template <typename T, int VEC>
 __device__ __forceinline__ void lds_any(const T* p, float* v)
@@ -317,9 +318,17 @@ cudaError_t launch_tile_opts(const Problem& p, const softmax_plan_t& plan, cudaS
     int64_t grid = plan.grid;
     if (grid <= 0) {
         // Latency-bound (a warp reduces its rows one after another): every
-        // resident CTA is worth more than a fuller last round.
-        const int resident = resident_ctas(reinterpret_cast<const void*>(k), kTileThreads, smem);
-        grid = tiles < resident ? tiles : resident;
+        // resident CTA is worth more than a fuller last round.  Inputs of at
+        // least eight tiles per resident CTA launch four whole waves of CTAs:
+        // CTAs that finish early are replaced, so the last tiles spread over
+        // every SM.  Measured against one wave on GB300: 65536 x 1024 bf16
+        // 5690 -> 6360 GB/s, 131072 x 512 bf16 5485 -> 6030, 262144 x 256
+        // bf16 4100 -> 4700.  Smaller inputs keep one wave: 32768 x 1024
+        // causal bf16 (6.7 tiles per CTA) measured 5830 at one wave, 5690 at
+        // two and 5050 at 1.12 (a partial wave runs its full shares alone).
+        const int64_t resident = resident_ctas(reinterpret_cast<const void*>(k), kTileThreads, smem);
+        const int64_t waves = resident > 0 && tiles >= 8 * resident ? kTileGridWaves : 1;
+        grid = tiles < waves * resident ? tiles : waves * resident;
     }
     if (grid < 1)
         grid = 1;
