@@ -55,16 +55,29 @@ __host__ __device__ __forceinline__ uint64_t mulhi_u64(uint64_t a, uint64_t b)
 
 // Columns [0, valid) of `row` take part in its softmax: all of them, or with
 // the causal mask those c <= (row mod period) + offset.
+// row mod period: the row's position in the mask period.
+__host__ __device__ __forceinline__ uint64_t logits_period_pos(const LogitsArg& lg, int64_t row)
+{
+    const uint64_t n = static_cast<uint64_t>(row);
+    const uint64_t t = mulhi_u64(lg.mul, n);
+    const uint64_t q = (t + ((n - t) >> lg.sh1)) >> lg.sh2;
+    return n - q * static_cast<uint64_t>(lg.period);
+}
+
+// Kept columns of a causally masked row at position `pos` of the period.
+__host__ __device__ __forceinline__ int64_t logits_lim(const LogitsArg& lg, uint64_t pos,
+                                                       int64_t n_cols)
+{
+    const int64_t lim = static_cast<int64_t>(pos) + lg.offset + 1;
+    return lim < 0 ? 0 : (lim > n_cols ? n_cols : lim);
+}
+
 __host__ __device__ __forceinline__ int64_t logits_valid(const LogitsArg& lg, int64_t row,
                                                          int64_t n_cols)
 {
     if (!lg.causal)
         return n_cols;
-    const uint64_t n = static_cast<uint64_t>(row);
-    const uint64_t t = mulhi_u64(lg.mul, n);
-    const uint64_t q = (t + ((n - t) >> lg.sh1)) >> lg.sh2;
-    const int64_t lim = static_cast<int64_t>(n - q * static_cast<uint64_t>(lg.period)) + lg.offset + 1;
-    return lim < 0 ? 0 : (lim > n_cols ? n_cols : lim);
+    return logits_lim(lg, logits_period_pos(lg, row), n_cols);
 }
 
 // Kernels are compiled twice: OPTS = false for the plain softmax (scale 1, no

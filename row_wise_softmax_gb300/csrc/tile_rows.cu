@@ -96,9 +96,17 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
         issued[s] += 1;
         if constexpr (OPTS) {
             // One pass: each copy raises the phase's byte count before it
-            // starts; the single arrival comes after the last copy.
+            // starts; the single arrival comes after the last copy.  The
+            // tile's rows are consecutive: row r0's position in the mask
+            // period (one division), then one step per row.
+            uint64_t pos = lg.causal && nr > 0 ? logits_period_pos(lg, r0) : 0;
             for (int r = 0; r < nr; ++r) {
-                const int64_t lim = logits_valid(lg, r0 + r, n_cols);
+                int64_t lim = n_cols;
+                if (lg.causal) {
+                    lim = logits_lim(lg, pos, n_cols);
+                    if (++pos == static_cast<uint64_t>(lg.period))
+                        pos = 0;
+                }
                 row_keep[s][r] = static_cast<int>(lim);
                 const uint32_t n = copy_bytes(r0 + r, lim);
                 if (n) {
