@@ -63,9 +63,10 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ __align__(8) unsigned long long full[kTileMaxStages];
     __shared__ unsigned issued[kTileMaxStages];
-    // Options build: each row's kept columns, written by the issuing thread
-    // with the tile's copies (read after the stage's mbarrier completes).
-    __shared__ int row_keep[OPTS ? kTileMaxStages : 1][OPTS ? kTileMaxRows : 1];
+    // Options build: each row's kept and copied columns, written by the
+    // issuing thread with the tile's copies (read after the stage's mbarrier
+    // completes).
+    __shared__ int2 row_keep[OPTS ? kTileMaxStages : 1][OPTS ? kTileMaxRows : 1];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float kk = OPTS ? lg.k : kLog2e;       // exponent multiplier, scale * log2 e
@@ -107,8 +108,8 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
                     if (++pos == static_cast<uint64_t>(lg.period))
                         pos = 0;
                 }
-                row_keep[s][r] = static_cast<int>(lim);
                 const uint32_t n = copy_bytes(r0 + r, lim);
+                row_keep[s][r] = make_int2(static_cast<int>(lim), static_cast<int>(n / sizeof(T)));
                 if (n) {
                     mbar_expect_tx(bar, n);
                     bulk_g2s(smem_addr(row_ptr(s, r)), in + (r0 + r) * ld_in, n, bar);
@@ -166,12 +167,15 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
             // Columns [0, avail) are in shared memory, [avail, lim) is a
             // < 16-byte tail read from HBM, and from lim on the row is masked
             // or padding (-inf).
-            int lim;
-            if constexpr (OPTS)
-                lim = row_keep[s][r];
-            else
+            int lim, copied;
+            if constexpr (OPTS) {
+                const int2 kc = row_keep[s][r];          // kept and copied columns
+                lim = kc.x;
+                copied = kc.y;
+            } else {
                 lim = n_cols;
-            const int copied = static_cast<int>(copy_bytes(row, lim) / sizeof(T));
+                copied = static_cast<int>(copy_bytes(row, lim) / sizeof(T));
+            }
             const int avail = copied < lim ? copied : lim;
             // Whole vectors first: a vector that starts below `avail` is read
             // from shared memory (inside the row's ring slot), any other is
