@@ -156,3 +156,16 @@ def test_torch_binding_scale_and_causal():
     assert (y.double() - ref).abs().max().item() <= parity.F32_ABS_TOL
     with pytest.raises(rws.SoftmaxError):
         rws.softmax_rows(x, scale=-1.0)
+
+
+def test_mask_from_indices_on_a_multi_wave_tile_grid():
+    """65536 x 1024 bf16 (four waves of the staged tile kernel): the causal mask
+    from indices with a period of 1000 rows (tiles cross period boundaries) and
+    an offset that leaves the first rows of each period with no kept column."""
+    w = wl.random_rows(65536, 1024, dtype=wl.BF16, seed=21, scale=6.0)
+    opt = dict(scale=0.125, causal=True, causal_period=1000, causal_offset=-3)
+    got = run_ex(w, **opt)
+    zero = ~visible(w.n_rows, w.n_cols, **opt)
+    empty = zero.all(axis=1)                                            # rows keeping nothing
+    assert empty.sum() == 3 * 66
+    parity.compare(got, expected_ex(w, **opt), w.dtype, "mask from indices, four waves")

@@ -238,3 +238,29 @@ def test_plan_describe_matches_plan():
     with pytest.raises(rws.SoftmaxError):
         rws.plan_describe(4, 4, 9)
     assert rws.launch_count() == before
+
+
+# Shapes whose automatic grid is several waves of resident CTAs: the CTA path
+# (fp32 ten waves capped at 1.5 rows per CTA; 16-bit two waves) and the
+# staged tile kernel (four waves from eight tiles per resident CTA).  Every
+# row is compared with the oracle.
+MULTI_WAVE = [
+    (16384, 2048, wl.F32, rws.PATH_CTA),
+    (3000, 4100, wl.F32, rws.PATH_CTA),        # fewer rows than 1.5 per CTA of ten waves
+    (16384, 4096, wl.BF16, rws.PATH_CTA),
+    (65536, 1024, wl.BF16, rws.PATH_WARP),     # 16384 tiles of 4 rows
+    (262144, 256, wl.F16, rws.PATH_WARP),      # 16384 tiles of 16 rows
+]
+
+
+@pytest.mark.parametrize("n_rows,n_cols,dtype,path", MULTI_WAVE,
+                         ids=["cta_f32_ten_waves", "cta_f32_few_rows", "cta_bf16_two_waves",
+                              "tile_bf16_four_waves", "tile_f16_four_waves"])
+def test_multi_wave_grids(n_rows, n_cols, dtype, path):
+    w = wl.random_rows(n_rows, n_cols, dtype=dtype, seed=n_cols, scale=4.0)
+    p = rws.plan(w.n_rows, w.n_cols, dtype=dtype)
+    assert p.path == path and p.grid == 0 and p.bulk_copy == 1, str(p)
+    before = rws.launch_count()
+    got = run(w)
+    assert rws.launch_count() - before == 1
+    parity.compare(got, parity.expected(w), dtype, "%dx%d %s" % (n_rows, n_cols, str(p)))
