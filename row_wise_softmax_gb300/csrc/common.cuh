@@ -502,6 +502,16 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (no destination, no completion):
+// src 16-byte aligned, bytes a nonzero multiple of 16.  L2 is the point of
+// coherence for device memory, so lines prefetched before a preceding grid
+// has finished writing them are updated by those writes: a kernel may warm
+// L2 with its first inputs before griddepcontrol.wait.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
+}
+
 // The same copy with an L2 cache policy (createpolicy) for the source lines.
 __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes,
                                               uint32_t bar, uint64_t pol)

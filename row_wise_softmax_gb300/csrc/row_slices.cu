@@ -169,6 +169,21 @@ row_slices_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in
                 issued[s] = 0;
             }
             fence_mbar_init();
+            // The first rows' bytes into L2 while the preceding grid drains
+            // (a prefetch reads nothing into this CTA: the copies after
+            // griddepcontrol.wait see the preceding grid's writes).  Later
+            // waves prefetch too: their copies wait for the ring's set-up,
+            // the prefetch does not (measured +1% against the first wave
+            // alone on 4096x4096 fp32).
+            for (int s = 0; s < stages; ++s) {
+                const int64_t row = cluster_id + s * n_clusters;
+                if (row >= n_rows)
+                    break;
+                const uint32_t bytes = OPTS ? span_copy_bytes<T>(row_lim(row), n_cols - c0) : plain_bytes;
+                const char* src = reinterpret_cast<const char*>(in + row * ld_in + c0);
+                for (uint32_t off = 0; off < bytes; off += kBulkChunkBytes)
+                    bulk_prefetch_l2(src + off, bytes - off < kBulkChunkBytes ? bytes - off : kBulkChunkBytes);
+            }
         }
         if constexpr (!OPTS) {
             // Every row copies the same span: positions of the last vector

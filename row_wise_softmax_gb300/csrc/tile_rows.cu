@@ -57,7 +57,8 @@ __device__ __forceinline__ void lds_any(const T* p, float* v)
 template <typename T, int VEC, int CHUNKS, bool OPTS>
 __global__ void __launch_bounds__(kTileThreads, 8)
 tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
-                 int64_t ld_out, int rows_per_warp, int stages, int row_pad, LogitsArg lg)
+                 int64_t ld_out, int rows_per_warp, int stages, int row_pad, int64_t prefetch_ctas,
+                 LogitsArg lg)
 {
     constexpr int E = VEC * CHUNKS;
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -140,6 +141,30 @@ tile_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols, int64_t ld_in,
             issued[s] = 0;
         }
         fence_mbar_init();
+        // The first tiles' rows into L2 while the preceding grid drains (a
+        // prefetch reads nothing into this CTA: the copies after
+        // griddepcontrol.wait see the preceding grid's writes).  Only the
+        // CTAs that can be resident before the preceding grid ends (the
+        // first wave) do so; later waves copy at once.
+        for (int s = 0; s < stages && static_cast<int64_t>(blockIdx.x) < prefetch_ctas; ++s) {
+            const int64_t t = blockIdx.x + static_cast<int64_t>(s) * gridDim.x;
+            if (t >= n_tiles)
+                break;
+            const int64_t r0 = t * R;
+            const int nr = static_cast<int>(n_rows - r0 < R ? n_rows - r0 : R);
+            uint64_t pos = OPTS && lg.causal ? logits_period_pos(lg, r0) : 0;
+            for (int r = 0; r < nr; ++r) {
+                int64_t lim = n_cols;
+                if (OPTS && lg.causal) {
+                    lim = logits_lim(lg, pos, n_cols);
+                    if (++pos == static_cast<uint64_t>(lg.period))
+                        pos = 0;
+                }
+                const uint32_t n = copy_bytes(r0 + r, lim);
+                if (n)
+                    bulk_prefetch_l2(in + (r0 + r) * ld_in, n);
+            }
+        }
     }
     __syncthreads();
     pdl_wait();
@@ -328,6 +353,7 @@ cudaError_t launch_tile_opts(const Problem& p, const softmax_plan_t& plan, cudaS
     const int64_t R = int64_t{kTileWarps} * plan.rows_per_warp;
     const int64_t tiles = (p.n_rows + R - 1) / R;
     int64_t grid = plan.grid;
+    const int64_t resident = resident_ctas(reinterpret_cast<const void*>(k), kTileThreads, smem);
     if (grid <= 0) {
         // Latency-bound (a warp reduces its rows one after another): every
         // resident CTA is worth more than a fuller last round.  Inputs of at
@@ -338,7 +364,6 @@ cudaError_t launch_tile_opts(const Problem& p, const softmax_plan_t& plan, cudaS
         // bf16 4100 -> 4700.  Smaller inputs keep one wave: 32768 x 1024
         // causal bf16 (6.7 tiles per CTA) measured 5830 at one wave, 5690 at
         // two and 5050 at 1.12 (a partial wave runs its full shares alone).
-        const int64_t resident = resident_ctas(reinterpret_cast<const void*>(k), kTileThreads, smem);
         const int64_t waves = resident > 0 && tiles >= 8 * resident ? kTileGridWaves : 1;
         grid = tiles < waves * resident ? tiles : waves * resident;
     }
@@ -355,7 +380,7 @@ cudaError_t launch_tile_opts(const Problem& p, const softmax_plan_t& plan, cudaS
     cfg.numAttrs = static_cast<unsigned>(launch_attrs(attr, 1));
     err = cudaLaunchKernelEx(&cfg, k, static_cast<const T*>(p.in), static_cast<T*>(p.out),
                              p.n_rows, static_cast<int>(p.n_cols), p.ld_in, p.ld_out,
-                             plan.rows_per_warp, plan.stages, row_pad, logits_of(p));
+                             plan.rows_per_warp, plan.stages, row_pad, resident, logits_of(p));
     note_launch();
     return err;
 }

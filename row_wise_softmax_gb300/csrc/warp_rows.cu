@@ -82,7 +82,7 @@ __device__ __forceinline__ void softmax_group(T* out, int64_t g, int64_t n_rows,
 template <typename T, int VEC, int CHUNKS, int ROWS, bool OPTS>
 __global__ void __launch_bounds__(kWarpPathThreads)
 warp_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols,
-                 int64_t ld_in, int64_t ld_out, LogitsArg lg)
+                 int64_t ld_in, int64_t ld_out, int64_t prefetch_ctas, LogitsArg lg)
 {
     constexpr int E = VEC * CHUNKS;
     const int lane = threadIdx.x & 31;
@@ -90,6 +90,23 @@ warp_rows_kernel(const T* in, T* out, int64_t n_rows, int n_cols,
     const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int64_t n_groups = (n_rows + ROWS - 1) / ROWS;
     pdl_launch_dependents();
+    // CTAs of the first wave (resident before the preceding grid ends) bring
+    // their first group's rows into L2 while it drains: the loads after
+    // griddepcontrol.wait still see its writes (L2 is the point of
+    // coherence).  prefetch_ctas is 0 unless the rows are 16-byte aligned
+    // device memory.
+    if (lane == 0 && static_cast<int64_t>(blockIdx.x) < prefetch_ctas && warp0 < n_groups) {
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            const int64_t row = warp0 * ROWS + r;
+            if (row < n_rows) {
+                const uint32_t bytes =
+                    static_cast<uint32_t>(kept_cols<OPTS>(lg, row, n_cols) * sizeof(T)) & ~15u;
+                if (bytes)
+                    bulk_prefetch_l2(in + row * ld_in, bytes);
+            }
+        }
+    }
     pdl_wait();
     if (warp0 >= n_groups)
         return;
@@ -132,13 +149,16 @@ static cudaError_t launch_opts(const Problem& p, const softmax_plan_t& plan, cud
     const int warps_per_cta = kWarpPathThreads / 32;
     int64_t want = (groups + warps_per_cta - 1) / warps_per_cta;
     int64_t grid = plan.grid;
+    const int resident = resident_ctas(reinterpret_cast<const void*>(k), kWarpPathThreads, 0);
+    const size_t esz = p.dtype == SOFTMAX_F32 ? 4 : 2;
+    const bool aligned_device = !p.no_bulk && reinterpret_cast<uintptr_t>(p.in) % 16 == 0 &&
+                                (static_cast<size_t>(p.ld_in) * esz) % 16 == 0;
     if (grid <= 0) {
         // Four times the resident CTAs (at most one row group per warp): CTAs
         // that finish early are replaced by fresh ones whose loads start at
         // once, so the last rows are spread over every SM.  Measured on
         // GB300 against one resident wave: 262144 x 127 fp32 5935 -> 6547,
         // 65536 x 512 5941 -> 6717, 32768 x 1000 5902 -> 6697 GB/s.
-        const int resident = resident_ctas(reinterpret_cast<const void*>(k), kWarpPathThreads, 0);
         const int64_t cap = int64_t{kWarpGridWaves} * resident;
         grid = want < cap ? want : cap;
     }
@@ -154,6 +174,7 @@ static cudaError_t launch_opts(const Problem& p, const softmax_plan_t& plan, cud
     const cudaError_t err = cudaLaunchKernelEx(&cfg, k, static_cast<const T*>(p.in),
                                                static_cast<T*>(p.out), p.n_rows,
                                                static_cast<int>(p.n_cols), p.ld_in, p.ld_out,
+                                               aligned_device ? int64_t{resident} : int64_t{0},
                                                logits_of(p));
     note_launch();
     return err;
