@@ -26,16 +26,34 @@ namespace {
 constexpr int kBwdWarpThreads = 128;
 constexpr int kBwdGridWaves = 2;
 
+// The first row's y and dy (its first n elements) into L2 while the
+// preceding grid drains: CTAs of the first wave, resident before it ends,
+// call this before griddepcontrol.wait; the loads after the wait still see
+// the preceding grid's writes (L2 is the point of coherence).  Rows 16-byte
+// aligned in device memory.
+template <typename T>
+__device__ __forceinline__ void prefetch_row_pair(const T* y, const T* dy, int64_t n)
+{
+    const int64_t bytes = (n * static_cast<int64_t>(sizeof(T))) & ~int64_t{15};
+    for (int64_t off = 0; off < bytes; off += 32768) {
+        const uint32_t b = static_cast<uint32_t>(bytes - off < 32768 ? bytes - off : 32768);
+        bulk_prefetch_l2(reinterpret_cast<const char*>(y) + off, b);
+        bulk_prefetch_l2(reinterpret_cast<const char*>(dy) + off, b);
+    }
+}
+
 template <typename T, int VEC, int CHUNKS>
 __global__ void __launch_bounds__(kBwdWarpThreads)
 backward_warp_kernel(const T* y, const T* dy, T* dx, int64_t n_rows, int n_cols, int64_t ld_y,
-                     int64_t ld_dy, int64_t ld_dx)
+                     int64_t ld_dy, int64_t ld_dx, int64_t prefetch_ctas)
 {
     constexpr int E = VEC * CHUNKS;
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     pdl_launch_dependents();
+    if (lane == 0 && static_cast<int64_t>(blockIdx.x) < prefetch_ctas && warp0 < n_rows)
+        prefetch_row_pair(y + warp0 * ld_y, dy + warp0 * ld_dy, n_cols);
     pdl_wait();
     for (int64_t row = warp0; row < n_rows; row += n_warps) {
         float a[E], g[E];
@@ -85,13 +103,16 @@ __device__ __forceinline__ float cta_sum(float v, float* red)
 template <typename T, int THREADS, int VEC, int NV>
 __global__ void __launch_bounds__(THREADS)
 backward_cta_kernel(const T* y, const T* dy, T* dx, int64_t n_rows, int64_t n_cols, int64_t ld_y,
-                    int64_t ld_dy, int64_t ld_dx)
+                    int64_t ld_dy, int64_t ld_dx, int64_t prefetch_ctas)
 {
     constexpr int E = NV * VEC;
     constexpr int64_t SPAN = int64_t{THREADS} * E;      // columns held in registers
     __shared__ float red[THREADS / 32];
     const int tid = threadIdx.x;
     pdl_launch_dependents();
+    if (tid == 0 && static_cast<int64_t>(blockIdx.x) < prefetch_ctas && blockIdx.x < n_rows)
+        prefetch_row_pair(y + blockIdx.x * ld_y, dy + blockIdx.x * ld_dy,
+                          n_cols < SPAN ? n_cols : SPAN);
     pdl_wait();
     for (int64_t row = blockIdx.x; row < n_rows; row += gridDim.x) {
         const T* yr = y + row * ld_y;
@@ -155,9 +176,10 @@ backward_cta_kernel(const T* y, const T* dy, T* dx, int64_t n_rows, int64_t n_co
 // 4096 fp32 5499 -> 5674 GB/s, 32768 x 1024 bf16 5450 -> 5593 (one to six
 // waves tried).
 template <typename K>
-int64_t persistent_grid(K* k, int threads, int64_t units, int waves)
+int64_t persistent_grid(K* k, int threads, int64_t units, int waves, int64_t* resident_out)
 {
     const int resident = resident_ctas(reinterpret_cast<const void*>(k), threads, 0);
+    *resident_out = resident;
     const int64_t cap = static_cast<int64_t>(waves) * resident;
     int64_t g = units < cap ? units : cap;
     return g < 1 ? 1 : g;
@@ -186,11 +208,14 @@ cudaError_t launch_warp(const BackwardProblem& p, cudaStream_t s)
     const int64_t chunks = (p.n_cols + per_chunk - 1) / per_chunk;
     const int64_t rows_per_cta = kBwdWarpThreads / 32;
     auto go = [&](auto* k) {
-        return launch_pdl(k, persistent_grid(k, kBwdWarpThreads, (p.n_rows + rows_per_cta - 1) /
-                                                                     rows_per_cta, kBwdGridWaves),
-                          kBwdWarpThreads, s, static_cast<const T*>(p.y),
+        int64_t resident = 0;
+        const int64_t grid = persistent_grid(k, kBwdWarpThreads, (p.n_rows + rows_per_cta - 1) /
+                                                                     rows_per_cta, kBwdGridWaves,
+                                             &resident);
+        return launch_pdl(k, grid, kBwdWarpThreads, s, static_cast<const T*>(p.y),
                           static_cast<const T*>(p.dy), static_cast<T*>(p.dx), p.n_rows,
-                          static_cast<int>(p.n_cols), p.ld_y, p.ld_dy, p.ld_dx);
+                          static_cast<int>(p.n_cols), p.ld_y, p.ld_dy, p.ld_dx,
+                          VEC > 1 ? resident : int64_t{0});
     };
     if (chunks <= 1) return go(backward_warp_kernel<T, VEC, 1>);
     if (chunks <= 2) return go(backward_warp_kernel<T, VEC, 2>);
@@ -212,9 +237,11 @@ cudaError_t launch_cta(const BackwardProblem& p, cudaStream_t s)
     constexpr int THREADS = 512;
     constexpr int NV = 16 / VEC > 8 ? 8 : 16 / VEC;           // up to 16 elements a thread
     auto* k = backward_cta_kernel<T, THREADS, VEC, NV>;
-    return launch_pdl(k, persistent_grid(k, THREADS, p.n_rows, kBwdGridWaves), THREADS, s,
-                      static_cast<const T*>(p.y), static_cast<const T*>(p.dy),
-                      static_cast<T*>(p.dx), p.n_rows, p.n_cols, p.ld_y, p.ld_dy, p.ld_dx);
+    int64_t resident = 0;
+    const int64_t grid = persistent_grid(k, THREADS, p.n_rows, kBwdGridWaves, &resident);
+    return launch_pdl(k, grid, THREADS, s, static_cast<const T*>(p.y),
+                      static_cast<const T*>(p.dy), static_cast<T*>(p.dx), p.n_rows, p.n_cols,
+                      p.ld_y, p.ld_dy, p.ld_dx, VEC > 1 ? resident : int64_t{0});
 }
 
 template <typename T>

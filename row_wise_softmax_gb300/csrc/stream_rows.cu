@@ -123,6 +123,16 @@ stream_rows_kernel(const T* in, T* out, int64_t n_rows, int64_t n_cols, int64_t 
         mbar_init(smem_addr(&xbar[1]), static_cast<uint32_t>(cs));
         s_failed = 0;
         fence_mbar_init();
+        // The first row's first chunks into L2 while the preceding grid
+        // drains (the grid is one resident wave; the copies after
+        // griddepcontrol.wait still see the preceding grid's writes, L2
+        // being the point of coherence).
+        if (cluster_id < n_rows)
+            for (int64_t chunk = 0; chunk < K && chunk < stages; ++chunk) {
+                const uint32_t bytes = copy_bytes(cluster_id, chunk);
+                if (bytes)
+                    bulk_prefetch_l2(in + cluster_id * ld_in + c0 + chunk * CHUNK, bytes);
+            }
     }
     // Peers arrive on this CTA's exchange mbarriers: they must be initialised
     // cluster-wide first.
