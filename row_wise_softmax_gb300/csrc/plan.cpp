@@ -49,6 +49,15 @@ constexpr int kStreamVectors = 4;
 constexpr int kStreamStagesOneCta = 6;       // 192 KB: one CTA per SM
 constexpr int kStreamStagesTwoCtas = 3;      // 96 KB: two CTAs per SM
 constexpr int kStreamStagesLongSlice = 4;    // fp32 slices beyond 256 KB
+// A row under 96 KB on one CTA: 256 threads x 4 vectors (16 KB chunks), six
+// stages (96 KB: two CTAs per SM, launched as two waves).  Measured on GB300
+// against 32 KB chunks and one CTA per SM: 2730 x 12288 fp32 4832 -> 6576
+// GB/s, 3947 x 8500 fp32 3440 -> 4861, 4096 x 32768 bf16 5512 -> 5863, 2048
+// x 32768 bf16 5141 -> 5301 (4096 x 16384 fp32 6778 -> 6479); 96 KB rows and
+// longer keep 32 KB chunks (1365 x 24576 fp32: 6626 against 5909).
+constexpr int64_t kStreamShortSliceBytes = 96 * 1024;
+constexpr int kStreamThreadsShort = 256;
+constexpr int kStreamStagesShort = 6;
 constexpr int64_t kStreamMaxClusterAuto = 4;
 constexpr int64_t kTwoPassMaxCluster = 8;
 constexpr int64_t kTwoPassMinSliceBytes = 64 * 1024;     // when clusters grow for few rows
@@ -307,7 +316,8 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
     case SOFTMAX_PATH_TWOPASS: {
         // Staged: 512 consumer threads stream 32 KB chunks; slices of about
         // 256 KB (fp32) or 1 MB (16-bit) on clusters of up to 4 CTAs, with a
-        // 192 KB ring when one CTA holds the SM and 96-128 KB for two.  The
+        // 192 KB ring when one CTA holds the SM and 96-128 KB for two; rows
+        // under 96 KB on one CTA stream 16 KB chunks, two CTAs per SM.  The
         // register kernel (unaligned input): about 256 KB and at least two
         // CTAs.  A single CTA when forced on short rows.
         const int64_t per_cta = in_al ? (esz == 4 ? kStreamSliceBytesF32 : kStreamSliceBytes16)
@@ -332,10 +342,12 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
             q.bulk_copy = 1;
             q.vec = vmax;
             q.out_vec = out_al ? vmax : 1;
-            q.threads = kStreamThreads;
-            q.chunks = kStreamVectors;
             const int64_t slice_bytes = q.slice_cols * esz;
-            int stages = (esz != 4 || cs == 1) ? kStreamStagesOneCta
+            const bool short_slice = cs == 1 && slice_bytes < kStreamShortSliceBytes;
+            q.threads = short_slice ? kStreamThreadsShort : kStreamThreads;
+            q.chunks = kStreamVectors;
+            int stages = short_slice ? kStreamStagesShort
+                         : (esz != 4 || cs == 1) ? kStreamStagesOneCta
                          : (slice_bytes > kStreamSliceBytesF32 ? kStreamStagesLongSlice
                                                                : kStreamStagesTwoCtas);
             const int64_t chunk_bytes = int64_t{q.threads} * q.chunks * 16;

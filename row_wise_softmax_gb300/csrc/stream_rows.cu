@@ -418,7 +418,16 @@ cudaError_t launch_stream_opts(const Problem& p, const softmax_plan_t& plan, cud
         }
         if (active < 1)
             active = 1;
-        clusters = balanced_grid(p.n_rows, active, cs == 1 ? sm_count_current() : 0);
+        const int sms = sm_count_current();
+        if (cs == 1 && sms > 0 && active >= 2 * sms) {
+            // Two or more CTAs share an SM: two waves, so that SMs whose
+            // rows finish first take the remaining ones (a balanced single
+            // wave can leave some SMs one CTA short: 4096 x 16384 fp32 on
+            // 16 KB chunks 5091 GB/s, 6479 as two waves).
+            clusters = p.n_rows < 2 * int64_t{active} ? p.n_rows : 2 * int64_t{active};
+        } else {
+            clusters = balanced_grid(p.n_rows, active, cs == 1 ? sms : 0);
+        }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * cs), 1, 1);

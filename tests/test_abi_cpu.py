@@ -65,6 +65,13 @@ def test_scheduler_paths_for_the_five_workloads(lib):
     assert (p.vec, p.out_vec, p.bulk_copy, p.chunks, p.stages, p.smem_bytes) == (4, 4, 1, 4, 3, 98304)
     p = plan(1024, 65536)                                 # one CTA per row: a 192 KB ring
     assert (p.cluster, p.stages, p.smem_bytes) == (1, 6, 196608)
+    p = plan(2730, 12288)                                 # 48 KB rows: 16 KB chunks, 2 CTAs/SM
+    assert (p.path, p.cluster, p.threads, p.chunks, p.stages, p.smem_bytes) == (
+        rws.PATH_TWOPASS, 1, 256, 4, 6, 98304)
+    p = plan(1365, 24576)                                 # 96 KB rows keep 32 KB chunks
+    assert (p.path, p.cluster, p.threads, p.stages) == (rws.PATH_TWOPASS, 1, 512, 6)
+    p = plan(2048, 65536, dtype=rws.BF16)
+    assert (p.path, p.cluster, p.threads, p.stages) == (rws.PATH_TWOPASS, 1, 512, 6)
     p = plan(256, 262144, dtype=rws.BF16)                 # 16-bit: slices up to 1 MB
     assert (p.path, p.cluster, p.threads, p.chunks, p.stages) == (rws.PATH_TWOPASS, 1, 512, 4, 6)
     p = plan(256, 262144, in_ptr=(1 << 20) + 4)           # unaligned: register two-pass
