@@ -517,6 +517,7 @@ template <typename T>
 cudaError_t launch_threads(const Problem& p, const softmax_plan_t& plan, cudaStream_t s)
 {
     switch (plan.threads) {
+    case 64: return launch_nv<T, 64>(p, plan, s);
     case 128: return launch_nv<T, 128>(p, plan, s);
     case 256: return launch_nv<T, 256>(p, plan, s);
     case 512: return launch_nv<T, 512>(p, plan, s);
