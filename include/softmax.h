@@ -351,6 +351,10 @@ typedef struct {
                             (4-byte elements) or two (2-byte), at least 1.5
                             rows per CTA; WARP path up to four; cluster and
                             two-pass paths one persistent wave */
+    int lanes_per_row;   /* WARP path, rows in registers (bulk_copy 0): lanes
+                            that share one row, a power of two; below 32 a
+                            warp holds 32 / lanes_per_row rows side by side
+                            (short rows, chunks 1).  0 is read as 32. */
 } softmax_plan_t;
 
 /*

@@ -73,7 +73,7 @@ class Plan(ctypes.Structure):
                 ("rows_per_warp", ctypes.c_int), ("chunks", ctypes.c_int),
                 ("slice_cols", ctypes.c_int64), ("stages", ctypes.c_int),
                 ("smem_bytes", ctypes.c_int),
-                ("grid", ctypes.c_int64)]
+                ("grid", ctypes.c_int64), ("lanes_per_row", ctypes.c_int)]
 
     def __str__(self) -> str:
         buf = ctypes.create_string_buffer(256)

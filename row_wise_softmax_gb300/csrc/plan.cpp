@@ -95,6 +95,10 @@ bool aligned16(const void* ptr, int64_t n_rows, int64_t ld, int esz)
     return (a % 16 == 0) && (n_rows <= 1 || (ld * esz) % 16 == 0);
 }
 
+// Rows a lane holds at once in the sub-warp kernel, one vector each (must
+// match warp_rows.cu).
+int sub_rows_for(int vec) { return vec >= 8 ? 4 : (vec == 4 ? 8 : 16); }
+
 // Rows held in flight per warp on the WARP path (must match warp_rows.cu).
 int warp_rows_for(int e)
 {
@@ -258,7 +262,13 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
         q.grid = 0;
         // 16-bit rows go through the staged tile kernel; fp32 rows measured
         // faster in the register kernel (its loads are all in flight at once).
-        if (in_al && (p.dtype != SOFTMAX_F32 || !automatic)) {
+        // 16-bit rows of at most 16 vectors take the register kernel too,
+        // several rows to a warp (on GB300: 64 bf16 columns 1565 -> 3778
+        // GB/s, 128 columns 2924 -> 3676; from 200 columns the tile kernel
+        // is faster).
+        const bool short16 = p.dtype != SOFTMAX_F32 && automatic && in_vec && out_al &&
+                             p.n_cols <= 16 * vmax;
+        if (in_al && (p.dtype != SOFTMAX_F32 || !automatic) && !short16) {
             // Staged tile kernel: stages of 4 * rows_per_warp rows of
             // row_pad elements (about 16 KB), about 64 KB of ring per CTA.
             const int64_t row_pad = round_up(p.n_cols, vmax);
@@ -275,6 +285,7 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
             q.out_vec = q.vec;
             q.chunks = static_cast<int>(pow2_ceil(ceil_div(p.n_cols, 32 * q.vec)));
             q.rows_per_warp = static_cast<int>(rpw);
+            q.lanes_per_row = 32;
             q.slice_cols = row_pad;
             q.stages = static_cast<int>(stages);
             q.smem_bytes = static_cast<int>(stages * stage_bytes);
@@ -283,6 +294,16 @@ int make_plan(const softmax_device_desc_t& dev, const Problem& p, int path, soft
             q.out_vec = q.vec;
             q.chunks = static_cast<int>(pow2_ceil(ceil_div(p.n_cols, 32 * q.vec)));
             q.rows_per_warp = warp_rows_for(q.vec * q.chunks);
+            q.lanes_per_row = 32;
+            if (q.chunks == 1) {
+                // Rows of at most 16 vectors: several rows side by side in a
+                // warp, each on the smallest power-of-two group of lanes.
+                const int64_t lanes = pow2_ceil(ceil_div(p.n_cols, q.vec));
+                if (lanes < 32) {
+                    q.lanes_per_row = static_cast<int>(lanes);
+                    q.rows_per_warp = (32 / q.lanes_per_row) * sub_rows_for(q.vec);
+                }
+            }
             q.slice_cols = p.n_cols;
         }
         break;
@@ -398,6 +419,10 @@ int check_plan(const softmax_device_desc_t& dev, const Problem& p, const softmax
             return SOFTMAX_ERR_INVALID_ARG;
         if (!pow2_in(q.chunks, 1, 32) || q.vec * q.chunks > 32 ||
             int64_t{32} * q.vec * q.chunks < p.n_cols)
+            return SOFTMAX_ERR_INVALID_ARG;
+        const int lanes = q.lanes_per_row ? q.lanes_per_row : 32;
+        if (!pow2_in(lanes, 1, 32) ||
+            (lanes < 32 && (q.bulk_copy != 0 || q.chunks != 1 || int64_t{lanes} * q.vec < p.n_cols)))
             return SOFTMAX_ERR_INVALID_ARG;
         if (q.bulk_copy == 0)
             return vec_ok(q.vec, in_vec && out_al) ? SOFTMAX_OK : SOFTMAX_ERR_INVALID_ARG;

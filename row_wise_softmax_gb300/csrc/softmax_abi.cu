@@ -216,13 +216,15 @@ int softmax_plan_format(const softmax_plan_t* plan, char* buf, size_t len)
     const char* name = (plan->path >= 0 && plan->path <= 3) ? names[plan->path] : "?";
     return std::snprintf(buf, len,
                          "path=%s dtype=%s vec=%d out_vec=%d bulk=%d threads=%d cluster=%d "
-                         "rows_per_warp=%d chunks=%d slice_cols=%lld stages=%d smem=%d grid=%lld",
+                         "rows_per_warp=%d chunks=%d slice_cols=%lld stages=%d smem=%d grid=%lld "
+                         "lanes_per_row=%d",
                          name, plan->dtype == SOFTMAX_F32 ? "f32" : plan->dtype == SOFTMAX_BF16 ? "bf16" : "f16",
                          plan->vec,
                          plan->out_vec, plan->bulk_copy, plan->threads, plan->cluster,
                          plan->rows_per_warp, plan->chunks,
                          static_cast<long long>(plan->slice_cols), plan->stages, plan->smem_bytes,
-                         static_cast<long long>(plan->grid));
+                         static_cast<long long>(plan->grid),
+                         plan->lanes_per_row > 0 ? plan->lanes_per_row : 32);
 }
 
 int softmax_plan_describe(int64_t n_rows, int64_t n_cols, int dtype, char* buf, size_t len)

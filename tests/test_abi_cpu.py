@@ -58,6 +58,12 @@ def test_scheduler_paths_for_the_five_workloads(lib):
     p = plan(32768, 1024, dtype=rws.BF16)                 # bf16 short rows: staged tiles
     assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 1, 8, 4, 1)
     assert (p.stages, p.smem_bytes) == (2, 16384)
+    p = plan(1 << 20, 16)                                 # short rows: 4 lanes a row
+    assert (p.path, p.bulk_copy, p.vec, p.chunks, p.lanes_per_row) == (rws.PATH_WARP, 0, 4, 1, 4)
+    p = plan(1 << 20, 64, dtype=rws.BF16)                 # 16-bit too, up to 128 columns
+    assert (p.path, p.bulk_copy, p.vec, p.chunks, p.lanes_per_row) == (rws.PATH_WARP, 0, 8, 1, 8)
+    p = plan(1 << 20, 200, dtype=rws.BF16)                # longer: the staged tile kernel
+    assert (p.path, p.bulk_copy, p.lanes_per_row) == (rws.PATH_WARP, 1, 32)
     p = plan(262144, 127, in_row_stride=128, out_row_stride=127)
     assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 0, 1, 4, 4)
     p = plan(256, 262144)                                 # staged two-pass, 32 KB chunks

@@ -264,3 +264,49 @@ def test_multi_wave_grids(n_rows, n_cols, dtype, path):
     got = run(w)
     assert rws.launch_count() - before == 1
     parity.compare(got, parity.expected(w), dtype, "%dx%d %s" % (n_rows, n_cols, str(p)))
+
+
+# Short rows shared by fewer than 32 lanes, several rows to a warp: every
+# group size, ragged row counts (a partly filled last group), degenerate rows,
+# and the options build (scale and causal mask from indices).
+SUB_WARP = [(1, wl.F32), (3, wl.F32), (8, wl.F32), (16, wl.F32), (60, wl.F32), (64, wl.F32),
+            (8, wl.BF16), (24, wl.BF16), (64, wl.BF16), (128, wl.BF16), (16, wl.F16), (96, wl.F16)]
+
+
+@pytest.mark.parametrize("n_cols,dtype", SUB_WARP, ids=lambda v: str(v))
+def test_sub_warp_rows(n_cols, dtype):
+    n_rows = 4099
+    w = wl.random_rows(n_rows, n_cols, dtype=dtype, seed=n_cols + 40, scale=5.0)
+    p = rws.plan(w.n_rows, w.n_cols, dtype=dtype)
+    assert p.path == rws.PATH_WARP and p.bulk_copy == 0 and p.lanes_per_row < 32, str(p)
+    got = run(w)
+    parity.compare(got, parity.expected(w), dtype, "sub-warp %s" % str(p))
+    # Degenerate rows: all -inf (NaN row), a NaN, a lone finite value.
+    data = w.data.copy()
+    neg = 0xFF80 if dtype == wl.BF16 else (0xFC00 if dtype == wl.F16 else None)
+    nan = 0x7FC0 if dtype == wl.BF16 else (0x7E00 if dtype == wl.F16 else None)
+    rows = data.reshape(n_rows, n_cols)
+    if dtype == wl.F32:
+        rows[5, :] = -np.inf
+        rows[6, 0] = np.nan
+        rows[7, :] = -np.inf
+        rows[7, n_cols // 2] = 1.0
+    else:
+        rows[5, :] = neg
+        rows[6, 0] = nan
+        rows[7, :] = neg
+        rows[7, n_cols // 2] = 0x3F80 if dtype == wl.BF16 else 0x3C00
+    wd = wl.Workload("degenerate", n_rows, n_cols, n_cols, n_cols, dtype, data, 0)
+    got = run(wd)
+    parity.compare(got, parity.expected(wd), dtype, "sub-warp degenerate")
+    # The options build: scale 1/4 and a causal mask from indices.
+    import oracle
+    opt = dict(scale=0.25, causal=True, causal_period=97, causal_offset=n_cols // 3)
+    x = parity.device_input(w)
+    y = parity.empty_output(w)
+    st = rws.softmax_rows_ex_ptr(x.data_ptr(), y.data_ptr(), w.n_rows, w.n_cols, w.in_row_stride,
+                                 w.out_row_stride, w.dtype, **opt)
+    assert st == rws.OK, rws.status_string(st)
+    torch.cuda.synchronize()
+    want = oracle.softmax_rows(w.data, w.n_rows, w.n_cols, w.in_row_stride, w.dtype, **opt)
+    parity.compare(parity.host_output(y, w), want, dtype, "sub-warp options")
