@@ -349,8 +349,9 @@ typedef struct {
     int64_t grid;        /* CTAs launched; 0 = sized at launch from occupancy
                             in waves of resident CTAs: CTA path up to ten
                             (4-byte elements) or two (2-byte), at least 1.5
-                            rows per CTA; WARP path up to four; cluster and
-                            two-pass paths one persistent wave */
+                            rows per CTA; WARP path up to four; cluster
+                            path one persistent wave; two-pass path one,
+                            or two when two CTAs of one row share an SM */
     int lanes_per_row;   /* WARP path, rows in registers (bulk_copy 0): lanes
                             that share one row, a power of two; below 32 a
                             warp holds 32 / lanes_per_row rows side by side
