@@ -351,7 +351,8 @@ typedef struct {
                             (4-byte elements) or two (2-byte), at least 1.5
                             rows per CTA; WARP path up to four; cluster
                             path one persistent wave; two-pass path one,
-                            or two when two CTAs of one row share an SM */
+                            or two when each CTA owns whole rows and two
+                            CTAs fit on an SM */
     int lanes_per_row;   /* WARP path, rows in registers (bulk_copy 0): lanes
                             that share one row, a power of two; below 32 a
                             warp holds 32 / lanes_per_row rows side by side
