@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define SOFTMAX_ABI_VERSION 1
+#define SOFTMAX_ABI_VERSION 2
 
 typedef enum {
     SOFTMAX_F32 = 0,
@@ -369,6 +369,19 @@ typedef struct {
 int softmax_plan(const softmax_device_desc_t* dev, const void* in, const void* out,
                  int64_t n_rows, int64_t n_cols, int64_t in_row_stride,
                  int64_t out_row_stride, int dtype, int path, softmax_plan_t* plan);
+
+/*
+ * softmax_plan_check: the checks softmax_rows_planned applies to *plan before
+ * it launches, without launching: SOFTMAX_OK when the plan describes this
+ * problem and fits the device, else the code softmax_rows_planned would
+ * return (SOFTMAX_ERR_INVALID_ARG for a plan that could read or write outside
+ * the rows).  dev == NULL checks against the current CUDA device (needs a
+ * GPU); a non-NULL dev makes this a pure host computation.  Pointers are
+ * only inspected for alignment and overlap.
+ */
+int softmax_plan_check(const softmax_device_desc_t* dev, const void* in, const void* out,
+                       int64_t n_rows, int64_t n_cols, int64_t in_row_stride,
+                       int64_t out_row_stride, int dtype, const softmax_plan_t* plan);
 
 /*
  * softmax_rows_planned: launch with an explicit scheduler decision (tuning

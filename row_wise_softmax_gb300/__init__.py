@@ -140,6 +140,9 @@ def lib() -> ctypes.CDLL:
         L.softmax_plan_format.restype = ci
         L.softmax_plan_describe.argtypes = [i64, i64, ci, ctypes.c_char_p, ctypes.c_size_t]
         L.softmax_plan_describe.restype = ci
+        L.softmax_plan_check.argtypes = [ctypes.POINTER(DeviceDesc), vp, vp, i64, i64, i64, i64, ci,
+                                         ctypes.POINTER(Plan)]
+        L.softmax_plan_check.restype = ci
         L.softmax_device_status.argtypes = [ci]
         L.softmax_device_status.restype = ci
         L.softmax_selftest_wait_timeout.argtypes = [vp]
@@ -438,6 +441,23 @@ def plan_for_device(desc: dict | DeviceDesc | None, n_rows: int, n_cols: int,
     if st != OK:
         raise SoftmaxError(st, "softmax_plan")
     return p
+
+
+def plan_check(desc: dict | DeviceDesc | None, plan_: Plan, n_rows: int, n_cols: int,
+               in_row_stride: int | None = None, out_row_stride: int | None = None,
+               dtype: int = F32, in_ptr: int = 1 << 20, out_ptr: int = 1 << 30) -> int:
+    """softmax_plan_check: the status softmax_rows_planned would give this plan
+    before launching (desc=None: the current GPU; a dict or DeviceDesc: host only)."""
+    if in_row_stride is None:
+        in_row_stride = n_cols
+    if out_row_stride is None:
+        out_row_stride = n_cols
+    dp = None
+    if desc is not None:
+        d = desc if isinstance(desc, DeviceDesc) else DeviceDesc(**desc)
+        dp = ctypes.byref(d)
+    return lib().softmax_plan_check(dp, in_ptr, out_ptr, n_rows, n_cols, in_row_stride,
+                                    out_row_stride, dtype, ctypes.byref(plan_))
 
 
 def plan(n_rows: int, n_cols: int, **kw) -> Plan:

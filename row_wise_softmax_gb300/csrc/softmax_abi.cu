@@ -254,6 +254,30 @@ int softmax_rows_path(const void* in, void* out, int64_t n_rows, int64_t n_cols,
                            nullptr, path, stream);
 }
 
+int softmax_plan_check(const softmax_device_desc_t* dev, const void* in, const void* out,
+                       int64_t n_rows, int64_t n_cols, int64_t in_row_stride,
+                       int64_t out_row_stride, int dtype, const softmax_plan_t* plan)
+{
+    if (!plan)
+        return SOFTMAX_ERR_INVALID_ARG;
+    const int st = rwsm::validate(in, out, n_rows, n_cols, in_row_stride, out_row_stride, dtype);
+    if (st != SOFTMAX_OK)
+        return st;
+    if (n_rows == 0 || n_cols == 0)
+        return SOFTMAX_OK;
+    softmax_device_desc_t d;
+    if (dev) {
+        d = *dev;
+    } else {
+        const int ds = rwsm::current_device(&d);
+        if (ds != SOFTMAX_OK)
+            return ds;
+    }
+    const Problem p{in, const_cast<void*>(out), n_rows, n_cols, in_row_stride, out_row_stride,
+                    dtype};
+    return rwsm::check_plan(d, p, *plan);
+}
+
 int softmax_rows_planned(const void* in, void* out, int64_t n_rows, int64_t n_cols,
                          int64_t in_row_stride, int64_t out_row_stride, int dtype,
                          const softmax_plan_t* plan, void* stream)

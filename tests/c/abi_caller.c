@@ -50,6 +50,18 @@ int main(void)
     CHECK(softmax_plan(&gb300, (void*)0x10000, (void*)0x20000000, 256, 262144, 262144, 262144,
                        SOFTMAX_F32, SOFTMAX_PATH_AUTO, &plan) == SOFTMAX_OK);
     CHECK(plan.path == SOFTMAX_PATH_TWOPASS && plan.cluster == 4 && plan.stages == 3);
+    /* softmax_plan_check: the scheduler's plan passes; one that no longer
+     * covers the row is refused. */
+    CHECK(softmax_plan_check(&gb300, (void*)0x10000, (void*)0x20000000, 256, 262144, 262144,
+                             262144, SOFTMAX_F32, &plan) == SOFTMAX_OK);
+    plan.slice_cols /= 2;
+    CHECK(softmax_plan_check(&gb300, (void*)0x10000, (void*)0x20000000, 256, 262144, 262144,
+                             262144, SOFTMAX_F32, &plan) == SOFTMAX_ERR_INVALID_ARG);
+    CHECK(softmax_plan_check(&gb300, (void*)0x10000, (void*)0x20000000, 256, 262144, 262144,
+                             262144, SOFTMAX_F32, NULL) == SOFTMAX_ERR_INVALID_ARG);
+    CHECK(softmax_plan(&gb300, (void*)0x10000, (void*)0x20000000, 1 << 20, 16, 16, 16,
+                       SOFTMAX_F32, SOFTMAX_PATH_AUTO, &plan) == SOFTMAX_OK);
+    CHECK(plan.path == SOFTMAX_PATH_WARP && plan.lanes_per_row == 4);
     /* softmax_plan_describe: the same decision on the current device (none
      * here: UNSUPPORTED, never a made-up plan); its arguments are checked
      * first. */

@@ -42,7 +42,7 @@ def test_status_strings(lib):
     assert rws.status_string(rws.OK) == "ok"
     for s in (rws.ERR_INVALID_ARG, rws.ERR_UNSUPPORTED, rws.ERR_CUDA, rws.ERR_DEVICE_TIMEOUT, 99):
         assert isinstance(rws.status_string(s), str) and rws.status_string(s)
-    assert rws.abi_version() == 1
+    assert rws.abi_version() == 2
 
 
 def plan(n_rows, n_cols, **kw):
@@ -317,3 +317,46 @@ def test_strided_and_backward_without_a_device(lib):
     assert rws.softmax_strided_ptr(A, B, 32, 64, 1, 32, 1, 32, rws.F32) == rws.ERR_UNSUPPORTED
     assert rws.softmax_backward_rows_ptr(A, B, C, 8, 100, 100, 100, 100,
                                          rws.F32) == rws.ERR_UNSUPPORTED
+
+
+def test_every_scheduled_plan_passes_its_own_check(lib):
+    """Host-only: across row lengths, row counts, dtypes, strides and
+    alignments, every plan the scheduler makes passes softmax_plan_check, and
+    the same plan with its coverage shrunk (fewer vectors, fewer lanes per
+    row, a narrower slice) is rejected."""
+    import itertools
+    checked = rejected = 0
+    cols = [1, 3, 8, 16, 33, 64, 100, 127, 128, 200, 1000, 1024, 1025, 1536, 2048, 3000, 4096,
+            6144, 8192, 8500, 12288, 16384, 20000, 32768, 65536, 262144, 1600000]
+    for n_cols, dtype, pad, off in itertools.product(cols, (rws.F32, rws.BF16, rws.F16),
+                                                       (0, 1, 8), (0, 4)):
+        for n_rows in (1, 7, 4099):
+            stride = n_cols + pad
+            in_ptr = (1 << 20) + off
+            try:
+                p = plan(n_rows, n_cols, in_row_stride=stride, out_row_stride=stride, dtype=dtype,
+                         in_ptr=in_ptr)
+            except rws.SoftmaxError:
+                continue
+            st = rws.plan_check(rws.GB300, p, n_rows, n_cols, stride, stride, dtype, in_ptr)
+            assert st == rws.OK, (n_rows, n_cols, dtype, pad, off, str(p), rws.status_string(st))
+            checked += 1
+            bad = rws.Plan.from_buffer_copy(p)
+            if p.path == rws.PATH_WARP and 2 <= p.lanes_per_row < 32:
+                bad.lanes_per_row = p.lanes_per_row // 2
+                if bad.lanes_per_row * p.vec >= n_cols:
+                    continue
+            elif p.path in (rws.PATH_CTA, rws.PATH_CLUSTER) and p.slice_cols > (16 // (4 if dtype == rws.F32 else 2)):
+                bad.slice_cols = p.slice_cols // 2 // 8 * 8
+                if bad.slice_cols * p.cluster >= n_cols:
+                    continue
+            elif p.path == rws.PATH_WARP and p.chunks > 1:
+                bad.chunks = p.chunks // 2
+                if 32 * bad.vec * bad.chunks >= n_cols:
+                    continue
+            else:
+                continue
+            st = rws.plan_check(rws.GB300, bad, n_rows, n_cols, stride, stride, dtype, in_ptr)
+            assert st == rws.ERR_INVALID_ARG, (n_cols, dtype, str(bad))
+            rejected += 1
+    assert checked > 500 and rejected > 100, (checked, rejected)
