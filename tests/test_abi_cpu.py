@@ -58,6 +58,10 @@ def test_scheduler_paths_for_the_five_workloads(lib):
     p = plan(32768, 1024, dtype=rws.BF16)                 # bf16 short rows: staged tiles
     assert (p.path, p.bulk_copy, p.vec, p.chunks, p.rows_per_warp) == (rws.PATH_WARP, 1, 8, 4, 1)
     assert (p.stages, p.smem_bytes) == (2, 16384)
+    p = plan(32768, 2048, dtype=rws.BF16)                 # 4 KB rows: 64-thread CTAs
+    assert (p.path, p.threads, p.chunks, p.stages) == (rws.PATH_CTA, 64, 4, 2)
+    p = plan(21845, 1536)                                 # 6 KB fp32 rows: 64 x 8 vectors
+    assert (p.path, p.threads, p.chunks) == (rws.PATH_CTA, 64, 8)
     p = plan(1 << 20, 16)                                 # short rows: 4 lanes a row
     assert (p.path, p.bulk_copy, p.vec, p.chunks, p.lanes_per_row) == (rws.PATH_WARP, 0, 4, 1, 4)
     p = plan(1 << 20, 64, dtype=rws.BF16)                 # 16-bit too, up to 128 columns
